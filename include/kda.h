@@ -1,0 +1,131 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention forward.
+ *
+ * The operator (one independent chain per sequence n and head h):
+ *
+ *     S = h0[n,h]  (dk x dv, or zeros)
+ *     for each token t of the sequence, in order:
+ *         S   <- diag(exp(g_t)) S                   channel-wise forget gate
+ *         S   <- S + beta_t k_t (v_t - S^T k_t)^T   delta-rule write
+ *         o_t  = scale * S^T q_t                    read-out after the write
+ *     hT[n,h] = S
+ *
+ * Sources: "Kimi K3 技术报告摘要" (gkm0120.cn/p/60370.html), section 1
+ * 预训练 Recipe, 训练策略 table, KDA row (delta-rule recurrence with a
+ * channel-wise forget gate, computed chunk-wise: parallel inside a chunk,
+ * recurrent across chunks); "Kimi K3 NPU Training", section 模型结构 (L2
+ * normalised q/k, per-channel decay and beta; a fixed matrix state per head
+ * at decode) and section 定长与 TND (the state resets at every packed
+ * sequence boundary; cu_seqlens).  g carries log(alpha) in natural-log units.
+ *
+ * Conventions shared by every entry point:
+ *   - The caller owns every buffer.  The library allocates no memory and
+ *     keeps no global state; calls are reentrant.
+ *   - Tensor pointers are DEVICE pointers, 16-byte aligned, dense and
+ *     row-major with the innermost dimension contiguous.  Activations are
+ *     token-major [B, T, H, d]; a packed batch is [1, T_total, H, d] with
+ *     int32 cu_seqlens[N+1].  States are float32 [N, H, dk, dv], dv fastest.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  No host synchronisation except in
+ *     kda_read_device_status().
+ *   - Host-checkable argument errors return before anything is launched.
+ *     Launch failures return KDA_ERR_CUDA.  Errors found on the device
+ *     (malformed cu_seqlens, a bounded wait that ran out, a decay outside
+ *     the supported range) are latched in the workspace status word; read
+ *     them with kda_read_device_status().
+ *   - `out` must not alias any input.  `hT` may alias `h0`.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1,    /* null pointer, bad size, misalignment, B/T/H out of range */
+  KDA_ERR_UNSUPPORTED = 2,    /* valid but not implemented (e.g. dk != dv, d not 64/128) */
+  KDA_ERR_WORKSPACE = 3,      /* workspace missing, misaligned or smaller than kda_workspace_size */
+  KDA_ERR_CUDA = 4,           /* a CUDA call or kernel launch failed */
+  KDA_ERR_BAD_SEQLENS = 5,    /* device: cu_seqlens not non-decreasing from 0 to T */
+  KDA_ERR_DEVICE_TIMEOUT = 6, /* device: a bounded wait inside a kernel ran out */
+  KDA_ERR_DECAY_RANGE = 7     /* device: a decay factor left the range the bf16 path supports */
+} kda_status;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+typedef struct {
+  int32_t B;            /* fixed length: batch size.  Packed: must be 1. */
+  int32_t T;            /* tokens per sequence (fixed) or total tokens (packed), >= 0 */
+  int32_t H;            /* heads, >= 1 */
+  int32_t dk, dv;       /* head dims; supported: dk == dv in {64, 128} */
+  int32_t num_seqs;     /* packed: N = number of sequences; ignored when cu_seqlens is NULL */
+  kda_dtype in_dtype;   /* dtype of q, k, v, g, beta (all the same) */
+  kda_dtype out_dtype;  /* dtype of o; KDA_F32 recommended (bf16 output rounding alone
+                           costs about 2^-9 of each output) */
+  float scale;          /* read-out scale, usually dk^-1/2 */
+} kda_shape;
+
+/* Bytes of workspace kda_fwd / kda_decode need for `s` (always >= 256: the first
+ * 256 bytes hold the device status word).  Returns 0 if `s` is NULL. */
+size_t kda_workspace_size(const kda_shape* s);
+
+/*
+ * Chunkwise prefill over fixed-length or packed variable-length sequences.
+ *
+ *   q, k, g  [B,T,H,dk]   in_dtype.  q and k L2-normalised per (token, head);
+ *                         g = log(alpha) <= 0.
+ *   v        [B,T,H,dv]   in_dtype.
+ *   beta     [B,T,H]      in_dtype, in [0, 1].
+ *   cu_seqlens  device int32 [num_seqs+1] or NULL (fixed length, N = B).
+ *   h0       device float32 [N,H,dk,dv] start states, or NULL for zeros.
+ *   out      device [B,T,H,dv] out_dtype.
+ *   hT       device float32 [N,H,dk,dv] final states, or NULL.
+ *   workspace   device, 256-byte aligned, >= kda_workspace_size(s) bytes; its
+ *               contents on entry do not matter.
+ * When B*T == 0 the activation pointers may be NULL (hT is still written).
+ * Chunks of 64 tokens start at each sequence start; the last chunk of a
+ * sequence may be partial.  A zero-length sequence writes hT = h0 (or 0).
+ * The float32 path (in_dtype KDA_F32) evaluates every product in float32;
+ * the bf16 path uses tensor cores with split bf16 operands and float32
+ * accumulation.
+ */
+kda_status kda_fwd(const kda_shape* s, const void* q, const void* k, const void* v,
+                   const void* g, const void* beta, const int32_t* cu_seqlens,
+                   const float* h0, void* out, float* hT, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
+/*
+ * Decode step: T_step = s->T tokens (1..8) per sequence applied in order to a
+ * state pool resident in device memory, updated in place (the replay form of
+ * speculative-decode rollback: the cached inputs of the accepted tokens are
+ * re-applied on chip; "Kimi K3 模型结构（7）：结构决定系统", section KDA 状态回滚).
+ *
+ *   q, k, g  [B,T_step,H,dk], v [B,T_step,H,dv], beta [B,T_step,H]   in_dtype
+ *   state    device float32 [B,H,dk,dv], read and written in place
+ *   out      device [B,T_step,H,dv] out_dtype (one output per token)
+ * B is the number of sequences; cu_seqlens is not used.
+ */
+kda_status kda_decode(const kda_shape* s, const void* q, const void* k, const void* v,
+                      const void* g, const void* beta, float* state, void* out,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, then returns (and clears) the status latched in the
+ * workspace by the kernels of the latest kda_fwd / kda_decode call that used
+ * it (each call clears the word when it starts): KDA_OK or a device error. */
+kda_status kda_read_device_status(void* workspace, void* stream);
+
+/* Static description of a status code; never NULL. */
+const char* kda_status_string(kda_status st);
+
+/* Library version, e.g. "kda-gb300 0.1". */
+const char* kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KDA_H_ */

@@ -1,0 +1,150 @@
+// C ABI entry points: argument validation, workspace carving and dispatch.
+// Every check that can be made on the host is made before anything is
+// launched; nothing here allocates memory.
+#include <stdio.h>
+
+#include "kda_internal.cuh"
+
+using namespace kda;
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+size_t dsize(kda_dtype t) { return t == KDA_F32 ? 4 : 2; }
+
+// Shape checks shared by prefill and decode.
+kda_status check_shape(const kda_shape* s, bool packed) {
+  if (!s) return KDA_ERR_INVALID_ARG;
+  if (s->H < 1 || s->T < 0 || s->dk < 1 || s->dv < 1) return KDA_ERR_INVALID_ARG;
+  if (packed ? (s->B != 1 || s->num_seqs < 0) : s->B < 0) return KDA_ERR_INVALID_ARG;
+  if ((s->in_dtype != KDA_F32 && s->in_dtype != KDA_BF16) ||
+      (s->out_dtype != KDA_F32 && s->out_dtype != KDA_BF16))
+    return KDA_ERR_INVALID_ARG;
+  if (!(s->scale == s->scale)) return KDA_ERR_INVALID_ARG;  // NaN scale
+  if (s->dk != s->dv || (s->dk != 64 && s->dk != 128)) return KDA_ERR_UNSUPPORTED;
+  // the largest index used is (B*T*H) * d; keep it well inside int64 and the grid
+  const int64_t toks = (int64_t)s->B * s->T;
+  if (toks > ((int64_t)1 << 40) / ((int64_t)s->H * s->dk)) return KDA_ERR_INVALID_ARG;
+  return KDA_OK;
+}
+
+kda_status check_ws(const kda_shape* s, void* ws, size_t bytes) {
+  if (!ws || !aligned(ws, 256)) return KDA_ERR_WORKSPACE;
+  if (bytes < kda_workspace_size(s)) return KDA_ERR_WORKSPACE;
+  return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kda_workspace_size(const kda_shape* s) {
+  if (!s) return 0;
+  size_t b = kWsHeader;
+  if (s->num_seqs > 0) b += ws_order_bytes(s->num_seqs);
+  return b;
+}
+
+kda_status kda_fwd(const kda_shape* s, const void* q, const void* k, const void* v,
+                   const void* g, const void* beta, const int32_t* cu_seqlens,
+                   const float* h0, void* out, float* hT, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  const bool packed = cu_seqlens != nullptr;
+  kda_status st = check_shape(s, packed);
+  if (st != KDA_OK) return st;
+  // with no tokens the activation buffers are empty and may be NULL
+  const bool any_tokens = (int64_t)s->B * s->T > 0;
+  if (any_tokens && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, g, out, h0, hT};
+  for (const void* p : ptrs)
+    if (p && !aligned(p, 16)) return KDA_ERR_INVALID_ARG;
+  if (!aligned(beta, dsize(s->in_dtype)) || (packed && !aligned(cu_seqlens, 4)))
+    return KDA_ERR_INVALID_ARG;
+  st = check_ws(s, workspace, workspace_bytes);
+  if (st != KDA_OK) return st;
+
+  FwdArgs a{};
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
+  a.cu = cu_seqlens; a.h0 = h0; a.out = out; a.hT = hT;
+  a.T = s->T;
+  a.N = packed ? s->num_seqs : s->B;
+  a.H = s->H;
+  a.D = s->dk;
+  a.scale = s->scale;
+  a.in_dtype = s->in_dtype;
+  a.out_dtype = s->out_dtype;
+  a.status = static_cast<unsigned int*>(workspace);
+  a.stream = static_cast<cudaStream_t>(stream);
+
+  if (cudaMemsetAsync(workspace, 0, kWsHeader, a.stream) != cudaSuccess) return KDA_ERR_CUDA;
+  if (packed) {
+    int32_t* order = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + kWsHeader);
+    if (launch_schedule(a, order) != cudaSuccess) return KDA_ERR_CUDA;
+    a.order = order;
+  }
+  cudaError_t e;
+  if (s->in_dtype == KDA_BF16 && s->dk == 128)
+    e = launch_prefill_bf16(a);
+  else
+    e = launch_prefill_f32(a);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_decode(const kda_shape* s, const void* q, const void* k, const void* v,
+                      const void* g, const void* beta, float* state, void* out,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  kda_status st = check_shape(s, false);
+  if (st != KDA_OK) return st;
+  if (s->T < 1 || s->T > 8) return KDA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !g || !beta || !state || !out) return KDA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, g, state, out};
+  for (const void* p : ptrs)
+    if (!aligned(p, 16)) return KDA_ERR_INVALID_ARG;
+  if (!aligned(beta, dsize(s->in_dtype))) return KDA_ERR_INVALID_ARG;
+  st = check_ws(s, workspace, workspace_bytes);
+  if (st != KDA_OK) return st;
+
+  DecodeArgs a{};
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
+  a.state = state; a.out = out;
+  a.B = s->B; a.Tstep = s->T; a.H = s->H; a.D = s->dk;
+  a.scale = s->scale;
+  a.in_dtype = s->in_dtype;
+  a.out_dtype = s->out_dtype;
+  a.stream = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, kWsHeader, a.stream) != cudaSuccess) return KDA_ERR_CUDA;
+  return launch_decode(a) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_read_device_status(void* workspace, void* stream) {
+  if (!workspace || !aligned(workspace, 256)) return KDA_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned int code = 0;
+  if (cudaMemcpyAsync(&code, workspace, sizeof(code), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
+  if (code != 0) {
+    if (cudaMemsetAsync(workspace, 0, sizeof(code), s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
+  }
+  return static_cast<kda_status>(code);
+}
+
+const char* kda_status_string(kda_status st) {
+  switch (st) {
+    case KDA_OK: return "ok";
+    case KDA_ERR_INVALID_ARG: return "invalid argument";
+    case KDA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case KDA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case KDA_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case KDA_ERR_BAD_SEQLENS: return "cu_seqlens is not non-decreasing from 0 to T";
+    case KDA_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel ran out";
+    case KDA_ERR_DECAY_RANGE: return "a decay factor left the range the bf16 path supports";
+  }
+  return "unknown status";
+}
+
+const char* kda_version(void) { return "kda-gb300 0.1"; }
+
+}  // extern "C"

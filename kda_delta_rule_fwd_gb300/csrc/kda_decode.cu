@@ -1,0 +1,167 @@
+// KDA decode: T_step (1..8) tokens applied in order to per-head float32 states
+// resident in device memory, updated in place.
+//
+// Per token (one fixed matrix state per head at decode: "Kimi K3 NPU Training",
+// section 模型结构, step 4; replay of cached inputs to rebuild the state:
+// "Kimi K3 模型结构（7）：结构决定系统", section KDA 状态回滚):
+//     S <- diag(alpha) S;  p = S^T k;  u = beta (v - p);  S <- S + k u^T;
+//     o = scale S^T q = scale ((diag(alpha) S)^T q + u (k . q))
+// The second form of o lets one cross-warp reduction produce both S^T k and
+// S^T q from the decayed state.
+//
+// Layout and work split: one CTA of 256 threads per (sequence, head).  The
+// state S [D x D] (row = key channel, dv contiguous) lives in registers: warp w
+// owns rows [w*D/8, (w+1)*D/8) and lane l owns columns [l*D/32, (l+1)*D/32), so
+// every warp load/store of a state row is one contiguous, vectorised access.
+// The kernel is HBM-bound: each head reads and writes 4*D*D bytes of state.
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kDecodeThreads = 256;
+constexpr int kMaxTstep = 8;
+
+template <int N> struct VecF;
+template <> struct VecF<2> { using T = float2; };
+template <> struct VecF<4> { using T = float4; };
+
+template <int D, typename TIn, typename TOut>
+__global__ void __launch_bounds__(kDecodeThreads, 2)
+kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
+                  const TIn* __restrict__ v, const TIn* __restrict__ g,
+                  const TIn* __restrict__ beta, float* __restrict__ state,
+                  TOut* __restrict__ out, int H, int Tstep, float scale) {
+  constexpr int R = D / 8;     // state rows per warp
+  constexpr int CPL = D / 32;  // state columns per lane
+  using Vec = typename VecF<CPL>::T;
+
+  __shared__ float s_k[kMaxTstep][D];
+  __shared__ float s_q[kMaxTstep][D];
+  __shared__ float s_a[kMaxTstep][D];   // alpha = exp(g)
+  __shared__ float s_v[kMaxTstep][D];
+  __shared__ float s_b[kMaxTstep];
+  __shared__ float s_kq[kMaxTstep];
+  __shared__ float s_red[8][2][D];      // per-warp partial S^T k and S^T q
+  __shared__ float s_u[D];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t nh = blockIdx.x;  // n * H + h
+  const int64_t n = nh / H, h = nh % H;
+
+  // Issue the state loads first: they are the HBM traffic that matters.
+  float* Sg = state + nh * (int64_t)D * D;
+  float S[R][CPL];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const Vec x = *reinterpret_cast<const Vec*>(Sg + (int64_t)(warp * R + r) * D + lane * CPL);
+    const float* xf = reinterpret_cast<const float*>(&x);
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) S[r][c] = xf[c];
+  }
+
+  // Stage the step's inputs (Tstep tokens) in shared memory as float32.
+  for (int i = tid; i < Tstep * D; i += kDecodeThreads) {
+    const int t = i / D, c = i % D;
+    const int64_t x = ((n * Tstep + t) * H + h) * D + c;
+    s_k[t][c] = to_f32(k[x]);
+    s_q[t][c] = to_f32(q[x]);
+    s_a[t][c] = expf(to_f32(g[x]));
+    s_v[t][c] = to_f32(v[x]);
+  }
+  if (tid < Tstep) s_b[tid] = to_f32(beta[(n * Tstep + tid) * H + h]);
+  __syncthreads();
+  // k . q per token, one warp per token
+  if (warp < Tstep) {
+    float acc = 0.f;
+    for (int c = lane; c < D; c += 32) acc += s_k[warp][c] * s_q[warp][c];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) s_kq[warp] = acc;
+  }
+  __syncthreads();
+
+  for (int t = 0; t < Tstep; ++t) {
+    // decay and partial reductions over this warp's rows
+    float pk[CPL], pq[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) pk[c] = pq[c] = 0.f;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int i = warp * R + r;
+      const float a = s_a[t][i], ki = s_k[t][i], qi = s_q[t][i];
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) {
+        S[r][c] *= a;
+        pk[c] = fmaf(S[r][c], ki, pk[c]);
+        pq[c] = fmaf(S[r][c], qi, pq[c]);
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+      s_red[warp][0][lane * CPL + c] = pk[c];
+      s_red[warp][1][lane * CPL + c] = pq[c];
+    }
+    __syncthreads();
+    if (tid < D) {
+      float sk = 0.f, sq = 0.f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        sk += s_red[w][0][tid];
+        sq += s_red[w][1][tid];
+      }
+      const float u = s_b[t] * (s_v[t][tid] - sk);
+      s_u[tid] = u;
+      const float o = scale * fmaf(u, s_kq[t], sq);
+      out[((n * Tstep + t) * H + h) * D + tid] = from_f32<TOut>(o);
+    }
+    __syncthreads();
+    // rank-1 write S <- S + k u^T
+    float u[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) u[c] = s_u[lane * CPL + c];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const float ki = s_k[t][warp * R + r];
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) S[r][c] = fmaf(ki, u[c], S[r][c]);
+    }
+  }
+
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    Vec x;
+    float* xf = reinterpret_cast<float*>(&x);
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) xf[c] = S[r][c];
+    *reinterpret_cast<Vec*>(Sg + (int64_t)(warp * R + r) * D + lane * CPL) = x;
+  }
+}
+
+template <int D, typename TIn>
+cudaError_t launch_d_in(const DecodeArgs& a) {
+  const int64_t blocks = (int64_t)a.B * a.H;
+  if (blocks == 0 || a.Tstep == 0) return cudaSuccess;
+  const TIn* q = static_cast<const TIn*>(a.q);
+  const TIn* k = static_cast<const TIn*>(a.k);
+  const TIn* v = static_cast<const TIn*>(a.v);
+  const TIn* g = static_cast<const TIn*>(a.g);
+  const TIn* b = static_cast<const TIn*>(a.beta);
+  if (a.out_dtype == KDA_F32)
+    kda_decode_kernel<D, TIn, float><<<(unsigned)blocks, kDecodeThreads, 0, a.stream>>>(
+        q, k, v, g, b, a.state, static_cast<float*>(a.out), a.H, a.Tstep, a.scale);
+  else
+    kda_decode_kernel<D, TIn, __nv_bfloat16><<<(unsigned)blocks, kDecodeThreads, 0, a.stream>>>(
+        q, k, v, g, b, a.state, static_cast<__nv_bfloat16*>(a.out), a.H, a.Tstep, a.scale);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs& a) {
+  if (a.D == 128)
+    return a.in_dtype == KDA_F32 ? launch_d_in<128, float>(a) : launch_d_in<128, __nv_bfloat16>(a);
+  return a.in_dtype == KDA_F32 ? launch_d_in<64, float>(a) : launch_d_in<64, __nv_bfloat16>(a);
+}
+
+}  // namespace kda

@@ -1,0 +1,125 @@
+"""The C ABI library on a machine without a GPU: it loads, exports every entry
+point the header declares, and rejects bad arguments on the host before any
+CUDA call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build_library()
+    import kda_delta_rule_fwd_gb300 as m
+    return m, m.load()
+
+
+def _declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"\b(kda_\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(lib):
+    m, L = lib
+    declared = _declared_functions()
+    assert {"kda_fwd", "kda_decode", "kda_workspace_size", "kda_read_device_status",
+            "kda_status_string"} <= set(declared)
+    for name in declared:
+        assert hasattr(L, name), f"{name} declared in include/ but not exported"
+
+
+def test_status_strings_and_version(lib):
+    m, L = lib
+    for code in range(8):
+        s = m.status_string(code)
+        assert s and s != "unknown status"
+    assert m.status_string(99) == "unknown status"
+    assert m.version().startswith("kda-gb300")
+
+
+def _shape(m, **kw):
+    d = dict(B=2, T=100, H=4, dk=128, dv=128, num_seqs=0, in_dtype=m.KDA_BF16,
+             out_dtype=m.KDA_F32, scale=128 ** -0.5)
+    d.update(kw)
+    return m.Shape(**d)
+
+
+def test_workspace_size(lib):
+    m, L = lib
+    assert L.kda_workspace_size(None) == 0
+    assert m.workspace_size(_shape(m)) == 256
+    # packed batches add a 64-entry-aligned int32 order list
+    assert m.workspace_size(_shape(m, B=1, num_seqs=1)) == 256 + 256
+    assert m.workspace_size(_shape(m, B=1, num_seqs=65)) == 256 + 512
+
+
+FAKE = 1 << 32  # an aligned, never-dereferenced stand-in for a device pointer
+
+
+def _fwd(L, shape, *, q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, cu=None, h0=None, out=FAKE,
+         hT=None, ws=FAKE, ws_bytes=1 << 20):
+    vp = ctypes.c_void_p
+    return L.kda_fwd(None if shape is None else ctypes.byref(shape), vp(q), vp(k), vp(v), vp(g),
+                     vp(beta), vp(cu), vp(h0), vp(out), vp(hT), vp(ws), ws_bytes, None)
+
+
+def _decode(L, shape, *, state=FAKE, out=FAKE, ws=FAKE, ws_bytes=1 << 20, beta=FAKE):
+    vp = ctypes.c_void_p
+    return L.kda_decode(ctypes.byref(shape), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(beta),
+                        vp(state), vp(out), vp(ws), ws_bytes, None)
+
+
+def test_argument_errors_return_before_launch(lib):
+    m, L = lib
+    assert _fwd(L, None) == m.KDA_ERR_INVALID_ARG
+    assert _fwd(L, _shape(m, H=0)) == m.KDA_ERR_INVALID_ARG
+    assert _fwd(L, _shape(m, T=-1)) == m.KDA_ERR_INVALID_ARG
+    assert _fwd(L, _shape(m, in_dtype=7)) == m.KDA_ERR_INVALID_ARG
+    assert _fwd(L, _shape(m, scale=float("nan"))) == m.KDA_ERR_INVALID_ARG
+    assert _fwd(L, _shape(m, dk=96, dv=96)) == m.KDA_ERR_UNSUPPORTED
+    assert _fwd(L, _shape(m, dk=128, dv=64)) == m.KDA_ERR_UNSUPPORTED
+    assert _fwd(L, _shape(m), q=0) == m.KDA_ERR_INVALID_ARG
+    assert _fwd(L, _shape(m), out=0) == m.KDA_ERR_INVALID_ARG
+    assert _fwd(L, _shape(m), k=FAKE + 8) == m.KDA_ERR_INVALID_ARG       # not 16-byte aligned
+    assert _fwd(L, _shape(m), h0=FAKE + 4) == m.KDA_ERR_INVALID_ARG
+    assert _fwd(L, _shape(m), beta=FAKE + 1) == m.KDA_ERR_INVALID_ARG    # bf16 beta misaligned
+    assert _fwd(L, _shape(m), ws=0) == m.KDA_ERR_WORKSPACE
+    assert _fwd(L, _shape(m), ws=FAKE + 16) == m.KDA_ERR_WORKSPACE       # not 256-byte aligned
+    assert _fwd(L, _shape(m), ws_bytes=255) == m.KDA_ERR_WORKSPACE
+    # packed batches need B == 1 and room for the order list
+    assert _fwd(L, _shape(m, B=2, num_seqs=3), cu=FAKE) == m.KDA_ERR_INVALID_ARG
+    assert _fwd(L, _shape(m, B=1, num_seqs=3), cu=FAKE, ws_bytes=256) == m.KDA_ERR_WORKSPACE
+    assert _fwd(L, _shape(m, B=1, num_seqs=3), cu=FAKE + 2) == m.KDA_ERR_INVALID_ARG
+    # decode: 1..8 tokens per step
+    assert _decode(L, _shape(m, T=0)) == m.KDA_ERR_UNSUPPORTED
+    assert _decode(L, _shape(m, T=9)) == m.KDA_ERR_UNSUPPORTED
+    assert _decode(L, _shape(m, T=1), state=0) == m.KDA_ERR_INVALID_ARG
+    assert _decode(L, _shape(m, T=1), state=FAKE + 8) == m.KDA_ERR_INVALID_ARG
+    assert _decode(L, _shape(m, T=1), ws_bytes=0) == m.KDA_ERR_WORKSPACE
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="would launch on fake pointers")
+def test_valid_call_without_a_gpu_reports_cuda_error(lib):
+    """With valid arguments the first CUDA call fails on a GPU-less host, and the
+    library maps that to KDA_ERR_CUDA instead of crashing."""
+    m, L = lib
+    assert _fwd(L, _shape(m)) == m.KDA_ERR_CUDA
+    assert _decode(L, _shape(m, T=8)) == m.KDA_ERR_CUDA
+    assert L.kda_read_device_status(ctypes.c_void_p(FAKE), None) == m.KDA_ERR_CUDA
+    assert L.kda_read_device_status(ctypes.c_void_p(FAKE + 16), None) == m.KDA_ERR_WORKSPACE
+
+
+def test_binding_refuses_to_run_without_library(tmp_path):
+    import kda_delta_rule_fwd_gb300 as m
+    with pytest.raises(RuntimeError, match="not built"):
+        m.load(str(tmp_path / "missing.so"))

@@ -1,0 +1,132 @@
+"""GPU parity on small shapes: the CUDA path through the C ABI against the
+float64 oracle, element by element.  Shapes span several chunks and a ragged
+tail, packed batches with empty and one-token sequences, both head sizes and
+both input dtypes."""
+import numpy as np
+import pytest
+import torch
+
+import kda_inputs
+from _util import TOL_BF16, TOL_F32, rel_err
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+TOL = {torch.float32: TOL_F32, torch.bfloat16: TOL_BF16}
+
+
+def _check_fwd(kda, oracle_mod, x, dtype, out_dtype=torch.float32):
+    o, hT = kda.fwd(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens, h0=x.h0,
+                    out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    o_ref, h_ref = oracle_mod.recurrent(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens,
+                                        h0=x.h0)
+    eo, eh = rel_err(o, o_ref), rel_err(hT, h_ref)
+    tol = TOL[dtype]
+    if out_dtype == torch.bfloat16:  # the output rounding itself: half a bf16 ulp of |o|
+        d = np.abs(o.float().cpu().numpy() - o_ref)
+        bound = tol * np.sqrt(np.mean(o_ref ** 2)) + np.abs(o_ref) * 2.0 ** -8
+        assert np.all(d <= bound)
+    else:
+        assert eo <= tol, f"o: {eo:.3e} > {tol}"
+    assert eh <= tol, f"hT: {eh:.3e} > {tol}"
+    return eo, eh
+
+
+def test_tiny_fp32_workload(kda, oracle_mod):
+    """B=1, T=256, H=2, d=64, float32 in and out, h0 = 0."""
+    x = kda_inputs.workload(0, device=DEV)
+    _check_fwd(kda, oracle_mod, x, torch.float32)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 200])
+def test_fixed_length(kda, oracle_mod, dtype, d, T):
+    x = kda_inputs.fixed(2, T, 3, d, dtype=dtype, device=DEV, seed=T * 7 + d, h0_std=0.1)
+    _check_fwd(kda, oracle_mod, x, dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("d", [64, 128])
+def test_packed_varlen(kda, oracle_mod, dtype, d):
+    x = kda_inputs.packed([1, 2, 64, 0, 65, 130, 200], 2, d, dtype=dtype, device=DEV,
+                          seed=11 + d, h0_std=0.1)
+    _check_fwd(kda, oracle_mod, x, dtype)
+
+
+def test_zero_start_state_and_no_final_state(kda, oracle_mod):
+    x = kda_inputs.fixed(1, 100, 2, 128, dtype=torch.bfloat16, device=DEV, seed=5)
+    o, hT = kda.fwd(x.q, x.k, x.v, x.g, x.beta, output_final_state=False)
+    assert hT is None
+    o_ref, _ = oracle_mod.recurrent(x.q, x.k, x.v, x.g, x.beta)
+    assert rel_err(o, o_ref) <= TOL_BF16
+
+
+def test_bf16_output(kda, oracle_mod):
+    x = kda_inputs.fixed(1, 130, 2, 128, dtype=torch.bfloat16, device=DEV, seed=6, h0_std=0.1)
+    _check_fwd(kda, oracle_mod, x, torch.bfloat16, out_dtype=torch.bfloat16)
+
+
+def test_empty_batch_writes_start_state(kda, oracle_mod):
+    x = kda_inputs.packed([0, 0, 0], 2, 128, dtype=torch.bfloat16, device=DEV, seed=3,
+                          h0_std=0.1)
+    o, hT = kda.fwd(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens, h0=x.h0)
+    torch.cuda.synchronize()
+    assert o.numel() == 0
+    assert torch.equal(hT, x.h0)
+
+
+def test_repeatable_bit_for_bit(kda):
+    x = kda_inputs.packed([90, 300, 17], 4, 128, dtype=torch.bfloat16, device=DEV, seed=21,
+                          h0_std=0.1)
+    o1, h1 = kda.fwd(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens, h0=x.h0)
+    o2, h2 = kda.fwd(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens, h0=x.h0)
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+
+
+def test_bad_cu_seqlens_is_reported_not_executed(kda):
+    x = kda_inputs.packed([50, 50], 2, 128, dtype=torch.bfloat16, device=DEV, seed=4)
+    bad = torch.tensor([0, 60, 40], dtype=torch.int32, device=DEV)  # decreasing
+    ws = kda.new_workspace(kda.make_shape(x.q, x.v, packed_seqs=2), DEV)
+    o = torch.full((1, 100, 2, 128), 7.0, device=DEV)
+    kda.fwd(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=bad, out=o, workspace=ws)
+    assert kda.read_device_status(ws) == kda.KDA_ERR_BAD_SEQLENS
+    assert torch.all(o == 7.0)  # nothing was written
+    assert kda.read_device_status(ws) == kda.KDA_OK  # reading clears the latch
+    short = torch.tensor([0, 50, 90], dtype=torch.int32, device=DEV)  # does not end at T
+    kda.fwd(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=short, out=o, workspace=ws)
+    assert kda.read_device_status(ws) == kda.KDA_ERR_BAD_SEQLENS
+
+
+# decode ---------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("T_step", [1, 3, 8])
+def test_decode(kda, oracle_mod, dtype, d, T_step):
+    x = kda_inputs.decode_pool(num_seqs=5, H=3, d=d, T_step=T_step, dtype=dtype, device=DEV,
+                               seed=100 + T_step)
+    state = x.h0.clone()
+    o = kda.decode(x.q, x.k, x.v, x.g, x.beta, state)
+    torch.cuda.synchronize()
+    o_ref, h_ref = oracle_mod.recurrent(x.q, x.k, x.v, x.g, x.beta, h0=x.h0)
+    tol = TOL[dtype]
+    assert rel_err(o, o_ref) <= tol
+    assert rel_err(state, h_ref) <= tol
+
+
+def test_decode_replay_equals_single_steps_and_prefill(kda):
+    """One 8-token replay step == eight 1-token steps == prefill from the same state."""
+    x = kda_inputs.decode_pool(num_seqs=3, H=2, d=128, T_step=8, dtype=torch.float32,
+                               device=DEV, seed=55)
+    s8 = x.h0.clone()
+    o8 = kda.decode(x.q, x.k, x.v, x.g, x.beta, s8)
+    s1 = x.h0.clone()
+    o1 = torch.cat([kda.decode(x.q[:, t:t + 1].contiguous(), x.k[:, t:t + 1].contiguous(),
+                               x.v[:, t:t + 1].contiguous(), x.g[:, t:t + 1].contiguous(),
+                               x.beta[:, t:t + 1].contiguous(), s1) for t in range(8)], dim=1)
+    op, hp = kda.fwd(x.q, x.k, x.v, x.g, x.beta, h0=x.h0)
+    torch.cuda.synchronize()
+    ref = o8.double().cpu().numpy()
+    assert rel_err(o1, ref) <= 1e-5 and rel_err(s1, s8.double().cpu().numpy()) <= 1e-5
+    assert rel_err(op, ref) <= 1e-4 and rel_err(hp, s8.double().cpu().numpy()) <= 1e-4
