@@ -1,0 +1,329 @@
+"""Benchmark of the KDA forward on GB300.
+
+Default workload (one "step" = one kda_fwd call over the whole batch):
+    fixed-length prefill, B=4, T=4096, H=32, dk=dv=128, bf16 q/k/v/g/beta,
+    float32 state and output, chunk 64, h0 = 0.
+The decode pool (1024 sequences, H=32, d=128, float32 states resident in HBM;
+T_step = 1 and an 8-token replay step) is timed in the same run and reported
+under "decode".
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  Under torchrun every rank runs its own batch (weak
+scaling, no data-path collective); the barrier and the max over ranks of the
+timed region are the only communication.  ``--impl reference`` times the
+float64 CPU oracle on the host's cores on a bounded sample of the same
+workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+B, T, H, D = 4, 4096, 32, 128
+CHUNK = 64
+# algorithmic work per token per head (chunk 64, d = 128): dense 64x64 tiles
+FLOP_PER_TOKEN_HEAD = 10 * CHUNK * D + 6 * D * D          # 180,224
+# minimum HBM bytes per token per head: q, k, v, g bf16 + beta bf16 + o float32
+BYTES_PER_TOKEN_HEAD = 4 * D * 2 + 2 + D * 4               # 1,538
+STATE_BYTES = D * D * 4                                    # one head's float32 state
+WORKLOAD = "KDA prefill, fixed length: B=4, T=4096, H=32, dk=dv=128, bf16 in, fp32 state/out, chunk 64"
+METRIC = "KDA fwd tokens/s at H=32,d=128 (prefill+decode); % of tensor/HBM roofline"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = [r.split(",") for r in open(self.path).read().strip().splitlines() if r.strip()]
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+                for name, val in zip(names, r[5:9]):
+                    if val.strip() == "Active":
+                        reasons.add(name)
+            except (ValueError, IndexError):
+                pass
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _cpu_baseline(x, budget_s=20.0):
+    """The float64 oracle on the host's cores: whole sequences of the first few
+    heads, as many heads as fit the time budget (estimated from one head)."""
+    import numpy as np
+    import torch
+    import oracle
+    cores = oracle.max_threads()
+    # sample: batch element 0, one head, first 1024 tokens -> per-token-head rate
+    t0 = time.perf_counter()
+    sl = lambda a: a[:1, :1024, :1].contiguous()
+    oracle.recurrent(sl(x.q), sl(x.k), sl(x.v), sl(x.g), x.beta[:1, :1024, :1].contiguous(),
+                     n_threads=1)
+    rate1 = 1024 / (time.perf_counter() - t0)          # token-heads/s on one core
+    heads = max(1, min(H, int(budget_s * rate1 * cores / (B * T))))
+    sub = lambda a: a[:, :, :heads].contiguous()
+    t0 = time.perf_counter()
+    oracle.recurrent(sub(x.q), sub(x.k), sub(x.v), sub(x.g), x.beta[:, :, :heads].contiguous(),
+                     n_threads=cores)
+    dt = time.perf_counter() - t0
+    head_tokens_per_s = B * T * heads / dt
+    return {"value": head_tokens_per_s / H, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"B={B}, T={T}, {heads} of {H} heads, all tokens ({dt:.1f} s); "
+                      f"tokens/s = head-tokens/s / H"}
+
+
+def _time_steps(fn, steps, warmup, stream, dist_on):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    if dist_on:
+        import torch.distributed as td
+        td.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist_on:
+        td.barrier()
+    return e0.elapsed_time(e1) / steps
+
+
+def run_ours(args):
+    import torch
+    import kda_inputs
+    import kda_delta_rule_fwd_gb300 as kda
+
+    rank, world, local = _dist()
+    dist_on = world > 1
+    if dist_on:
+        import torch.distributed as td
+        td.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
+    hbm_peak, bf16_peak, peak_kind = _peaks()
+
+    x = kda_inputs.workload(1, device=dev)
+    if rank:  # each rank its own batch of the same shape
+        x = kda_inputs.fixed(B, T, H, D, device=dev, seed=1001 + 97 * rank)
+    shape = kda.make_shape(x.q, x.v)
+    ws = kda.new_workspace(shape, dev)
+    o = torch.empty(B, T, H, D, device=dev)
+    hT = torch.empty(B, H, D, D, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        kda.fwd(x.q, x.k, x.v, x.g, x.beta, out=o, hT=hT, workspace=ws)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    ms = _time_steps(step, args.steps, args.warmup, stream, dist_on)
+    clk = clocks.stop()
+    st = kda.read_device_status(ws)
+    if st != kda.KDA_OK:
+        raise RuntimeError(f"device status {kda.status_string(st)}")
+
+    # end to end through the public API: pinned host inputs in, o and hT back to host
+    pin = lambda t: t.cpu().pin_memory()
+    hq, hk, hv, hg, hb = (pin(t) for t in (x.q, x.k, x.v, x.g, x.beta))
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hh = torch.empty(hT.shape, dtype=hT.dtype).pin_memory()
+    dq, dk_, dv, dg, db = (torch.empty_like(t) for t in (x.q, x.k, x.v, x.g, x.beta))
+
+    def e2e_step():
+        for d_, h_ in ((dq, hq), (dk_, hk), (dv, hv), (dg, hg), (db, hb)):
+            d_.copy_(h_, non_blocking=True)
+        kda.fwd(dq, dk_, dv, dg, db, out=o, hT=hT, workspace=ws)
+        ho.copy_(o, non_blocking=True)
+        hh.copy_(hT, non_blocking=True)
+
+    ms_e2e = _time_steps(e2e_step, max(3, args.steps // 4), 2, stream, dist_on)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg, hb))
+    d2h = ho.numel() * ho.element_size() + hh.numel() * hh.element_size()
+
+    # decode pool: T_step = 1 and 8, states resident in HBM (updated in place)
+    dec = {}
+    for T_step in (1, 8):
+        y = kda_inputs.decode_pool(num_seqs=1024, H=H, d=D, T_step=T_step, device=dev,
+                                   seed=1004 + 13 * rank)
+        state = y.h0
+        out_d = torch.empty(1024, T_step, H, D, device=dev)
+        dshape = kda.make_shape(y.q, y.v)
+        dws = kda.new_workspace(dshape, dev)
+        fn = lambda: kda.decode(y.q, y.k, y.v, y.g, y.beta, state, out=out_d, workspace=dws)
+        dms = _time_steps(fn, max(5, args.steps), max(3, args.warmup), stream, dist_on)
+        nbytes = 1024 * H * (2 * STATE_BYTES + T_step * BYTES_PER_TOKEN_HEAD)
+        dec[f"T{T_step}"] = {
+            "tokens_per_s": 1024 * T_step * world / (dms * 1e-3),
+            "ms_per_step": dms,
+            "roofline": {"bound": "hbm", "achieved": nbytes / (dms * 1e-3) / 1e9,
+                         "peak": hbm_peak, "unit": "GB/s",
+                         "frac": nbytes / (dms * 1e-3) / 1e9 / hbm_peak, "traffic": None},
+        }
+        del y, state, out_d
+
+    if dist_on:
+        t = torch.tensor([ms, ms_e2e], device=dev)
+        td.all_reduce(t, op=td.ReduceOp.MAX)
+        ms, ms_e2e = t.tolist()
+
+    tokens = B * T * world
+    alg_bytes = B * T * H * BYTES_PER_TOKEN_HEAD + B * H * STATE_BYTES
+    alg_flops = B * T * H * FLOP_PER_TOKEN_HEAD
+    achieved = alg_bytes / (ms * 1e-3) / 1e9
+    result = {
+        "metric": METRIC,
+        "value": tokens / (ms * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; q,k L2-normalised N(0,1); v N(0,1); g=-softplus(N(0,1)); "
+                "beta=sigmoid(N(0,1)))",
+        "config": {"workload": WORKLOAD, "B": B, "T": T, "H": H, "dk": D, "dv": D,
+                   "chunk": CHUNK, "tokens_per_rank": B * T,
+                   "l2": "inputs and outputs (~0.8 GB) exceed L2; no flush"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": None,
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "kernel": "kda_prefill (one launch per step)",
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "tensor_tflops_algorithmic": alg_flops / (ms * 1e-3) / 1e12,
+                     "tensor_frac_of_bf16_peak": alg_flops / (ms * 1e-3) / 1e12 / bf16_peak},
+        "e2e": {"value": tokens / (ms_e2e * 1e-3), "unit": "tokens/s", "ms_per_step": ms_e2e,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "decode": dec,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = _cpu_baseline(kda_inputs.workload(1, device=dev))
+    if dist_on:
+        td.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def run_reference(args):
+    """The float64 oracle, as it stands, on the host's cores.  Each step is a
+    bounded sample of the workload: the whole batch (B=4, T=4096) on a subset of
+    heads sized from a one-head probe so the run stays within minutes."""
+    rank, world, _ = _dist()
+    if rank != 0:
+        return
+    import kda_inputs
+    import oracle
+    x = kda_inputs.workload(1, device="cpu")
+    cores = oracle.max_threads()
+    t0 = time.perf_counter()
+    oracle.recurrent(x.q[:1, :512, :1].contiguous(), x.k[:1, :512, :1].contiguous(),
+                     x.v[:1, :512, :1].contiguous(), x.g[:1, :512, :1].contiguous(),
+                     x.beta[:1, :512, :1].contiguous(), n_threads=1)
+    rate1 = 512 / (time.perf_counter() - t0)
+    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
+    heads = max(1, min(H, int(per_step_budget * rate1 * cores / (B * T))))
+    sub = lambda a: a[:, :, :heads].contiguous()
+    args_ = (sub(x.q), sub(x.k), sub(x.v), sub(x.g), x.beta[:, :, :heads].contiguous())
+    for _ in range(args.warmup):
+        oracle.recurrent(*args_, n_threads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.recurrent(*args_, n_threads=cores)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = B * T * heads / dt / H
+    sample = f"B={B}, T={T}, {heads} of {H} heads per step; tokens/s = head-tokens/s / H"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "T": T, "H": H, "dk": D, "dv": D},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
