@@ -114,6 +114,37 @@ kda_status kda_decode(const kda_shape* s, const void* q, const void* k, const vo
                       const void* g, const void* beta, float* state, void* out,
                       void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * kda_fwd without a workspace, for callers that cannot allocate device memory:
+ * code whose device memory is planned in full by a host framework before it
+ * runs and that may not request more at call time, or bindings that cannot
+ * reach a device allocator at all.  The pages describe no such entry point;
+ * it has no counterpart there.
+ *
+ * Same arguments and results as kda_fwd, minus the workspace.  The scratch
+ * (status word and packed-batch sequence order) lives in a fixed array inside
+ * the library: 256 + 4 * 16384 bytes of device memory per GPU that loads the
+ * library, held until the process exits.  Limits and behaviour:
+ *   - packed batches of more than 16384 sequences return KDA_ERR_UNSUPPORTED
+ *     before anything is launched;
+ *   - the first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture;
+ *   - nothing is allocated: no cudaMalloc, no cudaFree, no allocating library
+ *     routine;
+ *   - every call on a device shares the one array, and each call clears the
+ *     status word it needs when it starts; calls whose work overlaps on the GPU
+ *     (other streams, or other host threads) race on the array, so serialise
+ *     them;
+ *   - status_out: optional DEVICE pointer to one unsigned int; when non-NULL,
+ *     the call's device status (KDA_OK or a device error code) is copied there
+ *     in stream order after the kernels.
+ */
+kda_status kda_fwd_noalloc(const kda_shape* s, const void* q, const void* k, const void* v,
+                           const void* g, const void* beta, const int32_t* cu_seqlens,
+                           const float* h0, void* out, float* hT, unsigned int* status_out,
+                           void* stream);
+
 /* Synchronises `stream`, then returns (and clears) the status latched in the
  * workspace by the kernels of the latest kda_fwd / kda_decode call that used
  * it (each call clears the word when it starts): KDA_OK or a device error. */
