@@ -38,7 +38,7 @@ def test_tiny_fp32_workload(kda, oracle_mod):
     _check_fwd(kda, oracle_mod, x, torch.float32)
 
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("T", [1, 63, 64, 65, 200])
 def test_fixed_length(kda, oracle_mod, dtype, d, T):
@@ -46,7 +46,7 @@ def test_fixed_length(kda, oracle_mod, dtype, d, T):
     _check_fwd(kda, oracle_mod, x, dtype)
 
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
 @pytest.mark.parametrize("d", [64, 128])
 def test_packed_varlen(kda, oracle_mod, dtype, d):
     x = kda_inputs.packed([1, 2, 64, 0, 65, 130, 200], 2, d, dtype=dtype, device=DEV,
@@ -100,7 +100,7 @@ def test_bad_cu_seqlens_is_reported_not_executed(kda):
 
 # decode ---------------------------------------------------------------------------------
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("T_step", [1, 3, 8])
 def test_decode(kda, oracle_mod, dtype, d, T_step):
