@@ -1,7 +1,748 @@
-// Placeholder until the tensor-core bf16 prefill lands: bf16 inputs run through
-// the float32 SIMT chunk kernel.
+// KDA chunkwise prefill, bf16 inputs, on the sm_100-family tensor cores.
+//
+// Chunkwise form of the recurrence ("Kimi K3 技术报告摘要", section 1, 训练策略
+// table, KDA row: parallel inside a chunk, recurrent across chunks; the
+// transition (I - beta k k^T) diag(alpha) is diagonal-plus-low-rank: "Kimi K3
+// NPU Training", section NPU 算子支持度, DPLR chunk kernel).  Per chunk of 64
+// tokens with Gam = inclusive per-channel prefix sum of g and one reference
+// rho = Gam at token 31 (mid chunk):
+//
+//   Akk = (K e^(Gam-rho)) (K e^(rho-Gam))^T      Aqk = (Q e^(Gam-rho)) (K e^(rho-Gam))^T
+//   T   = (I + strict_lower(diag(beta) Akk))^-1  (forward substitution)
+//   W   = T diag(beta) (K e^Gam)                 U~ = T diag(beta) V
+//   U   = U~ - W S                               O  = scale ((Q e^Gam) S + lower(Aqk) U)
+//   S  <- diag(e^Gam_last) S + (K e^(Gam_last - Gam))^T U
+//
+// Every product runs on tcgen05 with M = 128 and float32 accumulators in
+// tensor memory.  The state products are taken transposed (rows = value
+// channel) so that S^T lives in TMEM as the accumulator and as the A operand.
+// Operands on the output path are split into bf16 hi + lo parts (x = hi + lo,
+// products hi*hi + hi*lo + lo*hi), which keeps every product near float32
+// accuracy: a single bf16 rounding of an operand on the dominant path
+// already exceeds a 1e-2 max-error budget on heavy-tailed outputs.
+//
+// One CTA (256 threads) owns one (sequence, head) chain and walks its chunks
+// in order; the inputs of chunk n+1 are fetched by TMA while chunk n's state
+// update runs.  Each mbarrier wait is bounded: on expiry the CTA latches
+// KDA_ERR_DEVICE_TIMEOUT, drains its in-flight copies, frees TMEM and exits.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "kda_internal.cuh"
+#include "kda_sm100.cuh"
 
 namespace kda {
-cudaError_t launch_prefill_bf16(const FwdArgs& a) { return launch_prefill_f32(a); }
+namespace {
+
+using namespace sm100;
+
+constexpr int C = 64;            // chunk length (tokens)
+constexpr int D = 128;           // head dim (dk == dv)
+constexpr int kThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kMaxExp = 80.f;  // |Gam - rho| beyond this overflows the factorisation
+
+// ---- shared memory map (bytes) --------------------------------------------
+constexpr uint32_t SM_IN_Q = 0;          // TMA tiles, [8-channel group][token][8] bf16
+constexpr uint32_t SM_IN_K = 16384;
+constexpr uint32_t SM_IN_G = 32768;
+constexpr uint32_t SM_IN_V = 49152;
+constexpr uint32_t SM_X = 65536;         // 96 KB, reused across phases
+constexpr uint32_t X_R_HI = 0, X_R_LO = 32768, X_CK_HI = 65536, X_CK_LO = 81920;
+constexpr uint32_t X_A32 = 0, X_T32 = 16384, X_M32 = 32768;   // forward substitution
+constexpr uint32_t X_KBAR = 0, X_QH_HI = 16384, X_QH_LO = 32768, X_KH_HI = 49152,
+                   X_KH_LO = 65536, X_WT = 0;
+constexpr uint32_t SM_Y = 163840;        // 32 KB
+constexpr uint32_t Y_TB_HI = 0, Y_TB_LO = 8192, Y_AQK_HI = 16384, Y_AQK_LO = 24576;
+constexpr uint32_t SM_LL = 196608;       // [L; L] 128 x 64 bf16 (lower-triangular ones)
+constexpr uint32_t SM_MISC = 212992;
+constexpr uint32_t MISC_RHO = 0, MISC_GL = 512, MISC_ERHO = 1024, MISC_ECRHO = 1536,
+                   MISC_GAMC = 2048, MISC_BETA = 2560, MISC_BAR = 2816, MISC_TMEM = 2848,
+                   MISC_FLAG = 2852;
+constexpr uint32_t SMEM_BYTES = SM_MISC + 2880;
+
+// ---- tensor memory map (columns) -------------------------------------------
+constexpr uint32_t TM_S = 0;       // S^T float32 master: lane = value channel, col = key channel
+constexpr uint32_t TM_SHI = 128;   // S^T bf16 hi, two key channels per column
+constexpr uint32_t TM_SLO = 192;   // S^T bf16 lo
+constexpr uint32_t TM_ACC1 = 256;  // Gam (with ACC2) -> [Akk; Aqk]
+constexpr uint32_t TM_ACC2 = 320;  // Gam (upper half) -> W^T -> O^T
+constexpr uint32_t TM_ACC3 = 384;  // U~^T -> U^T
+constexpr uint32_t TM_UHI = 448;   // U^T bf16 hi, two tokens per column
+constexpr uint32_t TM_ULO = 480;   // U^T bf16 lo
+constexpr uint32_t TM_COLS = 512;
+
+// Canonical no-swizzle layouts (8 rows x 16 bytes per core matrix).  For an
+// operand with `rows` (M or N) and K = `kdim`, core (rb, kb) sits at
+// rb*(kdim/8)*128 + kb*128: LBO (K-adjacent cores) = 128 and SBO (M/N-adjacent
+// cores) = (kdim/8)*128.  K-major cores hold 8 rows of 8 K-values; MN-major
+// cores hold 8 K-rows of 8 M/N-values.
+__device__ __forceinline__ uint32_t off_kmaj(int r, int k, int kdim) {
+  return (r >> 3) * (kdim >> 3) * 128 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
+}
+__device__ __forceinline__ uint32_t off_mnmaj(int r, int k, int kdim) {
+  return (r >> 3) * (kdim >> 3) * 128 + (k >> 3) * 128 + (k & 7) * 16 + (r & 7) * 2;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+         ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+}
+// x = hi + lo with hi = bf16(x), lo = x - hi (stored rounded to bf16)
+__device__ __forceinline__ void split2(float x, float& hi, float& lo) {
+  hi = __bfloat162float(__float2bfloat16_rn(x));
+  lo = x - hi;
+}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// 8 bf16 from a 16-byte shared-memory vector
+__device__ __forceinline__ void ld8(const unsigned char* p, float (&x)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x); x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
+  x[4] = bf16_lo(u.z); x[5] = bf16_hi(u.z); x[6] = bf16_lo(u.w); x[7] = bf16_hi(u.w);
+}
+__device__ __forceinline__ void st8(unsigned char* p, const float (&x)[8]) {
+  uint4 u;
+  u.x = pack_bf16(x[0], x[1]); u.y = pack_bf16(x[2], x[3]);
+  u.z = pack_bf16(x[4], x[5]); u.w = pack_bf16(x[6], x[7]);
+  *reinterpret_cast<uint4*>(p) = u;
+}
+// store hi and lo parts of 8 values
+__device__ __forceinline__ void st8_split(unsigned char* phi, unsigned char* plo,
+                                          const float (&x)[8]) {
+  float h[8], l[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) split2(x[i], h[i], l[i]);
+  st8(phi, h);
+  st8(plo, l);
+}
+// hi and lo parts of 16 values, packed two per 32-bit word
+__device__ __forceinline__ void pack_split16(const float (&x)[16], uint32_t (&hi)[8],
+                                             uint32_t (&lo)[8]) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    float h0, l0, h1, l1;
+    split2(x[2 * e], h0, l0);
+    split2(x[2 * e + 1], h1, l1);
+    hi[e] = pack_bf16(h0, h1);
+    lo[e] = pack_bf16(l0, l1);
+  }
+}
+
+struct Bf16Params {
+  const __nv_bfloat16* beta;
+  SeqView seqs;
+  const int32_t* order;
+  const float* h0;
+  void* out;
+  float* hT;
+  int H;
+  float scale;
+  int out_bf16;
+  unsigned int* status;
+};
+
+// The CTA's bounded waits.  Every thread waits on the barrier itself; a thread
+// whose wait runs out raises the shared flag, and the CTA barrier that follows
+// each wait makes all threads see the same flag before they branch on it.
+struct Waits {
+  uint64_t* tma_bar;
+  uint64_t* mma_bar;
+  uint32_t mma_phase;
+  uint32_t tma_waited;  // TMA phases consumed so far
+  uint32_t* flag;       // nonzero once a wait ran out
+  unsigned int* status;
+  __device__ __forceinline__ void on_timeout() {
+    atomicExch(flag, 1u);
+    latch_status(status, KDA_ERR_DEVICE_TIMEOUT);
+  }
+  // wait for the MMAs committed last; returns true if the CTA must stop
+  __device__ __forceinline__ bool wait_mma() {
+    if (!mbar_wait(mma_bar, mma_phase)) on_timeout();
+    mma_phase ^= 1u;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    return *(volatile uint32_t*)flag != 0;
+  }
+  __device__ __forceinline__ bool wait_tma() {
+    if (!mbar_wait(tma_bar, tma_waited & 1u)) on_timeout();
+    ++tma_waited;
+    __syncthreads();
+    return *(volatile uint32_t*)flag != 0;
+  }
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_g,
+                        const __grid_constant__ CUtensorMap tm_v, Bf16Params p) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int qd = warp & 3;          // TMEM lane quarter of this warp
+  const int hw = warp >> 2;         // which half of the columns this warp handles
+  const int row = qd * 32 + lane;   // TMEM lane (accumulator row) of this thread
+
+  float* s_rho = reinterpret_cast<float*>(smem + SM_MISC + MISC_RHO);
+  float* s_gl = reinterpret_cast<float*>(smem + SM_MISC + MISC_GL);
+  float* s_erho = reinterpret_cast<float*>(smem + SM_MISC + MISC_ERHO);
+  float* s_ecrho = reinterpret_cast<float*>(smem + SM_MISC + MISC_ECRHO);
+  float* s_gamc = reinterpret_cast<float*>(smem + SM_MISC + MISC_GAMC);
+  float* s_beta = reinterpret_cast<float*>(smem + SM_MISC + MISC_BETA);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM_MISC + MISC_BAR);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + SM_MISC + MISC_TMEM);
+  uint32_t* s_flag = reinterpret_cast<uint32_t*>(smem + SM_MISC + MISC_FLAG);
+
+  // A malformed cu_seqlens is latched by the scheduler before this kernel
+  // starts; the value cannot change while it runs, so the test is CTA-uniform.
+  if (p.status && *(volatile const unsigned int*)p.status == (unsigned)KDA_ERR_BAD_SEQLENS)
+    return;
+
+  const int item = blockIdx.x;
+  const int n = p.order ? p.order[item / p.H] : item / p.H;
+  const int h = item % p.H;
+  int64_t t0, len;
+  p.seqs.get(n, t0, len);
+
+  if (tid == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    *s_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_g);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == 0) {
+    tmem_alloc(s_tmem, TM_COLS);
+    tmem_relinquish();
+  }
+  // [L; L]: rows r and 64 + r hold row r of the 64 x 64 lower-triangular ones
+  for (int i = tid; i < 128 * 8; i += kThreads) {
+    const int r = i >> 3, kb = i & 7;
+    float x[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = (kb * 8 + e) <= (r & 63) ? 1.f : 0.f;
+    st8(smem + SM_LL + off_kmaj(r, kb * 8, 64), x);
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = *s_tmem;
+  const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+  Waits wt{&bars[0], &bars[1], 0u, 0u, s_flag, p.status};
+  uint32_t tma_issued = 0;
+
+  const int nchunks = (int)((len + C - 1) / C);
+  auto issue_tma = [&](int chunk) {  // thread 0 only
+    ++tma_issued;
+    const int32_t y = (int32_t)(t0 + (int64_t)chunk * C);
+    const int32_t z = h * (D / 8);
+    mbar_arrive_expect_tx(wt.tma_bar, 4 * 16384);
+    tma_load_3d(smem + SM_IN_Q, &tm_q, 0, y, z, wt.tma_bar);
+    tma_load_3d(smem + SM_IN_K, &tm_k, 0, y, z, wt.tma_bar);
+    tma_load_3d(smem + SM_IN_G, &tm_g, 0, y, z, wt.tma_bar);
+    tma_load_3d(smem + SM_IN_V, &tm_v, 0, y, z, wt.tma_bar);
+  };
+  if (tid == 0 && nchunks > 0) issue_tma(0);
+
+  // start state S^T (lane = value channel j, columns = key channels) from h0
+  {
+    const int j = row;
+    const float* h0p = p.h0 ? p.h0 + (((int64_t)n * p.H + h) * D) * D : nullptr;
+#pragma unroll 1
+    for (int c0 = hw * 64; c0 < hw * 64 + 64; c0 += 16) {
+      float x[16];
+      uint32_t u[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) x[e] = h0p ? h0p[(int64_t)(c0 + e) * D + j] : 0.f;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) u[e] = __float_as_uint(x[e]);
+      tmem_st16(tb + lane_base + TM_S + c0, u);
+      uint32_t hi[8], lo[8];
+      pack_split16(x, hi, lo);
+      tmem_st8(tb + lane_base + TM_SHI + c0 / 2, hi);
+      tmem_st8(tb + lane_base + TM_SLO + c0 / 2, lo);
+    }
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t idesc_cum = idesc_bf16(128, 128, 0, 1);
+  const uint32_t idesc_kk = idesc_bf16(128, 64, 0, 0);
+  const uint32_t idesc_mnk = idesc_bf16(128, 64, 1, 0);
+  const uint32_t idesc_su = idesc_bf16(128, 64, 0, 1, 1);
+  const uint32_t idesc_sq = idesc_bf16(128, 64, 0, 0);
+  const uint32_t idesc_s = idesc_bf16(128, 128, 0, 1);
+  const uint32_t sbase = smem_u32(smem);
+  bool range_err = false;
+
+#pragma unroll 1
+  for (int ci = 0; ci < nchunks; ++ci) {
+    const int64_t cs = (int64_t)ci * C;
+    const int nv = (int)(len - cs < C ? len - cs : C);
+    const int rho_t = nv - 1 < 31 ? nv - 1 : 31;
+
+    // ---- P1: beta, wait for the tiles, cumulative log-decay on the tensor core
+    if (tid < C) {
+      const float b = tid < nv ? __bfloat162float(p.beta[(t0 + cs + tid) * p.H + h]) : 0.f;
+      s_beta[tid] = b;
+    }
+    if (wt.wait_tma()) break;
+    if (tid == 0) {
+      tc_fence_after();
+      // Gam (rows 0..63 and again 64..127) = [L; L] G, G = the g tile as an MN-major B
+#pragma unroll
+      for (int kk = 0; kk < C / 16; ++kk)
+        mma_ss(tb + TM_ACC1, smem_desc(sbase + SM_LL + kk * 256, 128, 1024),
+               smem_desc(sbase + SM_IN_G + kk * 256, 128, 1024), idesc_cum, kk > 0);
+      mma_commit(wt.mma_bar);
+    }
+    if (wt.wait_mma()) break;
+
+    // ---- P3 (pass A): decay factors and the decayed key/query operands
+    const int t = row & 63;
+    const int cg0 = (2 * (row >> 6) + hw) * 4;  // first 8-channel group of this thread
+    const bool valid = t < nv;
+    float gam[32];
+    {
+      float a[16];
+      tmem_ld16(tb + lane_base + TM_ACC1 + cg0 * 8, a);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) gam[e] = a[e];
+      tmem_ld16(tb + lane_base + TM_ACC1 + cg0 * 8 + 16, a);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) gam[16 + e] = a[e];
+      tmem_wait_ld();
+    }
+    if (t == rho_t)
+#pragma unroll
+      for (int e = 0; e < 32; ++e) s_rho[cg0 * 8 + e] = gam[e];
+    if (t == nv - 1)
+#pragma unroll
+      for (int e = 0; e < 32; ++e) s_gl[cg0 * 8 + e] = gam[e];
+    tc_fence_before();
+    __syncthreads();
+    if (tid < D) {
+      const float r = s_rho[tid], gl = s_gl[tid];
+      s_erho[tid] = exp2f(r * kLog2e);
+      s_ecrho[tid] = exp2f((gl - r) * kLog2e);
+      s_gamc[tid] = exp2f(gl * kLog2e);
+    }
+    float er[32], ec[32];
+#pragma unroll
+    for (int g4 = 0; g4 < 4; ++g4) {
+      const int cg = cg0 + g4;
+      float kx[8], qx[8];
+      ld8(smem + SM_IN_K + cg * 1024 + t * 16, kx);
+      ld8(smem + SM_IN_Q + cg * 1024 + t * 16, qx);
+      float rk[8], rq[8], ck[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float d = gam[g4 * 8 + e] - s_rho[cg * 8 + e];
+        if (valid && fabsf(d) > kMaxExp) range_err = true;
+        d = fminf(fmaxf(d, -kMaxExp), kMaxExp);
+        er[g4 * 8 + e] = exp2f(d * kLog2e);
+        ec[g4 * 8 + e] = exp2f(-d * kLog2e);
+        const float kv = valid ? kx[e] : 0.f, qv = valid ? qx[e] : 0.f;
+        rk[e] = kv * er[g4 * 8 + e];
+        rq[e] = qv * er[g4 * 8 + e];
+        ck[e] = kv * ec[g4 * 8 + e];
+      }
+      st8_split(smem + SM_X + X_R_HI + off_kmaj(t, cg * 8, 128),
+                smem + SM_X + X_R_LO + off_kmaj(t, cg * 8, 128), rk);
+      st8_split(smem + SM_X + X_R_HI + off_kmaj(64 + t, cg * 8, 128),
+                smem + SM_X + X_R_LO + off_kmaj(64 + t, cg * 8, 128), rq);
+      st8_split(smem + SM_X + X_CK_HI + off_kmaj(t, cg * 8, 128),
+                smem + SM_X + X_CK_LO + off_kmaj(t, cg * 8, 128), ck);
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+
+    // ---- P4: [Akk; Aqk] = R Ck^T with split operands
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t r_hi = sbase + SM_X + X_R_HI, r_lo = sbase + SM_X + X_R_LO;
+      const uint32_t c_hi = sbase + SM_X + X_CK_HI, c_lo = sbase + SM_X + X_CK_LO;
+      const uint32_t as[3] = {r_hi, r_hi, r_lo}, bs[3] = {c_hi, c_lo, c_hi};
+#pragma unroll
+      for (int pr = 0; pr < 3; ++pr)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tb + TM_ACC1, smem_desc(as[pr] + kk * 256, 128, 2048),
+                 smem_desc(bs[pr] + kk * 256, 128, 2048), idesc_kk, (pr | kk) != 0);
+      mma_commit(wt.mma_bar);
+    }
+    if (wt.wait_mma()) break;
+
+    // ---- P5: A = strict_lower(beta Akk) (float32, for the substitution), Aqk split
+    {
+      float a[32];
+      {
+        float x[16];
+        tmem_ld16(tb + lane_base + TM_ACC1 + hw * 32, x);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) a[e] = x[e];
+        tmem_ld16(tb + lane_base + TM_ACC1 + hw * 32 + 16, x);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) a[16 + e] = x[e];
+        tmem_wait_ld();
+      }
+      if (row < 64) {
+        const int i = row;
+        const float bi = s_beta[i];
+        float* A32 = reinterpret_cast<float*>(smem + SM_X + X_A32);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int j = hw * 32 + e;
+          A32[i * 64 + j] = j < i ? bi * a[e] : 0.f;
+        }
+      } else {
+        const int i = row - 64;
+#pragma unroll
+        for (int e8 = 0; e8 < 4; ++e8) {
+          float x[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int j = hw * 32 + e8 * 8 + e;
+            x[e] = j <= i ? a[e8 * 8 + e] : 0.f;
+          }
+          const uint32_t o = off_kmaj(i, hw * 32 + e8 * 8, 64);
+          st8_split(smem + SM_Y + Y_AQK_HI + o, smem + SM_Y + Y_AQK_LO + o, x);
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- P6: T = (I + A)^-1 by blocks of 16, then TB = T diag(beta) split
+    {
+      const float* A32 = reinterpret_cast<const float*>(smem + SM_X + X_A32);
+      float* T32 = reinterpret_cast<float*>(smem + SM_X + X_T32);
+      float* M32 = reinterpret_cast<float*>(smem + SM_X + X_M32);
+      if (tid < 64) {  // diagonal blocks: thread owns column jj of block I
+        const int I = tid >> 4, jj = tid & 15, base = I * 16;
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float acc = 0.f;
+#pragma unroll
+          for (int m = 0; m < i; ++m) acc = fmaf(A32[(base + i) * 64 + base + m], x[m], acc);
+          x[i] = i < jj ? 0.f : (i == jj ? 1.f : -acc);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) T32[(base + i) * 64 + base + jj] = x[i];
+      }
+      __syncthreads();
+#pragma unroll 1
+      for (int L = 1; L < 4; ++L) {  // block sub-diagonal L: (I, J) = (J + L, J)
+        const int nblk = 4 - L;
+        for (int idx = tid; idx < nblk * 256; idx += kThreads) {
+          const int J = idx >> 8, i = (idx >> 4) & 15, j = idx & 15, I = J + L;
+          float acc = 0.f;
+          for (int m = J * 16; m < I * 16; ++m)
+            acc = fmaf(A32[(I * 16 + i) * 64 + m], T32[m * 64 + J * 16 + j], acc);
+          M32[J * 256 + i * 16 + j] = acc;
+        }
+        __syncthreads();
+        for (int idx = tid; idx < nblk * 256; idx += kThreads) {
+          const int J = idx >> 8, i = (idx >> 4) & 15, j = idx & 15, I = J + L;
+          float acc = 0.f;
+#pragma unroll
+          for (int m = 0; m < 16; ++m)
+            acc = fmaf(T32[(I * 16 + i) * 64 + I * 16 + m], M32[J * 256 + m * 16 + j], acc);
+          T32[(I * 16 + i) * 64 + J * 16 + j] = -acc;
+        }
+        __syncthreads();
+      }
+      for (int idx = tid; idx < 64 * 8; idx += kThreads) {
+        const int i = idx >> 3, j0 = (idx & 7) * 8;
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int j = j0 + e;
+          x[e] = j <= i ? T32[i * 64 + j] * s_beta[j] : 0.f;
+        }
+        const uint32_t o = off_kmaj(i, j0, 64);
+        st8_split(smem + SM_Y + Y_TB_HI + o, smem + SM_Y + Y_TB_LO + o, x);
+      }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+
+    // ---- P7 (pass B): Kbar = K e^Gam (single), Qhat = Q e^Gam, Khat = K e^(Gl - Gam)
+#pragma unroll
+    for (int g4 = 0; g4 < 4; ++g4) {
+      const int cg = cg0 + g4;
+      float kx[8], qx[8], kb[8], qh[8], kh[8];
+      ld8(smem + SM_IN_K + cg * 1024 + t * 16, kx);
+      ld8(smem + SM_IN_Q + cg * 1024 + t * 16, qx);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int c = cg * 8 + e;
+        const float kv = valid ? kx[e] : 0.f, qv = valid ? qx[e] : 0.f;
+        const float eg = er[g4 * 8 + e] * s_erho[c];
+        kb[e] = kv * eg;
+        qh[e] = qv * eg;
+        kh[e] = kv * ec[g4 * 8 + e] * s_ecrho[c];
+      }
+      st8(smem + SM_X + X_KBAR + cg * 1024 + t * 16, kb);  // MN-major A (M = channel)
+      st8_split(smem + SM_X + X_QH_HI + off_kmaj(t, cg * 8, 128),
+                smem + SM_X + X_QH_LO + off_kmaj(t, cg * 8, 128), qh);  // K-major B
+      st8_split(smem + SM_X + X_KH_HI + cg * 1024 + t * 16,
+                smem + SM_X + X_KH_LO + cg * 1024 + t * 16, kh);  // MN-major B (N = channel)
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+
+    // ---- P8: W^T = Kbar^T TB^T, U~^T = V^T TB^T
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t tbh = sbase + SM_Y + Y_TB_HI, tbl = sbase + SM_Y + Y_TB_LO;
+#pragma unroll
+      for (int kk = 0; kk < C / 16; ++kk)
+        mma_ss(tb + TM_ACC2, smem_desc(sbase + SM_X + X_KBAR + kk * 256, 128, 1024),
+               smem_desc(tbh + kk * 256, 128, 1024), idesc_mnk, kk > 0);
+#pragma unroll
+      for (int pr = 0; pr < 2; ++pr)
+#pragma unroll
+        for (int kk = 0; kk < C / 16; ++kk)
+          mma_ss(tb + TM_ACC3, smem_desc(sbase + SM_IN_V + kk * 256, 128, 1024),
+                 smem_desc((pr ? tbl : tbh) + kk * 256, 128, 1024), idesc_mnk,
+                 (pr | kk) != 0);
+      mma_commit(wt.mma_bar);
+    }
+    if (wt.wait_mma()) break;
+
+    // ---- P9: prefetch chunk ci+1; W^T to shared memory as an MN-major B (N = token)
+    if (tid == 0 && ci + 1 < nchunks) issue_tma(ci + 1);
+    {
+      const int c = row;  // W^T lane = key channel
+#pragma unroll
+      for (int h16 = 0; h16 < 2; ++h16) {
+        float w[16];
+        tmem_ld16(tb + lane_base + TM_ACC2 + hw * 32 + h16 * 16, w);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e8 = 0; e8 < 2; ++e8) {
+          const int tt = hw * 32 + h16 * 16 + e8 * 8;
+          float x[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = w[e8 * 8 + e];
+          st8(smem + SM_X + X_WT + off_mnmaj(tt, c, 128), x);
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- P10: U^T = U~^T - S^T W^T (S split); O^T = S^T Qhat^T (both split)
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t wtb = sbase + SM_X + X_WT;
+#pragma unroll
+      for (int pr = 0; pr < 2; ++pr)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ts(tb + TM_ACC3, tb + (pr ? TM_SLO : TM_SHI) + kk * 8,
+                 smem_desc(wtb + kk * 256, 128, 2048), idesc_su, 1);
+      const uint32_t qh = sbase + SM_X + X_QH_HI, ql = sbase + SM_X + X_QH_LO;
+      const uint32_t as[3] = {TM_SHI, TM_SHI, TM_SLO};
+      const uint32_t bs[3] = {qh, ql, qh};
+#pragma unroll
+      for (int pr = 0; pr < 3; ++pr)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ts(tb + TM_ACC2, tb + as[pr] + kk * 8, smem_desc(bs[pr] + kk * 256, 128, 2048),
+                 idesc_sq, (pr | kk) != 0);
+      mma_commit(wt.mma_bar);
+    }
+    if (wt.wait_mma()) break;
+
+    // ---- P11: U^T split into TMEM (A operand); S^T <- S^T diag(e^Gam_last)
+    {
+#pragma unroll
+      for (int h16 = 0; h16 < 2; ++h16) {
+        float u[16];
+        tmem_ld16(tb + lane_base + TM_ACC3 + hw * 32 + h16 * 16, u);
+        tmem_wait_ld();
+        uint32_t hi[8], lo[8];
+        pack_split16(u, hi, lo);
+        tmem_st8(tb + lane_base + TM_UHI + hw * 16 + h16 * 8, hi);
+        tmem_st8(tb + lane_base + TM_ULO + hw * 16 + h16 * 8, lo);
+      }
+#pragma unroll 1
+      for (int c0 = hw * 64; c0 < hw * 64 + 64; c0 += 16) {
+        float s[16];
+        tmem_ld16(tb + lane_base + TM_S + c0, s);
+        tmem_wait_ld();
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(s[e] * s_gamc[c0 + e]);
+        tmem_st16(tb + lane_base + TM_S + c0, w);
+      }
+      tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- P12: O^T += U^T Aqk^T; S^T += U^T Khat (all split)
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t ah = sbase + SM_Y + Y_AQK_HI, al = sbase + SM_Y + Y_AQK_LO;
+      const uint32_t kh = sbase + SM_X + X_KH_HI, kl = sbase + SM_X + X_KH_LO;
+      const uint32_t ua[3] = {TM_UHI, TM_UHI, TM_ULO};
+      const uint32_t bq[3] = {ah, al, ah}, bk[3] = {kh, kl, kh};
+#pragma unroll
+      for (int pr = 0; pr < 3; ++pr)
+#pragma unroll
+        for (int kk = 0; kk < C / 16; ++kk)
+          mma_ts(tb + TM_ACC2, tb + ua[pr] + kk * 8, smem_desc(bq[pr] + kk * 256, 128, 1024),
+                 idesc_sq, 1);
+#pragma unroll
+      for (int pr = 0; pr < 3; ++pr)
+#pragma unroll
+        for (int kk = 0; kk < C / 16; ++kk)
+          mma_ts(tb + TM_S, tb + ua[pr] + kk * 8, smem_desc(bk[pr] + kk * 256, 128, 1024),
+                 idesc_s, 1);
+      mma_commit(wt.mma_bar);
+    }
+    if (wt.wait_mma()) break;
+
+    // ---- P13: outputs; refresh the bf16 copies of S^T
+    {
+      const int j = row;
+#pragma unroll
+      for (int h16 = 0; h16 < 2; ++h16) {
+        float o[16];
+        tmem_ld16(tb + lane_base + TM_ACC2 + hw * 32 + h16 * 16, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int tt = hw * 32 + h16 * 16 + e;
+          if (tt < nv) {
+            const int64_t oi = ((t0 + cs + tt) * p.H + h) * D + j;
+            if (p.out_bf16)
+              static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(p.scale * o[e]);
+            else
+              static_cast<float*>(p.out)[oi] = p.scale * o[e];
+          }
+        }
+      }
+#pragma unroll 1
+      for (int c0 = hw * 64; c0 < hw * 64 + 64; c0 += 16) {
+        float s[16];
+        tmem_ld16(tb + lane_base + TM_S + c0, s);
+        tmem_wait_ld();
+        uint32_t hi[8], lo[8];
+        pack_split16(s, hi, lo);
+        tmem_st8(tb + lane_base + TM_SHI + c0 / 2, hi);
+        tmem_st8(tb + lane_base + TM_SLO + c0 / 2, lo);
+      }
+      tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
+
+  if (range_err) latch_status(p.status, KDA_ERR_DECAY_RANGE);
+  const bool aborted = *(volatile uint32_t*)s_flag != 0;
+  if (!aborted && p.hT) {
+    const int j = row;
+    float* hTp = p.hT + (((int64_t)n * p.H + h) * D) * D;
+    tc_fence_after();
+#pragma unroll 1
+    for (int c0 = hw * 64; c0 < hw * 64 + 64; c0 += 16) {
+      float s[16];
+      tmem_ld16(tb + lane_base + TM_S + c0, s);
+      tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) hTp[(int64_t)(c0 + e) * D + j] = s[e];
+    }
+  }
+  if (aborted && tid == 0) {
+    // drain what may still be in flight before the memory goes away (bounded)
+    for (uint32_t ph = wt.tma_waited; ph < tma_issued; ++ph)
+      mbar_wait(wt.tma_bar, ph & 1u, 20000000ll);
+    mbar_wait(wt.mma_bar, wt.mma_phase ^ 1u, 20000000ll);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tb, TM_COLS);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// Tile map over one activation tensor [tokens, H, D] (bf16): box = 64 tokens x
+// 16 groups of 8 channels, written to shared memory as [group][token][8].
+bool make_map(CUtensorMap* m, const void* base, int64_t tokens, int H) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {8, (cuuint64_t)tokens, (cuuint64_t)H * (D / 8)};
+  cuuint64_t strides[2] = {(cuuint64_t)H * D * 2, 16};
+  cuuint32_t box[3] = {8, C, D / 8};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_bf16(const FwdArgs& a) {
+  const int64_t items = (int64_t)a.N * a.H;
+  if (items == 0) return cudaSuccess;
+  const int64_t tokens = a.cu ? a.T : (int64_t)a.N * a.T;
+  // A map needs a non-empty tensor.  With no tokens every chain is empty and no
+  // tile is loaded; map a valid state pointer instead (or skip when none).
+  const void* dummy = a.h0 ? (const void*)a.h0 : (const void*)a.hT;
+  if (tokens == 0 && !dummy) return cudaSuccess;
+  auto pick = [&](const void* x) { return tokens > 0 ? x : dummy; };
+  const int64_t map_tokens = tokens > 0 ? tokens : 1;
+  CUtensorMap mq, mk, mg, mv;
+  if (!make_map(&mq, pick(a.q), map_tokens, a.H) || !make_map(&mk, pick(a.k), map_tokens, a.H) ||
+      !make_map(&mg, pick(a.g), map_tokens, a.H) || !make_map(&mv, pick(a.v), map_tokens, a.H))
+    return cudaErrorInvalidValue;
+  Bf16Params p;
+  p.beta = static_cast<const __nv_bfloat16*>(a.beta);
+  p.seqs = SeqView{a.cu, a.T};
+  p.order = a.order;
+  p.h0 = a.h0;
+  p.out = a.out;
+  p.hT = a.hT;
+  p.H = a.H;
+  p.scale = a.scale;
+  p.out_bf16 = a.out_dtype == KDA_BF16;
+  p.status = a.status;
+  cudaError_t e = cudaFuncSetAttribute(kda_prefill_bf16_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  kda_prefill_bf16_kernel<<<(unsigned)items, kThreads, SMEM_BYTES, a.stream>>>(mq, mk, mg, mv, p);
+  return cudaGetLastError();
+}
+
 }  // namespace kda
