@@ -50,7 +50,8 @@ constexpr uint32_t SM_IN_G = 32768;
 constexpr uint32_t SM_IN_V = 49152;
 constexpr uint32_t SM_X = 65536;         // 96 KB, reused across phases
 constexpr uint32_t X_R_HI = 0, X_R_LO = 32768, X_CK_HI = 65536, X_CK_LO = 81920;
-constexpr uint32_t X_A32 = 0, X_T32 = 16384, X_M32 = 32768;   // forward substitution
+constexpr uint32_t X_A32 = 0, X_T32 = 16384, X_M32 = 33792;   // forward substitution
+constexpr int TLD = 66;  // padded row stride of T (float): 8-byte rows, few bank conflicts
 constexpr uint32_t X_KBAR = 0, X_QH_HI = 16384, X_QH_LO = 32768, X_KH_HI = 49152,
                    X_KH_LO = 65536, X_WT = 0;
 constexpr uint32_t SM_Y = 163840;        // 32 KB
@@ -85,50 +86,56 @@ __device__ __forceinline__ uint32_t off_mnmaj(int r, int k, int kdim) {
   return (r >> 3) * (kdim >> 3) * 128 + (k >> 3) * 128 + (k & 7) * 16 + (r & 7) * 2;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
-         ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
-}
-// x = hi + lo with hi = bf16(x), lo = x - hi (stored rounded to bf16)
-__device__ __forceinline__ void split2(float x, float& hi, float& lo) {
-  hi = __bfloat162float(__float2bfloat16_rn(x));
-  lo = x - hi;
-}
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// 2^x on the special-function unit (relative error about 2^-22; tiny results
+// flush to zero, which only drops terms far below the operands they join)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// hi/lo split of two values, each part packed as bf16x2 (first value in the low half)
+__device__ __forceinline__ void split_pack2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
 // 8 bf16 from a 16-byte shared-memory vector
 __device__ __forceinline__ void ld8(const unsigned char* p, float (&x)[8]) {
   const uint4 u = *reinterpret_cast<const uint4*>(p);
   x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x); x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
   x[4] = bf16_lo(u.z); x[5] = bf16_hi(u.z); x[6] = bf16_lo(u.w); x[7] = bf16_hi(u.w);
 }
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
 __device__ __forceinline__ void st8(unsigned char* p, const float (&x)[8]) {
   uint4 u;
-  u.x = pack_bf16(x[0], x[1]); u.y = pack_bf16(x[2], x[3]);
-  u.z = pack_bf16(x[4], x[5]); u.w = pack_bf16(x[6], x[7]);
+  u.x = pack2(x[0], x[1]); u.y = pack2(x[2], x[3]);
+  u.z = pack2(x[4], x[5]); u.w = pack2(x[6], x[7]);
   *reinterpret_cast<uint4*>(p) = u;
 }
 // store hi and lo parts of 8 values
 __device__ __forceinline__ void st8_split(unsigned char* phi, unsigned char* plo,
                                           const float (&x)[8]) {
-  float h[8], l[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) split2(x[i], h[i], l[i]);
-  st8(phi, h);
-  st8(plo, l);
+  uint4 h, l;
+  split_pack2(x[0], x[1], h.x, l.x);
+  split_pack2(x[2], x[3], h.y, l.y);
+  split_pack2(x[4], x[5], h.z, l.z);
+  split_pack2(x[6], x[7], h.w, l.w);
+  *reinterpret_cast<uint4*>(phi) = h;
+  *reinterpret_cast<uint4*>(plo) = l;
 }
 // hi and lo parts of 16 values, packed two per 32-bit word
 __device__ __forceinline__ void pack_split16(const float (&x)[16], uint32_t (&hi)[8],
                                              uint32_t (&lo)[8]) {
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    float h0, l0, h1, l1;
-    split2(x[2 * e], h0, l0);
-    split2(x[2 * e + 1], h1, l1);
-    hi[e] = pack_bf16(h0, h1);
-    lo[e] = pack_bf16(l0, l1);
-  }
+  for (int e = 0; e < 8; ++e) split_pack2(x[2 * e], x[2 * e + 1], hi[e], lo[e]);
 }
 
 struct Bf16Params {
@@ -250,6 +257,13 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     tma_load_3d(smem + SM_IN_V, &tm_v, 0, y, z, wt.tma_bar);
   };
   if (tid == 0 && nchunks > 0) issue_tma(0);
+  // beta of the chunk in flight, loaded one chunk ahead (its latency overlaps the
+  // current chunk); tokens past the sequence end read as 0
+  auto load_beta = [&](int chunk) -> float {
+    const int64_t tt = (int64_t)chunk * C + tid;
+    return (tid < C && tt < len) ? __bfloat162float(p.beta[(t0 + tt) * p.H + h]) : 0.f;
+  };
+  float beta_next = nchunks > 0 ? load_beta(0) : 0.f;
 
   // start state S^T (lane = value channel j, columns = key channels) from h0
   {
@@ -291,10 +305,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int rho_t = nv - 1 < 31 ? nv - 1 : 31;
 
     // ---- P1: beta, wait for the tiles, cumulative log-decay on the tensor core
-    if (tid < C) {
-      const float b = tid < nv ? __bfloat162float(p.beta[(t0 + cs + tid) * p.H + h]) : 0.f;
-      s_beta[tid] = b;
-    }
+    if (tid < C) s_beta[tid] = beta_next;
     if (wt.wait_tma()) break;
     if (tid == 0) {
       tc_fence_after();
@@ -332,9 +343,9 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     __syncthreads();
     if (tid < D) {
       const float r = s_rho[tid], gl = s_gl[tid];
-      s_erho[tid] = exp2f(r * kLog2e);
-      s_ecrho[tid] = exp2f((gl - r) * kLog2e);
-      s_gamc[tid] = exp2f(gl * kLog2e);
+      s_erho[tid] = ex2(r * kLog2e);
+      s_ecrho[tid] = ex2((gl - r) * kLog2e);
+      s_gamc[tid] = ex2(gl * kLog2e);
     }
     float er[32], ec[32];
 #pragma unroll
@@ -349,8 +360,8 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         float d = gam[g4 * 8 + e] - s_rho[cg * 8 + e];
         if (valid && fabsf(d) > kMaxExp) range_err = true;
         d = fminf(fmaxf(d, -kMaxExp), kMaxExp);
-        er[g4 * 8 + e] = exp2f(d * kLog2e);
-        ec[g4 * 8 + e] = exp2f(-d * kLog2e);
+        er[g4 * 8 + e] = ex2(d * kLog2e);
+        ec[g4 * 8 + e] = ex2(-d * kLog2e);
         const float kv = valid ? kx[e] : 0.f, qv = valid ? qx[e] : 0.f;
         rk[e] = kv * er[g4 * 8 + e];
         rq[e] = qv * er[g4 * 8 + e];
@@ -398,11 +409,11 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (row < 64) {
         const int i = row;
         const float bi = s_beta[i];
-        float* A32 = reinterpret_cast<float*>(smem + SM_X + X_A32);
+        float* AT = reinterpret_cast<float*>(smem + SM_X + X_A32);  // AT[j][i] = A[i][j]
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int j = hw * 32 + e;
-          A32[i * 64 + j] = j < i ? bi * a[e] : 0.f;
+          AT[j * 64 + i] = j < i ? bi * a[e] : 0.f;
         }
       } else {
         const int i = row - 64;
@@ -424,51 +435,71 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 
     // ---- P6: T = (I + A)^-1 by blocks of 16, then TB = T diag(beta) split
     {
-      const float* A32 = reinterpret_cast<const float*>(smem + SM_X + X_A32);
+      const float* AT = reinterpret_cast<const float*>(smem + SM_X + X_A32);  // AT[j][i]
       float* T32 = reinterpret_cast<float*>(smem + SM_X + X_T32);
       float* M32 = reinterpret_cast<float*>(smem + SM_X + X_M32);
-      if (tid < 64) {  // diagonal blocks: thread owns column jj of block I
-        const int I = tid >> 4, jj = tid & 15, base = I * 16;
-        float x[16];
+      if (warp < 4 && lane < 16) {
+        // diagonal block I = warp, column jj = lane: right-looking substitution, so
+        // each of the 16 steps is a set of independent updates
+        const int base = warp * 16, jj = lane;
+        float acc[16], x[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float acc = 0.f;
+        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
 #pragma unroll
-          for (int m = 0; m < i; ++m) acc = fmaf(A32[(base + i) * 64 + base + m], x[m], acc);
-          x[i] = i < jj ? 0.f : (i == jj ? 1.f : -acc);
+        for (int m = 0; m < 16; ++m) {
+          x[m] = m < jj ? 0.f : (m == jj ? 1.f : acc[m]);
+#pragma unroll
+          for (int i = m + 1; i < 16; ++i)
+            acc[i] = fmaf(-AT[(base + m) * 64 + base + i], x[m], acc[i]);
         }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) T32[(base + i) * 64 + base + jj] = x[i];
+        for (int i = 0; i < 16; ++i) T32[(base + i) * TLD + base + jj] = x[i];
       }
       __syncthreads();
 #pragma unroll 1
       for (int L = 1; L < 4; ++L) {  // block sub-diagonal L: (I, J) = (J + L, J)
-        const int nblk = 4 - L;
-        for (int idx = tid; idx < nblk * 256; idx += kThreads) {
-          const int J = idx >> 8, i = (idx >> 4) & 15, j = idx & 15, I = J + L;
-          float acc = 0.f;
-          for (int m = J * 16; m < I * 16; ++m)
-            acc = fmaf(A32[(I * 16 + i) * 64 + m], T32[m * 64 + J * 16 + j], acc);
-          M32[J * 256 + i * 16 + j] = acc;
+        // 64 threads per block, each a 2 x 2 tile of the 16 x 16 block
+        const int J = tid >> 6, ti = (tid >> 3) & 7, tj = tid & 7, I = J + L;
+        const bool act = J < 4 - L;
+        if (act) {  // M = A[I, J..I-1] T[J..I-1, J]
+          float m00 = 0.f, m01 = 0.f, m10 = 0.f, m11 = 0.f;
+#pragma unroll 4
+          for (int m = J * 16; m < I * 16; ++m) {
+            const float2 a = *reinterpret_cast<const float2*>(AT + m * 64 + I * 16 + 2 * ti);
+            const float2 b = *reinterpret_cast<const float2*>(T32 + m * TLD + J * 16 + 2 * tj);
+            m00 = fmaf(a.x, b.x, m00); m01 = fmaf(a.x, b.y, m01);
+            m10 = fmaf(a.y, b.x, m10); m11 = fmaf(a.y, b.y, m11);
+          }
+          *reinterpret_cast<float2*>(M32 + J * 256 + (2 * ti) * 16 + 2 * tj) = make_float2(m00, m01);
+          *reinterpret_cast<float2*>(M32 + J * 256 + (2 * ti + 1) * 16 + 2 * tj) =
+              make_float2(m10, m11);
         }
         __syncthreads();
-        for (int idx = tid; idx < nblk * 256; idx += kThreads) {
-          const int J = idx >> 8, i = (idx >> 4) & 15, j = idx & 15, I = J + L;
-          float acc = 0.f;
+        if (act) {  // T[I, J] = -T[I, I] M
+          float t00 = 0.f, t01 = 0.f, t10 = 0.f, t11 = 0.f;
+          const float* r0 = T32 + (I * 16 + 2 * ti) * TLD + I * 16;
+          const float* r1 = r0 + TLD;
 #pragma unroll
-          for (int m = 0; m < 16; ++m)
-            acc = fmaf(T32[(I * 16 + i) * 64 + I * 16 + m], M32[J * 256 + m * 16 + j], acc);
-          T32[(I * 16 + i) * 64 + J * 16 + j] = -acc;
+          for (int m = 0; m < 16; ++m) {
+            const float2 b = *reinterpret_cast<const float2*>(M32 + J * 256 + m * 16 + 2 * tj);
+            const float a0 = r0[m], a1 = r1[m];
+            t00 = fmaf(a0, b.x, t00); t01 = fmaf(a0, b.y, t01);
+            t10 = fmaf(a1, b.x, t10); t11 = fmaf(a1, b.y, t11);
+          }
+          *reinterpret_cast<float2*>(T32 + (I * 16 + 2 * ti) * TLD + J * 16 + 2 * tj) =
+              make_float2(-t00, -t01);
+          *reinterpret_cast<float2*>(T32 + (I * 16 + 2 * ti + 1) * TLD + J * 16 + 2 * tj) =
+              make_float2(-t10, -t11);
         }
         __syncthreads();
       }
       for (int idx = tid; idx < 64 * 8; idx += kThreads) {
-        const int i = idx >> 3, j0 = (idx & 7) * 8;
+        const int j0 = (idx >> 6) * 8, i = idx & 63;  // lanes walk rows: distinct banks
         float x[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int j = j0 + e;
-          x[e] = j <= i ? T32[i * 64 + j] * s_beta[j] : 0.f;
+          x[e] = j <= i ? T32[i * TLD + j] * s_beta[j] : 0.f;
         }
         const uint32_t o = off_kmaj(i, j0, 64);
         st8_split(smem + SM_Y + Y_TB_HI + o, smem + SM_Y + Y_TB_LO + o, x);
@@ -523,22 +554,23 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 
     // ---- P9: prefetch chunk ci+1; W^T to shared memory as an MN-major B (N = token)
     if (tid == 0 && ci + 1 < nchunks) issue_tma(ci + 1);
+    if (ci + 1 < nchunks) beta_next = load_beta(ci + 1);
     {
       const int c = row;  // W^T lane = key channel
+      float w[2][16];
+      tmem_ld16(tb + lane_base + TM_ACC2 + hw * 32, w[0]);
+      tmem_ld16(tb + lane_base + TM_ACC2 + hw * 32 + 16, w[1]);
+      tmem_wait_ld();
 #pragma unroll
-      for (int h16 = 0; h16 < 2; ++h16) {
-        float w[16];
-        tmem_ld16(tb + lane_base + TM_ACC2 + hw * 32 + h16 * 16, w);
-        tmem_wait_ld();
+      for (int h16 = 0; h16 < 2; ++h16)
 #pragma unroll
         for (int e8 = 0; e8 < 2; ++e8) {
           const int tt = hw * 32 + h16 * 16 + e8 * 8;
           float x[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = w[e8 * 8 + e];
+          for (int e = 0; e < 8; ++e) x[e] = w[h16][e8 * 8 + e];
           st8(smem + SM_X + X_WT + off_mnmaj(tt, c, 128), x);
         }
-      }
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -569,24 +601,25 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 
     // ---- P11: U^T split into TMEM (A operand); S^T <- S^T diag(e^Gam_last)
     {
+      float u[2][16], sv[4][16];
+      tmem_ld16(tb + lane_base + TM_ACC3 + hw * 32, u[0]);
+      tmem_ld16(tb + lane_base + TM_ACC3 + hw * 32 + 16, u[1]);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(tb + lane_base + TM_S + hw * 64 + q4 * 16, sv[q4]);
+      tmem_wait_ld();
 #pragma unroll
       for (int h16 = 0; h16 < 2; ++h16) {
-        float u[16];
-        tmem_ld16(tb + lane_base + TM_ACC3 + hw * 32 + h16 * 16, u);
-        tmem_wait_ld();
         uint32_t hi[8], lo[8];
-        pack_split16(u, hi, lo);
+        pack_split16(u[h16], hi, lo);
         tmem_st8(tb + lane_base + TM_UHI + hw * 16 + h16 * 8, hi);
         tmem_st8(tb + lane_base + TM_ULO + hw * 16 + h16 * 8, lo);
       }
-#pragma unroll 1
-      for (int c0 = hw * 64; c0 < hw * 64 + 64; c0 += 16) {
-        float s[16];
-        tmem_ld16(tb + lane_base + TM_S + c0, s);
-        tmem_wait_ld();
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int c0 = hw * 64 + q4 * 16;
         uint32_t w[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(s[e] * s_gamc[c0 + e]);
+        for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(sv[q4][e] * s_gamc[c0 + e]);
         tmem_st16(tb + lane_base + TM_S + c0, w);
       }
       tmem_wait_st();
@@ -620,33 +653,36 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     // ---- P13: outputs; refresh the bf16 copies of S^T
     {
       const int j = row;
+      float o[2][16], sv[4][16];
+      tmem_ld16(tb + lane_base + TM_ACC2 + hw * 32, o[0]);
+      tmem_ld16(tb + lane_base + TM_ACC2 + hw * 32 + 16, o[1]);
 #pragma unroll
-      for (int h16 = 0; h16 < 2; ++h16) {
-        float o[16];
-        tmem_ld16(tb + lane_base + TM_ACC2 + hw * 32 + h16 * 16, o);
-        tmem_wait_ld();
+      for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(tb + lane_base + TM_S + hw * 64 + q4 * 16, sv[q4]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int c0 = hw * 64 + q4 * 16;
+        uint32_t hi[8], lo[8];
+        pack_split16(sv[q4], hi, lo);
+        tmem_st8(tb + lane_base + TM_SHI + c0 / 2, hi);
+        tmem_st8(tb + lane_base + TM_SLO + c0 / 2, lo);
+      }
+      float* outf = static_cast<float*>(p.out);
+      __nv_bfloat16* outb = static_cast<__nv_bfloat16*>(p.out);
+      const int64_t obase = ((t0 + cs) * p.H + h) * D + j;
+      const int64_t ostride = (int64_t)p.H * D;
+#pragma unroll
+      for (int h16 = 0; h16 < 2; ++h16)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int tt = hw * 32 + h16 * 16 + e;
           if (tt < nv) {
-            const int64_t oi = ((t0 + cs + tt) * p.H + h) * D + j;
             if (p.out_bf16)
-              static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(p.scale * o[e]);
+              outb[obase + tt * ostride] = __float2bfloat16_rn(p.scale * o[h16][e]);
             else
-              static_cast<float*>(p.out)[oi] = p.scale * o[e];
+              outf[obase + tt * ostride] = p.scale * o[h16][e];
           }
         }
-      }
-#pragma unroll 1
-      for (int c0 = hw * 64; c0 < hw * 64 + 64; c0 += 16) {
-        float s[16];
-        tmem_ld16(tb + lane_base + TM_S + c0, s);
-        tmem_wait_ld();
-        uint32_t hi[8], lo[8];
-        pack_split16(s, hi, lo);
-        tmem_st8(tb + lane_base + TM_SHI + c0 / 2, hi);
-        tmem_st8(tb + lane_base + TM_SLO + c0 / 2, lo);
-      }
       tmem_wait_st();
     }
     tc_fence_before();
