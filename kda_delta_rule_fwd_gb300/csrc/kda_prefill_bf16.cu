@@ -21,7 +21,7 @@
 // accuracy: a single bf16 rounding of an operand on the dominant path
 // already exceeds a 1e-2 max-error budget on heavy-tailed outputs.
 //
-// One CTA (256 threads) owns one (sequence, head) chain and walks its chunks
+// One CTA (512 threads) owns one (sequence, head) chain and walks its chunks
 // in order; the inputs of chunk n+1 are fetched by TMA while chunk n's state
 // update runs.  Each mbarrier wait is bounded: on expiry the CTA latches
 // KDA_ERR_DEVICE_TIMEOUT, drains its in-flight copies, frees TMEM and exits.
@@ -39,7 +39,12 @@ using namespace sm100;
 
 constexpr int C = 64;            // chunk length (tokens)
 constexpr int D = 128;           // head dim (dk == dv)
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
+constexpr int NCOL = kThreads / 128;  // threads sharing one accumulator row (column slices)
+constexpr int TCOL = 64 / NCOL;       // columns of a 64-wide accumulator per thread
+constexpr int SCOL = 128 / NCOL;      // state columns per thread
+constexpr int GPT = 16 / (2 * NCOL);  // 8-channel groups per thread in the elementwise passes
+static_assert(TCOL == 16 && SCOL % 16 == 0 && GPT >= 1, "thread mapping");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kMaxExp = 80.f;  // |Gam - rho| beyond this overflows the factorisation
 
@@ -190,7 +195,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qd = warp & 3;          // TMEM lane quarter of this warp
-  const int hw = warp >> 2;         // which half of the columns this warp handles
+  const int cq = warp >> 2;         // which column slice of the accumulators this warp handles
   const int row = qd * 32 + lane;   // TMEM lane (accumulator row) of this thread
 
   float* s_rho = reinterpret_cast<float*>(smem + SM_MISC + MISC_RHO);
@@ -270,7 +275,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int j = row;
     const float* h0p = p.h0 ? p.h0 + (((int64_t)n * p.H + h) * D) * D : nullptr;
 #pragma unroll 1
-    for (int c0 = hw * 64; c0 < hw * 64 + 64; c0 += 16) {
+    for (int c0 = cq * SCOL; c0 < cq * SCOL + SCOL; c0 += 16) {
       float x[16];
       uint32_t u[16];
 #pragma unroll
@@ -320,25 +325,24 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 
     // ---- P3 (pass A): decay factors and the decayed key/query operands
     const int t = row & 63;
-    const int cg0 = (2 * (row >> 6) + hw) * 4;  // first 8-channel group of this thread
+    const int cg0 = (NCOL * (row >> 6) + cq) * GPT;  // first 8-channel group of this thread
     const bool valid = t < nv;
-    float gam[32];
+    float gam[GPT * 8];
     {
-      float a[16];
-      tmem_ld16(tb + lane_base + TM_ACC1 + cg0 * 8, a);
+      float a[GPT * 8 / 16][16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) gam[e] = a[e];
-      tmem_ld16(tb + lane_base + TM_ACC1 + cg0 * 8 + 16, a);
-#pragma unroll
-      for (int e = 0; e < 16; ++e) gam[16 + e] = a[e];
+      for (int q = 0; q < GPT * 8 / 16; ++q)
+        tmem_ld16(tb + lane_base + TM_ACC1 + cg0 * 8 + q * 16, a[q]);
       tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < GPT * 8; ++e) gam[e] = a[e >> 4][e & 15];
     }
     if (t == rho_t)
 #pragma unroll
-      for (int e = 0; e < 32; ++e) s_rho[cg0 * 8 + e] = gam[e];
+      for (int e = 0; e < GPT * 8; ++e) s_rho[cg0 * 8 + e] = gam[e];
     if (t == nv - 1)
 #pragma unroll
-      for (int e = 0; e < 32; ++e) s_gl[cg0 * 8 + e] = gam[e];
+      for (int e = 0; e < GPT * 8; ++e) s_gl[cg0 * 8 + e] = gam[e];
     tc_fence_before();
     __syncthreads();
     if (tid < D) {
@@ -347,9 +351,9 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       s_ecrho[tid] = ex2((gl - r) * kLog2e);
       s_gamc[tid] = ex2(gl * kLog2e);
     }
-    float er[32], ec[32];
+    float er[GPT * 8], ec[GPT * 8];
 #pragma unroll
-    for (int g4 = 0; g4 < 4; ++g4) {
+    for (int g4 = 0; g4 < GPT; ++g4) {
       const int cg = cg0 + g4;
       float kx[8], qx[8];
       ld8(smem + SM_IN_K + cg * 1024 + t * 16, kx);
@@ -395,37 +399,29 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 
     // ---- P5: A = strict_lower(beta Akk) (float32, for the substitution), Aqk split
     {
-      float a[32];
-      {
-        float x[16];
-        tmem_ld16(tb + lane_base + TM_ACC1 + hw * 32, x);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) a[e] = x[e];
-        tmem_ld16(tb + lane_base + TM_ACC1 + hw * 32 + 16, x);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) a[16 + e] = x[e];
-        tmem_wait_ld();
-      }
+      float a[TCOL];
+      tmem_ld16(tb + lane_base + TM_ACC1 + cq * TCOL, a);
+      tmem_wait_ld();
       if (row < 64) {
         const int i = row;
         const float bi = s_beta[i];
         float* AT = reinterpret_cast<float*>(smem + SM_X + X_A32);  // AT[j][i] = A[i][j]
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int j = hw * 32 + e;
+        for (int e = 0; e < TCOL; ++e) {
+          const int j = cq * TCOL + e;
           AT[j * 64 + i] = j < i ? bi * a[e] : 0.f;
         }
       } else {
         const int i = row - 64;
 #pragma unroll
-        for (int e8 = 0; e8 < 4; ++e8) {
+        for (int e8 = 0; e8 < TCOL / 8; ++e8) {
           float x[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const int j = hw * 32 + e8 * 8 + e;
+            const int j = cq * TCOL + e8 * 8 + e;
             x[e] = j <= i ? a[e8 * 8 + e] : 0.f;
           }
-          const uint32_t o = off_kmaj(i, hw * 32 + e8 * 8, 64);
+          const uint32_t o = off_kmaj(i, cq * TCOL + e8 * 8, 64);
           st8_split(smem + SM_Y + Y_AQK_HI + o, smem + SM_Y + Y_AQK_LO + o, x);
         }
       }
@@ -510,7 +506,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 
     // ---- P7 (pass B): Kbar = K e^Gam (single), Qhat = Q e^Gam, Khat = K e^(Gl - Gam)
 #pragma unroll
-    for (int g4 = 0; g4 < 4; ++g4) {
+    for (int g4 = 0; g4 < GPT; ++g4) {
       const int cg = cg0 + g4;
       float kx[8], qx[8], kb[8], qh[8], kh[8];
       ld8(smem + SM_IN_K + cg * 1024 + t * 16, kx);
@@ -557,20 +553,17 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (ci + 1 < nchunks) beta_next = load_beta(ci + 1);
     {
       const int c = row;  // W^T lane = key channel
-      float w[2][16];
-      tmem_ld16(tb + lane_base + TM_ACC2 + hw * 32, w[0]);
-      tmem_ld16(tb + lane_base + TM_ACC2 + hw * 32 + 16, w[1]);
+      float w[TCOL];
+      tmem_ld16(tb + lane_base + TM_ACC2 + cq * TCOL, w);
       tmem_wait_ld();
 #pragma unroll
-      for (int h16 = 0; h16 < 2; ++h16)
+      for (int e8 = 0; e8 < TCOL / 8; ++e8) {
+        const int tt = cq * TCOL + e8 * 8;
+        float x[8];
 #pragma unroll
-        for (int e8 = 0; e8 < 2; ++e8) {
-          const int tt = hw * 32 + h16 * 16 + e8 * 8;
-          float x[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = w[h16][e8 * 8 + e];
-          st8(smem + SM_X + X_WT + off_mnmaj(tt, c, 128), x);
-        }
+        for (int e = 0; e < 8; ++e) x[e] = w[e8 * 8 + e];
+        st8(smem + SM_X + X_WT + off_mnmaj(tt, c, 128), x);
+      }
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -601,22 +594,21 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 
     // ---- P11: U^T split into TMEM (A operand); S^T <- S^T diag(e^Gam_last)
     {
-      float u[2][16], sv[4][16];
-      tmem_ld16(tb + lane_base + TM_ACC3 + hw * 32, u[0]);
-      tmem_ld16(tb + lane_base + TM_ACC3 + hw * 32 + 16, u[1]);
+      float u[TCOL], sv[SCOL / 16][16];
+      tmem_ld16(tb + lane_base + TM_ACC3 + cq * TCOL, u);
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(tb + lane_base + TM_S + hw * 64 + q4 * 16, sv[q4]);
+      for (int q4 = 0; q4 < SCOL / 16; ++q4)
+        tmem_ld16(tb + lane_base + TM_S + cq * SCOL + q4 * 16, sv[q4]);
       tmem_wait_ld();
-#pragma unroll
-      for (int h16 = 0; h16 < 2; ++h16) {
+      {
         uint32_t hi[8], lo[8];
-        pack_split16(u[h16], hi, lo);
-        tmem_st8(tb + lane_base + TM_UHI + hw * 16 + h16 * 8, hi);
-        tmem_st8(tb + lane_base + TM_ULO + hw * 16 + h16 * 8, lo);
+        pack_split16(u, hi, lo);
+        tmem_st8(tb + lane_base + TM_UHI + cq * (TCOL / 2), hi);
+        tmem_st8(tb + lane_base + TM_ULO + cq * (TCOL / 2), lo);
       }
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int c0 = hw * 64 + q4 * 16;
+      for (int q4 = 0; q4 < SCOL / 16; ++q4) {
+        const int c0 = cq * SCOL + q4 * 16;
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(sv[q4][e] * s_gamc[c0 + e]);
@@ -653,15 +645,15 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     // ---- P13: outputs; refresh the bf16 copies of S^T
     {
       const int j = row;
-      float o[2][16], sv[4][16];
-      tmem_ld16(tb + lane_base + TM_ACC2 + hw * 32, o[0]);
-      tmem_ld16(tb + lane_base + TM_ACC2 + hw * 32 + 16, o[1]);
+      float o[TCOL], sv[SCOL / 16][16];
+      tmem_ld16(tb + lane_base + TM_ACC2 + cq * TCOL, o);
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(tb + lane_base + TM_S + hw * 64 + q4 * 16, sv[q4]);
+      for (int q4 = 0; q4 < SCOL / 16; ++q4)
+        tmem_ld16(tb + lane_base + TM_S + cq * SCOL + q4 * 16, sv[q4]);
       tmem_wait_ld();
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int c0 = hw * 64 + q4 * 16;
+      for (int q4 = 0; q4 < SCOL / 16; ++q4) {
+        const int c0 = cq * SCOL + q4 * 16;
         uint32_t hi[8], lo[8];
         pack_split16(sv[q4], hi, lo);
         tmem_st8(tb + lane_base + TM_SHI + c0 / 2, hi);
@@ -672,17 +664,15 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       const int64_t obase = ((t0 + cs) * p.H + h) * D + j;
       const int64_t ostride = (int64_t)p.H * D;
 #pragma unroll
-      for (int h16 = 0; h16 < 2; ++h16)
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int tt = hw * 32 + h16 * 16 + e;
-          if (tt < nv) {
-            if (p.out_bf16)
-              outb[obase + tt * ostride] = __float2bfloat16_rn(p.scale * o[h16][e]);
-            else
-              outf[obase + tt * ostride] = p.scale * o[h16][e];
-          }
+      for (int e = 0; e < TCOL; ++e) {
+        const int tt = cq * TCOL + e;
+        if (tt < nv) {
+          if (p.out_bf16)
+            outb[obase + tt * ostride] = __float2bfloat16_rn(p.scale * o[e]);
+          else
+            outf[obase + tt * ostride] = p.scale * o[e];
         }
+      }
       tmem_wait_st();
     }
     tc_fence_before();
@@ -696,7 +686,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     float* hTp = p.hT + (((int64_t)n * p.H + h) * D) * D;
     tc_fence_after();
 #pragma unroll 1
-    for (int c0 = hw * 64; c0 < hw * 64 + 64; c0 += 16) {
+    for (int c0 = cq * SCOL; c0 < cq * SCOL + SCOL; c0 += 16) {
       float s[16];
       tmem_ld16(tb + lane_base + TM_S + c0, s);
       tmem_wait_ld();
