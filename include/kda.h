@@ -70,8 +70,14 @@ typedef struct {
   float scale;          /* read-out scale, usually dk^-1/2 */
 } kda_shape;
 
-/* Bytes of workspace kda_fwd / kda_decode need for `s` (always >= 256: the first
- * 256 bytes hold the device status word).  Returns 0 if `s` is NULL. */
+/* Bytes of workspace that let kda_fwd / kda_decode use every path for `s`
+ * (always >= 256: the first 256 bytes hold the device status word).  For a
+ * fixed-length bf16 batch of a few very long sequences this includes the
+ * segment states of the long-chain split (chains of (sequence, head) cut into
+ * up to 16 segments joined through their affine state maps).  The minimum a
+ * call accepts is 256 bytes plus, for packed batches, 4 bytes per sequence
+ * rounded up to 64 sequences; with less than kda_workspace_size the split is
+ * skipped.  Returns 0 if `s` is NULL. */
 size_t kda_workspace_size(const kda_shape* s);
 
 /*
@@ -85,8 +91,9 @@ size_t kda_workspace_size(const kda_shape* s);
  *   h0       device float32 [N,H,dk,dv] start states, or NULL for zeros.
  *   out      device [B,T,H,dv] out_dtype.
  *   hT       device float32 [N,H,dk,dv] final states, or NULL.
- *   workspace   device, 256-byte aligned, >= kda_workspace_size(s) bytes; its
- *               contents on entry do not matter.
+ *   workspace   device, 256-byte aligned, kda_workspace_size(s) bytes (or at
+ *               least the minimum described there); contents on entry do not
+ *               matter.
  * When B*T == 0 the activation pointers may be NULL (hT is still written).
  * Chunks of 64 tokens start at each sequence start; the last chunk of a
  * sequence may be partial.  A zero-length sequence writes hT = h0 (or 0).

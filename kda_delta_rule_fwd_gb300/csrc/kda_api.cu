@@ -29,9 +29,13 @@ kda_status check_shape(const kda_shape* s, bool packed) {
   return KDA_OK;
 }
 
+// The minimum workspace: status header plus the packed-batch order list.  The
+// long-chain segment states are optional (the split is skipped without them).
 kda_status check_ws(const kda_shape* s, void* ws, size_t bytes) {
   if (!ws || !aligned(ws, 256)) return KDA_ERR_WORKSPACE;
-  if (bytes < kda_workspace_size(s)) return KDA_ERR_WORKSPACE;
+  size_t need = kWsHeader;
+  if (s->num_seqs > 0) need += ws_order_bytes(s->num_seqs);
+  if (bytes < need) return KDA_ERR_WORKSPACE;
   return KDA_OK;
 }
 
@@ -43,6 +47,10 @@ size_t kda_workspace_size(const kda_shape* s) {
   if (!s) return 0;
   size_t b = kWsHeader;
   if (s->num_seqs > 0) b += ws_order_bytes(s->num_seqs);
+  // fixed-length batches of a few very long chains also keep segment states
+  const bool bf16_d128 = s->in_dtype == KDA_BF16 && s->dk == 128 && s->dv == 128;
+  const int64_t chains = (int64_t)(s->B > 0 ? s->B : 0) * (s->H > 0 ? s->H : 0);
+  b += seg_bytes(seg_plan(false, bf16_d128, chains, s->T), chains, s->dk);
   return b;
 }
 
@@ -82,6 +90,13 @@ kda_status kda_fwd(const kda_shape* s, const void* q, const void* k, const void*
     int32_t* order = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + kWsHeader);
     if (launch_schedule(a, order) != cudaSuccess) return KDA_ERR_CUDA;
     a.order = order;
+  } else {
+    // long-chain split: segment states follow the header when the plan asks for them
+    const bool bf16_d128 = s->in_dtype == KDA_BF16 && s->dk == 128;
+    const SegPlan pl = seg_plan(false, bf16_d128, (int64_t)s->B * s->H, s->T);
+    const size_t need = kWsHeader + seg_bytes(pl, (int64_t)s->B * s->H, s->dk);
+    if (pl.nseg > 1 && workspace_bytes >= need)
+      a.seg_ws = reinterpret_cast<float*>(static_cast<char*>(workspace) + kWsHeader);
   }
   cudaError_t e;
   if (s->in_dtype == KDA_BF16 && s->dk == 128)

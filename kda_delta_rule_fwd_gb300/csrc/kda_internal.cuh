@@ -54,6 +54,40 @@ struct SeqView {
 constexpr size_t kWsHeader = 256;
 inline size_t ws_order_bytes(int64_t n) { return (size_t)((n + 63) / 64) * 64 * 4; }
 
+// Long-chain split for fixed-length bf16 batches with few (sequence, head)
+// chains: each chain is cut into nseg segments of seg_len tokens so that the
+// device has enough independent work (the segments are joined exactly through
+// their affine state transitions).  A pure function of the shape, so that the
+// workspace size can be computed without a device.
+struct SegPlan {
+  int nseg = 1;
+  int64_t seg_len = 0;
+};
+constexpr int kSegMaxChains = 64;       // split only when chains leave most SMs idle
+constexpr int64_t kSegMinChunks = 64;   // at least this many 64-token chunks per segment
+constexpr int kSegMaxSegs = 16;
+constexpr int kSegTargetChains = 512;
+inline SegPlan seg_plan(bool packed, bool bf16_d128, int64_t chains, int64_t T) {
+  SegPlan pl;
+  const int64_t chunks = (T + 63) / 64;
+  if (packed || !bf16_d128 || chains <= 0 || chains > kSegMaxChains ||
+      chunks < 4 * kSegMinChunks)
+    return pl;
+  int64_t ns = kSegTargetChains / chains;
+  if (ns > kSegMaxSegs) ns = kSegMaxSegs;
+  if (ns > chunks / kSegMinChunks) ns = chunks / kSegMinChunks;
+  if (ns < 2) return pl;
+  pl.seg_len = ((chunks + ns - 1) / ns) * 64;
+  pl.nseg = (int)((T + pl.seg_len - 1) / pl.seg_len);
+  if (pl.nseg < 2) pl = SegPlan{};
+  return pl;
+}
+// bytes of segment states: b and M for segments 0..nseg-2, start states for 0..nseg-1
+inline size_t seg_bytes(const SegPlan& pl, int64_t chains, int D) {
+  if (pl.nseg < 2) return 0;
+  return (size_t)chains * (size_t)(3 * pl.nseg - 2) * (size_t)D * D * sizeof(float);
+}
+
 // ---------------------------------------------------------------------------
 // launchers (each returns cudaSuccess or the launch error)
 // ---------------------------------------------------------------------------
@@ -69,6 +103,7 @@ struct FwdArgs {
   kda_dtype in_dtype, out_dtype;
   unsigned int* status;
   const int32_t* order;  // scheduler output: sequences longest first (packed), or nullptr
+  float* seg_ws;         // segment-state area of the workspace (long-chain split), or nullptr
   cudaStream_t stream;
 };
 

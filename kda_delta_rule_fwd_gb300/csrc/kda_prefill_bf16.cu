@@ -143,6 +143,17 @@ __device__ __forceinline__ void pack_split16(const float (&x)[16], uint32_t (&hi
   for (int e = 0; e < 8; ++e) split_pack2(x[2 * e], x[2 * e + 1], hi[e], lo[e]);
 }
 
+// Work item modes.  CHAIN: one CTA per (sequence, head).  The two SEG modes
+// split each chain of a fixed-length batch into nseg segments of seg_len
+// tokens (the associative affine form of the recurrence: a segment maps its
+// start state S to M S + b):
+//   SEG_TRANSITION: per (chain, segment < nseg-1) two CTAs: b = end state from
+//                   S = 0; M = end state from S = I with v = 0 (no outputs).
+//   SEG_OUTPUT:     per (chain, segment) one CTA from the segment's true start
+//                   state (computed by the scan kernel); writes o, and hT from
+//                   the last segment.
+enum ItemMode { MODE_CHAIN = 0, MODE_SEG_TRANSITION = 1, MODE_SEG_OUTPUT = 2 };
+
 struct Bf16Params {
   const __nv_bfloat16* beta;
   SeqView seqs;
@@ -154,6 +165,12 @@ struct Bf16Params {
   float scale;
   int out_bf16;
   unsigned int* status;
+  int mode;
+  int nseg;
+  int64_t seg_len;       // tokens per segment (multiple of the chunk length)
+  float* seg_b;          // [chains][nseg-1][D][D] zero-start end states
+  float* seg_m;          // [chains][nseg-1][D][D] transitions
+  const float* seg_s;    // [chains][nseg][D][D] segment start states (index 0 unused)
 };
 
 // The CTA's bounded waits.  Every thread waits on the barrier itself; a thread
@@ -214,10 +231,45 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     return;
 
   const int item = blockIdx.x;
-  const int n = p.order ? p.order[item / p.H] : item / p.H;
-  const int h = item % p.H;
+  int n, h;
   int64_t t0, len;
-  p.seqs.get(n, t0, len);
+  // start state (nullptr = zeros), identity start, end-state destination, flags
+  const float* s_in = nullptr;
+  float* s_out = nullptr;
+  bool ident = false, zero_v = false, want_o = true;
+  if (p.mode == MODE_CHAIN) {
+    n = p.order ? p.order[item / p.H] : item / p.H;
+    h = item % p.H;
+    p.seqs.get(n, t0, len);
+    s_in = p.h0 ? p.h0 + (((int64_t)n * p.H + h) * D) * D : nullptr;
+    s_out = p.hT ? p.hT + (((int64_t)n * p.H + h) * D) * D : nullptr;
+  } else {
+    int seg, chain;
+    if (p.mode == MODE_SEG_TRANSITION) {
+      const int kind = item & 1, rest = item >> 1;
+      seg = rest % (p.nseg - 1);
+      chain = rest / (p.nseg - 1);
+      ident = zero_v = kind == 1;
+      want_o = false;
+      s_out = (kind ? p.seg_m : p.seg_b) + ((int64_t)chain * (p.nseg - 1) + seg) * D * D;
+    } else {
+      seg = item % p.nseg;
+      chain = item / p.nseg;
+      if (seg == 0)
+        s_in = p.h0 ? p.h0 + (int64_t)chain * D * D : nullptr;
+      else
+        s_in = p.seg_s + ((int64_t)chain * p.nseg + seg) * D * D;
+      if (seg == p.nseg - 1 && p.hT) s_out = p.hT + (int64_t)chain * D * D;
+    }
+    n = chain / p.H;
+    h = chain % p.H;
+    int64_t st, ln;
+    p.seqs.get(n, st, ln);
+    const int64_t a = (int64_t)seg * p.seg_len;
+    t0 = st + a;
+    len = ln - a < p.seg_len ? ln - a : p.seg_len;
+    if (len < 0) len = 0;
+  }
 
   if (tid == 0) {
     mbar_init(&bars[0], 1);
@@ -273,13 +325,13 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   // start state S^T (lane = value channel j, columns = key channels) from h0
   {
     const int j = row;
-    const float* h0p = p.h0 ? p.h0 + (((int64_t)n * p.H + h) * D) * D : nullptr;
 #pragma unroll 1
     for (int c0 = cq * SCOL; c0 < cq * SCOL + SCOL; c0 += 16) {
       float x[16];
       uint32_t u[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) x[e] = h0p ? h0p[(int64_t)(c0 + e) * D + j] : 0.f;
+      for (int e = 0; e < 16; ++e)
+        x[e] = s_in ? s_in[(int64_t)(c0 + e) * D + j] : (ident && c0 + e == j ? 1.f : 0.f);
 #pragma unroll
       for (int e = 0; e < 16; ++e) u[e] = __float_as_uint(x[e]);
       tmem_st16(tb + lane_base + TM_S + c0, u);
@@ -411,7 +463,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           const int j = cq * TCOL + e;
           AT[j * 64 + i] = j < i ? bi * a[e] : 0.f;
         }
-      } else {
+      } else if (want_o) {
         const int i = row - 64;
 #pragma unroll
         for (int e8 = 0; e8 < TCOL / 8; ++e8) {
@@ -521,8 +573,9 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         kh[e] = kv * ec[g4 * 8 + e] * s_ecrho[c];
       }
       st8(smem + SM_X + X_KBAR + cg * 1024 + t * 16, kb);  // MN-major A (M = channel)
-      st8_split(smem + SM_X + X_QH_HI + off_kmaj(t, cg * 8, 128),
-                smem + SM_X + X_QH_LO + off_kmaj(t, cg * 8, 128), qh);  // K-major B
+      if (want_o)
+        st8_split(smem + SM_X + X_QH_HI + off_kmaj(t, cg * 8, 128),
+                  smem + SM_X + X_QH_LO + off_kmaj(t, cg * 8, 128), qh);  // K-major B
       st8_split(smem + SM_X + X_KH_HI + cg * 1024 + t * 16,
                 smem + SM_X + X_KH_LO + cg * 1024 + t * 16, kh);  // MN-major B (N = channel)
     }
@@ -537,6 +590,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       for (int kk = 0; kk < C / 16; ++kk)
         mma_ss(tb + TM_ACC2, smem_desc(sbase + SM_X + X_KBAR + kk * 256, 128, 1024),
                smem_desc(tbh + kk * 256, 128, 1024), idesc_mnk, kk > 0);
+      if (!zero_v)
 #pragma unroll
       for (int pr = 0; pr < 2; ++pr)
 #pragma unroll
@@ -578,10 +632,12 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_ts(tb + TM_ACC3, tb + (pr ? TM_SLO : TM_SHI) + kk * 8,
-                 smem_desc(wtb + kk * 256, 128, 2048), idesc_su, 1);
+                 smem_desc(wtb + kk * 256, 128, 2048), idesc_su,
+                 ((pr | kk) != 0) || !zero_v);  // with v = 0, U = -W S
       const uint32_t qh = sbase + SM_X + X_QH_HI, ql = sbase + SM_X + X_QH_LO;
       const uint32_t as[3] = {TM_SHI, TM_SHI, TM_SLO};
       const uint32_t bs[3] = {qh, ql, qh};
+      if (want_o)
 #pragma unroll
       for (int pr = 0; pr < 3; ++pr)
 #pragma unroll
@@ -626,6 +682,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       const uint32_t kh = sbase + SM_X + X_KH_HI, kl = sbase + SM_X + X_KH_LO;
       const uint32_t ua[3] = {TM_UHI, TM_UHI, TM_ULO};
       const uint32_t bq[3] = {ah, al, ah}, bk[3] = {kh, kl, kh};
+      if (want_o)
 #pragma unroll
       for (int pr = 0; pr < 3; ++pr)
 #pragma unroll
@@ -666,7 +723,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
       for (int e = 0; e < TCOL; ++e) {
         const int tt = cq * TCOL + e;
-        if (tt < nv) {
+        if (want_o && tt < nv) {
           if (p.out_bf16)
             outb[obase + tt * ostride] = __float2bfloat16_rn(p.scale * o[e]);
           else
@@ -681,9 +738,9 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   if (range_err) latch_status(p.status, KDA_ERR_DECAY_RANGE);
   const bool aborted = *(volatile uint32_t*)s_flag != 0;
-  if (!aborted && p.hT) {
+  if (!aborted && s_out) {
     const int j = row;
-    float* hTp = p.hT + (((int64_t)n * p.H + h) * D) * D;
+    float* hTp = s_out;
     tc_fence_after();
 #pragma unroll 1
     for (int c0 = cq * SCOL; c0 < cq * SCOL + SCOL; c0 += 16) {
@@ -703,6 +760,62 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tb, TM_COLS);
+}
+
+// ---------------------------------------------------------------------------
+// Segment scan: S_{p+1} = M_p S_p + b_p along each chain, in float32.  The
+// state maps of the segments compose associatively ("Kimi K3 模型结构（7）：结构
+// 决定系统", section 上下文并行: each part contributes a local transition matrix
+// and a zero-start state, combined by a prefix scan).  One CTA per chain; each
+// thread owns an 8 x 8 tile of the D x D state.
+// ---------------------------------------------------------------------------
+constexpr int kScanThreads = 256;
+constexpr size_t kScanSmem = 2 * (size_t)D * D * sizeof(float);
+
+__global__ void __launch_bounds__(kScanThreads, 1)
+kda_segment_scan_kernel(const float* __restrict__ h0, const float* __restrict__ seg_m,
+                        const float* __restrict__ seg_b, float* __restrict__ seg_s, int nseg) {
+  extern __shared__ __align__(16) float sc[];
+  float* S = sc;            // current start state S_p [D][D]
+  float* MT = sc + D * D;   // M_p transposed: MT[k][i] = M_p[i][k]
+  const int tid = threadIdx.x, chain = blockIdx.x;
+  const int i0 = (tid >> 4) * 8, j0 = (tid & 15) * 8;
+  const float* h0c = h0 ? h0 + (int64_t)chain * D * D : nullptr;
+  for (int x = tid; x < D * D; x += kScanThreads) S[x] = h0c ? h0c[x] : 0.f;
+  for (int sp = 0; sp + 1 < nseg; ++sp) {
+    const float* M = seg_m + ((int64_t)chain * (nseg - 1) + sp) * D * D;
+    const float* b = seg_b + ((int64_t)chain * (nseg - 1) + sp) * D * D;
+    for (int x = tid; x < D * D; x += kScanThreads) MT[(x % D) * D + x / D] = M[x];
+    __syncthreads();
+    float acc[8][8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) acc[r][c] = b[(int64_t)(i0 + r) * D + j0 + c];
+#pragma unroll 4
+    for (int k = 0; k < D; ++k) {
+      const float4 m0 = *reinterpret_cast<const float4*>(MT + k * D + i0);
+      const float4 m1 = *reinterpret_cast<const float4*>(MT + k * D + i0 + 4);
+      const float4 s0 = *reinterpret_cast<const float4*>(S + k * D + j0);
+      const float4 s1 = *reinterpret_cast<const float4*>(S + k * D + j0 + 4);
+      const float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+      const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(mv[r], sv[c], acc[r][c]);
+    }
+    __syncthreads();  // every thread is done reading S and MT
+    float* out = seg_s + ((int64_t)chain * nseg + sp + 1) * D * D;
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        S[(i0 + r) * D + j0 + c] = acc[r][c];
+        out[(int64_t)(i0 + r) * D + j0 + c] = acc[r][c];
+      }
+    __syncthreads();
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -764,10 +877,42 @@ cudaError_t launch_prefill_bf16(const FwdArgs& a) {
   p.scale = a.scale;
   p.out_bf16 = a.out_dtype == KDA_BF16;
   p.status = a.status;
+  p.mode = MODE_CHAIN;
+  p.nseg = 1;
+  p.seg_len = 0;
+  p.seg_b = p.seg_m = nullptr;
+  p.seg_s = nullptr;
   cudaError_t e = cudaFuncSetAttribute(kda_prefill_bf16_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  kda_prefill_bf16_kernel<<<(unsigned)items, kThreads, SMEM_BYTES, a.stream>>>(mq, mk, mg, mv, p);
+  const SegPlan pl = seg_plan(a.cu != nullptr, true, items, a.T);
+  if (pl.nseg < 2 || !a.seg_ws) {
+    kda_prefill_bf16_kernel<<<(unsigned)items, kThreads, SMEM_BYTES, a.stream>>>(mq, mk, mg, mv,
+                                                                                p);
+    return cudaGetLastError();
+  }
+  // long chains: transitions of all but the last segment, scan, then outputs
+  const int64_t per = (int64_t)D * D;
+  p.nseg = pl.nseg;
+  p.seg_len = pl.seg_len;
+  p.seg_b = a.seg_ws;
+  p.seg_m = a.seg_ws + items * (pl.nseg - 1) * per;
+  float* seg_s = a.seg_ws + 2 * items * (pl.nseg - 1) * per;
+  p.seg_s = seg_s;
+  p.mode = MODE_SEG_TRANSITION;
+  kda_prefill_bf16_kernel<<<(unsigned)(items * (pl.nseg - 1) * 2), kThreads, SMEM_BYTES,
+                            a.stream>>>(mq, mk, mg, mv, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(kda_segment_scan_kernel,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kScanSmem)) != cudaSuccess)
+    return e;
+  kda_segment_scan_kernel<<<(unsigned)items, kScanThreads, kScanSmem, a.stream>>>(
+      a.h0, p.seg_m, p.seg_b, seg_s, pl.nseg);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  p.mode = MODE_SEG_OUTPUT;
+  kda_prefill_bf16_kernel<<<(unsigned)(items * pl.nseg), kThreads, SMEM_BYTES, a.stream>>>(
+      mq, mk, mg, mv, p);
   return cudaGetLastError();
 }
 

@@ -123,3 +123,17 @@ def test_binding_refuses_to_run_without_library(tmp_path):
     import kda_delta_rule_fwd_gb300 as m
     with pytest.raises(RuntimeError, match="not built"):
         m.load(str(tmp_path / "missing.so"))
+
+
+def test_workspace_size_long_chain_split(lib):
+    """A fixed-length bf16 batch of few, very long chains reserves segment states:
+    B=1, T=2^20, H=32 -> 16 segments per chain, (3*16 - 2) states of 128x128 fp32."""
+    m, L = lib
+    assert m.workspace_size(_shape(m, B=1, T=1 << 20, H=32)) == 256 + 32 * 46 * 128 * 128 * 4
+    # float32 inputs, many chains or short chains never split
+    assert m.workspace_size(_shape(m, B=1, T=1 << 20, H=32, in_dtype=m.KDA_F32)) == 256
+    assert m.workspace_size(_shape(m, B=4, T=4096, H=32)) == 256
+    assert m.workspace_size(_shape(m, B=1, T=64 * 255, H=2)) == 256
+    # the split is optional: the minimum workspace is still accepted
+    if not torch.cuda.is_available():  # would launch on fake pointers otherwise
+        assert _fwd(L, _shape(m, B=1, T=1 << 20, H=32), ws_bytes=256) == m.KDA_ERR_CUDA

@@ -130,3 +130,21 @@ def test_decode_replay_equals_single_steps_and_prefill(kda):
     ref = o8.double().cpu().numpy()
     assert rel_err(o1, ref) <= 1e-5 and rel_err(s1, s8.double().cpu().numpy()) <= 1e-5
     assert rel_err(op, ref) <= 1e-4 and rel_err(hp, s8.double().cpu().numpy()) <= 1e-4
+
+
+def test_long_chain_split_matches_oracle_and_unsplit_run(kda, oracle_mod):
+    """Two very long chains: the segment split (4 segments joined by their state
+    maps) is used with the full workspace and skipped with the minimum one; both
+    match the oracle."""
+    x = kda_inputs.fixed(1, 64 * 257 + 37, 2, 128, dtype=torch.bfloat16, device=DEV, seed=77,
+                         h0_std=0.1)
+    shape = kda.make_shape(x.q, x.v)
+    assert kda.workspace_size(shape) > 256  # the split plan is active for this shape
+    o_s, h_s = kda.fwd(x.q, x.k, x.v, x.g, x.beta, h0=x.h0)
+    small = torch.empty(256, dtype=torch.uint8, device=DEV)
+    o_u, h_u = kda.fwd(x.q, x.k, x.v, x.g, x.beta, h0=x.h0, workspace=small)
+    torch.cuda.synchronize()
+    o_ref, h_ref = oracle_mod.recurrent(x.q, x.k, x.v, x.g, x.beta, h0=x.h0)
+    for o, h in ((o_s, h_s), (o_u, h_u)):
+        assert rel_err(o, o_ref) <= TOL_BF16
+        assert rel_err(h, h_ref) <= TOL_BF16
