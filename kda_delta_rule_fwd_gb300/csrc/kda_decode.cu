@@ -36,14 +36,14 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
   constexpr int CPL = D / 32;  // state columns per lane
   using Vec = typename VecF<CPL>::T;
 
-  __shared__ float s_k[kMaxTstep][D];
-  __shared__ float s_q[kMaxTstep][D];
-  __shared__ float s_a[kMaxTstep][D];   // alpha = exp(g)
-  __shared__ float s_v[kMaxTstep][D];
+  __shared__ __align__(16) float s_k[kMaxTstep][D];
+  __shared__ __align__(16) float s_q[kMaxTstep][D];
+  __shared__ __align__(16) float s_a[kMaxTstep][D];   // alpha = exp(g)
+  __shared__ __align__(16) float s_v[kMaxTstep][D];
   __shared__ float s_b[kMaxTstep];
   __shared__ float s_kq[kMaxTstep];
-  __shared__ float s_red[8][2][D];      // per-warp partial S^T k and S^T q
-  __shared__ float s_u[D];
+  __shared__ __align__(16) float s_red[8][2][D];      // per-warp partial S^T k and S^T q
+  __shared__ __align__(16) float s_u[D];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t nh = blockIdx.x;  // n * H + h
@@ -82,25 +82,38 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
   __syncthreads();
 
   for (int t = 0; t < Tstep; ++t) {
+    // this warp's rows of alpha, k and q, read as 16-byte vectors
+    float a[R], kr[R], qr[R];
+#pragma unroll
+    for (int r4 = 0; r4 < R / 4; ++r4) {
+      const float4 av = *reinterpret_cast<const float4*>(&s_a[t][warp * R + 4 * r4]);
+      const float4 kv = *reinterpret_cast<const float4*>(&s_k[t][warp * R + 4 * r4]);
+      const float4 qv = *reinterpret_cast<const float4*>(&s_q[t][warp * R + 4 * r4]);
+      a[4 * r4] = av.x; a[4 * r4 + 1] = av.y; a[4 * r4 + 2] = av.z; a[4 * r4 + 3] = av.w;
+      kr[4 * r4] = kv.x; kr[4 * r4 + 1] = kv.y; kr[4 * r4 + 2] = kv.z; kr[4 * r4 + 3] = kv.w;
+      qr[4 * r4] = qv.x; qr[4 * r4 + 1] = qv.y; qr[4 * r4 + 2] = qv.z; qr[4 * r4 + 3] = qv.w;
+    }
     // decay and partial reductions over this warp's rows
     float pk[CPL], pq[CPL];
 #pragma unroll
     for (int c = 0; c < CPL; ++c) pk[c] = pq[c] = 0.f;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      const int i = warp * R + r;
-      const float a = s_a[t][i], ki = s_k[t][i], qi = s_q[t][i];
 #pragma unroll
       for (int c = 0; c < CPL; ++c) {
-        S[r][c] *= a;
-        pk[c] = fmaf(S[r][c], ki, pk[c]);
-        pq[c] = fmaf(S[r][c], qi, pq[c]);
+        S[r][c] *= a[r];
+        pk[c] = fmaf(S[r][c], kr[r], pk[c]);
+        pq[c] = fmaf(S[r][c], qr[r], pq[c]);
       }
     }
+    {
+      Vec vk, vq;
+      float* fk = reinterpret_cast<float*>(&vk);
+      float* fq = reinterpret_cast<float*>(&vq);
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) {
-      s_red[warp][0][lane * CPL + c] = pk[c];
-      s_red[warp][1][lane * CPL + c] = pq[c];
+      for (int c = 0; c < CPL; ++c) { fk[c] = pk[c]; fq[c] = pq[c]; }
+      *reinterpret_cast<Vec*>(&s_red[warp][0][lane * CPL]) = vk;
+      *reinterpret_cast<Vec*>(&s_red[warp][1][lane * CPL]) = vq;
     }
     __syncthreads();
     if (tid < D) {
@@ -118,13 +131,16 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
     __syncthreads();
     // rank-1 write S <- S + k u^T
     float u[CPL];
+    {
+      const Vec uv = *reinterpret_cast<const Vec*>(&s_u[lane * CPL]);
+      const float* uf = reinterpret_cast<const float*>(&uv);
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) u[c] = s_u[lane * CPL + c];
+      for (int c = 0; c < CPL; ++c) u[c] = uf[c];
+    }
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      const float ki = s_k[t][warp * R + r];
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) S[r][c] = fmaf(ki, u[c], S[r][c]);
+      for (int c = 0; c < CPL; ++c) S[r][c] = fmaf(kr[r], u[c], S[r][c]);
     }
   }
 
