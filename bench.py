@@ -102,6 +102,24 @@ def _dist():
     return rank, world, local
 
 
+def rank_seed(rank):
+    """Seed of a rank's batch: rank 0 runs the workload's own seed, every other
+    rank an independent batch of the same shape (weak scaling: per-rank work is
+    fixed, no data crosses ranks)."""
+    return 1001 + 97 * rank
+
+
+def max_over_ranks(values, device):
+    """Element-wise maximum of per-rank timings (the slowest rank sets the step
+    time).  The only collective the benchmark makes besides its barriers."""
+    import torch
+    import torch.distributed as td
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if td.is_available() and td.is_initialized() and td.get_world_size() > 1:
+        td.all_reduce(t, op=td.ReduceOp.MAX)
+    return t.tolist()
+
+
 def _cpu_baseline(x, budget_s=20.0):
     """The float64 oracle on the host's cores: whole sequences of the first few
     heads, as many heads as fit the time budget (estimated from one head)."""
@@ -164,7 +182,7 @@ def run_ours(args):
 
     x = kda_inputs.workload(1, device=dev)
     if rank:  # each rank its own batch of the same shape
-        x = kda_inputs.fixed(B, T, H, D, device=dev, seed=1001 + 97 * rank)
+        x = kda_inputs.fixed(B, T, H, D, device=dev, seed=rank_seed(rank))
     shape = kda.make_shape(x.q, x.v)
     ws = kda.new_workspace(shape, dev)
     o = torch.empty(B, T, H, D, device=dev)
@@ -221,10 +239,9 @@ def run_ours(args):
         }
         del y, state, out_d
 
-    if dist_on:
-        t = torch.tensor([ms, ms_e2e], device=dev)
-        td.all_reduce(t, op=td.ReduceOp.MAX)
-        ms, ms_e2e = t.tolist()
+    ms, ms_e2e = max_over_ranks([ms, ms_e2e], dev)
+    for key in dec:
+        dec[key]["ms_per_step"] = max_over_ranks([dec[key]["ms_per_step"]], dev)[0]
 
     tokens = B * T * world
     alg_bytes = B * T * H * BYTES_PER_TOKEN_HEAD + B * H * STATE_BYTES
