@@ -55,10 +55,12 @@ constexpr uint32_t SM_IN_G = 32768;
 constexpr uint32_t SM_IN_V = 49152;
 constexpr uint32_t SM_X = 65536;         // 96 KB, reused across phases
 constexpr uint32_t X_R_HI = 0, X_R_LO = 32768, X_CK_HI = 65536, X_CK_LO = 81920;
-constexpr uint32_t X_A32 = 0, X_T32 = 16384, X_M32 = 33792;   // forward substitution
-constexpr int TLD = 66;  // padded row stride of T (float): 8-byte rows, few bank conflicts
+constexpr uint32_t X_A32 = 0, X_T32 = 17408, X_M32 = 34304;   // forward substitution
+constexpr int ALD = 68;  // row stride of A^T (float): fragment loads hit distinct banks
+constexpr int TLD = 66;  // row stride of T (float): 8-byte rows, few bank conflicts
 constexpr uint32_t X_KBAR = 0, X_QH_HI = 16384, X_QH_LO = 32768, X_KH_HI = 49152,
                    X_KH_LO = 65536, X_WT = 0;
+constexpr uint32_t X_OUT = 0;  // output staging for the bulk store, [64 tokens][128] (32 KB)
 constexpr uint32_t SM_Y = 163840;        // 32 KB
 constexpr uint32_t Y_TB_HI = 0, Y_TB_LO = 8192, Y_AQK_HI = 16384, Y_AQK_LO = 24576;
 constexpr uint32_t SM_LL = 196608;       // [L; L] 128 x 64 bf16 (lower-triangular ones)
@@ -136,6 +138,44 @@ __device__ __forceinline__ void st8_split(unsigned char* phi, unsigned char* plo
   *reinterpret_cast<uint4*>(phi) = h;
   *reinterpret_cast<uint4*>(plo) = l;
 }
+// Warp-level m16n8k8 tf32 product with fp32 accumulation, split three ways
+// for float32 accuracy: acc[0] += hi(a) hi(b), acc[1] += hi(a) lo(b),
+// acc[2] += lo(a) hi(b), with hi = tf32 rounding and lo = x - hi rounded again.
+// Fragments: a = (row g, col t), (g+8, t), (g, t+4), (g+8, t+4);
+// b = (row t, col g), (t+4, g); c = (g, 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1)
+// with g = lane/4, t = lane%4.  Used for the 16 x 16 blocks of the triangular
+// inverse, which are below the tensor-memory MMA's minimum M.
+__device__ __forceinline__ uint32_t tf32_rn(float x) {
+  uint32_t y;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4],
+                                         const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+__device__ __forceinline__ void mma_tf32x3(float (&acc)[3][4], const float (&a)[4],
+                                           const float (&b)[2]) {
+  uint32_t ah[4], al[4], bh[2], bl[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    ah[i] = tf32_rn(a[i]);
+    al[i] = tf32_rn(a[i] - __uint_as_float(ah[i]));
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    bh[i] = tf32_rn(b[i]);
+    bl[i] = tf32_rn(b[i] - __uint_as_float(bh[i]));
+  }
+  mma_tf32(acc[0], ah, bh);
+  mma_tf32(acc[1], ah, bl);
+  mma_tf32(acc[2], al, bh);
+}
+
 // hi and lo parts of 16 values, packed two per 32-bit word
 __device__ __forceinline__ void pack_split16(const float (&x)[16], uint32_t (&hi)[8],
                                              uint32_t (&lo)[8]) {
@@ -208,7 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_g,
-                        const __grid_constant__ CUtensorMap tm_v, Bf16Params p) {
+                        const __grid_constant__ CUtensorMap tm_v,
+                        const __grid_constant__ CUtensorMap tm_o, Bf16Params p) {
   extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qd = warp & 3;          // TMEM lane quarter of this warp
@@ -376,6 +417,8 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (wt.wait_mma()) break;
 
     // ---- P3 (pass A): decay factors and the decayed key/query operands
+    // (the previous chunk's output store reads X until it completes)
+    if (tid == 0) bulk_wait_read();
     const int t = row & 63;
     const int cg0 = (NCOL * (row >> 6) + cq) * GPT;  // first 8-channel group of this thread
     const bool valid = t < nv;
@@ -461,7 +504,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
         for (int e = 0; e < TCOL; ++e) {
           const int j = cq * TCOL + e;
-          AT[j * 64 + i] = j < i ? bi * a[e] : 0.f;
+          AT[j * ALD + i] = j < i ? bi * a[e] : 0.f;
         }
       } else if (want_o) {
         const int i = row - 64;
@@ -498,7 +541,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           x[m] = m < jj ? 0.f : (m == jj ? 1.f : acc[m]);
 #pragma unroll
           for (int i = m + 1; i < 16; ++i)
-            acc[i] = fmaf(-AT[(base + m) * 64 + base + i], x[m], acc[i]);
+            acc[i] = fmaf(-AT[(base + m) * ALD + base + i], x[m], acc[i]);
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) T32[(base + i) * TLD + base + jj] = x[i];
@@ -506,38 +549,68 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       __syncthreads();
 #pragma unroll 1
       for (int L = 1; L < 4; ++L) {  // block sub-diagonal L: (I, J) = (J + L, J)
-        // 64 threads per block, each a 2 x 2 tile of the 16 x 16 block
-        const int J = tid >> 6, ti = (tid >> 3) & 7, tj = tid & 7, I = J + L;
-        const bool act = J < 4 - L;
-        if (act) {  // M = A[I, J..I-1] T[J..I-1, J]
-          float m00 = 0.f, m01 = 0.f, m10 = 0.f, m11 = 0.f;
-#pragma unroll 4
-          for (int m = J * 16; m < I * 16; ++m) {
-            const float2 a = *reinterpret_cast<const float2*>(AT + m * 64 + I * 16 + 2 * ti);
-            const float2 b = *reinterpret_cast<const float2*>(T32 + m * TLD + J * 16 + 2 * tj);
-            m00 = fmaf(a.x, b.x, m00); m01 = fmaf(a.x, b.y, m01);
-            m10 = fmaf(a.y, b.x, m10); m11 = fmaf(a.y, b.y, m11);
-          }
-          *reinterpret_cast<float2*>(M32 + J * 256 + (2 * ti) * 16 + 2 * tj) = make_float2(m00, m01);
-          *reinterpret_cast<float2*>(M32 + J * 256 + (2 * ti + 1) * 16 + 2 * tj) =
-              make_float2(m10, m11);
-        }
-        __syncthreads();
-        if (act) {  // T[I, J] = -T[I, I] M
-          float t00 = 0.f, t01 = 0.f, t10 = 0.f, t11 = 0.f;
-          const float* r0 = T32 + (I * 16 + 2 * ti) * TLD + I * 16;
-          const float* r1 = r0 + TLD;
+        // one warp per block: M = A[I, J..I-1] T[J..I-1, J], then T[I, J] = -T[I, I] M,
+        // as m16n8k8 tf32 products with 3-term splitting (hi*hi + hi*lo + lo*hi)
+        if (warp < 4 - L) {
+          const int J = warp, I = J + L, g = lane >> 2, t4 = lane & 3;
+          float* Mw = M32 + warp * 256;
+          float acc[2][3][4];
 #pragma unroll
-          for (int m = 0; m < 16; ++m) {
-            const float2 b = *reinterpret_cast<const float2*>(M32 + J * 256 + m * 16 + 2 * tj);
-            const float a0 = r0[m], a1 = r1[m];
-            t00 = fmaf(a0, b.x, t00); t01 = fmaf(a0, b.y, t01);
-            t10 = fmaf(a1, b.x, t10); t11 = fmaf(a1, b.y, t11);
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int q = 0; q < 3; ++q)
+#pragma unroll
+              for (int r = 0; r < 4; ++r) acc[nt][q][r] = 0.f;
+          for (int kb = J; kb < I; ++kb)
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+              const int k0 = kb * 16 + ks * 8;
+              const float af[4] = {AT[(k0 + t4) * ALD + I * 16 + g],
+                                   AT[(k0 + t4) * ALD + I * 16 + g + 8],
+                                   AT[(k0 + t4 + 4) * ALD + I * 16 + g],
+                                   AT[(k0 + t4 + 4) * ALD + I * 16 + g + 8]};
+#pragma unroll
+              for (int nt = 0; nt < 2; ++nt) {
+                const float bf[2] = {T32[(k0 + t4) * TLD + J * 16 + nt * 8 + g],
+                                     T32[(k0 + t4 + 4) * TLD + J * 16 + nt * 8 + g]};
+                mma_tf32x3(acc[nt], af, bf);
+              }
+            }
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            const int c = nt * 8 + 2 * t4;
+            Mw[g * 16 + c] = acc[nt][0][0] + acc[nt][1][0] + acc[nt][2][0];
+            Mw[g * 16 + c + 1] = acc[nt][0][1] + acc[nt][1][1] + acc[nt][2][1];
+            Mw[(g + 8) * 16 + c] = acc[nt][0][2] + acc[nt][1][2] + acc[nt][2][2];
+            Mw[(g + 8) * 16 + c + 1] = acc[nt][0][3] + acc[nt][1][3] + acc[nt][2][3];
           }
-          *reinterpret_cast<float2*>(T32 + (I * 16 + 2 * ti) * TLD + J * 16 + 2 * tj) =
-              make_float2(-t00, -t01);
-          *reinterpret_cast<float2*>(T32 + (I * 16 + 2 * ti + 1) * TLD + J * 16 + 2 * tj) =
-              make_float2(-t10, -t11);
+          __syncwarp();
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int q = 0; q < 3; ++q)
+#pragma unroll
+              for (int r = 0; r < 4; ++r) acc[nt][q][r] = 0.f;
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks) {
+            const float* Ti = T32 + (I * 16) * TLD + I * 16 + ks * 8;
+            const float af[4] = {Ti[g * TLD + t4], Ti[(g + 8) * TLD + t4], Ti[g * TLD + t4 + 4],
+                                 Ti[(g + 8) * TLD + t4 + 4]};
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+              const float bf[2] = {Mw[(ks * 8 + t4) * 16 + nt * 8 + g],
+                                   Mw[(ks * 8 + t4 + 4) * 16 + nt * 8 + g]};
+              mma_tf32x3(acc[nt], af, bf);
+            }
+          }
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            float* To = T32 + (I * 16) * TLD + J * 16 + nt * 8 + 2 * t4;
+            To[g * TLD] = -(acc[nt][0][0] + acc[nt][1][0] + acc[nt][2][0]);
+            To[g * TLD + 1] = -(acc[nt][0][1] + acc[nt][1][1] + acc[nt][2][1]);
+            To[(g + 8) * TLD] = -(acc[nt][0][2] + acc[nt][1][2] + acc[nt][2][2]);
+            To[(g + 8) * TLD + 1] = -(acc[nt][0][3] + acc[nt][1][3] + acc[nt][2][3]);
+          }
         }
         __syncthreads();
       }
@@ -716,26 +789,47 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         tmem_st8(tb + lane_base + TM_SHI + c0 / 2, hi);
         tmem_st8(tb + lane_base + TM_SLO + c0 / 2, lo);
       }
-      float* outf = static_cast<float*>(p.out);
-      __nv_bfloat16* outb = static_cast<__nv_bfloat16*>(p.out);
-      const int64_t obase = ((t0 + cs) * p.H + h) * D + j;
-      const int64_t ostride = (int64_t)p.H * D;
+      if (want_o && nv == C) {
+        // full chunk: stage [token][value channel] in X, one bulk tensor store below
+        if (p.out_bf16) {
+          __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(smem + SM_X + X_OUT);
 #pragma unroll
-      for (int e = 0; e < TCOL; ++e) {
-        const int tt = cq * TCOL + e;
-        if (want_o && tt < nv) {
-          if (p.out_bf16)
-            outb[obase + tt * ostride] = __float2bfloat16_rn(p.scale * o[e]);
-          else
-            outf[obase + tt * ostride] = p.scale * o[e];
+          for (int e = 0; e < TCOL; ++e)
+            st[(cq * TCOL + e) * D + j] = __float2bfloat16_rn(p.scale * o[e]);
+        } else {
+          float* st = reinterpret_cast<float*>(smem + SM_X + X_OUT);
+#pragma unroll
+          for (int e = 0; e < TCOL; ++e) st[(cq * TCOL + e) * D + j] = p.scale * o[e];
+        }
+        fence_proxy_async_smem();
+      } else if (want_o) {
+        // partial last chunk: element stores, only for tokens of this sequence
+        float* outf = static_cast<float*>(p.out);
+        __nv_bfloat16* outb = static_cast<__nv_bfloat16*>(p.out);
+        const int64_t obase = ((t0 + cs) * p.H + h) * D + j;
+        const int64_t ostride = (int64_t)p.H * D;
+#pragma unroll
+        for (int e = 0; e < TCOL; ++e) {
+          const int tt = cq * TCOL + e;
+          if (tt < nv) {
+            if (p.out_bf16)
+              outb[obase + tt * ostride] = __float2bfloat16_rn(p.scale * o[e]);
+            else
+              outf[obase + tt * ostride] = p.scale * o[e];
+          }
         }
       }
       tmem_wait_st();
     }
     tc_fence_before();
     __syncthreads();
+    if (tid == 0 && want_o && nv == C) {
+      tma_store_2d(&tm_o, h * D, (int32_t)(t0 + cs), smem + SM_X + X_OUT);
+      bulk_commit();
+    }
   }
 
+  if (tid == 0) bulk_wait_all();  // outputs complete before shared memory is released
   if (range_err) latch_status(p.status, KDA_ERR_DECAY_RANGE);
   const bool aborted = *(volatile uint32_t*)s_flag != 0;
   if (!aborted && s_out) {
@@ -837,6 +931,21 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 
 // Tile map over one activation tensor [tokens, H, D] (bf16): box = 64 tokens x
 // 16 groups of 8 channels, written to shared memory as [group][token][8].
+// Store map over the output [tokens, H, D] (float32 or bf16): box = 64 tokens x D
+// channels of one head, read from shared memory as [token][channel].
+bool make_out_map(CUtensorMap* m, void* base, int64_t tokens, int H, bool bf16) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  const cuuint64_t es = bf16 ? 2 : 4;
+  cuuint64_t dims[2] = {(cuuint64_t)H * D, (cuuint64_t)tokens};
+  cuuint64_t strides[1] = {(cuuint64_t)H * D * es};
+  cuuint32_t box[2] = {D, C};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base,
+             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map(CUtensorMap* m, const void* base, int64_t tokens, int H) {
   auto enc = get_encode();
   if (!enc) return false;
@@ -862,9 +971,11 @@ cudaError_t launch_prefill_bf16(const FwdArgs& a) {
   if (tokens == 0 && !dummy) return cudaSuccess;
   auto pick = [&](const void* x) { return tokens > 0 ? x : dummy; };
   const int64_t map_tokens = tokens > 0 ? tokens : 1;
-  CUtensorMap mq, mk, mg, mv;
+  CUtensorMap mq, mk, mg, mv, mo;
   if (!make_map(&mq, pick(a.q), map_tokens, a.H) || !make_map(&mk, pick(a.k), map_tokens, a.H) ||
-      !make_map(&mg, pick(a.g), map_tokens, a.H) || !make_map(&mv, pick(a.v), map_tokens, a.H))
+      !make_map(&mg, pick(a.g), map_tokens, a.H) || !make_map(&mv, pick(a.v), map_tokens, a.H) ||
+      !make_out_map(&mo, tokens > 0 ? a.out : const_cast<void*>(dummy), map_tokens, a.H,
+                    tokens > 0 && a.out_dtype == KDA_BF16))
     return cudaErrorInvalidValue;
   Bf16Params p;
   p.beta = static_cast<const __nv_bfloat16*>(a.beta);
@@ -888,7 +999,7 @@ cudaError_t launch_prefill_bf16(const FwdArgs& a) {
   const SegPlan pl = seg_plan(a.cu != nullptr, true, items, a.T);
   if (pl.nseg < 2 || !a.seg_ws) {
     kda_prefill_bf16_kernel<<<(unsigned)items, kThreads, SMEM_BYTES, a.stream>>>(mq, mk, mg, mv,
-                                                                                p);
+                                                                                mo, p);
     return cudaGetLastError();
   }
   // long chains: transitions of all but the last segment, scan, then outputs
@@ -901,7 +1012,7 @@ cudaError_t launch_prefill_bf16(const FwdArgs& a) {
   p.seg_s = seg_s;
   p.mode = MODE_SEG_TRANSITION;
   kda_prefill_bf16_kernel<<<(unsigned)(items * (pl.nseg - 1) * 2), kThreads, SMEM_BYTES,
-                            a.stream>>>(mq, mk, mg, mv, p);
+                            a.stream>>>(mq, mk, mg, mv, mo, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(kda_segment_scan_kernel,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -912,7 +1023,7 @@ cudaError_t launch_prefill_bf16(const FwdArgs& a) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   p.mode = MODE_SEG_OUTPUT;
   kda_prefill_bf16_kernel<<<(unsigned)(items * pl.nseg), kThreads, SMEM_BYTES, a.stream>>>(
-      mq, mk, mg, mv, p);
+      mq, mk, mg, mv, mo, p);
   return cudaGetLastError();
 }
 
