@@ -47,6 +47,25 @@ def _peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+def profiled_traffic():
+    """DRAM bytes per prefill launch from the committed ncu summary, or None when
+    the kernel source has changed since those counters were taken."""
+    import hashlib
+    import re
+    src = os.path.join(ROOT, "kda_delta_rule_fwd_gb300", "csrc", "kda_prefill_bf16.cu")
+    prof = os.path.join(ROOT, "profiles", "prefill_bf16_B4_T4096_H32.txt")
+    try:
+        txt = open(prof).read()
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    m = re.search(r"kernel_source_sha256_16: (\w+)", txt)
+    b = re.search(r"dram_bytes_per_launch: (\d+)", txt)
+    if m and b and m.group(1) == digest:
+        return int(b.group(1))
+    return None
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle sampling during the timed region."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -265,7 +284,7 @@ def run_ours(args):
                    "chunk": CHUNK, "tokens_per_rank": B * T,
                    "l2": "inputs and outputs (~0.8 GB) exceed L2; no flush"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": None,
+                     "frac": achieved / hbm_peak, "traffic": profiled_traffic(),
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "kernel": "kda_prefill (one launch per step)",
                      "algorithmic_bytes_per_launch": alg_bytes,
