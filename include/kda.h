@@ -157,6 +157,13 @@ kda_status kda_fwd_noalloc(const kda_shape* s, const void* q, const void* k, con
  * it (each call clears the word when it starts): KDA_OK or a device error. */
 kda_status kda_read_device_status(void* workspace, void* stream);
 
+/* Self-test of the device-side bounded waits: launches one tiny kernel that
+ * waits on a barrier nothing completes, gives up after about 1 ms and latches
+ * KDA_ERR_DEVICE_TIMEOUT in the workspace status word (read it with
+ * kda_read_device_status).  The wait never traps and the context stays
+ * usable.  workspace: device, 256-byte aligned, >= 256 bytes. */
+kda_status kda_selftest_bounded_wait(void* workspace, void* stream);
+
 /* Static description of a status code; never NULL. */
 const char* kda_status_string(kda_status st);
 

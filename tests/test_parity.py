@@ -148,3 +148,41 @@ def test_long_chain_split_matches_oracle_and_unsplit_run(kda, oracle_mod):
     for o, h in ((o_s, h_s), (o_u, h_u)):
         assert rel_err(o, o_ref) <= TOL_BF16
         assert rel_err(h, h_ref) <= TOL_BF16
+
+
+def test_bounded_wait_runs_out_and_is_reported(kda, oracle_mod):
+    """A device wait that can never complete gives up after its budget, latches
+    KDA_ERR_DEVICE_TIMEOUT, and leaves the context usable for the next call."""
+    import ctypes
+    L = kda.load()
+    L.kda_selftest_bounded_wait.restype = ctypes.c_int
+    L.kda_selftest_bounded_wait.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    ws = torch.empty(256, dtype=torch.uint8, device=DEV)
+    rc = L.kda_selftest_bounded_wait(ctypes.c_void_p(ws.data_ptr()),
+                                     ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == kda.KDA_OK
+    assert kda.read_device_status(ws) == kda.KDA_ERR_DEVICE_TIMEOUT
+    x = kda_inputs.fixed(1, 70, 2, 128, dtype=torch.bfloat16, device=DEV, seed=8)
+    o, hT = kda.fwd(x.q, x.k, x.v, x.g, x.beta)
+    torch.cuda.synchronize()
+    o_ref, _ = oracle_mod.recurrent(x.q, x.k, x.v, x.g, x.beta)
+    assert rel_err(o, o_ref) <= TOL_BF16
+
+
+def test_decay_outside_bf16_range_is_reported(kda):
+    """A per-chunk log-decay span beyond what the bf16 factorisation holds
+    (|Gam - rho| > 80 within a chunk) is latched as KDA_ERR_DECAY_RANGE; the
+    kernel clamps the factors, stays finite and does not fault."""
+    x = kda_inputs.fixed(1, 128, 2, 128, dtype=torch.bfloat16, device=DEV, seed=9)
+    g = x.g.clone()
+    g[:, 40:44] = -30.0  # 4 tokens of -30 per channel: a span of 120 inside the chunk
+    shape = kda.make_shape(x.q, x.v)
+    ws = kda.new_workspace(shape, DEV)
+    o, hT = kda.fwd(x.q, x.k, x.v, g, x.beta, workspace=ws)
+    assert kda.read_device_status(ws) == kda.KDA_ERR_DECAY_RANGE
+    assert torch.isfinite(hT).all()
+    # the float32 path has no such limit
+    o32, h32 = kda.fwd(x.q.float(), x.k.float(), x.v.float(), g.float(), x.beta.float(),
+                       workspace=ws)
+    assert kda.read_device_status(ws) == kda.KDA_OK
+    assert torch.isfinite(o32).all() and torch.isfinite(h32).all()
