@@ -74,9 +74,9 @@ constexpr uint32_t SMEM_BYTES = SM_MISC + 2880;
 constexpr uint32_t TM_S = 0;       // S^T float32 master: lane = value channel, col = key channel
 constexpr uint32_t TM_SHI = 128;   // S^T bf16 hi, two key channels per column
 constexpr uint32_t TM_SLO = 192;   // S^T bf16 lo
-constexpr uint32_t TM_ACC1 = 256;  // Gam (with ACC2) -> [Akk; Aqk]
-constexpr uint32_t TM_ACC2 = 320;  // Gam (upper half) -> W^T -> O^T
-constexpr uint32_t TM_ACC3 = 384;  // U~^T -> U^T
+constexpr uint32_t TM_ACC1 = 256;  // Gam (with TM_U) -> [Akk; Aqk]
+constexpr uint32_t TM_U = 320;     // Gam (upper half) -> U~^T -> U^T
+constexpr uint32_t TM_O = 384;     // W^T -> O^T (adjacent to TM_U: one N=128 MMA feeds both)
 constexpr uint32_t TM_UHI = 448;   // U^T bf16 hi, two tokens per column
 constexpr uint32_t TM_ULO = 480;   // U^T bf16 lo
 constexpr uint32_t TM_COLS = 512;
@@ -390,7 +390,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   const uint32_t idesc_cum = idesc_bf16(128, 128, 0, 1);
   const uint32_t idesc_kk = idesc_bf16(128, 64, 0, 0);
   const uint32_t idesc_mnk = idesc_bf16(128, 64, 1, 0);
-  const uint32_t idesc_su = idesc_bf16(128, 64, 0, 1, 1);
+  const uint32_t idesc_sw = idesc_bf16(128, 128, 0, 0);
   const uint32_t idesc_sq = idesc_bf16(128, 64, 0, 0);
   const uint32_t idesc_s = idesc_bf16(128, 128, 0, 1);
   const uint32_t sbase = smem_u32(smem);
@@ -410,8 +410,8 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       // Gam (rows 0..63 and again 64..127) = [L; L] G, G = the g tile as an MN-major B
 #pragma unroll
       for (int kk = 0; kk < C / 16; ++kk)
-        mma_ss(tb + TM_ACC1, smem_desc(sbase + SM_LL + kk * 256, 128, 1024),
-               smem_desc(sbase + SM_IN_G + kk * 256, 128, 1024), idesc_cum, kk > 0);
+        mma_ss(tb + TM_ACC1, (smem_desc(sbase + SM_LL, 128, 1024) + (uint64_t)(kk * 16)),
+               (smem_desc(sbase + SM_IN_G, 128, 1024) + (uint64_t)(kk * 16)), idesc_cum, kk > 0);
       mma_commit(wt.mma_bar);
     }
     if (wt.wait_mma()) break;
@@ -486,8 +486,8 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       for (int pr = 0; pr < 3; ++pr)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tb + TM_ACC1, smem_desc(as[pr] + kk * 256, 128, 2048),
-                 smem_desc(bs[pr] + kk * 256, 128, 2048), idesc_kk, (pr | kk) != 0);
+          mma_ss(tb + TM_ACC1, (smem_desc(as[pr], 128, 2048) + (uint64_t)(kk * 16)),
+                 (smem_desc(bs[pr], 128, 2048) + (uint64_t)(kk * 16)), idesc_kk, (pr | kk) != 0);
       mma_commit(wt.mma_bar);
     }
     if (wt.wait_mma()) break;
@@ -549,18 +549,17 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       __syncthreads();
 #pragma unroll 1
       for (int L = 1; L < 4; ++L) {  // block sub-diagonal L: (I, J) = (J + L, J)
-        // one warp per block: M = A[I, J..I-1] T[J..I-1, J], then T[I, J] = -T[I, I] M,
-        // as m16n8k8 tf32 products with 3-term splitting (hi*hi + hi*lo + lo*hi)
-        if (warp < 4 - L) {
-          const int J = warp, I = J + L, g = lane >> 2, t4 = lane & 3;
-          float* Mw = M32 + warp * 256;
-          float acc[2][3][4];
+        // two warps per block, one per 8-column n-tile: M = A[I, J..I-1] T[J..I-1, J],
+        // then T[I, J] = -T[I, I] M, as m16n8k8 tf32 products with 3-term splitting.
+        // Each warp only ever reads back its own columns of M.
+        if (warp < 2 * (4 - L)) {
+          const int J = warp >> 1, nt = warp & 1, I = J + L, g = lane >> 2, t4 = lane & 3;
+          float* Mw = M32 + J * 256;
+          float acc[3][4];
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
+          for (int q = 0; q < 3; ++q)
 #pragma unroll
-            for (int q = 0; q < 3; ++q)
-#pragma unroll
-              for (int r = 0; r < 4; ++r) acc[nt][q][r] = 0.f;
+            for (int r = 0; r < 4; ++r) acc[q][r] = 0.f;
           for (int kb = J; kb < I; ++kb)
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks) {
@@ -569,48 +568,36 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                                    AT[(k0 + t4) * ALD + I * 16 + g + 8],
                                    AT[(k0 + t4 + 4) * ALD + I * 16 + g],
                                    AT[(k0 + t4 + 4) * ALD + I * 16 + g + 8]};
-#pragma unroll
-              for (int nt = 0; nt < 2; ++nt) {
-                const float bf[2] = {T32[(k0 + t4) * TLD + J * 16 + nt * 8 + g],
-                                     T32[(k0 + t4 + 4) * TLD + J * 16 + nt * 8 + g]};
-                mma_tf32x3(acc[nt], af, bf);
-              }
+              const float bf[2] = {T32[(k0 + t4) * TLD + J * 16 + nt * 8 + g],
+                                   T32[(k0 + t4 + 4) * TLD + J * 16 + nt * 8 + g]};
+              mma_tf32x3(acc, af, bf);
             }
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
+          {
             const int c = nt * 8 + 2 * t4;
-            Mw[g * 16 + c] = acc[nt][0][0] + acc[nt][1][0] + acc[nt][2][0];
-            Mw[g * 16 + c + 1] = acc[nt][0][1] + acc[nt][1][1] + acc[nt][2][1];
-            Mw[(g + 8) * 16 + c] = acc[nt][0][2] + acc[nt][1][2] + acc[nt][2][2];
-            Mw[(g + 8) * 16 + c + 1] = acc[nt][0][3] + acc[nt][1][3] + acc[nt][2][3];
+            Mw[g * 16 + c] = acc[0][0] + acc[1][0] + acc[2][0];
+            Mw[g * 16 + c + 1] = acc[0][1] + acc[1][1] + acc[2][1];
+            Mw[(g + 8) * 16 + c] = acc[0][2] + acc[1][2] + acc[2][2];
+            Mw[(g + 8) * 16 + c + 1] = acc[0][3] + acc[1][3] + acc[2][3];
           }
           __syncwarp();
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
+          for (int q = 0; q < 3; ++q)
 #pragma unroll
-            for (int q = 0; q < 3; ++q)
-#pragma unroll
-              for (int r = 0; r < 4; ++r) acc[nt][q][r] = 0.f;
+            for (int r = 0; r < 4; ++r) acc[q][r] = 0.f;
 #pragma unroll
           for (int ks = 0; ks < 2; ++ks) {
             const float* Ti = T32 + (I * 16) * TLD + I * 16 + ks * 8;
             const float af[4] = {Ti[g * TLD + t4], Ti[(g + 8) * TLD + t4], Ti[g * TLD + t4 + 4],
                                  Ti[(g + 8) * TLD + t4 + 4]};
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-              const float bf[2] = {Mw[(ks * 8 + t4) * 16 + nt * 8 + g],
-                                   Mw[(ks * 8 + t4 + 4) * 16 + nt * 8 + g]};
-              mma_tf32x3(acc[nt], af, bf);
-            }
+            const float bf[2] = {Mw[(ks * 8 + t4) * 16 + nt * 8 + g],
+                                 Mw[(ks * 8 + t4 + 4) * 16 + nt * 8 + g]};
+            mma_tf32x3(acc, af, bf);
           }
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            float* To = T32 + (I * 16) * TLD + J * 16 + nt * 8 + 2 * t4;
-            To[g * TLD] = -(acc[nt][0][0] + acc[nt][1][0] + acc[nt][2][0]);
-            To[g * TLD + 1] = -(acc[nt][0][1] + acc[nt][1][1] + acc[nt][2][1]);
-            To[(g + 8) * TLD] = -(acc[nt][0][2] + acc[nt][1][2] + acc[nt][2][2]);
-            To[(g + 8) * TLD + 1] = -(acc[nt][0][3] + acc[nt][1][3] + acc[nt][2][3]);
-          }
+          float* To = T32 + (I * 16) * TLD + J * 16 + nt * 8 + 2 * t4;
+          To[g * TLD] = -(acc[0][0] + acc[1][0] + acc[2][0]);
+          To[g * TLD + 1] = -(acc[0][1] + acc[1][1] + acc[2][1]);
+          To[(g + 8) * TLD] = -(acc[0][2] + acc[1][2] + acc[2][2]);
+          To[(g + 8) * TLD + 1] = -(acc[0][3] + acc[1][3] + acc[2][3]);
         }
         __syncthreads();
       }
@@ -661,14 +648,14 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       const uint32_t tbh = sbase + SM_Y + Y_TB_HI, tbl = sbase + SM_Y + Y_TB_LO;
 #pragma unroll
       for (int kk = 0; kk < C / 16; ++kk)
-        mma_ss(tb + TM_ACC2, smem_desc(sbase + SM_X + X_KBAR + kk * 256, 128, 1024),
-               smem_desc(tbh + kk * 256, 128, 1024), idesc_mnk, kk > 0);
+        mma_ss(tb + TM_O, (smem_desc(sbase + SM_X + X_KBAR, 128, 1024) + (uint64_t)(kk * 16)),
+               (smem_desc(tbh, 128, 1024) + (uint64_t)(kk * 16)), idesc_mnk, kk > 0);
       if (!zero_v)
 #pragma unroll
       for (int pr = 0; pr < 2; ++pr)
 #pragma unroll
         for (int kk = 0; kk < C / 16; ++kk)
-          mma_ss(tb + TM_ACC3, smem_desc(sbase + SM_IN_V + kk * 256, 128, 1024),
+          mma_ss(tb + TM_U, (smem_desc(sbase + SM_IN_V, 128, 1024) + (uint64_t)(kk * 16)),
                  smem_desc((pr ? tbl : tbh) + kk * 256, 128, 1024), idesc_mnk,
                  (pr | kk) != 0);
       mma_commit(wt.mma_bar);
@@ -679,44 +666,44 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (tid == 0 && ci + 1 < nchunks) issue_tma(ci + 1);
     if (ci + 1 < nchunks) beta_next = load_beta(ci + 1);
     {
-      const int c = row;  // W^T lane = key channel
+      // W^T lane = key channel c; store -W as rows 0..63 (token) of the K-major
+      // operand [-W; Qhat_hi], then clear the accumulator for O^T
+      const int c = row;
       float w[TCOL];
-      tmem_ld16(tb + lane_base + TM_ACC2 + cq * TCOL, w);
+      tmem_ld16(tb + lane_base + TM_O + cq * TCOL, w);
       tmem_wait_ld();
 #pragma unroll
-      for (int e8 = 0; e8 < TCOL / 8; ++e8) {
-        const int tt = cq * TCOL + e8 * 8;
-        float x[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = w[e8 * 8 + e];
-        st8(smem + SM_X + X_WT + off_mnmaj(tt, c, 128), x);
+      for (int e = 0; e < TCOL; ++e) {
+        const int tt = cq * TCOL + e;
+        *reinterpret_cast<__nv_bfloat16*>(smem + SM_X + X_WT + off_kmaj(tt, c, 128)) =
+            __float2bfloat16_rn(-w[e]);
       }
+      uint32_t z[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) z[e] = 0u;
+      tmem_st16(tb + lane_base + TM_O + cq * TCOL, z);
+      tmem_wait_st();
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
 
-    // ---- P10: U^T = U~^T - S^T W^T (S split); O^T = S^T Qhat^T (both split)
+    // ---- P10: [U^T | O^T] += S^T [-W; Qhat]^T  (U^T starts from U~^T, O^T from 0):
+    // S split against [-W; Qhat_hi] as N = 128 products, plus S_hi Qhat_lo^T
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t wtb = sbase + SM_X + X_WT;
+      const uint64_t bw = smem_desc(sbase + SM_X + X_WT, 128, 2048);      // [-W; Qhat_hi]
+      const uint64_t bl = smem_desc(sbase + SM_X + X_QH_LO, 128, 2048);   // Qhat_lo
 #pragma unroll
       for (int pr = 0; pr < 2; ++pr)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ts(tb + TM_ACC3, tb + (pr ? TM_SLO : TM_SHI) + kk * 8,
-                 smem_desc(wtb + kk * 256, 128, 2048), idesc_su,
-                 ((pr | kk) != 0) || !zero_v);  // with v = 0, U = -W S
-      const uint32_t qh = sbase + SM_X + X_QH_HI, ql = sbase + SM_X + X_QH_LO;
-      const uint32_t as[3] = {TM_SHI, TM_SHI, TM_SLO};
-      const uint32_t bs[3] = {qh, ql, qh};
+          mma_ts(tb + TM_U, tb + (pr ? TM_SLO : TM_SHI) + kk * 8, bw + (uint64_t)(kk * 16),
+                 idesc_sw, ((pr | kk) != 0) || !zero_v);  // with v = 0, U = -W S
       if (want_o)
 #pragma unroll
-      for (int pr = 0; pr < 3; ++pr)
-#pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ts(tb + TM_ACC2, tb + as[pr] + kk * 8, smem_desc(bs[pr] + kk * 256, 128, 2048),
-                 idesc_sq, (pr | kk) != 0);
+          mma_ts(tb + TM_O, tb + TM_SHI + kk * 8, bl + (uint64_t)(kk * 16), idesc_sq, 1);
       mma_commit(wt.mma_bar);
     }
     if (wt.wait_mma()) break;
@@ -724,7 +711,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     // ---- P11: U^T split into TMEM (A operand); S^T <- S^T diag(e^Gam_last)
     {
       float u[TCOL], sv[SCOL / 16][16];
-      tmem_ld16(tb + lane_base + TM_ACC3 + cq * TCOL, u);
+      tmem_ld16(tb + lane_base + TM_U + cq * TCOL, u);
 #pragma unroll
       for (int q4 = 0; q4 < SCOL / 16; ++q4)
         tmem_ld16(tb + lane_base + TM_S + cq * SCOL + q4 * 16, sv[q4]);
@@ -760,13 +747,13 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       for (int pr = 0; pr < 3; ++pr)
 #pragma unroll
         for (int kk = 0; kk < C / 16; ++kk)
-          mma_ts(tb + TM_ACC2, tb + ua[pr] + kk * 8, smem_desc(bq[pr] + kk * 256, 128, 1024),
+          mma_ts(tb + TM_O, tb + ua[pr] + kk * 8, (smem_desc(bq[pr], 128, 1024) + (uint64_t)(kk * 16)),
                  idesc_sq, 1);
 #pragma unroll
       for (int pr = 0; pr < 3; ++pr)
 #pragma unroll
         for (int kk = 0; kk < C / 16; ++kk)
-          mma_ts(tb + TM_S, tb + ua[pr] + kk * 8, smem_desc(bk[pr] + kk * 256, 128, 1024),
+          mma_ts(tb + TM_S, tb + ua[pr] + kk * 8, (smem_desc(bk[pr], 128, 1024) + (uint64_t)(kk * 16)),
                  idesc_s, 1);
       mma_commit(wt.mma_bar);
     }
@@ -776,7 +763,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     {
       const int j = row;
       float o[TCOL], sv[SCOL / 16][16];
-      tmem_ld16(tb + lane_base + TM_ACC2 + cq * TCOL, o);
+      tmem_ld16(tb + lane_base + TM_O + cq * TCOL, o);
 #pragma unroll
       for (int q4 = 0; q4 < SCOL / 16; ++q4)
         tmem_ld16(tb + lane_base + TM_S + cq * SCOL + q4 * 16, sv[q4]);
