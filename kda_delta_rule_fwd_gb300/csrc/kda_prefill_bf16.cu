@@ -296,10 +296,9 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     } else {
       seg = item % p.nseg;
       chain = item / p.nseg;
-      if (seg == 0)
-        s_in = p.h0 ? p.h0 + (int64_t)chain * D * D : nullptr;
-      else
-        s_in = p.seg_s + ((int64_t)chain * p.nseg + seg) * D * D;
+      // every segment, the first included, starts from the scan's copy: hT may
+      // alias h0 and the last segment's CTA writes hT while others still run
+      s_in = p.seg_s + ((int64_t)chain * p.nseg + seg) * D * D;
       if (seg == p.nseg - 1 && p.hT) s_out = p.hT + (int64_t)chain * D * D;
     }
     n = chain / p.H;
@@ -862,7 +861,12 @@ kda_segment_scan_kernel(const float* __restrict__ h0, const float* __restrict__ 
   const int tid = threadIdx.x, chain = blockIdx.x;
   const int i0 = (tid >> 4) * 8, j0 = (tid & 15) * 8;
   const float* h0c = h0 ? h0 + (int64_t)chain * D * D : nullptr;
-  for (int x = tid; x < D * D; x += kScanThreads) S[x] = h0c ? h0c[x] : 0.f;
+  float* s0 = seg_s + (int64_t)chain * nseg * D * D;  // slot 0: copy of the start state
+  for (int x = tid; x < D * D; x += kScanThreads) {
+    const float v = h0c ? h0c[x] : 0.f;
+    S[x] = v;
+    s0[x] = v;
+  }
   for (int sp = 0; sp + 1 < nseg; ++sp) {
     const float* M = seg_m + ((int64_t)chain * (nseg - 1) + sp) * D * D;
     const float* b = seg_b + ((int64_t)chain * (nseg - 1) + sp) * D * D;

@@ -186,3 +186,30 @@ def test_decay_outside_bf16_range_is_reported(kda):
                        workspace=ws)
     assert kda.read_device_status(ws) == kda.KDA_OK
     assert torch.isfinite(o32).all() and torch.isfinite(h32).all()
+
+
+@pytest.mark.parametrize("T", [200, 64 * 257 + 37], ids=["chain", "segment-split"])
+def test_final_state_may_alias_start_state(kda, oracle_mod, T):
+    """hT written into the h0 buffer (in place) gives the same result as separate buffers,
+    both for whole chains and for long chains cut into segments."""
+    x = kda_inputs.fixed(1, T, 2, 128, dtype=torch.bfloat16, device=DEV, seed=31, h0_std=0.1)
+    o_ref, h_ref = oracle_mod.recurrent(x.q, x.k, x.v, x.g, x.beta, h0=x.h0)
+    state = x.h0.clone()
+    o, hT = kda.fwd(x.q, x.k, x.v, x.g, x.beta, h0=state, hT=state)
+    torch.cuda.synchronize()
+    assert hT.data_ptr() == state.data_ptr()
+    assert rel_err(o, o_ref) <= TOL_BF16
+    assert rel_err(state, h_ref) <= TOL_BF16
+
+
+def test_nondefault_scale_single_head_bf16_output_packed(kda, oracle_mod):
+    x = kda_inputs.packed([300, 1, 77], 1, 128, dtype=torch.bfloat16, device=DEV, seed=41,
+                          h0_std=0.1)
+    o, hT = kda.fwd(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens, h0=x.h0, scale=0.37,
+                    out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    o_ref, h_ref = oracle_mod.recurrent(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens,
+                                        h0=x.h0, scale=0.37)
+    d = np.abs(o.float().cpu().numpy() - o_ref)
+    assert np.all(d <= TOL_BF16 * np.sqrt(np.mean(o_ref ** 2)) + np.abs(o_ref) * 2.0 ** -8)
+    assert rel_err(hT, h_ref) <= TOL_BF16
