@@ -115,6 +115,25 @@ def test_decode(kda, oracle_mod, dtype, d, T_step):
     assert rel_err(state, h_ref) <= tol
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_extreme_gates(kda, oracle_mod, d):
+    """Gates strong enough that the product of alpha over the step underflows
+    float32 (head 0: g = -25 on a few channels; head 1: alpha = 0 on one channel)
+    take the explicit per-token decay; head 2 keeps ordinary gates.  All match
+    the oracle."""
+    x = kda_inputs.decode_pool(num_seqs=4, H=3, d=d, T_step=8, dtype=torch.float32, device=DEV,
+                               seed=321)
+    g = x.g.clone()
+    g[:, :, 0, :5] = -25.0
+    g[:, :, 1, 7] = float("-inf")
+    state = x.h0.clone()
+    o = kda.decode(x.q, x.k, x.v, g, x.beta, state)
+    torch.cuda.synchronize()
+    o_ref, h_ref = oracle_mod.recurrent(x.q, x.k, x.v, g, x.beta, h0=x.h0)
+    assert rel_err(o, o_ref) <= TOL_F32
+    assert rel_err(state, h_ref) <= TOL_F32
+
+
 def test_decode_replay_equals_single_steps_and_prefill(kda):
     """One 8-token replay step == eight 1-token steps == prefill from the same state."""
     x = kda_inputs.decode_pool(num_seqs=3, H=2, d=128, T_step=8, dtype=torch.float32,
