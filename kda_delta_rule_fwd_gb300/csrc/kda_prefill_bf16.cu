@@ -4,14 +4,19 @@
 // table, KDA row: parallel inside a chunk, recurrent across chunks; the
 // transition (I - beta k k^T) diag(alpha) is diagonal-plus-low-rank: "Kimi K3
 // NPU Training", section NPU 算子支持度, DPLR chunk kernel).  Per chunk of 64
-// tokens with Gam = inclusive per-channel prefix sum of g and one reference
-// rho = Gam at token 31 (mid chunk):
+// tokens with Gam = inclusive per-channel prefix sum of g and a per-channel
+// reference c = 2^round(log2 e * Gam at token 31) (mid chunk, a power of two):
 //
-//   Akk = (K e^(Gam-rho)) (K e^(rho-Gam))^T      Aqk = (Q e^(Gam-rho)) (K e^(rho-Gam))^T
+//   R_K = K e^Gam / c,  R_Q = Q e^Gam / c,  Ck = K c e^-Gam   (c cancels in R Ck^T)
+//   [Akk; Aqk] = [R_K; R_Q] Ck^T
 //   T   = (I + strict_lower(diag(beta) Akk))^-1  (forward substitution)
-//   W   = T diag(beta) (K e^Gam)                 U~ = T diag(beta) V
-//   U   = U~ - W S                               O  = scale ((Q e^Gam) S + lower(Aqk) U)
-//   S  <- diag(e^Gam_last) S + (K e^(Gam_last - Gam))^T U
+//   S'  = diag(c) S                              (exact: c is a power of two)
+//   X'  = R_K S' - V   (= (K e^Gam) S - V)       U  = (-T diag(beta)) X' 
+//   O   = scale (R_Q S' + lower(Aqk) U)          (R_Q S' = (Q e^Gam) S)
+//   S  <- diag(e^Gam_last / c) (S' + Ck^T U)     (= diag(e^Gam_last) S + (K e^(Gam_last-Gam))^T U)
+//
+// The products with S' need nothing from the substitution, so they run on the
+// tensor cores while the CUDA cores solve for T.
 //
 // Every product runs on tcgen05 with M = 128 and float32 accumulators in
 // tensor memory.  The state products are taken transposed (rows = value
@@ -23,7 +28,7 @@
 //
 // One CTA (512 threads) owns one (sequence, head) chain and walks its chunks
 // in order; the inputs of chunk n+1 are fetched by TMA while chunk n's state
-// update runs.  Each mbarrier wait is bounded: on expiry the CTA latches
+// update runs.  During the substitution (warps 0-7) warps 8-15 split X.  Each mbarrier wait is bounded: on expiry the CTA latches
 // KDA_ERR_DEVICE_TIMEOUT, drains its in-flight copies, frees TMEM and exits.
 #include <cudaTypedefs.h>
 
@@ -46,39 +51,41 @@ constexpr int SCOL = 128 / NCOL;      // state columns per thread
 constexpr int GPT = 16 / (2 * NCOL);  // 8-channel groups per thread in the elementwise passes
 static_assert(TCOL == 16 && SCOL % 16 == 0 && GPT >= 1, "thread mapping");
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kMaxExp = 80.f;  // |Gam - rho| beyond this overflows the factorisation
+constexpr float kMaxExp2 = 115.f;  // |log2 of a decay factor| beyond this overflows it
+constexpr float kRefExp2 = 100.f;  // |log2 c| is clamped here (S' and its bf16 parts stay normal)
 
 // ---- shared memory map (bytes) --------------------------------------------
 constexpr uint32_t SM_IN_Q = 0;          // TMA tiles, [8-channel group][token][8] bf16
 constexpr uint32_t SM_IN_K = 16384;
 constexpr uint32_t SM_IN_G = 32768;
 constexpr uint32_t SM_IN_V = 49152;
-constexpr uint32_t SM_X = 65536;         // 96 KB, reused across phases
-constexpr uint32_t X_R_HI = 0, X_R_LO = 32768, X_CK_HI = 65536, X_CK_LO = 81920;
-constexpr uint32_t X_A32 = 0, X_T32 = 17408, X_M32 = 34304;   // forward substitution
+// forward-substitution scratch, over the q, k and g tiles once pass A has read them
+constexpr uint32_t SV_AT = 0, SV_T32 = 17408, SV_M32 = 34304;
 constexpr int ALD = 68;  // row stride of A^T (float): fragment loads hit distinct banks
 constexpr int TLD = 66;  // row stride of T (float): 8-byte rows, few bank conflicts
-constexpr uint32_t X_KBAR = 0, X_QH_HI = 16384, X_QH_LO = 32768, X_KH_HI = 49152,
-                   X_KH_LO = 65536, X_WT = 0;
+static_assert(SV_M32 + 3 * 256 * 4 <= SM_IN_V, "substitution scratch overlaps the v tile");
+constexpr uint32_t SM_X = 65536;         // 96 KB: [R_K; R_Q] hi, lo (K-major), Ck hi, lo
+constexpr uint32_t X_R_HI = 0, X_R_LO = 32768, X_CK_HI = 65536, X_CK_LO = 81920;
 constexpr uint32_t X_OUT = 0;  // output staging for the bulk store, [64 tokens][128] (32 KB)
 constexpr uint32_t SM_Y = 163840;        // 32 KB
 constexpr uint32_t Y_TB_HI = 0, Y_TB_LO = 8192, Y_AQK_HI = 16384, Y_AQK_LO = 24576;
 constexpr uint32_t SM_LL = 196608;       // [L; L] 128 x 64 bf16 (lower-triangular ones)
 constexpr uint32_t SM_MISC = 212992;
-constexpr uint32_t MISC_RHO = 0, MISC_GL = 512, MISC_ERHO = 1024, MISC_ECRHO = 1536,
-                   MISC_GAMC = 2048, MISC_BETA = 2560, MISC_BAR = 2816, MISC_TMEM = 2848,
-                   MISC_FLAG = 2852;
-constexpr uint32_t SMEM_BYTES = SM_MISC + 2880;
+constexpr uint32_t MISC_RHO = 0, MISC_GL = 512, MISC_C = 1024, MISC_GAMC = 2048,
+                   MISC_BETA = 2560, MISC_BAR = 2816, MISC_TMEM = 2848, MISC_FLAG = 2852;
+constexpr uint32_t SM_NEGI = 216064;     // -I (64 x 64 bf16, K-major): adds -V^T on the tensor core
+constexpr uint32_t SMEM_BYTES = SM_NEGI + 8192;
+static_assert(SM_MISC + 2880 <= SM_NEGI && SMEM_BYTES <= 232448, "shared memory map");
 
 // ---- tensor memory map (columns) -------------------------------------------
-constexpr uint32_t TM_S = 0;       // S^T float32 master: lane = value channel, col = key channel
-constexpr uint32_t TM_SHI = 128;   // S^T bf16 hi, two key channels per column
-constexpr uint32_t TM_SLO = 192;   // S^T bf16 lo
+constexpr uint32_t TM_S = 0;       // S^T float32 (S'^T inside a chunk): lane = value channel
+constexpr uint32_t TM_SHI = 128;   // S'^T bf16 hi, two key channels per column
+constexpr uint32_t TM_SLO = 192;   // S'^T bf16 lo
 constexpr uint32_t TM_ACC1 = 256;  // Gam (with TM_U) -> [Akk; Aqk]
-constexpr uint32_t TM_U = 320;     // Gam (upper half) -> U~^T -> U^T
-constexpr uint32_t TM_O = 384;     // W^T -> O^T (adjacent to TM_U: one N=128 MMA feeds both)
-constexpr uint32_t TM_UHI = 448;   // U^T bf16 hi, two tokens per column
-constexpr uint32_t TM_ULO = 480;   // U^T bf16 lo
+constexpr uint32_t TM_U = 320;     // Gam (upper half) -> X'^T -> U^T
+constexpr uint32_t TM_O = 384;     // O^T (adjacent to TM_U: one N=128 product feeds both)
+constexpr uint32_t TM_UHI = 448;   // X'^T, then U^T, bf16 hi (two tokens per column)
+constexpr uint32_t TM_ULO = 480;   // X'^T, then U^T, bf16 lo
 constexpr uint32_t TM_COLS = 512;
 
 // Canonical no-swizzle layouts (8 rows x 16 bytes per core matrix).  For an
@@ -176,6 +183,11 @@ __device__ __forceinline__ void mma_tf32x3(float (&acc)[3][4], const float (&a)[
   mma_tf32(acc[2], al, bh);
 }
 
+// CTA-local named barrier over the first `count` threads (warps 0..count/32-1)
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // hi and lo parts of 16 values, packed two per 32-bit word
 __device__ __forceinline__ void pack_split16(const float (&x)[16], uint32_t (&hi)[8],
                                              uint32_t (&lo)[8]) {
@@ -258,8 +270,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   float* s_rho = reinterpret_cast<float*>(smem + SM_MISC + MISC_RHO);
   float* s_gl = reinterpret_cast<float*>(smem + SM_MISC + MISC_GL);
-  float* s_erho = reinterpret_cast<float*>(smem + SM_MISC + MISC_ERHO);
-  float* s_ecrho = reinterpret_cast<float*>(smem + SM_MISC + MISC_ECRHO);
+  float* s_c = reinterpret_cast<float*>(smem + SM_MISC + MISC_C);
   float* s_gamc = reinterpret_cast<float*>(smem + SM_MISC + MISC_GAMC);
   float* s_beta = reinterpret_cast<float*>(smem + SM_MISC + MISC_BETA);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM_MISC + MISC_BAR);
@@ -314,6 +325,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   if (tid == 0) {
     mbar_init(&bars[0], 1);
     mbar_init(&bars[1], 1);
+    mbar_init(&bars[2], 1);
     *s_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tm_q);
@@ -333,6 +345,13 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     for (int e = 0; e < 8; ++e) x[e] = (kb * 8 + e) <= (r & 63) ? 1.f : 0.f;
     st8(smem + SM_LL + off_kmaj(r, kb * 8, 64), x);
   }
+  for (int i = tid; i < 64 * 8; i += kThreads) {  // -I, rows = N (token), K = token
+    const int r = i >> 3, kb = i & 7;
+    float x[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = (kb * 8 + e) == r ? -1.f : 0.f;
+    st8(smem + SM_NEGI + off_kmaj(r, kb * 8, 64), x);
+  }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -343,42 +362,44 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   uint32_t tma_issued = 0;
 
   const int nchunks = (int)((len + C - 1) / C);
-  auto issue_tma = [&](int chunk) {  // thread 0 only
-    ++tma_issued;
+  // one of the four tiles of a chunk (part 0 also arms the barrier); the four
+  // parts are issued from different warps so their issue latencies overlap
+  // (a tile's bytes may land before the barrier is armed: the transaction count
+  // only has to balance when the arrival comes)
+  auto issue_tma_part = [&](int chunk, int part) {
     const int32_t y = (int32_t)(t0 + (int64_t)chunk * C);
     const int32_t z = h * (D / 8);
-    mbar_arrive_expect_tx(wt.tma_bar, 4 * 16384);
-    tma_load_3d(smem + SM_IN_Q, &tm_q, 0, y, z, wt.tma_bar);
-    tma_load_3d(smem + SM_IN_K, &tm_k, 0, y, z, wt.tma_bar);
-    tma_load_3d(smem + SM_IN_G, &tm_g, 0, y, z, wt.tma_bar);
-    tma_load_3d(smem + SM_IN_V, &tm_v, 0, y, z, wt.tma_bar);
+    if (part == 0) mbar_arrive_expect_tx(wt.tma_bar, 4 * 16384);
+    const CUtensorMap* m = part == 0 ? &tm_q : part == 1 ? &tm_k : part == 2 ? &tm_g : &tm_v;
+    tma_load_3d(smem + SM_IN_Q + part * 16384, m, 0, y, z, wt.tma_bar);
   };
-  if (tid == 0 && nchunks > 0) issue_tma(0);
-  // beta of the chunk in flight, loaded one chunk ahead (its latency overlaps the
-  // current chunk); tokens past the sequence end read as 0
-  auto load_beta = [&](int chunk) -> float {
+  if (tid == 0 && nchunks > 0)
+    for (int part = 0; part < 4; ++part) issue_tma_part(0, part);
+  if (nchunks > 0) ++tma_issued;
+  // raw bf16 bits of beta for a chunk, loaded a chunk ahead and converted only
+  // when used (no instruction waits on the load meanwhile); tokens past the
+  // sequence end read as 0
+  auto load_beta_bits = [&](int chunk) -> uint32_t {
     const int64_t tt = (int64_t)chunk * C + tid;
-    return (tid < C && tt < len) ? __bfloat162float(p.beta[(t0 + tt) * p.H + h]) : 0.f;
+    uint32_t bits = 0u;
+    if (tid < C && tt < len)
+      bits = __bfloat16_as_ushort(p.beta[(t0 + tt) * p.H + h]);
+    return bits;
   };
-  float beta_next = nchunks > 0 ? load_beta(0) : 0.f;
+  uint32_t beta_bits = nchunks > 0 ? load_beta_bits(0) : 0u;
 
-  // start state S^T (lane = value channel j, columns = key channels) from h0
+  // start state S^T (lane = value channel j, columns = key channels) from h0;
+  // its bf16 parts are made per chunk, after the rescaling by c
   {
     const int j = row;
 #pragma unroll 1
     for (int c0 = cq * SCOL; c0 < cq * SCOL + SCOL; c0 += 16) {
-      float x[16];
       uint32_t u[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e)
-        x[e] = s_in ? s_in[(int64_t)(c0 + e) * D + j] : (ident && c0 + e == j ? 1.f : 0.f);
-#pragma unroll
-      for (int e = 0; e < 16; ++e) u[e] = __float_as_uint(x[e]);
+        u[e] = __float_as_uint(s_in ? s_in[(int64_t)(c0 + e) * D + j]
+                                    : (ident && c0 + e == j ? 1.f : 0.f));
       tmem_st16(tb + lane_base + TM_S + c0, u);
-      uint32_t hi[8], lo[8];
-      pack_split16(x, hi, lo);
-      tmem_st8(tb + lane_base + TM_SHI + c0 / 2, hi);
-      tmem_st8(tb + lane_base + TM_SLO + c0 / 2, lo);
     }
     tmem_wait_st();
   }
@@ -389,11 +410,14 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   const uint32_t idesc_cum = idesc_bf16(128, 128, 0, 1);
   const uint32_t idesc_kk = idesc_bf16(128, 64, 0, 0);
   const uint32_t idesc_mnk = idesc_bf16(128, 64, 1, 0);
-  const uint32_t idesc_sw = idesc_bf16(128, 128, 0, 0);
   const uint32_t idesc_sq = idesc_bf16(128, 64, 0, 0);
   const uint32_t idesc_s = idesc_bf16(128, 128, 0, 1);
   const uint32_t sbase = smem_u32(smem);
+  uint64_t* xo_bar = &bars[2];  // completion of the products with S'
+  uint32_t xo_issued = 0;
   bool range_err = false;
+  // log2 of the chunk's per-channel reference c (an integer, clamped)
+  auto ref_log2 = [](float rho) { return fminf(fmaxf(rintf(rho * kLog2e), -kRefExp2), kRefExp2); };
 
 #pragma unroll 1
   for (int ci = 0; ci < nchunks; ++ci) {
@@ -402,7 +426,8 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int rho_t = nv - 1 < 31 ? nv - 1 : 31;
 
     // ---- P1: beta, wait for the tiles, cumulative log-decay on the tensor core
-    if (tid < C) s_beta[tid] = beta_next;
+    if (tid < C) s_beta[tid] = __uint_as_float(beta_bits << 16);
+    if (ci + 1 < nchunks) beta_bits = load_beta_bits(ci + 1);
     if (wt.wait_tma()) break;
     if (tid == 0) {
       tc_fence_after();
@@ -415,7 +440,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     if (wt.wait_mma()) break;
 
-    // ---- P3 (pass A): decay factors and the decayed key/query operands
+    // ---- P3 (pass A): per-channel reference, the decayed key/query operands
     // (the previous chunk's output store reads X until it completes)
     if (tid == 0) bulk_wait_read();
     const int t = row & 63;
@@ -431,39 +456,42 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
       for (int e = 0; e < GPT * 8; ++e) gam[e] = a[e >> 4][e & 15];
     }
-    if (t == rho_t)
+    if (t == rho_t)  // log2 c per channel (s_rho holds it from here on)
 #pragma unroll
-      for (int e = 0; e < GPT * 8; ++e) s_rho[cg0 * 8 + e] = gam[e];
+      for (int e = 0; e < GPT * 8; ++e) s_rho[cg0 * 8 + e] = ref_log2(gam[e]);
     if (t == nv - 1)
 #pragma unroll
       for (int e = 0; e < GPT * 8; ++e) s_gl[cg0 * 8 + e] = gam[e];
     tc_fence_before();
     __syncthreads();
     if (tid < D) {
-      const float r = s_rho[tid], gl = s_gl[tid];
-      s_erho[tid] = ex2(r * kLog2e);
-      s_ecrho[tid] = ex2((gl - r) * kLog2e);
-      s_gamc[tid] = ex2(gl * kLog2e);
+      const float e2 = s_rho[tid];
+      s_c[tid] = ldexpf(1.f, (int)e2);
+      s_gamc[tid] = ex2(s_gl[tid] * kLog2e - e2);  // e^Gam_last / c
     }
-    float er[GPT * 8], ec[GPT * 8];
+    float dmin = 0.f, dmax = 0.f;
 #pragma unroll
     for (int g4 = 0; g4 < GPT; ++g4) {
       const int cg = cg0 + g4;
       float kx[8], qx[8];
       ld8(smem + SM_IN_K + cg * 1024 + t * 16, kx);
       ld8(smem + SM_IN_Q + cg * 1024 + t * 16, qx);
+      const float4 e2a = *reinterpret_cast<const float4*>(s_rho + cg * 8);
+      const float4 e2b = *reinterpret_cast<const float4*>(s_rho + cg * 8 + 4);
+      const float e2[8] = {e2a.x, e2a.y, e2a.z, e2a.w, e2b.x, e2b.y, e2b.z, e2b.w};
       float rk[8], rq[8], ck[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        float d = gam[g4 * 8 + e] - s_rho[cg * 8 + e];
-        if (valid && fabsf(d) > kMaxExp) range_err = true;
-        d = fminf(fmaxf(d, -kMaxExp), kMaxExp);
-        er[g4 * 8 + e] = ex2(d * kLog2e);
-        ec[g4 * 8 + e] = ex2(-d * kLog2e);
+        // log2(e^Gam / c); rows past the sequence end take 0 (their k and q are 0)
+        float d = valid ? fmaf(gam[g4 * 8 + e], kLog2e, -e2[e]) : 0.f;
+        dmin = fminf(dmin, d);
+        dmax = fmaxf(dmax, d);
+        d = fminf(fmaxf(d, -kMaxExp2), kMaxExp2);  // keeps results finite when latched
+        const float er = ex2(d), ec = ex2(-d);
         const float kv = valid ? kx[e] : 0.f, qv = valid ? qx[e] : 0.f;
-        rk[e] = kv * er[g4 * 8 + e];
-        rq[e] = qv * er[g4 * 8 + e];
-        ck[e] = kv * ec[g4 * 8 + e];
+        rk[e] = kv * er;
+        rq[e] = qv * er;
+        ck[e] = kv * ec;
       }
       st8_split(smem + SM_X + X_R_HI + off_kmaj(t, cg * 8, 128),
                 smem + SM_X + X_R_LO + off_kmaj(t, cg * 8, 128), rk);
@@ -472,10 +500,13 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       st8_split(smem + SM_X + X_CK_HI + off_kmaj(t, cg * 8, 128),
                 smem + SM_X + X_CK_LO + off_kmaj(t, cg * 8, 128), ck);
     }
+    // a factor beyond 2^+-115 overflows the factorisation: latched (clamped above)
+    if (dmin < -kMaxExp2 || dmax > kMaxExp2) range_err = true;
     fence_proxy_async_smem();
     __syncthreads();
 
-    // ---- P4: [Akk; Aqk] = R Ck^T with split operands
+    // ---- P4: [Akk; Aqk] = R Ck^T with split operands, while every thread
+    // rescales its slice of the state: S' = S diag(c) (transposed), bf16 parts
     if (tid == 0) {
       tc_fence_after();
       const uint32_t r_hi = sbase + SM_X + X_R_HI, r_lo = sbase + SM_X + X_R_LO;
@@ -489,6 +520,53 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                  (smem_desc(bs[pr], 128, 2048) + (uint64_t)(kk * 16)), idesc_kk, (pr | kk) != 0);
       mma_commit(wt.mma_bar);
     }
+    {
+      float sv[SCOL / 16][16];
+#pragma unroll
+      for (int q4 = 0; q4 < SCOL / 16; ++q4)
+        tmem_ld16(tb + lane_base + TM_S + cq * SCOL + q4 * 16, sv[q4]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int q4 = 0; q4 < SCOL / 16; ++q4) {
+        const int c0 = cq * SCOL + q4 * 16;
+        uint32_t w[16], hi[8], lo[8];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          sv[q4][e] *= s_c[c0 + e];
+          w[e] = __float_as_uint(sv[q4][e]);
+        }
+        tmem_st16(tb + lane_base + TM_S + c0, w);
+        pack_split16(sv[q4], hi, lo);
+        tmem_st8(tb + lane_base + TM_SHI + c0 / 2, hi);
+        tmem_st8(tb + lane_base + TM_SLO + c0 / 2, lo);
+      }
+      tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncthreads();
+    // [X' | O]^T = S'^T [R_K; R_Q]^T as N = 128 products over the adjacent U and O
+    // accumulators (K = key channel, three split products), then X'^T -= V^T
+    // as V^T (-I) (V exact in bf16; A = the v tile as an MN-major operand)
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t rh = sbase + SM_X + X_R_HI, rl = sbase + SM_X + X_R_LO;
+      const uint32_t sa[3] = {TM_SHI, TM_SHI, TM_SLO};
+      const uint32_t bk[3] = {rh, rl, rh};
+      const uint32_t idesc_xo = want_o ? idesc_bf16(128, 128, 0, 0) : idesc_kk;
+#pragma unroll
+      for (int pr = 0; pr < 3; ++pr)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ts(tb + TM_U, tb + sa[pr] + kk * 8,
+                 (smem_desc(bk[pr], 128, 2048) + (uint64_t)(kk * 16)), idesc_xo, (pr | kk) != 0);
+      if (!zero_v)
+#pragma unroll
+        for (int kk = 0; kk < C / 16; ++kk)
+          mma_ss(tb + TM_U, (smem_desc(sbase + SM_IN_V, 128, 1024) + (uint64_t)(kk * 16)),
+                 (smem_desc(sbase + SM_NEGI, 128, 1024) + (uint64_t)(kk * 16)), idesc_mnk, 1);
+      mma_commit(xo_bar);
+    }
+    ++xo_issued;
     if (wt.wait_mma()) break;
 
     // ---- P5: A = strict_lower(beta Akk) (float32, for the substitution), Aqk split
@@ -499,7 +577,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (row < 64) {
         const int i = row;
         const float bi = s_beta[i];
-        float* AT = reinterpret_cast<float*>(smem + SM_X + X_A32);  // AT[j][i] = A[i][j]
+        float* AT = reinterpret_cast<float*>(smem + SV_AT);  // AT[j][i] = A[i][j]
 #pragma unroll
         for (int e = 0; e < TCOL; ++e) {
           const int j = cq * TCOL + e;
@@ -523,11 +601,12 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     tc_fence_before();
     __syncthreads();
 
-    // ---- P6: T = (I + A)^-1 by blocks of 16, then TB = T diag(beta) split
-    {
-      const float* AT = reinterpret_cast<const float*>(smem + SM_X + X_A32);  // AT[j][i]
-      float* T32 = reinterpret_cast<float*>(smem + SM_X + X_T32);
-      float* M32 = reinterpret_cast<float*>(smem + SM_X + X_M32);
+    // ---- P6: warps 0-7: T = (I + A)^-1 by blocks of 16 (named barrier 1);
+    // warps 8-15: X'^T split into TMEM; then -TB = -T diag(beta) split
+    if (warp < 8) {
+      const float* AT = reinterpret_cast<const float*>(smem + SV_AT);  // AT[j][i]
+      float* T32 = reinterpret_cast<float*>(smem + SV_T32);
+      float* M32 = reinterpret_cast<float*>(smem + SV_M32);
       if (warp < 4 && lane < 16) {
         // diagonal block I = warp, column jj = lane: right-looking substitution, so
         // each of the 16 steps is a set of independent updates
@@ -545,7 +624,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
         for (int i = 0; i < 16; ++i) T32[(base + i) * TLD + base + jj] = x[i];
       }
-      __syncthreads();
+      named_bar_sync(1, 256);
 #pragma unroll 1
       for (int L = 1; L < 4; ++L) {  // block sub-diagonal L: (I, J) = (J + L, J)
         // two warps per block, one per 8-column n-tile: M = A[I, J..I-1] T[J..I-1, J],
@@ -598,15 +677,39 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           To[(g + 8) * TLD] = -(acc[0][2] + acc[1][2] + acc[2][2]);
           To[(g + 8) * TLD + 1] = -(acc[0][3] + acc[1][3] + acc[2][3]);
         }
-        __syncthreads();
+        named_bar_sync(1, 256);
       }
+    } else {
+      // this warp: lane quarter qd, tokens h8 * 32 .. h8 * 32 + 31 of X'^T
+      if (!mbar_wait(xo_bar, (xo_issued - 1) & 1u)) wt.on_timeout();
+      tc_fence_after();
+      const int h8 = (warp >> 2) - 2;
+      float y[2][16];
+      tmem_ld16(tb + lane_base + TM_U + h8 * 32, y[0]);
+      tmem_ld16(tb + lane_base + TM_U + h8 * 32 + 16, y[1]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int tt0 = h8 * 32 + hh * 16;
+        uint32_t hi[8], lo[8];
+        pack_split16(y[hh], hi, lo);
+        tmem_st8(tb + lane_base + TM_UHI + tt0 / 2, hi);
+        tmem_st8(tb + lane_base + TM_ULO + tt0 / 2, lo);
+      }
+      tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (*(volatile uint32_t*)s_flag) break;
+    {
+      const float* T32 = reinterpret_cast<const float*>(smem + SV_T32);
       for (int idx = tid; idx < 64 * 8; idx += kThreads) {
         const int j0 = (idx >> 6) * 8, i = idx & 63;  // lanes walk rows: distinct banks
         float x[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int j = j0 + e;
-          x[e] = j <= i ? T32[i * TLD + j] * s_beta[j] : 0.f;
+          x[e] = j <= i ? -(T32[i * TLD + j] * s_beta[j]) : 0.f;
         }
         const uint32_t o = off_kmaj(i, j0, 64);
         st8_split(smem + SM_Y + Y_TB_HI + o, smem + SM_Y + Y_TB_LO + o, x);
@@ -615,150 +718,66 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     fence_proxy_async_smem();
     __syncthreads();
 
-    // ---- P7 (pass B): Kbar = K e^Gam (single), Qhat = Q e^Gam, Khat = K e^(Gl - Gam)
-#pragma unroll
-    for (int g4 = 0; g4 < GPT; ++g4) {
-      const int cg = cg0 + g4;
-      float kx[8], qx[8], kb[8], qh[8], kh[8];
-      ld8(smem + SM_IN_K + cg * 1024 + t * 16, kx);
-      ld8(smem + SM_IN_Q + cg * 1024 + t * 16, qx);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int c = cg * 8 + e;
-        const float kv = valid ? kx[e] : 0.f, qv = valid ? qx[e] : 0.f;
-        const float eg = er[g4 * 8 + e] * s_erho[c];
-        kb[e] = kv * eg;
-        qh[e] = qv * eg;
-        kh[e] = kv * ec[g4 * 8 + e] * s_ecrho[c];
-      }
-      st8(smem + SM_X + X_KBAR + cg * 1024 + t * 16, kb);  // MN-major A (M = channel)
-      if (want_o)
-        st8_split(smem + SM_X + X_QH_HI + off_kmaj(t, cg * 8, 128),
-                  smem + SM_X + X_QH_LO + off_kmaj(t, cg * 8, 128), qh);  // K-major B
-      st8_split(smem + SM_X + X_KH_HI + cg * 1024 + t * 16,
-                smem + SM_X + X_KH_LO + cg * 1024 + t * 16, kh);  // MN-major B (N = channel)
+    // ---- P8: prefetch chunk ci+1 (the q, k, g, v tiles are consumed; warps 1-4
+    // issue one tile each); U^T = X'^T (-TB)^T with split operands
+    if (ci + 1 < nchunks) {
+      if (lane == 0 && warp >= 1 && warp <= 4) issue_tma_part(ci + 1, warp - 1);
+      ++tma_issued;
     }
-    fence_proxy_async_smem();
-    __syncthreads();
-
-    // ---- P8: W^T = Kbar^T TB^T, U~^T = V^T TB^T
     if (tid == 0) {
       tc_fence_after();
       const uint32_t tbh = sbase + SM_Y + Y_TB_HI, tbl = sbase + SM_Y + Y_TB_LO;
+      const uint32_t xa[3] = {TM_UHI, TM_UHI, TM_ULO}, bt[3] = {tbh, tbl, tbh};
 #pragma unroll
-      for (int kk = 0; kk < C / 16; ++kk)
-        mma_ss(tb + TM_O, (smem_desc(sbase + SM_X + X_KBAR, 128, 1024) + (uint64_t)(kk * 16)),
-               (smem_desc(tbh, 128, 1024) + (uint64_t)(kk * 16)), idesc_mnk, kk > 0);
-      if (!zero_v)
-#pragma unroll
-      for (int pr = 0; pr < 2; ++pr)
+      for (int pr = 0; pr < 3; ++pr)
 #pragma unroll
         for (int kk = 0; kk < C / 16; ++kk)
-          mma_ss(tb + TM_U, (smem_desc(sbase + SM_IN_V, 128, 1024) + (uint64_t)(kk * 16)),
-                 smem_desc((pr ? tbl : tbh) + kk * 256, 128, 1024), idesc_mnk,
-                 (pr | kk) != 0);
+          mma_ts(tb + TM_U, tb + xa[pr] + kk * 8,
+                 (smem_desc(bt[pr], 128, 1024) + (uint64_t)(kk * 16)), idesc_sq, (pr | kk) != 0);
       mma_commit(wt.mma_bar);
     }
     if (wt.wait_mma()) break;
 
-    // ---- P9: prefetch chunk ci+1; W^T to shared memory as an MN-major B (N = token)
-    if (tid == 0 && ci + 1 < nchunks) issue_tma(ci + 1);
-    if (ci + 1 < nchunks) beta_next = load_beta(ci + 1);
+    // ---- P11: U^T split into TMEM (A operand of the last products)
     {
-      // W^T lane = key channel c; store -W as rows 0..63 (token) of the K-major
-      // operand [-W; Qhat_hi], then clear the accumulator for O^T
-      const int c = row;
-      float w[TCOL];
-      tmem_ld16(tb + lane_base + TM_O + cq * TCOL, w);
-      tmem_wait_ld();
-#pragma unroll
-      for (int e = 0; e < TCOL; ++e) {
-        const int tt = cq * TCOL + e;
-        *reinterpret_cast<__nv_bfloat16*>(smem + SM_X + X_WT + off_kmaj(tt, c, 128)) =
-            __float2bfloat16_rn(-w[e]);
-      }
-      uint32_t z[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) z[e] = 0u;
-      tmem_st16(tb + lane_base + TM_O + cq * TCOL, z);
-      tmem_wait_st();
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-
-    // ---- P10: [U^T | O^T] += S^T [-W; Qhat]^T  (U^T starts from U~^T, O^T from 0):
-    // S split against [-W; Qhat_hi] as N = 128 products, plus S_hi Qhat_lo^T
-    if (tid == 0) {
-      tc_fence_after();
-      const uint64_t bw = smem_desc(sbase + SM_X + X_WT, 128, 2048);      // [-W; Qhat_hi]
-      const uint64_t bl = smem_desc(sbase + SM_X + X_QH_LO, 128, 2048);   // Qhat_lo
-#pragma unroll
-      for (int pr = 0; pr < 2; ++pr)
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ts(tb + TM_U, tb + (pr ? TM_SLO : TM_SHI) + kk * 8, bw + (uint64_t)(kk * 16),
-                 idesc_sw, ((pr | kk) != 0) || !zero_v);  // with v = 0, U = -W S
-      if (want_o)
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ts(tb + TM_O, tb + TM_SHI + kk * 8, bl + (uint64_t)(kk * 16), idesc_sq, 1);
-      mma_commit(wt.mma_bar);
-    }
-    if (wt.wait_mma()) break;
-
-    // ---- P11: U^T split into TMEM (A operand); S^T <- S^T diag(e^Gam_last)
-    {
-      float u[TCOL], sv[SCOL / 16][16];
+      float u[TCOL];
       tmem_ld16(tb + lane_base + TM_U + cq * TCOL, u);
-#pragma unroll
-      for (int q4 = 0; q4 < SCOL / 16; ++q4)
-        tmem_ld16(tb + lane_base + TM_S + cq * SCOL + q4 * 16, sv[q4]);
       tmem_wait_ld();
-      {
-        uint32_t hi[8], lo[8];
-        pack_split16(u, hi, lo);
-        tmem_st8(tb + lane_base + TM_UHI + cq * (TCOL / 2), hi);
-        tmem_st8(tb + lane_base + TM_ULO + cq * (TCOL / 2), lo);
-      }
-#pragma unroll
-      for (int q4 = 0; q4 < SCOL / 16; ++q4) {
-        const int c0 = cq * SCOL + q4 * 16;
-        uint32_t w[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(sv[q4][e] * s_gamc[c0 + e]);
-        tmem_st16(tb + lane_base + TM_S + c0, w);
-      }
+      uint32_t hi[8], lo[8];
+      pack_split16(u, hi, lo);
+      tmem_st8(tb + lane_base + TM_UHI + cq * (TCOL / 2), hi);
+      tmem_st8(tb + lane_base + TM_ULO + cq * (TCOL / 2), lo);
       tmem_wait_st();
     }
     tc_fence_before();
     __syncthreads();
 
-    // ---- P12: O^T += U^T Aqk^T; S^T += U^T Khat (all split)
+    // ---- P12: O^T += U^T Aqk^T; S'^T += U^T Ck (all split; Ck is an MN-major B
+    // with N = key channel)
     if (tid == 0) {
       tc_fence_after();
       const uint32_t ah = sbase + SM_Y + Y_AQK_HI, al = sbase + SM_Y + Y_AQK_LO;
-      const uint32_t kh = sbase + SM_X + X_KH_HI, kl = sbase + SM_X + X_KH_LO;
+      const uint32_t kh = sbase + SM_X + X_CK_HI, kl = sbase + SM_X + X_CK_LO;
       const uint32_t ua[3] = {TM_UHI, TM_UHI, TM_ULO};
       const uint32_t bq[3] = {ah, al, ah}, bk[3] = {kh, kl, kh};
       if (want_o)
 #pragma unroll
+        for (int pr = 0; pr < 3; ++pr)
+#pragma unroll
+          for (int kk = 0; kk < C / 16; ++kk)
+            mma_ts(tb + TM_O, tb + ua[pr] + kk * 8,
+                   (smem_desc(bq[pr], 128, 1024) + (uint64_t)(kk * 16)), idesc_sq, 1);
+#pragma unroll
       for (int pr = 0; pr < 3; ++pr)
 #pragma unroll
         for (int kk = 0; kk < C / 16; ++kk)
-          mma_ts(tb + TM_O, tb + ua[pr] + kk * 8, (smem_desc(bq[pr], 128, 1024) + (uint64_t)(kk * 16)),
-                 idesc_sq, 1);
-#pragma unroll
-      for (int pr = 0; pr < 3; ++pr)
-#pragma unroll
-        for (int kk = 0; kk < C / 16; ++kk)
-          mma_ts(tb + TM_S, tb + ua[pr] + kk * 8, (smem_desc(bk[pr], 128, 1024) + (uint64_t)(kk * 16)),
-                 idesc_s, 1);
+          mma_ts(tb + TM_S, tb + ua[pr] + kk * 8,
+                 (smem_desc(bk[pr], 2048, 128) + (uint64_t)(kk * 256)), idesc_s, 1);
       mma_commit(wt.mma_bar);
     }
     if (wt.wait_mma()) break;
 
-    // ---- P13: outputs; refresh the bf16 copies of S^T
+    // ---- P13: outputs; S^T <- S'^T diag(e^Gam_last / c)
     {
       const int j = row;
       float o[TCOL], sv[SCOL / 16][16];
@@ -770,10 +789,10 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
       for (int q4 = 0; q4 < SCOL / 16; ++q4) {
         const int c0 = cq * SCOL + q4 * 16;
-        uint32_t hi[8], lo[8];
-        pack_split16(sv[q4], hi, lo);
-        tmem_st8(tb + lane_base + TM_SHI + c0 / 2, hi);
-        tmem_st8(tb + lane_base + TM_SLO + c0 / 2, lo);
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(sv[q4][e] * s_gamc[c0 + e]);
+        tmem_st16(tb + lane_base + TM_S + c0, w);
       }
       if (want_o && nv == C) {
         // full chunk: stage [token][value channel] in X, one bulk tensor store below
@@ -836,6 +855,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     for (uint32_t ph = wt.tma_waited; ph < tma_issued; ++ph)
       mbar_wait(wt.tma_bar, ph & 1u, 20000000ll);
     mbar_wait(wt.mma_bar, wt.mma_phase ^ 1u, 20000000ll);
+    if (xo_issued) mbar_wait(xo_bar, (xo_issued - 1) & 1u, 20000000ll);
   }
   tc_fence_before();
   __syncthreads();
