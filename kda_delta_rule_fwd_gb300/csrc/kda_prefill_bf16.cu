@@ -326,6 +326,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     mbar_init(&bars[0], 1);
     mbar_init(&bars[1], 1);
     mbar_init(&bars[2], 1);
+    mbar_init(&bars[3], 1);
     *s_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tm_q);
@@ -366,16 +367,25 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   // parts are issued from different warps so their issue latencies overlap
   // (a tile's bytes may land before the barrier is armed: the transaction count
   // only has to balance when the arrival comes)
+  // The g tile completes on its own barrier: the next chunk's cumulative sum is
+  // issued as soon as it lands, ahead of the q, k and v tiles' consumers.
+  uint64_t* g_bar = &bars[3];
+  uint32_t g_issued = 0, g_waited = 0;  // g_waited: thread 0's count
   auto issue_tma_part = [&](int chunk, int part) {
     const int32_t y = (int32_t)(t0 + (int64_t)chunk * C);
     const int32_t z = h * (D / 8);
-    if (part == 0) mbar_arrive_expect_tx(wt.tma_bar, 4 * 16384);
+    uint64_t* bar = part == 2 ? g_bar : wt.tma_bar;
+    if (part == 0) mbar_arrive_expect_tx(wt.tma_bar, 3 * 16384);
+    if (part == 2) mbar_arrive_expect_tx(g_bar, 16384);
     const CUtensorMap* m = part == 0 ? &tm_q : part == 1 ? &tm_k : part == 2 ? &tm_g : &tm_v;
-    tma_load_3d(smem + SM_IN_Q + part * 16384, m, 0, y, z, wt.tma_bar);
+    tma_load_3d(smem + SM_IN_Q + part * 16384, m, 0, y, z, bar);
   };
   if (tid == 0 && nchunks > 0)
     for (int part = 0; part < 4; ++part) issue_tma_part(0, part);
-  if (nchunks > 0) ++tma_issued;
+  if (nchunks > 0) {
+    ++tma_issued;
+    ++g_issued;
+  }
   // raw bf16 bits of beta for a chunk, loaded a chunk ahead and converted only
   // when used (no instruction waits on the load meanwhile); tokens past the
   // sequence end read as 0
@@ -418,6 +428,22 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   bool range_err = false;
   // log2 of the chunk's per-channel reference c (an integer, clamped)
   auto ref_log2 = [](float rho) { return fminf(fmaxf(rintf(rho * kLog2e), -kRefExp2), kRefExp2); };
+  // thread 0: once the g tile of `chunk` has landed, Gam (rows 0..63 and again
+  // 64..127) = [L; L] G with G the g tile as an MN-major B, committed to mma_bar;
+  // returns false if the wait ran out
+  auto issue_cumsum = [&](int chunk) -> bool {
+    const bool ok = mbar_wait(g_bar, (uint32_t)chunk & 1u);
+    ++g_waited;
+    if (!ok) return false;
+    tc_fence_after();
+#pragma unroll
+    for (int kk = 0; kk < C / 16; ++kk)
+      mma_ss(tb + TM_ACC1, (smem_desc(sbase + SM_LL, 128, 1024) + (uint64_t)(kk * 16)),
+             (smem_desc(sbase + SM_IN_G, 128, 1024) + (uint64_t)(kk * 16)), idesc_cum, kk > 0);
+    mma_commit(wt.mma_bar);
+    return true;
+  };
+  if (tid == 0 && nchunks > 0 && !issue_cumsum(0)) wt.on_timeout();
 
 #pragma unroll 1
   for (int ci = 0; ci < nchunks; ++ci) {
@@ -425,19 +451,11 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int nv = (int)(len - cs < C ? len - cs : C);
     const int rho_t = nv - 1 < 31 ? nv - 1 : 31;
 
-    // ---- P1: beta, wait for the tiles, cumulative log-decay on the tensor core
+    // ---- P1: beta; wait for the q, k, v tiles and for the cumulative log-decay
+    // (issued at the end of the previous chunk, or before the loop)
     if (tid < C) s_beta[tid] = __uint_as_float(beta_bits << 16);
     if (ci + 1 < nchunks) beta_bits = load_beta_bits(ci + 1);
     if (wt.wait_tma()) break;
-    if (tid == 0) {
-      tc_fence_after();
-      // Gam (rows 0..63 and again 64..127) = [L; L] G, G = the g tile as an MN-major B
-#pragma unroll
-      for (int kk = 0; kk < C / 16; ++kk)
-        mma_ss(tb + TM_ACC1, (smem_desc(sbase + SM_LL, 128, 1024) + (uint64_t)(kk * 16)),
-               (smem_desc(sbase + SM_IN_G, 128, 1024) + (uint64_t)(kk * 16)), idesc_cum, kk > 0);
-      mma_commit(wt.mma_bar);
-    }
     if (wt.wait_mma()) break;
 
     // ---- P3 (pass A): per-channel reference, the decayed key/query operands
@@ -723,6 +741,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (ci + 1 < nchunks) {
       if (lane == 0 && warp >= 1 && warp <= 4) issue_tma_part(ci + 1, warp - 1);
       ++tma_issued;
+      ++g_issued;
     }
     if (tid == 0) {
       tc_fence_after();
@@ -777,7 +796,9 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     if (wt.wait_mma()) break;
 
-    // ---- P13: outputs; S^T <- S'^T diag(e^Gam_last / c)
+    // ---- P13: next chunk's cumulative log-decay (ACC1 and U are free); outputs;
+    // S^T <- S'^T diag(e^Gam_last / c)
+    if (tid == 0 && ci + 1 < nchunks && !issue_cumsum(ci + 1)) wt.on_timeout();
     {
       const int j = row;
       float o[TCOL], sv[SCOL / 16][16];
@@ -856,6 +877,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       mbar_wait(wt.tma_bar, ph & 1u, 20000000ll);
     mbar_wait(wt.mma_bar, wt.mma_phase ^ 1u, 20000000ll);
     if (xo_issued) mbar_wait(xo_bar, (xo_issued - 1) & 1u, 20000000ll);
+    for (uint32_t ph = g_waited; ph < g_issued; ++ph) mbar_wait(g_bar, ph & 1u, 20000000ll);
   }
   tc_fence_before();
   __syncthreads();
