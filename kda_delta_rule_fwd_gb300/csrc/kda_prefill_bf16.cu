@@ -63,7 +63,7 @@ constexpr uint32_t SM_IN_V = 49152;
 constexpr uint32_t SV_AT = 0, SV_T32 = 17408, SV_M32 = 34304;
 constexpr int ALD = 68;  // row stride of A^T (float): fragment loads hit distinct banks
 constexpr int TLD = 66;  // row stride of T (float): 8-byte rows, few bank conflicts
-static_assert(SV_M32 + 3 * 256 * 4 <= SM_IN_V, "substitution scratch overlaps the v tile");
+static_assert(SV_M32 + 4 * 256 * 4 <= SM_IN_V, "substitution scratch overlaps the v tile");
 constexpr uint32_t SM_X = 65536;         // 96 KB: [R_K; R_Q] hi, lo (K-major), Ck hi, lo
 constexpr uint32_t X_R_HI = 0, X_R_LO = 32768, X_CK_HI = 65536, X_CK_LO = 81920;
 constexpr uint32_t X_OUT = 0;  // output staging for the bulk store, [64 tokens][128] (32 KB)
@@ -186,6 +186,46 @@ __device__ __forceinline__ void mma_tf32x3(float (&acc)[3][4], const float (&a)[
 // CTA-local named barrier over the first `count` threads (warps 0..count/32-1)
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// m16n8k8 fragments (see mma_tf32x3) read from float matrices in shared memory:
+// A rows r0.., columns k0.. of a row-major matrix (row stride ld), of A stored
+// transposed (AT[k][r] = A[r][k], row stride ALD), and B rows k0.., columns n0..
+__device__ __forceinline__ void load_a(const float* M, int ld, int r0, int k0, int g, int t4,
+                                       float (&a)[4]) {
+  a[0] = M[(r0 + g) * ld + k0 + t4];
+  a[1] = M[(r0 + g + 8) * ld + k0 + t4];
+  a[2] = M[(r0 + g) * ld + k0 + t4 + 4];
+  a[3] = M[(r0 + g + 8) * ld + k0 + t4 + 4];
+}
+__device__ __forceinline__ void load_a_t(const float* AT, int r0, int k0, int g, int t4,
+                                         float (&a)[4]) {
+  a[0] = AT[(k0 + t4) * ALD + r0 + g];
+  a[1] = AT[(k0 + t4) * ALD + r0 + g + 8];
+  a[2] = AT[(k0 + t4 + 4) * ALD + r0 + g];
+  a[3] = AT[(k0 + t4 + 4) * ALD + r0 + g + 8];
+}
+__device__ __forceinline__ void load_b(const float* M, int ld, int k0, int n0, int g, int t4,
+                                       float (&b)[2]) {
+  b[0] = M[(k0 + t4) * ld + n0 + g];
+  b[1] = M[(k0 + t4 + 4) * ld + n0 + g];
+}
+// zero the three partial accumulators of mma_tf32x3
+__device__ __forceinline__ void zero_acc(float (&acc)[3][4]) {
+#pragma unroll
+  for (int q = 0; q < 3; ++q)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) acc[q][r] = 0.f;
+}
+// C fragment (16 x 8 at columns c0 of a row-major matrix with row stride ld),
+// summed over the three partial products and scaled by `sign`
+__device__ __forceinline__ void store_c(float* Cm, int ld, int c0, const float (&acc)[3][4], int g,
+                                        int t4, float sign) {
+  const int c = c0 + 2 * t4;
+  Cm[g * ld + c] = sign * (acc[0][0] + acc[1][0] + acc[2][0]);
+  Cm[g * ld + c + 1] = sign * (acc[0][1] + acc[1][1] + acc[2][1]);
+  Cm[(g + 8) * ld + c] = sign * (acc[0][2] + acc[1][2] + acc[2][2]);
+  Cm[(g + 8) * ld + c + 1] = sign * (acc[0][3] + acc[1][3] + acc[2][3]);
 }
 
 // hi and lo parts of 16 values, packed two per 32-bit word
@@ -643,59 +683,58 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int i = 0; i < 16; ++i) T32[(base + i) * TLD + base + jj] = x[i];
       }
       named_bar_sync(1, 256);
-#pragma unroll 1
-      for (int L = 1; L < 4; ++L) {  // block sub-diagonal L: (I, J) = (J + L, J)
-        // two warps per block, one per 8-column n-tile: M = A[I, J..I-1] T[J..I-1, J],
-        // then T[I, J] = -T[I, I] M, as m16n8k8 tf32 products with 3-term splitting.
-        // Each warp only ever reads back its own columns of M.
-        if (warp < 2 * (4 - L)) {
-          const int J = warp >> 1, nt = warp & 1, I = J + L, g = lane >> 2, t4 = lane & 3;
-          float* Mw = M32 + J * 256;
-          float acc[3][4];
+      // 32 x 32 diagonal blocks: T[I, J] = -T[I, I] A[I, J] T[J, J] for (I, J) = (1, 0)
+      // and (3, 2), two warps per block (one per 8-column n-tile), as m16n8k8 tf32
+      // products with 3-term splitting; each warp only reads back its own columns.
+      const int g = lane >> 2, t4 = lane & 3;
+      float af[4], bf[2], acc[3][4];
+      if (warp < 4) {
+        const int J = (warp >> 1) * 2, I = J + 1, nt = warp & 1;
+        float* Mw = M32 + J * 256;
+        zero_acc(acc);
 #pragma unroll
-          for (int q = 0; q < 3; ++q)
+        for (int ks = 0; ks < 2; ++ks) {
+          const int k0 = J * 16 + ks * 8;
+          load_a_t(AT, I * 16, k0, g, t4, af);
+          load_b(T32, TLD, k0, J * 16 + nt * 8, g, t4, bf);
+          mma_tf32x3(acc, af, bf);
+        }
+        store_c(Mw, 16, nt * 8, acc, g, t4, 1.f);
+        __syncwarp();
+        zero_acc(acc);
 #pragma unroll
-            for (int r = 0; r < 4; ++r) acc[q][r] = 0.f;
-          for (int kb = J; kb < I; ++kb)
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-              const int k0 = kb * 16 + ks * 8;
-              const float af[4] = {AT[(k0 + t4) * ALD + I * 16 + g],
-                                   AT[(k0 + t4) * ALD + I * 16 + g + 8],
-                                   AT[(k0 + t4 + 4) * ALD + I * 16 + g],
-                                   AT[(k0 + t4 + 4) * ALD + I * 16 + g + 8]};
-              const float bf[2] = {T32[(k0 + t4) * TLD + J * 16 + nt * 8 + g],
-                                   T32[(k0 + t4 + 4) * TLD + J * 16 + nt * 8 + g]};
-              mma_tf32x3(acc, af, bf);
-            }
-          {
-            const int c = nt * 8 + 2 * t4;
-            Mw[g * 16 + c] = acc[0][0] + acc[1][0] + acc[2][0];
-            Mw[g * 16 + c + 1] = acc[0][1] + acc[1][1] + acc[2][1];
-            Mw[(g + 8) * 16 + c] = acc[0][2] + acc[1][2] + acc[2][2];
-            Mw[(g + 8) * 16 + c + 1] = acc[0][3] + acc[1][3] + acc[2][3];
-          }
-          __syncwarp();
-#pragma unroll
-          for (int q = 0; q < 3; ++q)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) acc[q][r] = 0.f;
+        for (int ks = 0; ks < 2; ++ks) {
+          load_a(T32, TLD, I * 16, I * 16 + ks * 8, g, t4, af);
+          load_b(Mw, 16, ks * 8, nt * 8, g, t4, bf);
+          mma_tf32x3(acc, af, bf);
+        }
+        store_c(T32 + (I * 16) * TLD + J * 16, TLD, nt * 8, acc, g, t4, -1.f);
+      }
+      named_bar_sync(1, 256);
+      // lower-left 32 x 32 block: M = A[2..3, 0..1] T[0..1, 0..1], then
+      // T[2..3, 0..1] = -T[2..3, 2..3] M; warp = (row block i, column block j, n-tile)
+      {
+        const int i = warp >> 2, j = (warp >> 1) & 1, nt = warp & 1;
+        zero_acc(acc);
+        for (int kb = j; kb < 2; ++kb)
 #pragma unroll
           for (int ks = 0; ks < 2; ++ks) {
-            const float* Ti = T32 + (I * 16) * TLD + I * 16 + ks * 8;
-            const float af[4] = {Ti[g * TLD + t4], Ti[(g + 8) * TLD + t4], Ti[g * TLD + t4 + 4],
-                                 Ti[(g + 8) * TLD + t4 + 4]};
-            const float bf[2] = {Mw[(ks * 8 + t4) * 16 + nt * 8 + g],
-                                 Mw[(ks * 8 + t4 + 4) * 16 + nt * 8 + g]};
+            const int k0 = kb * 16 + ks * 8;
+            load_a_t(AT, (2 + i) * 16, k0, g, t4, af);
+            load_b(T32, TLD, k0, j * 16 + nt * 8, g, t4, bf);
             mma_tf32x3(acc, af, bf);
           }
-          float* To = T32 + (I * 16) * TLD + J * 16 + nt * 8 + 2 * t4;
-          To[g * TLD] = -(acc[0][0] + acc[1][0] + acc[2][0]);
-          To[g * TLD + 1] = -(acc[0][1] + acc[1][1] + acc[2][1]);
-          To[(g + 8) * TLD] = -(acc[0][2] + acc[1][2] + acc[2][2]);
-          To[(g + 8) * TLD + 1] = -(acc[0][3] + acc[1][3] + acc[2][3]);
-        }
+        store_c(M32 + (i * 2 + j) * 256, 16, nt * 8, acc, g, t4, 1.f);
         named_bar_sync(1, 256);
+        zero_acc(acc);
+        for (int kb = 0; kb <= i; ++kb)
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks) {
+            load_a(T32, TLD, (2 + i) * 16, (2 + kb) * 16 + ks * 8, g, t4, af);
+            load_b(M32 + (kb * 2 + j) * 256, 16, ks * 8, nt * 8, g, t4, bf);
+            mma_tf32x3(acc, af, bf);
+          }
+        store_c(T32 + ((2 + i) * 16) * TLD + j * 16, TLD, nt * 8, acc, g, t4, -1.f);
       }
     } else {
       // this warp: lane quarter qd, tokens h8 * 32 .. h8 * 32 + 31 of X'^T
