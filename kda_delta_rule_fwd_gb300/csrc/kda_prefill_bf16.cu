@@ -602,66 +602,48 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     tc_fence_before();
     __syncthreads();
-    // [X' | O]^T = S'^T [R_K; R_Q]^T as N = 128 products over the adjacent U and O
-    // accumulators (K = key channel, three split products), then X'^T -= V^T
-    // as V^T (-I) (V exact in bf16; A = the v tile as an MN-major operand)
-    if (tid == 0) {
+    ++xo_issued;  // thread 256 commits to xo_bar once per chunk (below)
+    // From here to the join below the two halves of the CTA take different paths
+    // (waits that run out only raise the flag; the CTA leaves after the join).
+    //   warps 0-7:  P5 (A and Aqk from [Akk; Aqk]) and P6 (T = (I + A)^-1)
+    //   warps 8-15: thread 256 issues the products with S' once [Akk; Aqk] is done
+    //               (the two streams then do not interleave on the tensor pipe),
+    //               then the warps split X'
+    if (warp < 8) {
+      if (!mbar_wait(wt.mma_bar, wt.mma_phase)) wt.on_timeout();
       tc_fence_after();
-      const uint32_t rh = sbase + SM_X + X_R_HI, rl = sbase + SM_X + X_R_LO;
-      const uint32_t sa[3] = {TM_SHI, TM_SHI, TM_SLO};
-      const uint32_t bk[3] = {rh, rl, rh};
-      const uint32_t idesc_xo = want_o ? idesc_bf16(128, 128, 0, 0) : idesc_kk;
+      // ---- P5: A = strict_lower(beta Akk) (float32, for the substitution), Aqk split
+      {
+        float a[2][TCOL];
+        tmem_ld16(tb + lane_base + TM_ACC1 + cq * 32, a[0]);
+        tmem_ld16(tb + lane_base + TM_ACC1 + cq * 32 + 16, a[1]);
+        tmem_wait_ld();
+        if (row < 64) {
+          const int i = row;
+          const float bi = s_beta[i];
+          float* AT = reinterpret_cast<float*>(smem + SV_AT);  // AT[j][i] = A[i][j]
 #pragma unroll
-      for (int pr = 0; pr < 3; ++pr)
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ts(tb + TM_U, tb + sa[pr] + kk * 8,
-                 (smem_desc(bk[pr], 128, 2048) + (uint64_t)(kk * 16)), idesc_xo, (pr | kk) != 0);
-      if (!zero_v)
-#pragma unroll
-        for (int kk = 0; kk < C / 16; ++kk)
-          mma_ss(tb + TM_U, (smem_desc(sbase + SM_IN_V, 128, 1024) + (uint64_t)(kk * 16)),
-                 (smem_desc(sbase + SM_NEGI, 128, 1024) + (uint64_t)(kk * 16)), idesc_mnk, 1);
-      mma_commit(xo_bar);
-    }
-    ++xo_issued;
-    if (wt.wait_mma()) break;
-
-    // ---- P5: A = strict_lower(beta Akk) (float32, for the substitution), Aqk split
-    {
-      float a[TCOL];
-      tmem_ld16(tb + lane_base + TM_ACC1 + cq * TCOL, a);
-      tmem_wait_ld();
-      if (row < 64) {
-        const int i = row;
-        const float bi = s_beta[i];
-        float* AT = reinterpret_cast<float*>(smem + SV_AT);  // AT[j][i] = A[i][j]
-#pragma unroll
-        for (int e = 0; e < TCOL; ++e) {
-          const int j = cq * TCOL + e;
-          AT[j * ALD + i] = j < i ? bi * a[e] : 0.f;
-        }
-      } else if (want_o) {
-        const int i = row - 64;
-#pragma unroll
-        for (int e8 = 0; e8 < TCOL / 8; ++e8) {
-          float x[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int j = cq * TCOL + e8 * 8 + e;
-            x[e] = j <= i ? a[e8 * 8 + e] : 0.f;
+          for (int e = 0; e < 32; ++e) {
+            const int j = cq * 32 + e;
+            AT[j * ALD + i] = j < i ? bi * a[e >> 4][e & 15] : 0.f;
           }
-          const uint32_t o = off_kmaj(i, cq * TCOL + e8 * 8, 64);
-          st8_split(smem + SM_Y + Y_AQK_HI + o, smem + SM_Y + Y_AQK_LO + o, x);
+        } else if (want_o) {
+          const int i = row - 64;
+#pragma unroll
+          for (int e8 = 0; e8 < 4; ++e8) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int j = cq * 32 + e8 * 8 + e;
+              x[e] = j <= i ? a[e8 >> 1][(e8 & 1) * 8 + e] : 0.f;
+            }
+            const uint32_t o = off_kmaj(i, cq * 32 + e8 * 8, 64);
+            st8_split(smem + SM_Y + Y_AQK_HI + o, smem + SM_Y + Y_AQK_LO + o, x);
+          }
         }
       }
-    }
-    tc_fence_before();
-    __syncthreads();
-
-    // ---- P6: warps 0-7: T = (I + A)^-1 by blocks of 16 (named barrier 1);
-    // warps 8-15: X'^T split into TMEM; then -TB = -T diag(beta) split
-    if (warp < 8) {
+      named_bar_sync(1, 256);
+      // ---- P6 (warps 0-7): T = (I + A)^-1 by blocks of 16 (named barrier 1)
       const float* AT = reinterpret_cast<const float*>(smem + SV_AT);  // AT[j][i]
       float* T32 = reinterpret_cast<float*>(smem + SV_T32);
       float* M32 = reinterpret_cast<float*>(smem + SV_M32);
@@ -737,6 +719,34 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         store_c(T32 + ((2 + i) * 16) * TLD + j * 16, TLD, nt * 8, acc, g, t4, -1.f);
       }
     } else {
+      // thread 256: [X' | O]^T = S'^T [R_K; R_Q]^T as N = 128 products over the
+      // adjacent U and O accumulators (K = key channel, three split products), then
+      // X'^T -= V^T as V^T (-I) (V exact in bf16; A = the v tile as an MN-major
+      // operand).  Committed even when the wait ran out, so xo_bar still arrives.
+      if (tid == 256) {
+        const bool ok = mbar_wait(wt.mma_bar, wt.mma_phase);
+        if (!ok) wt.on_timeout();
+        tc_fence_after();
+        if (ok) {
+          const uint32_t rh = sbase + SM_X + X_R_HI, rl = sbase + SM_X + X_R_LO;
+          const uint32_t sa[3] = {TM_SHI, TM_SHI, TM_SLO};
+          const uint32_t bk[3] = {rh, rl, rh};
+          const uint32_t idesc_xo = want_o ? idesc_bf16(128, 128, 0, 0) : idesc_kk;
+#pragma unroll
+          for (int pr = 0; pr < 3; ++pr)
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_ts(tb + TM_U, tb + sa[pr] + kk * 8,
+                     (smem_desc(bk[pr], 128, 2048) + (uint64_t)(kk * 16)), idesc_xo,
+                     (pr | kk) != 0);
+          if (!zero_v)
+#pragma unroll
+            for (int kk = 0; kk < C / 16; ++kk)
+              mma_ss(tb + TM_U, (smem_desc(sbase + SM_IN_V, 128, 1024) + (uint64_t)(kk * 16)),
+                     (smem_desc(sbase + SM_NEGI, 128, 1024) + (uint64_t)(kk * 16)), idesc_mnk, 1);
+        }
+        mma_commit(xo_bar);
+      }
       // this warp: lane quarter qd, tokens h8 * 32 .. h8 * 32 + 31 of X'^T
       if (!mbar_wait(xo_bar, (xo_issued - 1) & 1u)) wt.on_timeout();
       tc_fence_after();
@@ -755,6 +765,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       }
       tmem_wait_st();
     }
+    wt.mma_phase ^= 1u;  // [Akk; Aqk] consumed (waited above by warps 0-7 and thread 256)
     tc_fence_before();
     __syncthreads();
     if (*(volatile uint32_t*)s_flag) break;
