@@ -28,8 +28,9 @@
 //
 // One CTA (512 threads) owns one (sequence, head) chain and walks its chunks
 // in order; the inputs of chunk n+1 are fetched by TMA while chunk n's state
-// update runs.  During the substitution (warps 0-7) warps 8-15 split X.  Each mbarrier wait is bounded: on expiry the CTA latches
-// KDA_ERR_DEVICE_TIMEOUT, drains its in-flight copies, frees TMEM and exits.
+// update runs.  During the substitution (warps 0-7) warps 8-15 split X'.  Each
+// mbarrier wait is bounded: on expiry the CTA latches KDA_ERR_DEVICE_TIMEOUT,
+// drains its in-flight copies, frees TMEM and exits.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -228,6 +229,43 @@ __device__ __forceinline__ void store_c(float* Cm, int ld, int c0, const float (
   Cm[(g + 8) * ld + c + 1] = sign * (acc[0][3] + acc[1][3] + acc[2][3]);
 }
 
+// -T diag(beta) in the K-major TB operand (rows = token i, K = token j), written
+// by the producers of T: one value, or two values of adjacent columns (j even)
+__device__ __forceinline__ void store_tb1(unsigned char* tb_hi, unsigned char* tb_lo, int i, int j,
+                                          float v) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  const uint32_t o = off_kmaj(i, j, 64);
+  *reinterpret_cast<__nv_bfloat16*>(tb_hi + o) = h;
+  *reinterpret_cast<__nv_bfloat16*>(tb_lo + o) = __float2bfloat16_rn(v - __bfloat162float(h));
+}
+__device__ __forceinline__ void store_tb2(unsigned char* tb_hi, unsigned char* tb_lo, int i, int j,
+                                          float v0, float v1) {
+  uint32_t hi, lo;
+  split_pack2(v0, v1, hi, lo);
+  const uint32_t o = off_kmaj(i, j, 64);
+  *reinterpret_cast<uint32_t*>(tb_hi + o) = hi;
+  *reinterpret_cast<uint32_t*>(tb_lo + o) = lo;
+}
+// T block fragment of mma_tf32x3 (sign applied) to T32 and, scaled by -beta of
+// its columns, to TB
+__device__ __forceinline__ void store_t_block(float* T32, int ld, int r0, int c0,
+                                              const float (&acc)[3][4], int g, int t4, float sign,
+                                              const float* beta, unsigned char* tb_hi,
+                                              unsigned char* tb_lo) {
+  const int c = c0 + 2 * t4;
+  const float v00 = sign * (acc[0][0] + acc[1][0] + acc[2][0]);
+  const float v01 = sign * (acc[0][1] + acc[1][1] + acc[2][1]);
+  const float v10 = sign * (acc[0][2] + acc[1][2] + acc[2][2]);
+  const float v11 = sign * (acc[0][3] + acc[1][3] + acc[2][3]);
+  T32[(r0 + g) * ld + c] = v00;
+  T32[(r0 + g) * ld + c + 1] = v01;
+  T32[(r0 + g + 8) * ld + c] = v10;
+  T32[(r0 + g + 8) * ld + c + 1] = v11;
+  const float b0 = -beta[c], b1 = -beta[c + 1];
+  store_tb2(tb_hi, tb_lo, r0 + g, c, v00 * b0, v01 * b1);
+  store_tb2(tb_hi, tb_lo, r0 + g + 8, c, v10 * b0, v11 * b1);
+}
+
 // hi and lo parts of 16 values, packed two per 32-bit word
 __device__ __forceinline__ void pack_split16(const float (&x)[16], uint32_t (&hi)[8],
                                              uint32_t (&lo)[8]) {
@@ -386,6 +424,9 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     for (int e = 0; e < 8; ++e) x[e] = (kb * 8 + e) <= (r & 63) ? 1.f : 0.f;
     st8(smem + SM_LL + off_kmaj(r, kb * 8, 64), x);
   }
+  // TB parts start at zero: its blocks above the diagonal are never written
+  for (int i = tid; i < 2 * 8192 / 16; i += kThreads)
+    reinterpret_cast<uint4*>(smem + SM_Y + Y_TB_HI)[i] = make_uint4(0u, 0u, 0u, 0u);
   for (int i = tid; i < 64 * 8; i += kThreads) {  // -I, rows = N (token), K = token
     const int r = i >> 3, kb = i & 7;
     float x[8];
@@ -605,7 +646,8 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     ++xo_issued;  // thread 256 commits to xo_bar once per chunk (below)
     // From here to the join below the two halves of the CTA take different paths
     // (waits that run out only raise the flag; the CTA leaves after the join).
-    //   warps 0-7:  P5 (A and Aqk from [Akk; Aqk]) and P6 (T = (I + A)^-1)
+    //   warps 0-7:  P5 (A and Aqk from [Akk; Aqk]) and P6 (T = (I + A)^-1, whose
+    //               producers also write -T diag(beta), split, into the TB operand)
     //   warps 8-15: thread 256 issues the products with S' once [Akk; Aqk] is done
     //               (the two streams then do not interleave on the tensor pipe),
     //               then the warps split X'
@@ -661,8 +703,12 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           for (int i = m + 1; i < 16; ++i)
             acc[i] = fmaf(-AT[(base + m) * ALD + base + i], x[m], acc[i]);
         }
+        const float nb = -s_beta[base + jj];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) T32[(base + i) * TLD + base + jj] = x[i];
+        for (int i = 0; i < 16; ++i) {
+          T32[(base + i) * TLD + base + jj] = x[i];
+          store_tb1(smem + SM_Y + Y_TB_HI, smem + SM_Y + Y_TB_LO, base + i, base + jj, x[i] * nb);
+        }
       }
       named_bar_sync(1, 256);
       // 32 x 32 diagonal blocks: T[I, J] = -T[I, I] A[I, J] T[J, J] for (I, J) = (1, 0)
@@ -690,7 +736,8 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           load_b(Mw, 16, ks * 8, nt * 8, g, t4, bf);
           mma_tf32x3(acc, af, bf);
         }
-        store_c(T32 + (I * 16) * TLD + J * 16, TLD, nt * 8, acc, g, t4, -1.f);
+        store_t_block(T32, TLD, I * 16, J * 16 + nt * 8, acc, g, t4, -1.f, s_beta,
+                      smem + SM_Y + Y_TB_HI, smem + SM_Y + Y_TB_LO);
       }
       named_bar_sync(1, 256);
       // lower-left 32 x 32 block: M = A[2..3, 0..1] T[0..1, 0..1], then
@@ -716,7 +763,8 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
             load_b(M32 + (kb * 2 + j) * 256, 16, ks * 8, nt * 8, g, t4, bf);
             mma_tf32x3(acc, af, bf);
           }
-        store_c(T32 + ((2 + i) * 16) * TLD + j * 16, TLD, nt * 8, acc, g, t4, -1.f);
+        store_t_block(T32, TLD, (2 + i) * 16, j * 16 + nt * 8, acc, g, t4, -1.f, s_beta,
+                      smem + SM_Y + Y_TB_HI, smem + SM_Y + Y_TB_LO);
       }
     } else {
       // thread 256: [X' | O]^T = S'^T [R_K; R_Q]^T as N = 128 products over the
@@ -766,25 +814,10 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       tmem_wait_st();
     }
     wt.mma_phase ^= 1u;  // [Akk; Aqk] consumed (waited above by warps 0-7 and thread 256)
+    fence_proxy_async_smem();  // TB, written by the substitution, is an MMA operand next
     tc_fence_before();
     __syncthreads();
     if (*(volatile uint32_t*)s_flag) break;
-    {
-      const float* T32 = reinterpret_cast<const float*>(smem + SV_T32);
-      for (int idx = tid; idx < 64 * 8; idx += kThreads) {
-        const int j0 = (idx >> 6) * 8, i = idx & 63;  // lanes walk rows: distinct banks
-        float x[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int j = j0 + e;
-          x[e] = j <= i ? -(T32[i * TLD + j] * s_beta[j]) : 0.f;
-        }
-        const uint32_t o = off_kmaj(i, j0, 64);
-        st8_split(smem + SM_Y + Y_TB_HI + o, smem + SM_Y + Y_TB_LO + o, x);
-      }
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
 
     // ---- P8: prefetch chunk ci+1 (the q, k, g, v tiles are consumed; warps 1-4
     // issue one tile each); U^T = X'^T (-TB)^T with split operands
