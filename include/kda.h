@@ -122,6 +122,31 @@ kda_status kda_decode(const kda_shape* s, const void* q, const void* k, const vo
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Decode step with per-sequence commit counts, for speculative decoding: the
+ * cached inputs of a step are replayed on chip, and only the state after the
+ * accepted prefix is kept ("Kimi K3 模型结构（7）：结构决定系统", section KDA
+ * 状态回滚: cache the small projected inputs instead of per-position state
+ * snapshots, and rebuild the accepted tokens' state by replay; replay and
+ * verification share one kernel).
+ *
+ * Same arguments as kda_decode, plus:
+ *   num_commit  device int32 [B]; for sequence n, the state written back to
+ *               `state` is the one after its first num_commit[n] tokens, each in
+ *               0..T_step (0 leaves the state unchanged: a verification pass;
+ *               T_step is kda_decode).  All T_step tokens are still applied in
+ *               order to produce their outputs.
+ *   out         device [B,T_step,H,dv] out_dtype, or NULL for no outputs (a pure
+ *               replay).
+ * A count outside 0..T_step latches KDA_ERR_INVALID_ARG in the workspace status
+ * word and leaves that sequence's state unchanged; its outputs are still
+ * written.  Host-checkable errors are those of kda_decode.
+ */
+kda_status kda_decode_commit(const kda_shape* s, const void* q, const void* k, const void* v,
+                             const void* g, const void* beta, const int32_t* num_commit,
+                             float* state, void* out, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/*
  * kda_fwd without a workspace, for callers that cannot allocate device memory:
  * code whose device memory is planned in full by a host framework before it
  * runs and that may not request more at call time, or bindings that cannot

@@ -71,6 +71,8 @@ def load(path: str | None = None):
         lib.kda_fwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         lib.kda_decode.restype = ctypes.c_int
         lib.kda_decode.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        lib.kda_decode_commit.restype = ctypes.c_int
+        lib.kda_decode_commit.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         lib.kda_read_device_status.restype = ctypes.c_int
         lib.kda_read_device_status.argtypes = [vp, vp]
         lib.kda_status_string.restype = ctypes.c_char_p
@@ -167,6 +169,30 @@ def decode(q, k, v, g, beta, state, *, scale=None, out_dtype=torch.float32, out=
                            _stream_ptr(stream))
     if rc != KDA_OK:
         raise KDAError(rc, "kda_decode")
+    return out
+
+
+def decode_commit(q, k, v, g, beta, state, num_commit, *, scale=None, out_dtype=torch.float32,
+                  out=None, want_out=True, workspace=None, stream=None):
+    """Decode step that keeps, per sequence n, the state after its first
+    ``num_commit[n]`` tokens (device int32 ``[B]``, each in 0..T_step) while every
+    token still produces its output (speculative-decode verification and replay).
+    Returns ``o [B,T_step,H,dv]``, or None when ``want_out`` is False."""
+    _check_inputs(q, k, v, g, beta)
+    if num_commit.dtype != torch.int32 or num_commit.numel() != q.shape[0]:
+        raise ValueError("num_commit must be int32 with one count per sequence")
+    shape = make_shape(q, v, scale=scale, out_dtype=out_dtype)
+    B, T, H, dk = q.shape
+    if out is None and want_out:
+        out = torch.empty(B, T, H, v.shape[-1], dtype=out_dtype, device=q.device)
+    if workspace is None:
+        workspace = new_workspace(shape, q.device)
+    rc = load().kda_decode_commit(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                  _ptr(beta), _ptr(num_commit), _ptr(state),
+                                  _ptr(out) if out is not None else None, _ptr(workspace),
+                                  workspace.numel(), _stream_ptr(stream))
+    if rc != KDA_OK:
+        raise KDAError(rc, "kda_decode_commit")
     return out
 
 

@@ -106,17 +106,21 @@ kda_status kda_fwd(const kda_shape* s, const void* q, const void* k, const void*
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
-kda_status kda_decode(const kda_shape* s, const void* q, const void* k, const void* v,
-                      const void* g, const void* beta, float* state, void* out,
-                      void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+// shared by kda_decode and kda_decode_commit; out may be NULL only with counts
+kda_status decode_common(const kda_shape* s, const void* q, const void* k, const void* v,
+                         const void* g, const void* beta, const int32_t* num_commit,
+                         float* state, void* out, void* workspace, size_t workspace_bytes,
+                         void* stream) {
   kda_status st = check_shape(s, false);
   if (st != KDA_OK) return st;
   if (s->T < 1 || s->T > 8) return KDA_ERR_UNSUPPORTED;
-  if (!q || !k || !v || !g || !beta || !state || !out) return KDA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !g || !beta || !state || (!out && !num_commit)) return KDA_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k, v, g, state, out};
   for (const void* p : ptrs)
-    if (!aligned(p, 16)) return KDA_ERR_INVALID_ARG;
+    if (p && !aligned(p, 16)) return KDA_ERR_INVALID_ARG;
   if (!aligned(beta, dsize(s->in_dtype))) return KDA_ERR_INVALID_ARG;
+  if (num_commit && !aligned(num_commit, 4)) return KDA_ERR_INVALID_ARG;
   st = check_ws(s, workspace, workspace_bytes);
   if (st != KDA_OK) return st;
 
@@ -127,9 +131,29 @@ kda_status kda_decode(const kda_shape* s, const void* q, const void* k, const vo
   a.scale = s->scale;
   a.in_dtype = s->in_dtype;
   a.out_dtype = s->out_dtype;
+  a.num_commit = num_commit;
+  a.status = static_cast<unsigned int*>(workspace);
   a.stream = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(workspace, 0, kWsHeader, a.stream) != cudaSuccess) return KDA_ERR_CUDA;
   return launch_decode(a) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+}  // namespace
+
+kda_status kda_decode(const kda_shape* s, const void* q, const void* k, const void* v,
+                      const void* g, const void* beta, float* state, void* out,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  if (!out) return KDA_ERR_INVALID_ARG;
+  return decode_common(s, q, k, v, g, beta, nullptr, state, out, workspace, workspace_bytes,
+                       stream);
+}
+
+kda_status kda_decode_commit(const kda_shape* s, const void* q, const void* k, const void* v,
+                             const void* g, const void* beta, const int32_t* num_commit,
+                             float* state, void* out, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  if (!num_commit) return KDA_ERR_INVALID_ARG;
+  return decode_common(s, q, k, v, g, beta, num_commit, state, out, workspace, workspace_bytes,
+                       stream);
 }
 
 kda_status kda_read_device_status(void* workspace, void* stream) {

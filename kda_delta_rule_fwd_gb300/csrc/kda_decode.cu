@@ -26,12 +26,15 @@ template <int N> struct VecF;
 template <> struct VecF<2> { using T = float2; };
 template <> struct VecF<4> { using T = float4; };
 
-template <int D, typename TIn, typename TOut>
+// kCommit: per-sequence commit counts (num_commit) decide which state is written
+// back; otherwise the state after all Tstep tokens is.
+template <int D, typename TIn, typename TOut, bool kCommit>
 __global__ void __launch_bounds__(kDecodeThreads, 2)
 kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                   const TIn* __restrict__ v, const TIn* __restrict__ g,
                   const TIn* __restrict__ beta, float* __restrict__ state,
-                  TOut* __restrict__ out, int H, int Tstep, float scale) {
+                  TOut* __restrict__ out, int H, int Tstep, float scale,
+                  const int32_t* __restrict__ num_commit, unsigned int* status) {
   constexpr int R = D / 8;     // state rows per warp
   constexpr int CPL = D / 32;  // state columns per lane
   using Vec = typename VecF<CPL>::T;
@@ -81,6 +84,28 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
   }
   __syncthreads();
 
+  // The state written back is the one after the first `commit` tokens (all of
+  // them unless per-sequence counts are given); every token still produces its
+  // output.  A count outside [0, Tstep] is latched and commits nothing.
+  int commit = Tstep;
+  if (kCommit) {
+    commit = num_commit[n];
+    if (commit < 0 || commit > Tstep) {
+      if (tid == 0) latch_status(status, KDA_ERR_INVALID_ARG);
+      commit = 0;
+    }
+  }
+  auto store_state = [&]() {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      Vec x;
+      float* xf = reinterpret_cast<float*>(&x);
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) xf[c] = S[r][c];
+      *reinterpret_cast<Vec*>(Sg + (int64_t)(warp * R + r) * D + lane * CPL) = x;
+    }
+  };
+
   for (int t = 0; t < Tstep; ++t) {
     // this warp's rows of alpha, k and q, read as 16-byte vectors
     float a[R], kr[R], qr[R];
@@ -126,7 +151,7 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
       const float u = s_b[t] * (s_v[t][tid] - sk);
       s_u[tid] = u;
       const float o = scale * fmaf(u, s_kq[t], sq);
-      out[((n * Tstep + t) * H + h) * D + tid] = from_f32<TOut>(o);
+      if (!kCommit || out) out[((n * Tstep + t) * H + h) * D + tid] = from_f32<TOut>(o);
     }
     __syncthreads();
     // rank-1 write S <- S + k u^T
@@ -142,16 +167,9 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
 #pragma unroll
       for (int c = 0; c < CPL; ++c) S[r][c] = fmaf(kr[r], u[c], S[r][c]);
     }
+    if (kCommit && t + 1 == commit) store_state();
   }
-
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    Vec x;
-    float* xf = reinterpret_cast<float*>(&x);
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) xf[c] = S[r][c];
-    *reinterpret_cast<Vec*>(Sg + (int64_t)(warp * R + r) * D + lane * CPL) = x;
-  }
+  if (!kCommit) store_state();
 }
 
 template <int D, typename TIn>
@@ -163,12 +181,25 @@ cudaError_t launch_d_in(const DecodeArgs& a) {
   const TIn* v = static_cast<const TIn*>(a.v);
   const TIn* g = static_cast<const TIn*>(a.g);
   const TIn* b = static_cast<const TIn*>(a.beta);
-  if (a.out_dtype == KDA_F32)
-    kda_decode_kernel<D, TIn, float><<<(unsigned)blocks, kDecodeThreads, 0, a.stream>>>(
-        q, k, v, g, b, a.state, static_cast<float*>(a.out), a.H, a.Tstep, a.scale);
-  else
-    kda_decode_kernel<D, TIn, __nv_bfloat16><<<(unsigned)blocks, kDecodeThreads, 0, a.stream>>>(
-        q, k, v, g, b, a.state, static_cast<__nv_bfloat16*>(a.out), a.H, a.Tstep, a.scale);
+  const bool f32 = a.out_dtype == KDA_F32;
+  float* of = static_cast<float*>(a.out);
+  __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(a.out);
+  const dim3 grid((unsigned)blocks);
+  if (a.num_commit) {
+    if (f32)
+      kda_decode_kernel<D, TIn, float, true><<<grid, kDecodeThreads, 0, a.stream>>>(
+          q, k, v, g, b, a.state, of, a.H, a.Tstep, a.scale, a.num_commit, a.status);
+    else
+      kda_decode_kernel<D, TIn, __nv_bfloat16, true><<<grid, kDecodeThreads, 0, a.stream>>>(
+          q, k, v, g, b, a.state, ob, a.H, a.Tstep, a.scale, a.num_commit, a.status);
+  } else {
+    if (f32)
+      kda_decode_kernel<D, TIn, float, false><<<grid, kDecodeThreads, 0, a.stream>>>(
+          q, k, v, g, b, a.state, of, a.H, a.Tstep, a.scale, nullptr, a.status);
+    else
+      kda_decode_kernel<D, TIn, __nv_bfloat16, false><<<grid, kDecodeThreads, 0, a.stream>>>(
+          q, k, v, g, b, a.state, ob, a.H, a.Tstep, a.scale, nullptr, a.status);
+  }
   return cudaGetLastError();
 }
 

@@ -118,6 +118,8 @@ struct DecodeArgs {
   int32_t B, Tstep, H, D;
   float scale;
   kda_dtype in_dtype, out_dtype;
+  const int32_t* num_commit;  // per-sequence commit counts, or nullptr (commit all)
+  unsigned int* status;
   cudaStream_t stream;
 };
 

@@ -108,6 +108,27 @@ def test_argument_errors_return_before_launch(lib):
     assert _decode(L, _shape(m, T=1), ws_bytes=0) == m.KDA_ERR_WORKSPACE
 
 
+def _decode_commit(L, shape, *, counts=FAKE, out=FAKE, state=FAKE, ws_bytes=1 << 20):
+    vp = ctypes.c_void_p
+    return L.kda_decode_commit(ctypes.byref(shape), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE),
+                               vp(FAKE), vp(counts), vp(state), vp(out), vp(FAKE), ws_bytes, None)
+
+
+def test_decode_commit_argument_errors(lib):
+    """Commit counts are required; outputs are optional only here; the counts must
+    be 4-byte aligned; the step-size and workspace rules are kda_decode's."""
+    m, L = lib
+    L.kda_decode_commit.restype = ctypes.c_int
+    assert _decode_commit(L, _shape(m, T=4), counts=0) == m.KDA_ERR_INVALID_ARG
+    assert _decode_commit(L, _shape(m, T=4), counts=FAKE + 2) == m.KDA_ERR_INVALID_ARG
+    assert _decode_commit(L, _shape(m, T=9)) == m.KDA_ERR_UNSUPPORTED
+    assert _decode_commit(L, _shape(m, T=4), state=0) == m.KDA_ERR_INVALID_ARG
+    assert _decode_commit(L, _shape(m, T=4), ws_bytes=0) == m.KDA_ERR_WORKSPACE
+    assert _decode(L, _shape(m, T=4), out=0) == m.KDA_ERR_INVALID_ARG  # kda_decode needs out
+    if not torch.cuda.is_available():  # valid arguments reach the (absent) device
+        assert _decode_commit(L, _shape(m, T=4), out=0) == m.KDA_ERR_CUDA
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="would launch on fake pointers")
 def test_valid_call_without_a_gpu_reports_cuda_error(lib):
     """With valid arguments the first CUDA call fails on a GPU-less host, and the

@@ -134,6 +134,86 @@ def test_decode_extreme_gates(kda, oracle_mod, d):
     assert rel_err(state, h_ref) <= TOL_F32
 
 
+# decode with commit counts (speculative-decode verification and replay) ---------------
+
+def _commit_refs(oracle_mod, x, counts):
+    """Oracle state after each sequence's first counts[n] tokens (h0 when 0)."""
+    refs = []
+    for n, c in enumerate(counts):
+        if c == 0:
+            refs.append(x.h0[n].double().cpu().numpy())
+            continue
+        sl = lambda t: t[n:n + 1, :c].contiguous()
+        _, h = oracle_mod.recurrent(sl(x.q), sl(x.k), sl(x.v), sl(x.g), sl(x.beta),
+                                    h0=x.h0[n:n + 1].contiguous())
+        refs.append(h[0])
+    return refs
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_commit_counts(kda, oracle_mod, dtype, d):
+    """Every token produces its output; the state kept is the one after the
+    accepted prefix (0 = verification only, T_step = plain decode)."""
+    x = kda_inputs.decode_pool(num_seqs=6, H=3, d=d, T_step=8, dtype=dtype, device=DEV, seed=91)
+    counts = [0, 1, 3, 5, 8, 8]
+    state = x.h0.clone()
+    o = kda.decode_commit(x.q, x.k, x.v, x.g, x.beta, state,
+                          torch.tensor(counts, dtype=torch.int32, device=DEV))
+    torch.cuda.synchronize()
+    o_ref, _ = oracle_mod.recurrent(x.q, x.k, x.v, x.g, x.beta, h0=x.h0)
+    tol = TOL[dtype]
+    assert rel_err(o, o_ref) <= tol
+    for n, ref in enumerate(_commit_refs(oracle_mod, x, counts)):
+        if counts[n] == 0:
+            assert torch.equal(state[n], x.h0[n])  # untouched
+        else:
+            assert rel_err(state[n], ref) <= tol
+
+
+def test_decode_commit_verify_then_replay(kda):
+    """The two-call flow: verify T_step drafts without committing, then replay the
+    same cached inputs committing the accepted prefix.  The kept state equals
+    kda_decode over that prefix; the verification outputs equal kda_decode's."""
+    x = kda_inputs.decode_pool(num_seqs=4, H=2, d=128, T_step=6, dtype=torch.bfloat16,
+                               device=DEV, seed=92)
+    accepted = 4
+    state = x.h0.clone()
+    zeros = torch.zeros(4, dtype=torch.int32, device=DEV)
+    o_verify = kda.decode_commit(x.q, x.k, x.v, x.g, x.beta, state, zeros)
+    assert torch.equal(state, x.h0)
+    none = kda.decode_commit(x.q, x.k, x.v, x.g, x.beta, state,
+                             torch.full((4,), accepted, dtype=torch.int32, device=DEV),
+                             want_out=False)
+    assert none is None
+    ref_state = x.h0.clone()
+    pre = lambda t: t[:, :accepted].contiguous()
+    kda.decode(pre(x.q), pre(x.k), pre(x.v), pre(x.g), pre(x.beta), ref_state)
+    full_state = x.h0.clone()
+    o_full = kda.decode(x.q, x.k, x.v, x.g, x.beta, full_state)
+    torch.cuda.synchronize()
+    assert rel_err(state, ref_state.double().cpu().numpy()) <= 1e-5
+    assert rel_err(o_verify, o_full.double().cpu().numpy()) <= 1e-6
+
+
+def test_decode_commit_bad_count_is_reported(kda):
+    """A count outside 0..T_step is latched; that sequence keeps its state and the
+    others commit normally."""
+    x = kda_inputs.decode_pool(num_seqs=3, H=2, d=64, T_step=4, dtype=torch.float32,
+                               device=DEV, seed=93)
+    state = x.h0.clone()
+    ref = x.h0.clone()
+    ws = torch.empty(256, dtype=torch.uint8, device=DEV)
+    kda.decode_commit(x.q, x.k, x.v, x.g, x.beta, state,
+                      torch.tensor([4, 5, -1], dtype=torch.int32, device=DEV), workspace=ws)
+    assert kda.read_device_status(ws) == kda.KDA_ERR_INVALID_ARG
+    kda.decode(x.q[:1].contiguous(), x.k[:1].contiguous(), x.v[:1].contiguous(),
+               x.g[:1].contiguous(), x.beta[:1].contiguous(), ref[:1])
+    torch.cuda.synchronize()
+    assert rel_err(state[0], ref[0].double().cpu().numpy()) <= 1e-6
+    assert torch.equal(state[1:], x.h0[1:])
+
+
 def test_decode_replay_equals_single_steps_and_prefill(kda):
     """One 8-token replay step == eight 1-token steps == prefill from the same state."""
     x = kda_inputs.decode_pool(num_seqs=3, H=2, d=128, T_step=8, dtype=torch.float32,
