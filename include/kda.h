@@ -107,6 +107,38 @@ kda_status kda_fwd(const kda_shape* s, const void* q, const void* k, const void*
                    size_t workspace_bytes, void* stream);
 
 /*
+ * kda_fwd plus prefix-cache checkpoints: the state of every (sequence, head)
+ * after each `interval` tokens of its sequence ("Kimi K3 模型结构（7）：结构决定
+ * 系统", section 前缀缓存: prefix hashes are cut into 512-token blocks and KDA state
+ * checkpoints are kept at hash-block end points, so a cache hit can land on any
+ * 512-token boundary).
+ *
+ * Same arguments and results as kda_fwd, plus:
+ *   interval      tokens between checkpoints, a positive multiple of 64 (the
+ *                 pages use 512).
+ *   ckpt          device float32 [ckpt_rows, H, dk, dv], the same [dk][dv] layout
+ *                 as hT.  Row base_n + j - 1 holds the state of sequence n after
+ *                 its first j * interval tokens, j = 1 .. floor(len_n / interval).
+ *   ckpt_offsets  device int32 [N+1] for packed batches: base_n = ckpt_offsets[n]
+ *                 and ckpt_offsets[n+1] - ckpt_offsets[n] = floor(len_n / interval).
+ *                 Ignored (may be NULL) for fixed-length batches, where
+ *                 base_n = n * floor(T / interval).
+ *   ckpt_rows     rows in ckpt.
+ * Offsets that disagree with a sequence's length, or rows past ckpt_rows, latch
+ * KDA_ERR_INVALID_ARG in the workspace status word; that sequence then writes no
+ * checkpoints (its o and hT are still computed).  Each checkpoint adds 4*dk*dv
+ * bytes of writes per (sequence, head).  Host-checkable errors: interval not a
+ * positive multiple of 64, ckpt NULL or not 16-byte aligned, ckpt_rows < 0, a
+ * packed batch without ckpt_offsets -> KDA_ERR_INVALID_ARG; otherwise those of
+ * kda_fwd.
+ */
+kda_status kda_fwd_checkpoints(const kda_shape* s, const void* q, const void* k, const void* v,
+                               const void* g, const void* beta, const int32_t* cu_seqlens,
+                               const float* h0, void* out, float* hT, int32_t interval,
+                               float* ckpt, const int32_t* ckpt_offsets, int64_t ckpt_rows,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Decode step: T_step = s->T tokens (1..8) per sequence applied in order to a
  * state pool resident in device memory, updated in place (the replay form of
  * speculative-decode rollback: the cached inputs of the accepted tokens are

@@ -69,6 +69,9 @@ def load(path: str | None = None):
         lib.kda_workspace_size.argtypes = [sp]
         lib.kda_fwd.restype = ctypes.c_int
         lib.kda_fwd.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        lib.kda_fwd_checkpoints.restype = ctypes.c_int
+        lib.kda_fwd_checkpoints.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                            ctypes.c_int32, vp, vp, ctypes.c_int64, vp, sz, vp]
         lib.kda_decode.restype = ctypes.c_int
         lib.kda_decode.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         lib.kda_decode_commit.restype = ctypes.c_int
@@ -151,6 +154,49 @@ def fwd(q, k, v, g, beta, *, cu_seqlens=None, h0=None, scale=None, out_dtype=tor
     if rc != KDA_OK:
         raise KDAError(rc, "kda_fwd")
     return out, hT
+
+
+def fwd_checkpoints(q, k, v, g, beta, *, interval=512, cu_seqlens=None, h0=None, scale=None,
+                    out_dtype=torch.float32, out=None, hT=None, output_final_state=True,
+                    workspace=None, stream=None):
+    """``fwd`` plus prefix-cache checkpoints: the state after every ``interval``
+    tokens (a multiple of 64) of each sequence.  Returns ``(o, hT, ckpt, offsets)``
+    with ``ckpt [rows, H, dk, dv]`` float32; sequence n's checkpoints are rows
+    ``offsets[n] .. offsets[n+1]-1`` (``offsets`` is a device int32 ``[N+1]``).  For
+    packed batches the offsets come from ``cu_seqlens`` on the device, and sizing
+    ``ckpt`` reads their total on the host (one synchronisation)."""
+    _check_inputs(q, k, v, g, beta)
+    N = q.shape[0] if cu_seqlens is None else cu_seqlens.numel() - 1
+    shape = make_shape(q, v, packed_seqs=None if cu_seqlens is None else N, scale=scale,
+                       out_dtype=out_dtype)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if cu_seqlens is None:
+        per = T // interval
+        offsets = torch.arange(N + 1, dtype=torch.int32, device=q.device) * per
+        rows = N * per
+    else:
+        counts = (cu_seqlens[1:] - cu_seqlens[:-1]) // interval
+        offsets = torch.zeros(N + 1, dtype=torch.int32, device=q.device)
+        offsets[1:] = torch.cumsum(counts, 0).to(torch.int32)
+        rows = int(offsets[-1].item())
+    ckpt = torch.empty(rows, H, dk, dv, dtype=torch.float32, device=q.device)
+    if out is None:
+        out = torch.empty(B, T, H, dv, dtype=out_dtype, device=q.device)
+    if hT is None and output_final_state:
+        hT = torch.empty(N, H, dk, dv, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = new_workspace(shape, q.device)
+    # an empty checkpoint buffer still needs a valid pointer
+    ck = ckpt if rows > 0 else torch.empty(4, dtype=torch.float32, device=q.device)
+    rc = load().kda_fwd_checkpoints(
+        ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens),
+        _ptr(h0), _ptr(out), _ptr(hT), int(interval), _ptr(ck),
+        _ptr(offsets) if cu_seqlens is not None else None, rows, _ptr(workspace),
+        workspace.numel(), _stream_ptr(stream))
+    if rc != KDA_OK:
+        raise KDAError(rc, "kda_fwd_checkpoints")
+    return out, hT, ckpt, offsets
 
 
 def decode(q, k, v, g, beta, state, *, scale=None, out_dtype=torch.float32, out=None,

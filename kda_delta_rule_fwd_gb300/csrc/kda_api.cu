@@ -54,10 +54,13 @@ size_t kda_workspace_size(const kda_shape* s) {
   return b;
 }
 
-kda_status kda_fwd(const kda_shape* s, const void* q, const void* k, const void* v,
-                   const void* g, const void* beta, const int32_t* cu_seqlens,
-                   const float* h0, void* out, float* hT, void* workspace,
-                   size_t workspace_bytes, void* stream) {
+namespace {
+// shared by kda_fwd and kda_fwd_checkpoints (ckpt == nullptr: no checkpoints)
+kda_status fwd_common(const kda_shape* s, const void* q, const void* k, const void* v,
+                      const void* g, const void* beta, const int32_t* cu_seqlens,
+                      const float* h0, void* out, float* hT, float* ckpt,
+                      const int32_t* ckpt_offsets, int64_t ckpt_rows, int32_t ckpt_interval,
+                      void* workspace, size_t workspace_bytes, void* stream) {
   const bool packed = cu_seqlens != nullptr;
   kda_status st = check_shape(s, packed);
   if (st != KDA_OK) return st;
@@ -83,6 +86,10 @@ kda_status kda_fwd(const kda_shape* s, const void* q, const void* k, const void*
   a.in_dtype = s->in_dtype;
   a.out_dtype = s->out_dtype;
   a.status = static_cast<unsigned int*>(workspace);
+  a.ckpt = ckpt;
+  a.ckpt_off = ckpt_offsets;
+  a.ckpt_rows = ckpt_rows;
+  a.ckpt_interval = ckpt_interval;
   a.stream = static_cast<cudaStream_t>(stream);
 
   if (cudaMemsetAsync(workspace, 0, kWsHeader, a.stream) != cudaSuccess) return KDA_ERR_CUDA;
@@ -104,6 +111,28 @@ kda_status kda_fwd(const kda_shape* s, const void* q, const void* k, const void*
   else
     e = launch_prefill_f32(a);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+}  // namespace
+
+kda_status kda_fwd(const kda_shape* s, const void* q, const void* k, const void* v,
+                   const void* g, const void* beta, const int32_t* cu_seqlens,
+                   const float* h0, void* out, float* hT, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  return fwd_common(s, q, k, v, g, beta, cu_seqlens, h0, out, hT, nullptr, nullptr, 0, 0,
+                    workspace, workspace_bytes, stream);
+}
+
+kda_status kda_fwd_checkpoints(const kda_shape* s, const void* q, const void* k, const void* v,
+                               const void* g, const void* beta, const int32_t* cu_seqlens,
+                               const float* h0, void* out, float* hT, int32_t interval,
+                               float* ckpt, const int32_t* ckpt_offsets, int64_t ckpt_rows,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  if (interval <= 0 || interval % 64 != 0 || !ckpt || !aligned(ckpt, 16) || ckpt_rows < 0)
+    return KDA_ERR_INVALID_ARG;
+  if (cu_seqlens && (!ckpt_offsets || !aligned(ckpt_offsets, 4))) return KDA_ERR_INVALID_ARG;
+  return fwd_common(s, q, k, v, g, beta, cu_seqlens, h0, out, hT, ckpt,
+                    cu_seqlens ? ckpt_offsets : nullptr, ckpt_rows, interval, workspace,
+                    workspace_bytes, stream);
 }
 
 namespace {

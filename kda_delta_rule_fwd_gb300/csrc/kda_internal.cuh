@@ -104,8 +104,31 @@ struct FwdArgs {
   unsigned int* status;
   const int32_t* order;  // scheduler output: sequences longest first (packed), or nullptr
   float* seg_ws;         // segment-state area of the workspace (long-chain split), or nullptr
+  // prefix-cache checkpoints (state after every ckpt_interval tokens), or ckpt == nullptr
+  float* ckpt;              // [ckpt_rows, H, D, D]
+  const int32_t* ckpt_off;  // [N+1] row offsets (packed batches), or nullptr (fixed length)
+  int64_t ckpt_rows;
+  int64_t ckpt_interval;    // tokens, a multiple of 64
   cudaStream_t stream;
 };
+
+// First checkpoint row of sequence n (rows base .. base + seq_len / interval - 1
+// hold the states after interval, 2 interval, ... tokens), or -1 when checkpoints
+// are off or the caller's offsets disagree with the sequence length or the
+// buffer (latched as KDA_ERR_INVALID_ARG by the leader thread; nothing written).
+__device__ __forceinline__ int64_t ckpt_base(const float* ckpt, const int32_t* off, int64_t rows,
+                                             int64_t interval, int n, int64_t seq_len,
+                                             unsigned int* status, bool leader) {
+  if (!ckpt) return -1;
+  const int64_t cnt = seq_len / interval;
+  const int64_t base = off ? (int64_t)off[n] : (int64_t)n * cnt;
+  const bool bad = (off && (int64_t)off[n + 1] - base != cnt) || base < 0 || base + cnt > rows;
+  if (bad) {
+    if (leader) latch_status(status, KDA_ERR_INVALID_ARG);
+    return -1;
+  }
+  return base;
+}
 
 cudaError_t launch_schedule(const FwdArgs& a, int32_t* order_out);
 cudaError_t launch_prefill_f32(const FwdArgs& a);

@@ -301,6 +301,10 @@ struct Bf16Params {
   float* seg_b;          // [chains][nseg-1][D][D] zero-start end states
   float* seg_m;          // [chains][nseg-1][D][D] transitions
   const float* seg_s;    // [chains][nseg][D][D] segment start states (index 0 unused)
+  float* ckpt;           // prefix-cache checkpoints [rows][H][D][D], or nullptr
+  const int32_t* ckpt_off;
+  int64_t ckpt_rows;
+  int64_t ckpt_interval;
 };
 
 // The CTA's bounded waits.  Every thread waits on the barrier itself; a thread
@@ -363,6 +367,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int item = blockIdx.x;
   int n, h;
   int64_t t0, len;
+  int64_t rel0 = 0, seq_len = 0;  // start of this item within its sequence; sequence length
   // start state (nullptr = zeros), identity start, end-state destination, flags
   const float* s_in = nullptr;
   float* s_out = nullptr;
@@ -371,6 +376,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     n = p.order ? p.order[item / p.H] : item / p.H;
     h = item % p.H;
     p.seqs.get(n, t0, len);
+    seq_len = len;
     s_in = p.h0 ? p.h0 + (((int64_t)n * p.H + h) * D) * D : nullptr;
     s_out = p.hT ? p.hT + (((int64_t)n * p.H + h) * D) * D : nullptr;
   } else {
@@ -395,6 +401,8 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     int64_t st, ln;
     p.seqs.get(n, st, ln);
     const int64_t a = (int64_t)seg * p.seg_len;
+    rel0 = a;
+    seq_len = ln;
     t0 = st + a;
     len = ln - a < p.seg_len ? ln - a : p.seg_len;
     if (len < 0) len = 0;
@@ -507,6 +515,11 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   uint64_t* xo_bar = &bars[2];  // completion of the products with S'
   uint32_t xo_issued = 0;
   bool range_err = false;
+  // prefix-cache checkpoints of this chain (output items only)
+  const int64_t ck_base =
+      want_o ? ckpt_base(p.ckpt, p.ckpt_off, p.ckpt_rows, p.ckpt_interval, n, seq_len, p.status,
+                         tid == 0)
+             : -1;
   // log2 of the chunk's per-channel reference c (an integer, clamped)
   auto ref_log2 = [](float rho) { return fminf(fmaxf(rintf(rho * kLog2e), -kRefExp2), kRefExp2); };
   // thread 0: once the g tile of `chunk` has landed, Gam (rows 0..63 and again
@@ -890,6 +903,12 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       for (int q4 = 0; q4 < SCOL / 16; ++q4)
         tmem_ld16(tb + lane_base + TM_S + cq * SCOL + q4 * 16, sv[q4]);
       tmem_wait_ld();
+      // a checkpoint when rel0 + (ci + 1) C tokens of the sequence are done and that
+      // is a multiple of the interval: state [key channel][value channel]
+      const int64_t done = rel0 + cs + C;
+      float* ck = (ck_base >= 0 && nv == C && done % p.ckpt_interval == 0)
+                      ? p.ckpt + ((ck_base + done / p.ckpt_interval - 1) * p.H + h) * D * D + j
+                      : nullptr;
 #pragma unroll
       for (int q4 = 0; q4 < SCOL / 16; ++q4) {
         const int c0 = cq * SCOL + q4 * 16;
@@ -897,6 +916,14 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
         for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(sv[q4][e] * s_gamc[c0 + e]);
         tmem_st16(tb + lane_base + TM_S + c0, w);
+      }
+      if (ck) {
+#pragma unroll
+        for (int q4 = 0; q4 < SCOL / 16; ++q4) {
+          const int c0 = cq * SCOL + q4 * 16;
+#pragma unroll
+          for (int e = 0; e < 16; ++e) ck[(int64_t)(c0 + e) * D] = sv[q4][e] * s_gamc[c0 + e];
+        }
       }
       if (want_o && nv == C) {
         // full chunk: stage [token][value channel] in X, one bulk tensor store below
@@ -1109,6 +1136,10 @@ cudaError_t launch_prefill_bf16(const FwdArgs& a) {
   p.seg_len = 0;
   p.seg_b = p.seg_m = nullptr;
   p.seg_s = nullptr;
+  p.ckpt = a.ckpt;
+  p.ckpt_off = a.ckpt_off;
+  p.ckpt_rows = a.ckpt_rows;
+  p.ckpt_interval = a.ckpt_interval > 0 ? a.ckpt_interval : 1;
   cudaError_t e = cudaFuncSetAttribute(kda_prefill_bf16_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;

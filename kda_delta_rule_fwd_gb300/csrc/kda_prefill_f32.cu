@@ -38,7 +38,9 @@ kda_prefill_f32_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                        const TIn* __restrict__ beta, SeqView seqs,
                        const int32_t* __restrict__ order, const float* __restrict__ h0,
                        TOut* __restrict__ out, float* __restrict__ hT, int H, float scale,
-                       const unsigned int* __restrict__ status) {
+                       unsigned int* __restrict__ status, float* __restrict__ ckpt,
+                       const int32_t* __restrict__ ckpt_off, int64_t ckpt_rows,
+                       int64_t ckpt_interval) {
   using L = F32Smem<D, C>;
   constexpr int LD = L::LD;
   extern __shared__ float smem[];
@@ -56,7 +58,8 @@ kda_prefill_f32_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
   float* sb = sT + C * C;
   float* sGl = sb + C;
 
-  if (status && *(volatile const unsigned int*)status != 0u) return;  // bad cu_seqlens
+  // a malformed cu_seqlens is latched by the scheduler before this kernel starts
+  if (status && *(volatile const unsigned int*)status == (unsigned)KDA_ERR_BAD_SEQLENS) return;
   const int tid = threadIdx.x;
   const int item = blockIdx.x;
   const int n = order ? order[item / H] : item / H;
@@ -66,6 +69,8 @@ kda_prefill_f32_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
 
   const int64_t st = ((int64_t)n * H + h) * D * D;
   for (int i = tid; i < D * D; i += kThreads) S[i] = h0 ? h0[st + i] : 0.f;
+  const int64_t ck_base =
+      ckpt_base(ckpt, ckpt_off, ckpt_rows, ckpt_interval, n, len, status, tid == 0);
 
   for (int64_t cs = 0; cs < len; cs += C) {
     const int nv = (int)(len - cs < C ? len - cs : C);
@@ -157,12 +162,18 @@ kda_prefill_f32_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
       out[((t0 + cs + r) * H + h) * D + c] = from_f32<TOut>(scale * acc);
     }
     __syncthreads();
-    // 9. S <- diag(e^Gam_last) S + Khat^T U
+    // 9. S <- diag(e^Gam_last) S + Khat^T U; a checkpoint when cs + C tokens of
+    // the sequence are done and that is a multiple of the interval
+    const int64_t done = cs + C;
+    float* ck = (ck_base >= 0 && done <= len && done % ckpt_interval == 0)
+                    ? ckpt + ((ck_base + done / ckpt_interval - 1) * H + h) * D * D
+                    : nullptr;
     for (int i = tid; i < D * D; i += kThreads) {
       const int m = i / D, c = i % D;
       float acc = expf(sGl[m]) * S[i];
       for (int j = 0; j < C; ++j) acc = fmaf(sk[j * LD + m], sU[j * LD + c], acc);
       S[i] = acc;
+      if (ck) ck[i] = acc;
     }
   }
   __syncthreads();
@@ -183,7 +194,8 @@ cudaError_t launch_t(const FwdArgs& a) {
   kern<<<(unsigned)items, kThreads, L::bytes, a.stream>>>(
       static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k), static_cast<const TIn*>(a.v),
       static_cast<const TIn*>(a.g), static_cast<const TIn*>(a.beta), sv, a.order, a.h0,
-      static_cast<TOut*>(a.out), a.hT, a.H, a.scale, a.status);
+      static_cast<TOut*>(a.out), a.hT, a.H, a.scale, a.status, a.ckpt, a.ckpt_off, a.ckpt_rows,
+      a.ckpt_interval);
   return cudaGetLastError();
 }
 

@@ -129,6 +129,33 @@ def test_decode_commit_argument_errors(lib):
         assert _decode_commit(L, _shape(m, T=4), out=0) == m.KDA_ERR_CUDA
 
 
+def _fwd_ckpt(L, shape, *, interval=512, ckpt=FAKE, offs=None, rows=8, cu=None):
+    vp = ctypes.c_void_p
+    L.kda_fwd_checkpoints.restype = ctypes.c_int
+    return L.kda_fwd_checkpoints(ctypes.byref(shape), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE),
+                                 vp(FAKE), vp(cu), vp(None), vp(FAKE), vp(FAKE),
+                                 ctypes.c_int32(interval), vp(ckpt), vp(offs),
+                                 ctypes.c_int64(rows), vp(FAKE), ctypes.c_size_t(1 << 20), None)
+
+
+def test_fwd_checkpoints_argument_errors(lib):
+    """The interval is a positive multiple of the chunk length; the buffer is
+    required and aligned; packed batches need row offsets."""
+    m, L = lib
+    for bad in (0, -64, 100, 32):
+        assert _fwd_ckpt(L, _shape(m), interval=bad) == m.KDA_ERR_INVALID_ARG
+    assert _fwd_ckpt(L, _shape(m), ckpt=0) == m.KDA_ERR_INVALID_ARG
+    assert _fwd_ckpt(L, _shape(m), ckpt=FAKE + 4) == m.KDA_ERR_INVALID_ARG
+    assert _fwd_ckpt(L, _shape(m), rows=-1) == m.KDA_ERR_INVALID_ARG
+    packed = _shape(m, B=1, num_seqs=3)
+    assert _fwd_ckpt(L, packed, cu=FAKE) == m.KDA_ERR_INVALID_ARG             # no offsets
+    assert _fwd_ckpt(L, packed, cu=FAKE, offs=FAKE + 2) == m.KDA_ERR_INVALID_ARG
+    assert _fwd_ckpt(L, _shape(m, dk=96, dv=96)) == m.KDA_ERR_UNSUPPORTED   # kda_fwd's rules
+    if not torch.cuda.is_available():  # valid arguments reach the (absent) device
+        assert _fwd_ckpt(L, _shape(m)) == m.KDA_ERR_CUDA
+        assert _fwd_ckpt(L, packed, cu=FAKE, offs=FAKE) == m.KDA_ERR_CUDA
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="would launch on fake pointers")
 def test_valid_call_without_a_gpu_reports_cuda_error(lib):
     """With valid arguments the first CUDA call fails on a GPU-less host, and the

@@ -98,6 +98,96 @@ def test_bad_cu_seqlens_is_reported_not_executed(kda):
     assert kda.read_device_status(ws) == kda.KDA_ERR_BAD_SEQLENS
 
 
+# prefix-cache checkpoints ------------------------------------------------------------
+
+def _ckpt_refs(oracle_mod, x, seqs, interval):
+    """Oracle states after each `interval` tokens of each sequence, built one
+    interval at a time.  seqs: (batch index, first token, length, h0 index or None)."""
+    refs = []
+    for b, t0, ln, hi in seqs:
+        state = None if hi is None else x.h0[hi:hi + 1].contiguous()
+        for j in range(ln // interval):
+            sl = lambda t: t[b:b + 1, t0 + j * interval:t0 + (j + 1) * interval].contiguous()
+            _, h = oracle_mod.recurrent(sl(x.q), sl(x.k), sl(x.v), sl(x.g), sl(x.beta), h0=state)
+            refs.append(h[0])
+            state = torch.from_numpy(h).float()
+    return refs
+
+
+def _check_ckpts(ck, refs, tol):
+    assert ck.shape[0] == len(refs)
+    for r, ref in enumerate(refs):
+        assert rel_err(ck[r], ref) <= tol, f"checkpoint row {r}"
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_checkpoints_fixed_length(kda, oracle_mod, dtype, d):
+    """B=2, T=1100: states after 512 and 1024 tokens of each sequence, with o and hT
+    unchanged from kda_fwd."""
+    x = kda_inputs.fixed(2, 1100, 2, d, dtype=dtype, device=DEV, seed=31 + d, h0_std=0.1)
+    o, hT, ck, off = kda.fwd_checkpoints(x.q, x.k, x.v, x.g, x.beta, h0=x.h0, interval=512)
+    o2, h2 = kda.fwd(x.q, x.k, x.v, x.g, x.beta, h0=x.h0)
+    torch.cuda.synchronize()
+    assert off.tolist() == [0, 2, 4]
+    assert torch.equal(o, o2) and torch.equal(hT, h2)
+    _check_ckpts(ck, _ckpt_refs(oracle_mod, x, [(0, 0, 1100, 0), (1, 0, 1100, 1)], 512),
+                 TOL[dtype])
+
+
+@pytest.mark.parametrize("dtype,d,interval", [(torch.bfloat16, 128, 512), (torch.bfloat16, 128, 64),
+                                              (torch.float32, 64, 64), (torch.float32, 128, 128)],
+                         ids=["bf16-512", "bf16-64", "f32-d64-64", "f32-d128-128"])
+def test_checkpoints_packed(kda, oracle_mod, dtype, d, interval):
+    """Packed lengths with empty, short and exact-multiple sequences: each sequence
+    checkpoints from its own start; row offsets follow the lengths."""
+    lens = [600, 1024, 100, 0, 1537, 64]
+    x = kda_inputs.packed(lens, 2, d, dtype=dtype, device=DEV, seed=37, h0_std=0.1)
+    o, hT, ck, off = kda.fwd_checkpoints(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens,
+                                         h0=x.h0, interval=interval)
+    torch.cuda.synchronize()
+    starts = [sum(lens[:i]) for i in range(len(lens))]
+    assert off.tolist() == [sum(l // interval for l in lens[:i]) for i in range(len(lens) + 1)]
+    refs = _ckpt_refs(oracle_mod, x, [(0, starts[i], lens[i], i) for i in range(len(lens))],
+                      interval)
+    _check_ckpts(ck, refs, TOL[dtype])
+
+
+def test_checkpoints_long_chain_split(kda, oracle_mod):
+    """The segment split computes the outputs of each segment from its scanned start
+    state; checkpoints are taken there too, at positions relative to the sequence."""
+    x = kda_inputs.fixed(1, 64 * 257 + 37, 2, 128, dtype=torch.bfloat16, device=DEV, seed=41,
+                         h0_std=0.1)
+    assert kda.workspace_size(kda.make_shape(x.q, x.v)) > 256  # the split plan is active
+    o, hT, ck, off = kda.fwd_checkpoints(x.q, x.k, x.v, x.g, x.beta, h0=x.h0, interval=512)
+    torch.cuda.synchronize()
+    _check_ckpts(ck, _ckpt_refs(oracle_mod, x, [(0, 0, x.q.shape[1], 0)], 512), TOL_BF16)
+
+
+def test_checkpoints_bad_offsets_are_reported(kda):
+    """Offsets that disagree with the lengths are latched; that sequence writes no
+    checkpoint, the others do, and o is unaffected."""
+    import ctypes
+    lens = [600, 1024]
+    x = kda_inputs.packed(lens, 2, 128, dtype=torch.bfloat16, device=DEV, seed=43)
+    shape = kda.make_shape(x.q, x.v, packed_seqs=2)
+    ws = kda.new_workspace(shape, DEV)
+    o = torch.empty(1, sum(lens), 2, 128, device=DEV)
+    ck = torch.full((4, 2, 128, 128), float("nan"), device=DEV)
+    offs = torch.tensor([0, 2, 4], dtype=torch.int32, device=DEV)  # sequence 0 has 1, not 2
+    vp = lambda t: ctypes.c_void_p(t.data_ptr())
+    rc = kda.load().kda_fwd_checkpoints(
+        ctypes.byref(shape), vp(x.q), vp(x.k), vp(x.v), vp(x.g), vp(x.beta), vp(x.cu_seqlens),
+        None, vp(o), None, 512, vp(ck), vp(offs), 4, vp(ws), ws.numel(), None)
+    assert rc == kda.KDA_OK
+    assert kda.read_device_status(ws) == kda.KDA_ERR_INVALID_ARG
+    o_ref, _ = kda.fwd(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ref)
+    assert torch.isnan(ck[:2]).all()     # sequence 0: refused, its rows untouched
+    assert torch.isfinite(ck[2:]).all()  # sequence 1: rows 2 and 3 written
+
+
 # decode ---------------------------------------------------------------------------------
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
