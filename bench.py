@@ -278,6 +278,43 @@ def run_ours(args):
                      "unit": "GB/s", "frac": pbytes / (pms * 1e-3) / 1e9 / hbm_peak},
     }
     del y, py_o, py_h
+
+    # rows beyond the hot path: prefix-cache checkpoints every 512 tokens on the
+    # fixed-length batch, and the decode step with per-sequence commit counts
+    ck_rows = B * (T // 512)
+    ck = torch.empty(ck_rows, H, D, D, device=dev)
+    cfn = lambda: kda.fwd_checkpoints(x.q, x.k, x.v, x.g, x.beta, interval=512, out=o, hT=hT,
+                                      ckpt=ck, workspace=ws)
+    cms = _time_steps(cfn, max(5, args.steps), max(3, args.warmup), stream, dist_on)
+    cbytes = B * T * H * BYTES_PER_TOKEN_HEAD + B * H * STATE_BYTES + ck_rows * H * STATE_BYTES
+    del ck
+    y = kda_inputs.decode_pool(num_seqs=1024, H=H, d=D, T_step=8, device=dev,
+                               seed=1004 + 13 * rank)
+    counts = torch.randint(0, 9, (1024,), generator=torch.Generator().manual_seed(7),
+                           dtype=torch.int32).to(dev)
+    out_d = torch.empty(1024, 8, H, D, device=dev)
+    dws = kda.new_workspace(kda.make_shape(y.q, y.v), dev)
+    kfn = lambda: kda.decode_commit(y.q, y.k, y.v, y.g, y.beta, y.h0, counts, out=out_d,
+                                    workspace=dws)
+    kms = _time_steps(kfn, max(5, args.steps), max(3, args.warmup), stream, dist_on)
+    kbytes = 1024 * H * (2 * STATE_BYTES + 8 * BYTES_PER_TOKEN_HEAD)  # upper bound: all commit
+    del y, out_d
+    cms, kms = max_over_ranks([cms, kms], dev)
+    next_rows = {
+        "prefill_checkpoints_512": {
+            "workload": WORKLOAD + "; state checkpoint every 512 tokens (32 per chain)",
+            "ms_per_step": cms, "overhead_vs_prefill": cms / ms - 1.0,
+            "roofline": {"bound": "hbm", "achieved": cbytes / (cms * 1e-3) / 1e9,
+                         "peak": hbm_peak, "unit": "GB/s",
+                         "frac": cbytes / (cms * 1e-3) / 1e9 / hbm_peak}},
+        "decode_commit_T8": {
+            "workload": "decode pool 1024 x 32 heads, T_step=8, commit counts uniform 0..8",
+            "ms_per_step": kms, "tokens_per_s": 1024 * 8 * world / (kms * 1e-3),
+            "roofline": {"bound": "hbm", "achieved": kbytes / (kms * 1e-3) / 1e9,
+                         "peak": hbm_peak, "unit": "GB/s",
+                         "frac": kbytes / (kms * 1e-3) / 1e9 / hbm_peak,
+                         "note": "bytes counted as if every sequence commits"}},
+    }
     clk = clocks.stop()
 
     ms, ms_e2e = max_over_ranks([ms, ms_e2e], dev)
@@ -318,6 +355,7 @@ def run_ours(args):
         "clocks": clk,
         "decode": dec,
         "prefill_packed": packed_line,
+        "next_rows": next_rows,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = _cpu_baseline(kda_inputs.workload(1, device=dev))

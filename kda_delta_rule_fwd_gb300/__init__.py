@@ -158,20 +158,26 @@ def fwd(q, k, v, g, beta, *, cu_seqlens=None, h0=None, scale=None, out_dtype=tor
 
 def fwd_checkpoints(q, k, v, g, beta, *, interval=512, cu_seqlens=None, h0=None, scale=None,
                     out_dtype=torch.float32, out=None, hT=None, output_final_state=True,
-                    workspace=None, stream=None):
+                    ckpt=None, offsets=None, workspace=None, stream=None):
     """``fwd`` plus prefix-cache checkpoints: the state after every ``interval``
     tokens (a multiple of 64) of each sequence.  Returns ``(o, hT, ckpt, offsets)``
     with ``ckpt [rows, H, dk, dv]`` float32; sequence n's checkpoints are rows
     ``offsets[n] .. offsets[n+1]-1`` (``offsets`` is a device int32 ``[N+1]``).  For
     packed batches the offsets come from ``cu_seqlens`` on the device, and sizing
-    ``ckpt`` reads their total on the host (one synchronisation)."""
+    ``ckpt`` reads their total on the host (one synchronisation).  A caller that
+    passes ``ckpt`` (and, for packed batches, ``offsets``) gets no device work from
+    this function besides the kernels; ``offsets`` is then returned as given."""
     _check_inputs(q, k, v, g, beta)
     N = q.shape[0] if cu_seqlens is None else cu_seqlens.numel() - 1
     shape = make_shape(q, v, packed_seqs=None if cu_seqlens is None else N, scale=scale,
                        out_dtype=out_dtype)
     B, T, H, dk = q.shape
     dv = v.shape[-1]
-    if cu_seqlens is None:
+    if ckpt is not None:
+        if cu_seqlens is not None and offsets is None:
+            raise ValueError("a packed batch with a given ckpt buffer needs its offsets")
+        rows = ckpt.shape[0]
+    elif cu_seqlens is None:
         per = T // interval
         offsets = torch.arange(N + 1, dtype=torch.int32, device=q.device) * per
         rows = N * per
@@ -180,7 +186,8 @@ def fwd_checkpoints(q, k, v, g, beta, *, interval=512, cu_seqlens=None, h0=None,
         offsets = torch.zeros(N + 1, dtype=torch.int32, device=q.device)
         offsets[1:] = torch.cumsum(counts, 0).to(torch.int32)
         rows = int(offsets[-1].item())
-    ckpt = torch.empty(rows, H, dk, dv, dtype=torch.float32, device=q.device)
+    if ckpt is None:
+        ckpt = torch.empty(rows, H, dk, dv, dtype=torch.float32, device=q.device)
     if out is None:
         out = torch.empty(B, T, H, dv, dtype=out_dtype, device=q.device)
     if hT is None and output_final_state:
