@@ -299,7 +299,36 @@ def run_ours(args):
     kms = _time_steps(kfn, max(5, args.steps), max(3, args.warmup), stream, dist_on)
     kbytes = 1024 * H * (2 * STATE_BYTES + 8 * BYTES_PER_TOKEN_HEAD)  # upper bound: all commit
     del y, out_d
-    cms, kms = max_over_ranks([cms, kms], dev)
+    # fused input preprocessing on raw inputs of the same shapes, against the same
+    # preprocessing done by torch ops followed by the plain prefill
+    r = kda_inputs.draw_raw((B, T), H, D, D, device=dev, seed=1001 + 13 * rank)
+    rfn = lambda: kda.fwd_preproc(r.q, r.k, r.v, r.g, r.beta, out=o, hT=hT, workspace=ws)
+    rms = _time_steps(rfn, max(5, args.steps), max(3, args.warmup), stream, dist_on)
+    st = kda.read_device_status(ws)
+    if st != kda.KDA_OK:
+        raise RuntimeError(f"device status {kda.status_string(st)}")
+
+    def unfused():
+        f = torch.nn.functional
+        qn = f.normalize(r.q.float(), dim=-1).to(r.q.dtype)
+        kn = f.normalize(r.k.float(), dim=-1).to(r.k.dtype)
+        gn = (-f.softplus(r.g.float())).to(r.g.dtype)
+        bn = torch.sigmoid(r.beta.float()).to(r.beta.dtype)
+        kda.fwd(qn, kn, r.v, gn, bn, out=o, hT=hT, workspace=ws)
+
+    ums = _time_steps(unfused, max(5, args.steps), max(3, args.warmup), stream, dist_on)
+    del r
+    y = kda_inputs.draw_raw((1024, 1), H, D, D, device=dev, seed=1004 + 13 * rank,
+                            num_states=1024, h0_std=0.1)
+    out_d = torch.empty(1024, 1, H, D, device=dev)
+    dws = kda.new_workspace(kda.make_shape(y.q, y.v), dev)
+    qfn = lambda: kda.decode_preproc(y.q, y.k, y.v, y.g, y.beta, y.h0, out=out_d,
+                                     workspace=dws)
+    qms = _time_steps(qfn, max(5, args.steps), max(3, args.warmup), stream, dist_on)
+    qbytes = 1024 * H * (2 * STATE_BYTES + BYTES_PER_TOKEN_HEAD)
+    del y, out_d
+    cms, kms, rms, ums, qms = max_over_ranks([cms, kms, rms, ums, qms], dev)
+    fbytes = B * T * H * BYTES_PER_TOKEN_HEAD + B * H * STATE_BYTES
     next_rows = {
         "prefill_checkpoints_512": {
             "workload": WORKLOAD + "; state checkpoint every 512 tokens (32 per chain)",
@@ -314,6 +343,20 @@ def run_ours(args):
                          "peak": hbm_peak, "unit": "GB/s",
                          "frac": kbytes / (kms * 1e-3) / 1e9 / hbm_peak,
                          "note": "bytes counted as if every sequence commits"}},
+        "prefill_preproc": {
+            "workload": WORKLOAD.replace("bf16", "bf16 raw") +
+            "; q/k L2 norm, -softplus gate, sigmoid beta fused",
+            "ms_per_step": rms, "overhead_vs_prefill": rms / ms - 1.0,
+            "unfused_ms_per_step": ums,
+            "roofline": {"bound": "hbm", "achieved": fbytes / (rms * 1e-3) / 1e9,
+                         "peak": hbm_peak, "unit": "GB/s",
+                         "frac": fbytes / (rms * 1e-3) / 1e9 / hbm_peak}},
+        "decode_preproc_T1": {
+            "workload": "decode pool 1024 x 32 heads, T_step=1, raw inputs, preprocessing fused",
+            "ms_per_step": qms, "tokens_per_s": 1024 * world / (qms * 1e-3),
+            "roofline": {"bound": "hbm", "achieved": qbytes / (qms * 1e-3) / 1e9,
+                         "peak": hbm_peak, "unit": "GB/s",
+                         "frac": qbytes / (qms * 1e-3) / 1e9 / hbm_peak}},
     }
     clk = clocks.stop()
 

@@ -139,6 +139,38 @@ kda_status kda_fwd_checkpoints(const kda_shape* s, const void* q, const void* k,
                                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Input preprocessing fused into the kernels ("Kimi K3 NPU Training", section
+ * 模型结构, steps 1 and 3: q/k are L2 normalised and the channel-wise decay and
+ * beta are built from the projected gate inputs).  Each enabled step is
+ * computed in float32 from the values passed in and rounded to in_dtype, which is
+ * what a separate preprocessing pass that stores in_dtype tensors produces:
+ *   qk_l2norm      q, k per (token, head):  x / max(||x||_2, 1e-12)
+ *   gate_softplus  g holds the raw gate:    log(alpha) = -softplus(g), with
+ *                  softplus(x) = x for x > 20, else log(1 + e^x)
+ *   beta_sigmoid   beta holds the raw value: beta = 1 / (1 + e^-beta)
+ * A zero-initialised struct disables everything (plain kda_fwd / kda_decode).
+ */
+typedef struct {
+  int32_t qk_l2norm;
+  int32_t gate_softplus;
+  int32_t beta_sigmoid;
+} kda_preproc;
+
+/* kda_fwd with the preprocessing `pre` (NULL = none) applied to q, k, g, beta
+ * inside the kernels.  Arguments, results and errors as kda_fwd. */
+kda_status kda_fwd_preproc(const kda_shape* s, const kda_preproc* pre, const void* q,
+                           const void* k, const void* v, const void* g, const void* beta,
+                           const int32_t* cu_seqlens, const float* h0, void* out, float* hT,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* kda_decode with the preprocessing `pre` (NULL = none).  Arguments, results and
+ * errors as kda_decode. */
+kda_status kda_decode_preproc(const kda_shape* s, const kda_preproc* pre, const void* q,
+                              const void* k, const void* v, const void* g, const void* beta,
+                              float* state, void* out, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/*
  * Decode step: T_step = s->T tokens (1..8) per sequence applied in order to a
  * state pool resident in device memory, updated in place (the replay form of
  * speculative-decode rollback: the cached inputs of the accepted tokens are

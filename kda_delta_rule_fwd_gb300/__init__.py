@@ -42,6 +42,12 @@ class Shape(ctypes.Structure):
                 ("scale", ctypes.c_float)]
 
 
+class Preproc(ctypes.Structure):
+    """Mirror of ``kda_preproc`` (fused input preprocessing flags)."""
+    _fields_ = [("qk_l2norm", ctypes.c_int32), ("gate_softplus", ctypes.c_int32),
+                ("beta_sigmoid", ctypes.c_int32)]
+
+
 class KDAError(RuntimeError):
     def __init__(self, code, where):
         self.code = code
@@ -72,6 +78,11 @@ def load(path: str | None = None):
         lib.kda_fwd_checkpoints.restype = ctypes.c_int
         lib.kda_fwd_checkpoints.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                             ctypes.c_int32, vp, vp, ctypes.c_int64, vp, sz, vp]
+        pp = ctypes.POINTER(Preproc)
+        lib.kda_fwd_preproc.restype = ctypes.c_int
+        lib.kda_fwd_preproc.argtypes = [sp, pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        lib.kda_decode_preproc.restype = ctypes.c_int
+        lib.kda_decode_preproc.argtypes = [sp, pp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         lib.kda_decode.restype = ctypes.c_int
         lib.kda_decode.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         lib.kda_decode_commit.restype = ctypes.c_int
@@ -204,6 +215,54 @@ def fwd_checkpoints(q, k, v, g, beta, *, interval=512, cu_seqlens=None, h0=None,
     if rc != KDA_OK:
         raise KDAError(rc, "kda_fwd_checkpoints")
     return out, hT, ckpt, offsets
+
+
+def fwd_preproc(q, k, v, g, beta, *, qk_l2norm=True, gate_softplus=True, beta_sigmoid=True,
+                cu_seqlens=None, h0=None, scale=None, out_dtype=torch.float32, out=None, hT=None,
+                output_final_state=True, workspace=None, stream=None):
+    """``fwd`` on raw inputs with the preprocessing fused into the kernels: q, k
+    L2-normalised per (token, head), log(alpha) = -softplus(g), beta = sigmoid(beta),
+    each computed in float32 and rounded to the input dtype (selected by the flags)."""
+    _check_inputs(q, k, v, g, beta)
+    N = q.shape[0] if cu_seqlens is None else cu_seqlens.numel() - 1
+    shape = make_shape(q, v, packed_seqs=None if cu_seqlens is None else N, scale=scale,
+                       out_dtype=out_dtype)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty(B, T, H, dv, dtype=out_dtype, device=q.device)
+    if hT is None and output_final_state:
+        hT = torch.empty(N, H, dk, dv, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = new_workspace(shape, q.device)
+    pre = Preproc(int(qk_l2norm), int(gate_softplus), int(beta_sigmoid))
+    rc = load().kda_fwd_preproc(ctypes.byref(shape), ctypes.byref(pre), _ptr(q), _ptr(k),
+                                _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), _ptr(h0),
+                                _ptr(out), _ptr(hT), _ptr(workspace), workspace.numel(),
+                                _stream_ptr(stream))
+    if rc != KDA_OK:
+        raise KDAError(rc, "kda_fwd_preproc")
+    return out, hT
+
+
+def decode_preproc(q, k, v, g, beta, state, *, qk_l2norm=True, gate_softplus=True,
+                   beta_sigmoid=True, scale=None, out_dtype=torch.float32, out=None,
+                   workspace=None, stream=None):
+    """``decode`` on raw inputs with the preprocessing of ``fwd_preproc`` fused in."""
+    _check_inputs(q, k, v, g, beta)
+    shape = make_shape(q, v, scale=scale, out_dtype=out_dtype)
+    B, T, H, dk = q.shape
+    if out is None:
+        out = torch.empty(B, T, H, v.shape[-1], dtype=out_dtype, device=q.device)
+    if workspace is None:
+        workspace = new_workspace(shape, q.device)
+    pre = Preproc(int(qk_l2norm), int(gate_softplus), int(beta_sigmoid))
+    rc = load().kda_decode_preproc(ctypes.byref(shape), ctypes.byref(pre), _ptr(q), _ptr(k),
+                                   _ptr(v), _ptr(g), _ptr(beta), _ptr(state), _ptr(out),
+                                   _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    if rc != KDA_OK:
+        raise KDAError(rc, "kda_decode_preproc")
+    return out
 
 
 def decode(q, k, v, g, beta, state, *, scale=None, out_dtype=torch.float32, out=None,

@@ -56,11 +56,22 @@ size_t kda_workspace_size(const kda_shape* s) {
 
 namespace {
 // shared by kda_fwd and kda_fwd_checkpoints (ckpt == nullptr: no checkpoints)
+Preproc to_preproc(const kda_preproc* p) {
+  Preproc r{0, 0, 0};
+  if (p) {
+    r.l2 = p->qk_l2norm != 0;
+    r.gate = p->gate_softplus != 0;
+    r.beta = p->beta_sigmoid != 0;
+  }
+  return r;
+}
+
 kda_status fwd_common(const kda_shape* s, const void* q, const void* k, const void* v,
                       const void* g, const void* beta, const int32_t* cu_seqlens,
                       const float* h0, void* out, float* hT, float* ckpt,
                       const int32_t* ckpt_offsets, int64_t ckpt_rows, int32_t ckpt_interval,
-                      void* workspace, size_t workspace_bytes, void* stream) {
+                      const kda_preproc* pre, void* workspace, size_t workspace_bytes,
+                      void* stream) {
   const bool packed = cu_seqlens != nullptr;
   kda_status st = check_shape(s, packed);
   if (st != KDA_OK) return st;
@@ -90,6 +101,7 @@ kda_status fwd_common(const kda_shape* s, const void* q, const void* k, const vo
   a.ckpt_off = ckpt_offsets;
   a.ckpt_rows = ckpt_rows;
   a.ckpt_interval = ckpt_interval;
+  a.pre = to_preproc(pre);
   a.stream = static_cast<cudaStream_t>(stream);
 
   if (cudaMemsetAsync(workspace, 0, kWsHeader, a.stream) != cudaSuccess) return KDA_ERR_CUDA;
@@ -119,6 +131,14 @@ kda_status kda_fwd(const kda_shape* s, const void* q, const void* k, const void*
                    const float* h0, void* out, float* hT, void* workspace,
                    size_t workspace_bytes, void* stream) {
   return fwd_common(s, q, k, v, g, beta, cu_seqlens, h0, out, hT, nullptr, nullptr, 0, 0,
+                    nullptr, workspace, workspace_bytes, stream);
+}
+
+kda_status kda_fwd_preproc(const kda_shape* s, const kda_preproc* pre, const void* q,
+                           const void* k, const void* v, const void* g, const void* beta,
+                           const int32_t* cu_seqlens, const float* h0, void* out, float* hT,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  return fwd_common(s, q, k, v, g, beta, cu_seqlens, h0, out, hT, nullptr, nullptr, 0, 0, pre,
                     workspace, workspace_bytes, stream);
 }
 
@@ -131,7 +151,7 @@ kda_status kda_fwd_checkpoints(const kda_shape* s, const void* q, const void* k,
     return KDA_ERR_INVALID_ARG;
   if (cu_seqlens && (!ckpt_offsets || !aligned(ckpt_offsets, 4))) return KDA_ERR_INVALID_ARG;
   return fwd_common(s, q, k, v, g, beta, cu_seqlens, h0, out, hT, ckpt,
-                    cu_seqlens ? ckpt_offsets : nullptr, ckpt_rows, interval, workspace,
+                    cu_seqlens ? ckpt_offsets : nullptr, ckpt_rows, interval, nullptr, workspace,
                     workspace_bytes, stream);
 }
 
@@ -139,8 +159,8 @@ namespace {
 // shared by kda_decode and kda_decode_commit; out may be NULL only with counts
 kda_status decode_common(const kda_shape* s, const void* q, const void* k, const void* v,
                          const void* g, const void* beta, const int32_t* num_commit,
-                         float* state, void* out, void* workspace, size_t workspace_bytes,
-                         void* stream) {
+                         float* state, void* out, const kda_preproc* pre, void* workspace,
+                         size_t workspace_bytes, void* stream) {
   kda_status st = check_shape(s, false);
   if (st != KDA_OK) return st;
   if (s->T < 1 || s->T > 8) return KDA_ERR_UNSUPPORTED;
@@ -162,6 +182,7 @@ kda_status decode_common(const kda_shape* s, const void* q, const void* k, const
   a.out_dtype = s->out_dtype;
   a.num_commit = num_commit;
   a.status = static_cast<unsigned int*>(workspace);
+  a.pre = to_preproc(pre);
   a.stream = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(workspace, 0, kWsHeader, a.stream) != cudaSuccess) return KDA_ERR_CUDA;
   return launch_decode(a) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
@@ -172,8 +193,17 @@ kda_status kda_decode(const kda_shape* s, const void* q, const void* k, const vo
                       const void* g, const void* beta, float* state, void* out,
                       void* workspace, size_t workspace_bytes, void* stream) {
   if (!out) return KDA_ERR_INVALID_ARG;
-  return decode_common(s, q, k, v, g, beta, nullptr, state, out, workspace, workspace_bytes,
-                       stream);
+  return decode_common(s, q, k, v, g, beta, nullptr, state, out, nullptr, workspace,
+                       workspace_bytes, stream);
+}
+
+kda_status kda_decode_preproc(const kda_shape* s, const kda_preproc* pre, const void* q,
+                              const void* k, const void* v, const void* g, const void* beta,
+                              float* state, void* out, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  if (!out) return KDA_ERR_INVALID_ARG;
+  return decode_common(s, q, k, v, g, beta, nullptr, state, out, pre, workspace,
+                       workspace_bytes, stream);
 }
 
 kda_status kda_decode_commit(const kda_shape* s, const void* q, const void* k, const void* v,
@@ -181,8 +211,8 @@ kda_status kda_decode_commit(const kda_shape* s, const void* q, const void* k, c
                              float* state, void* out, void* workspace, size_t workspace_bytes,
                              void* stream) {
   if (!num_commit) return KDA_ERR_INVALID_ARG;
-  return decode_common(s, q, k, v, g, beta, num_commit, state, out, workspace, workspace_bytes,
-                       stream);
+  return decode_common(s, q, k, v, g, beta, num_commit, state, out, nullptr, workspace,
+                       workspace_bytes, stream);
 }
 
 kda_status kda_read_device_status(void* workspace, void* stream) {

@@ -28,13 +28,15 @@ template <> struct VecF<4> { using T = float4; };
 
 // kCommit: per-sequence commit counts (num_commit) decide which state is written
 // back; otherwise the state after all Tstep tokens is.
-template <int D, typename TIn, typename TOut, bool kCommit>
+// kPre: the fused input preprocessing `pre` is applied while the inputs are staged.
+template <int D, typename TIn, typename TOut, bool kCommit, bool kPre>
 __global__ void __launch_bounds__(kDecodeThreads, 2)
 kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                   const TIn* __restrict__ v, const TIn* __restrict__ g,
                   const TIn* __restrict__ beta, float* __restrict__ state,
                   TOut* __restrict__ out, int H, int Tstep, float scale,
-                  const int32_t* __restrict__ num_commit, unsigned int* status) {
+                  const int32_t* __restrict__ num_commit, unsigned int* status,
+                  Preproc pre) {
   constexpr int R = D / 8;     // state rows per warp
   constexpr int CPL = D / 32;  // state columns per lane
   using Vec = typename VecF<CPL>::T;
@@ -69,13 +71,37 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
     const int64_t x = ((n * Tstep + t) * H + h) * D + c;
     s_k[t][c] = to_f32(k[x]);
     s_q[t][c] = to_f32(q[x]);
-    s_a[t][c] = expf(to_f32(g[x]));
+    float gv = to_f32(g[x]);
+    if (kPre && pre.gate) gv = round_to<TIn>(neg_softplus(gv));
+    s_a[t][c] = expf(gv);
     s_v[t][c] = to_f32(v[x]);
   }
-  if (tid < Tstep) s_b[tid] = to_f32(beta[(n * Tstep + tid) * H + h]);
+  if (tid < Tstep) {
+    float bv = to_f32(beta[(n * Tstep + tid) * H + h]);
+    if (kPre && pre.beta) bv = round_to<TIn>(sigmoid_f(bv));
+    s_b[tid] = bv;
+  }
   __syncthreads();
-  // k . q per token, one warp per token
+  // k . q per token, one warp per token (which first normalises that token's q
+  // and k when asked; each lane touches the same channels in both loops)
   if (warp < Tstep) {
+    if (kPre && pre.l2) {
+      float sk = 0.f, sq = 0.f;
+      for (int c = lane; c < D; c += 32) {
+        sk = fmaf(s_k[warp][c], s_k[warp][c], sk);
+        sq = fmaf(s_q[warp][c], s_q[warp][c], sq);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        sk += __shfl_xor_sync(0xffffffffu, sk, o);
+        sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      }
+      const float ik = inv_l2(sk), iq = inv_l2(sq);
+      for (int c = lane; c < D; c += 32) {
+        s_k[warp][c] = round_to<TIn>(s_k[warp][c] * ik);
+        s_q[warp][c] = round_to<TIn>(s_q[warp][c] * iq);
+      }
+    }
     float acc = 0.f;
     for (int c = lane; c < D; c += 32) acc += s_k[warp][c] * s_q[warp][c];
 #pragma unroll
@@ -172,10 +198,9 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
   if (!kCommit) store_state();
 }
 
-template <int D, typename TIn>
-cudaError_t launch_d_in(const DecodeArgs& a) {
+template <int D, typename TIn, bool kPre>
+cudaError_t launch_pre(const DecodeArgs& a) {
   const int64_t blocks = (int64_t)a.B * a.H;
-  if (blocks == 0 || a.Tstep == 0) return cudaSuccess;
   const TIn* q = static_cast<const TIn*>(a.q);
   const TIn* k = static_cast<const TIn*>(a.k);
   const TIn* v = static_cast<const TIn*>(a.v);
@@ -187,20 +212,27 @@ cudaError_t launch_d_in(const DecodeArgs& a) {
   const dim3 grid((unsigned)blocks);
   if (a.num_commit) {
     if (f32)
-      kda_decode_kernel<D, TIn, float, true><<<grid, kDecodeThreads, 0, a.stream>>>(
-          q, k, v, g, b, a.state, of, a.H, a.Tstep, a.scale, a.num_commit, a.status);
+      kda_decode_kernel<D, TIn, float, true, kPre><<<grid, kDecodeThreads, 0, a.stream>>>(
+          q, k, v, g, b, a.state, of, a.H, a.Tstep, a.scale, a.num_commit, a.status, a.pre);
     else
-      kda_decode_kernel<D, TIn, __nv_bfloat16, true><<<grid, kDecodeThreads, 0, a.stream>>>(
-          q, k, v, g, b, a.state, ob, a.H, a.Tstep, a.scale, a.num_commit, a.status);
+      kda_decode_kernel<D, TIn, __nv_bfloat16, true, kPre><<<grid, kDecodeThreads, 0, a.stream>>>(
+          q, k, v, g, b, a.state, ob, a.H, a.Tstep, a.scale, a.num_commit, a.status, a.pre);
   } else {
     if (f32)
-      kda_decode_kernel<D, TIn, float, false><<<grid, kDecodeThreads, 0, a.stream>>>(
-          q, k, v, g, b, a.state, of, a.H, a.Tstep, a.scale, nullptr, a.status);
+      kda_decode_kernel<D, TIn, float, false, kPre><<<grid, kDecodeThreads, 0, a.stream>>>(
+          q, k, v, g, b, a.state, of, a.H, a.Tstep, a.scale, nullptr, a.status, a.pre);
     else
-      kda_decode_kernel<D, TIn, __nv_bfloat16, false><<<grid, kDecodeThreads, 0, a.stream>>>(
-          q, k, v, g, b, a.state, ob, a.H, a.Tstep, a.scale, nullptr, a.status);
+      kda_decode_kernel<D, TIn, __nv_bfloat16, false, kPre><<<grid, kDecodeThreads, 0, a.stream>>>(
+          q, k, v, g, b, a.state, ob, a.H, a.Tstep, a.scale, nullptr, a.status, a.pre);
   }
   return cudaGetLastError();
+}
+
+template <int D, typename TIn>
+cudaError_t launch_d_in(const DecodeArgs& a) {
+  if ((int64_t)a.B * a.H == 0 || a.Tstep == 0) return cudaSuccess;
+  if (a.pre.l2 || a.pre.gate || a.pre.beta) return launch_pre<D, TIn, true>(a);
+  return launch_pre<D, TIn, false>(a);
 }
 
 }  // namespace

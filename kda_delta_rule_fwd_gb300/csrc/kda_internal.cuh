@@ -91,6 +91,25 @@ inline size_t seg_bytes(const SegPlan& pl, int64_t chains, int D) {
 // ---------------------------------------------------------------------------
 // launchers (each returns cudaSuccess or the launch error)
 // ---------------------------------------------------------------------------
+// Fused input preprocessing (kda_preproc): each enabled step in float32, rounded
+// to the input dtype, as a separate pass that stores input-dtype tensors would.
+struct Preproc {
+  int l2;    // q, k: x / max(||x||, 1e-12) per (token, head)
+  int gate;  // log(alpha) = -softplus(g)
+  int beta;  // beta = sigmoid(beta)
+};
+template <typename T> __device__ __forceinline__ float round_to(float x);
+template <> __device__ __forceinline__ float round_to<float>(float x) { return x; }
+template <> __device__ __forceinline__ float round_to<__nv_bfloat16>(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+// -softplus(x), with softplus(x) = x above 20 (where log(1 + e^x) rounds to x)
+__device__ __forceinline__ float neg_softplus(float x) {
+  return -(x > 20.f ? x : log1pf(expf(x)));
+}
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
+__device__ __forceinline__ float inv_l2(float sumsq) { return 1.f / fmaxf(sqrtf(sumsq), 1e-12f); }
+
 struct FwdArgs {
   const void *q, *k, *v, *g, *beta;
   const int32_t* cu;
@@ -109,6 +128,7 @@ struct FwdArgs {
   const int32_t* ckpt_off;  // [N+1] row offsets (packed batches), or nullptr (fixed length)
   int64_t ckpt_rows;
   int64_t ckpt_interval;    // tokens, a multiple of 64
+  Preproc pre;              // all zero: the inputs are used as given
   cudaStream_t stream;
 };
 
@@ -143,6 +163,7 @@ struct DecodeArgs {
   kda_dtype in_dtype, out_dtype;
   const int32_t* num_commit;  // per-sequence commit counts, or nullptr (commit all)
   unsigned int* status;
+  Preproc pre;                // all zero: the inputs are used as given
   cudaStream_t stream;
 };
 

@@ -305,6 +305,7 @@ struct Bf16Params {
   const int32_t* ckpt_off;
   int64_t ckpt_rows;
   int64_t ckpt_interval;
+  Preproc pre;           // fused input preprocessing (kPre instantiation only)
 };
 
 // The CTA's bounded waits.  Every thread waits on the barrier itself; a thread
@@ -338,6 +339,9 @@ struct Waits {
   }
 };
 
+// kPre: the fused input preprocessing p.pre is applied on chip (beta when it is
+// staged, q and k in pass A, the gate on the g tile before its cumulative sum).
+template <bool kPre>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -537,6 +541,21 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     mma_commit(wt.mma_bar);
     return true;
   };
+  // fused gate: log(alpha) = -softplus(raw) rounded to bf16, in place on the g tile of
+  // `chunk`, by every thread once the tile has landed (the cumulative sum reads it next)
+  auto activate_gate = [&](int chunk) {
+    if (!mbar_wait(g_bar, (uint32_t)chunk & 1u)) wt.on_timeout();
+    for (int i = tid; i < (D / 8) * C; i += kThreads) {  // rows of 8 channels
+      float x[8];
+      ld8(smem + SM_IN_G + i * 16, x);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = neg_softplus(x[e]);
+      st8(smem + SM_IN_G + i * 16, x);
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+  };
+  if (kPre && p.pre.gate && nchunks > 0) activate_gate(0);
   if (tid == 0 && nchunks > 0 && !issue_cumsum(0)) wt.on_timeout();
 
 #pragma unroll 1
@@ -547,7 +566,11 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 
     // ---- P1: beta; wait for the q, k, v tiles and for the cumulative log-decay
     // (issued at the end of the previous chunk, or before the loop)
-    if (tid < C) s_beta[tid] = __uint_as_float(beta_bits << 16);
+    if (tid < C) {
+      float bt = __uint_as_float(beta_bits << 16);
+      if (kPre && p.pre.beta && tid < nv) bt = round_to<__nv_bfloat16>(sigmoid_f(bt));
+      s_beta[tid] = bt;
+    }
     if (ci + 1 < nchunks) beta_bits = load_beta_bits(ci + 1);
     if (wt.wait_tma()) break;
     if (wt.wait_mma()) break;
@@ -574,8 +597,40 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (t == nv - 1)
 #pragma unroll
       for (int e = 0; e < GPT * 8; ++e) s_gl[cg0 * 8 + e] = gam[e];
+    // fused q/k normalisation: the 128 channels of a token are spread over NCOL * 2
+    // threads; each leaves its sums of squares in a slot (in the g tile's region,
+    // free once the cumulative sum has run)
+    float* s_nrm = reinterpret_cast<float*>(smem + SM_IN_G + 8192);  // [2][C][2 * NCOL]
+    const int nslot = (row >> 6) * NCOL + cq;
+    if (kPre && p.pre.l2) {
+      float s2k = 0.f, s2q = 0.f;
+#pragma unroll
+      for (int g4 = 0; g4 < GPT; ++g4) {
+        float kx[8], qx[8];
+        ld8(smem + SM_IN_K + (cg0 + g4) * 1024 + t * 16, kx);
+        ld8(smem + SM_IN_Q + (cg0 + g4) * 1024 + t * 16, qx);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          s2k = fmaf(kx[e], kx[e], s2k);
+          s2q = fmaf(qx[e], qx[e], s2q);
+        }
+      }
+      s_nrm[t * 2 * NCOL + nslot] = s2k;
+      s_nrm[(C + t) * 2 * NCOL + nslot] = s2q;
+    }
     tc_fence_before();
     __syncthreads();
+    float inv_k = 1.f, inv_q = 1.f;
+    if (kPre && p.pre.l2) {
+      float s2k = 0.f, s2q = 0.f;
+#pragma unroll
+      for (int j = 0; j < 2 * NCOL; ++j) {
+        s2k += s_nrm[t * 2 * NCOL + j];
+        s2q += s_nrm[(C + t) * 2 * NCOL + j];
+      }
+      inv_k = inv_l2(s2k);
+      inv_q = inv_l2(s2q);
+    }
     if (tid < D) {
       const float e2 = s_rho[tid];
       s_c[tid] = ldexpf(1.f, (int)e2);
@@ -588,6 +643,13 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       float kx[8], qx[8];
       ld8(smem + SM_IN_K + cg * 1024 + t * 16, kx);
       ld8(smem + SM_IN_Q + cg * 1024 + t * 16, qx);
+      if (kPre && p.pre.l2) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          kx[e] = round_to<__nv_bfloat16>(kx[e] * inv_k);
+          qx[e] = round_to<__nv_bfloat16>(qx[e] * inv_q);
+        }
+      }
       const float4 e2a = *reinterpret_cast<const float4*>(s_rho + cg * 8);
       const float4 e2b = *reinterpret_cast<const float4*>(s_rho + cg * 8 + 4);
       const float e2[8] = {e2a.x, e2a.y, e2a.z, e2a.w, e2b.x, e2b.y, e2b.z, e2b.w};
@@ -894,6 +956,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 
     // ---- P13: next chunk's cumulative log-decay (ACC1 and U are free); outputs;
     // S^T <- S'^T diag(e^Gam_last / c)
+    if (kPre && p.pre.gate && ci + 1 < nchunks) activate_gate(ci + 1);
     if (tid == 0 && ci + 1 < nchunks && !issue_cumsum(ci + 1)) wt.on_timeout();
     {
       const int j = row;
@@ -1104,6 +1167,46 @@ bool make_map(CUtensorMap* m, const void* base, int64_t tokens, int H) {
 
 }  // namespace
 
+namespace {
+template <bool kPre>
+cudaError_t run_bf16(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,
+                     const CUtensorMap& mg, const CUtensorMap& mv, const CUtensorMap& mo,
+                     Bf16Params p, int64_t items) {
+  cudaError_t e = cudaFuncSetAttribute(kda_prefill_bf16_kernel<kPre>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const SegPlan pl = seg_plan(a.cu != nullptr, true, items, a.T);
+  if (pl.nseg < 2 || !a.seg_ws) {
+    kda_prefill_bf16_kernel<kPre><<<(unsigned)items, kThreads, SMEM_BYTES, a.stream>>>(
+        mq, mk, mg, mv, mo, p);
+    return cudaGetLastError();
+  }
+  // long chains: transitions of all but the last segment, scan, then outputs
+  const int64_t per = (int64_t)D * D;
+  p.nseg = pl.nseg;
+  p.seg_len = pl.seg_len;
+  p.seg_b = a.seg_ws;
+  p.seg_m = a.seg_ws + items * (pl.nseg - 1) * per;
+  float* seg_s = a.seg_ws + 2 * items * (pl.nseg - 1) * per;
+  p.seg_s = seg_s;
+  p.mode = MODE_SEG_TRANSITION;
+  kda_prefill_bf16_kernel<kPre><<<(unsigned)(items * (pl.nseg - 1) * 2), kThreads, SMEM_BYTES,
+                            a.stream>>>(mq, mk, mg, mv, mo, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(kda_segment_scan_kernel,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kScanSmem)) != cudaSuccess)
+    return e;
+  kda_segment_scan_kernel<<<(unsigned)items, kScanThreads, kScanSmem, a.stream>>>(
+      a.h0, p.seg_m, p.seg_b, seg_s, pl.nseg);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  p.mode = MODE_SEG_OUTPUT;
+  kda_prefill_bf16_kernel<kPre><<<(unsigned)(items * pl.nseg), kThreads, SMEM_BYTES, a.stream>>>(
+      mq, mk, mg, mv, mo, p);
+  return cudaGetLastError();
+}
+}  // namespace
+
 cudaError_t launch_prefill_bf16(const FwdArgs& a) {
   const int64_t items = (int64_t)a.N * a.H;
   if (items == 0) return cudaSuccess;
@@ -1140,38 +1243,9 @@ cudaError_t launch_prefill_bf16(const FwdArgs& a) {
   p.ckpt_off = a.ckpt_off;
   p.ckpt_rows = a.ckpt_rows;
   p.ckpt_interval = a.ckpt_interval > 0 ? a.ckpt_interval : 1;
-  cudaError_t e = cudaFuncSetAttribute(kda_prefill_bf16_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  const SegPlan pl = seg_plan(a.cu != nullptr, true, items, a.T);
-  if (pl.nseg < 2 || !a.seg_ws) {
-    kda_prefill_bf16_kernel<<<(unsigned)items, kThreads, SMEM_BYTES, a.stream>>>(mq, mk, mg, mv,
-                                                                                mo, p);
-    return cudaGetLastError();
-  }
-  // long chains: transitions of all but the last segment, scan, then outputs
-  const int64_t per = (int64_t)D * D;
-  p.nseg = pl.nseg;
-  p.seg_len = pl.seg_len;
-  p.seg_b = a.seg_ws;
-  p.seg_m = a.seg_ws + items * (pl.nseg - 1) * per;
-  float* seg_s = a.seg_ws + 2 * items * (pl.nseg - 1) * per;
-  p.seg_s = seg_s;
-  p.mode = MODE_SEG_TRANSITION;
-  kda_prefill_bf16_kernel<<<(unsigned)(items * (pl.nseg - 1) * 2), kThreads, SMEM_BYTES,
-                            a.stream>>>(mq, mk, mg, mv, mo, p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if ((e = cudaFuncSetAttribute(kda_segment_scan_kernel,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)kScanSmem)) != cudaSuccess)
-    return e;
-  kda_segment_scan_kernel<<<(unsigned)items, kScanThreads, kScanSmem, a.stream>>>(
-      a.h0, p.seg_m, p.seg_b, seg_s, pl.nseg);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  p.mode = MODE_SEG_OUTPUT;
-  kda_prefill_bf16_kernel<<<(unsigned)(items * pl.nseg), kThreads, SMEM_BYTES, a.stream>>>(
-      mq, mk, mg, mv, mo, p);
-  return cudaGetLastError();
+  p.pre = a.pre;
+  if (a.pre.l2 || a.pre.gate || a.pre.beta) return run_bf16<true>(a, mq, mk, mg, mv, mo, p, items);
+  return run_bf16<false>(a, mq, mk, mg, mv, mo, p, items);
 }
 
 }  // namespace kda

@@ -31,7 +31,8 @@ struct F32Smem {
   static constexpr size_t bytes = floats * sizeof(float);
 };
 
-template <int D, int C, typename TIn, typename TOut>
+// kPre: the fused input preprocessing `pre` is applied while the chunk is loaded.
+template <int D, int C, typename TIn, typename TOut, bool kPre>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_prefill_f32_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                        const TIn* __restrict__ v, const TIn* __restrict__ g,
@@ -40,7 +41,7 @@ kda_prefill_f32_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                        TOut* __restrict__ out, float* __restrict__ hT, int H, float scale,
                        unsigned int* __restrict__ status, float* __restrict__ ckpt,
                        const int32_t* __restrict__ ckpt_off, int64_t ckpt_rows,
-                       int64_t ckpt_interval) {
+                       int64_t ckpt_interval, Preproc pre) {
   using L = F32Smem<D, C>;
   constexpr int LD = L::LD;
   extern __shared__ float smem[];
@@ -82,12 +83,37 @@ kda_prefill_f32_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
       if (t < nv) {
         const int64_t x = ((t0 + cs + t) * H + h) * D + c;
         xq = to_f32(q[x]); xk = to_f32(k[x]); xv = to_f32(v[x]); xg = to_f32(g[x]);
+        if (kPre && pre.gate) xg = round_to<TIn>(neg_softplus(xg));
       }
       sq[t * LD + c] = xq; sk[t * LD + c] = xk; sv[t * LD + c] = xv; sG[t * LD + c] = xg;
     }
-    for (int t = tid; t < C; t += kThreads)
-      sb[t] = t < nv ? to_f32(beta[(t0 + cs + t) * H + h]) : 0.f;
+    for (int t = tid; t < C; t += kThreads) {
+      float bt = t < nv ? to_f32(beta[(t0 + cs + t) * H + h]) : 0.f;
+      if (kPre && pre.beta && t < nv) bt = round_to<TIn>(sigmoid_f(bt));
+      sb[t] = bt;
+    }
     __syncthreads();
+    if (kPre && pre.l2) {  // q, k normalised per token, one warp per token
+      const int warp = tid >> 5, lane = tid & 31;
+      for (int t = warp; t < nv; t += kThreads / 32) {
+        float s2k = 0.f, s2q = 0.f;
+        for (int c = lane; c < D; c += 32) {
+          s2k = fmaf(sk[t * LD + c], sk[t * LD + c], s2k);
+          s2q = fmaf(sq[t * LD + c], sq[t * LD + c], s2q);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          s2k += __shfl_xor_sync(0xffffffffu, s2k, o);
+          s2q += __shfl_xor_sync(0xffffffffu, s2q, o);
+        }
+        const float ik = inv_l2(s2k), iq = inv_l2(s2q);
+        for (int c = lane; c < D; c += 32) {
+          sk[t * LD + c] = round_to<TIn>(sk[t * LD + c] * ik);
+          sq[t * LD + c] = round_to<TIn>(sq[t * LD + c] * iq);
+        }
+      }
+      __syncthreads();
+    }
     // 2. inclusive log-decay prefix sums per channel
     for (int c = tid; c < D; c += kThreads) {
       float run = 0.f;
@@ -181,10 +207,10 @@ kda_prefill_f32_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
     for (int i = tid; i < D * D; i += kThreads) hT[st + i] = S[i];
 }
 
-template <int D, int C, typename TIn, typename TOut>
-cudaError_t launch_t(const FwdArgs& a) {
+template <int D, int C, typename TIn, typename TOut, bool kPre>
+cudaError_t launch_p(const FwdArgs& a) {
   using L = F32Smem<D, C>;
-  auto kern = kda_prefill_f32_kernel<D, C, TIn, TOut>;
+  auto kern = kda_prefill_f32_kernel<D, C, TIn, TOut, kPre>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)L::bytes);
   if (e != cudaSuccess) return e;
@@ -195,8 +221,14 @@ cudaError_t launch_t(const FwdArgs& a) {
       static_cast<const TIn*>(a.q), static_cast<const TIn*>(a.k), static_cast<const TIn*>(a.v),
       static_cast<const TIn*>(a.g), static_cast<const TIn*>(a.beta), sv, a.order, a.h0,
       static_cast<TOut*>(a.out), a.hT, a.H, a.scale, a.status, a.ckpt, a.ckpt_off, a.ckpt_rows,
-      a.ckpt_interval);
+      a.ckpt_interval, a.pre);
   return cudaGetLastError();
+}
+
+template <int D, int C, typename TIn, typename TOut>
+cudaError_t launch_t(const FwdArgs& a) {
+  if (a.pre.l2 || a.pre.gate || a.pre.beta) return launch_p<D, C, TIn, TOut, true>(a);
+  return launch_p<D, C, TIn, TOut, false>(a);
 }
 
 template <int D, int C>

@@ -73,6 +73,27 @@ def draw(shape_tok, H, dk, dv, *, dtype=torch.bfloat16, device="cpu", seed=0,
                      dk ** -0.5)
 
 
+def draw_raw(shape_tok, H, dk, dv, *, dtype=torch.bfloat16, device="cpu", seed=0,
+             cu_seqlens=None, num_states=None, h0_std=None):
+    """Like ``draw`` but without the input conventions: q, k ~ N(0, 1) as drawn
+    (not normalised), g and beta the raw N(0, 1) gate inputs (no softplus or
+    sigmoid), all cast to ``dtype``; the inputs of the fused-preprocessing
+    entry points."""
+    gen = _gen(device, seed)
+    f32 = dict(device=device, dtype=torch.float32, generator=gen)
+    q = torch.randn(*shape_tok, H, dk, **f32)
+    k = torch.randn(*shape_tok, H, dk, **f32)
+    v = torch.randn(*shape_tok, H, dv, **f32)
+    graw = torch.randn(*shape_tok, H, dk, **f32)
+    braw = torch.randn(*shape_tok, H, **f32)
+    h0 = None
+    if h0_std is not None:
+        h0 = torch.randn(num_states, H, dk, dv, **f32) * float(h0_std)
+    cast = lambda x: x.to(dtype).contiguous()
+    return KDAInputs(cast(q), cast(k), cast(v), cast(graw), cast(braw), cu_seqlens, h0,
+                     dk ** -0.5)
+
+
 def fixed(B, T, H, d, *, dtype=torch.bfloat16, device="cpu", seed=0, h0_std=None):
     """Fixed-length batch [B, T, H, d]."""
     return draw((B, T), H, d, d, dtype=dtype, device=device, seed=seed,

@@ -20,6 +20,10 @@ Three forms are provided, each citing the passage it follows:
   decomposition that KDA context parallelism rests on ("Kimi K3 模型结构（7）：
   结构决定系统", section 上下文并行: each segment contributes a local transition
   matrix and a zero-start state; a prefix scan combines them).
+* :func:`preprocess` -- the input preprocessing that the fused entry points
+  apply ("Kimi K3 NPU Training", section 模型结构, steps 1 and 3: q/k L2
+  normalisation, channel-wise decay and beta from the gate inputs), evaluated
+  in float64 and rounded to the input dtype.
 
 Parity status: every function here is pinned by ``tests/test_oracle.py``
 against closed forms, special cases and a brute-force Kronecker formulation.
@@ -147,6 +151,30 @@ def recurrent(q, k, v, g, beta, *, cu_seqlens=None, h0=None, scale=None, n_threa
 # ---------------------------------------------------------------------------
 # chunkwise-parallel form (numpy, float64)
 # ---------------------------------------------------------------------------
+
+def preprocess(q, k, g, beta, *, qk_l2norm=True, gate_softplus=True, beta_sigmoid=True):
+    """Preprocessed (q, k, g, beta) as torch tensors of the inputs' dtype.
+
+    Each enabled step follows its definition in float64 on the given values and
+    is then rounded to the input dtype:
+      q, k:  x / max(||x||_2, 1e-12) over the head dimension
+      g:     -softplus(g), softplus(x) = log(1 + e^x) (= x above 20)
+      beta:  1 / (1 + e^-beta)
+    """
+    import torch
+    dt = q.dtype
+    f = lambda t: t.detach().double().cpu().numpy()
+    back = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dt)
+    Q, K, G, Bt = f(q), f(k), f(g), f(beta)
+    if qk_l2norm:
+        Q = Q / np.maximum(np.sqrt(np.sum(Q * Q, axis=-1, keepdims=True)), 1e-12)
+        K = K / np.maximum(np.sqrt(np.sum(K * K, axis=-1, keepdims=True)), 1e-12)
+    if gate_softplus:
+        G = -np.where(G > 20.0, G, np.log1p(np.exp(np.minimum(G, 20.0))))
+    if beta_sigmoid:
+        Bt = 1.0 / (1.0 + np.exp(-Bt))
+    return back(Q), back(K), back(G), back(Bt)
+
 
 def _tri_inv_unit_lower(A):
     """(I + A)^-1 for strictly lower-triangular A, by forward substitution."""

@@ -305,3 +305,75 @@ def test_segment_composition_reproduces_full_run(oracle_mod):
     np.testing.assert_allclose(l[1], r[1], rtol=1e-12, atol=1e-13)
     # the transition of a segment is not the identity-free sum of zero-start states
     assert not np.allclose(hT[0, 0], sum(s[1] for s in segs))
+
+
+# 6. input preprocessing ------------------------------------------------------------
+def test_preprocess_closed_forms(oracle_mod):
+    """sigmoid(0) = 1/2, softplus(0) = ln 2, softplus(x) - softplus(-x) = x,
+    exp(-softplus(x)) = sigmoid(-x), and softplus(x) -> x for large x."""
+    import torch
+    x = torch.tensor([0.0, -3.0, -0.5, 0.25, 2.0, 19.5, 20.5, 60.0], dtype=torch.float64)
+    q = torch.ones(x.numel(), 1, 4, dtype=torch.float64)
+    _, _, g, b = oracle_mod.preprocess(q, q, x.view(-1, 1, 1).expand(-1, 1, 4), x.view(-1, 1),
+                                       qk_l2norm=False)
+    _, _, gm, bm = oracle_mod.preprocess(q, q, (-x).view(-1, 1, 1).expand(-1, 1, 4),
+                                         (-x).view(-1, 1), qk_l2norm=False)
+    sp, spm = -g[:, 0, 0].numpy(), -gm[:, 0, 0].numpy()
+    sig, sigm = b[:, 0].numpy(), bm[:, 0].numpy()
+    xs = x.numpy()
+    assert sig[0] == 0.5
+    assert abs(sp[0] - np.log(2.0)) < 1e-15
+    exact = np.abs(xs) <= 20.0
+    np.testing.assert_allclose((sp - spm)[exact], xs[exact], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(np.exp(-sp)[exact], sigm[exact], rtol=1e-12, atol=0)
+    # above 20 softplus is taken as x: the error is log1p(e^-x) < e^-20
+    np.testing.assert_allclose((sp - spm)[~exact], xs[~exact], rtol=0, atol=np.exp(-20.0))
+    np.testing.assert_allclose(sig + sigm, 1.0, rtol=0, atol=1e-15)
+    assert sp[-1] == 60.0 and sp[-2] == 20.5
+    # a decay from the gate is in (0, 1]: -softplus(x) < 0
+    assert np.all(g.numpy() < 0)
+
+
+def test_preprocess_l2_norm(oracle_mod):
+    """Normalised q, k have unit norm and the same direction; a zero vector stays
+    zero (the 1e-12 floor); the steps are independent of one another."""
+    import torch
+    rng = np.random.default_rng(61)
+    q = torch.from_numpy(rng.standard_normal((5, 2, 7)) * 3.0)
+    k = torch.from_numpy(rng.standard_normal((5, 2, 7)) * 0.01)
+    k[2, 1] = 0.0
+    g = torch.from_numpy(rng.standard_normal((5, 2, 7)))
+    b = torch.from_numpy(rng.standard_normal((5, 2)))
+    qn, kn, gn, bn = oracle_mod.preprocess(q, k, g, b, gate_softplus=False, beta_sigmoid=False)
+    nq = torch.linalg.vector_norm(qn, dim=-1)
+    nk = torch.linalg.vector_norm(kn, dim=-1)
+    np.testing.assert_allclose(nq.numpy(), 1.0, rtol=0, atol=1e-14)
+    mask = torch.ones(5, 2, dtype=torch.bool)
+    mask[2, 1] = False
+    np.testing.assert_allclose(nk[mask].numpy(), 1.0, rtol=0, atol=1e-14)
+    assert torch.all(kn[2, 1] == 0)
+    # same direction: x = ||x|| * x_hat
+    np.testing.assert_allclose((qn * torch.linalg.vector_norm(q, dim=-1, keepdim=True)).numpy(),
+                               q.numpy(), rtol=1e-13, atol=1e-15)
+    assert torch.equal(gn, g) and torch.equal(bn, b)
+    # all steps off: identity
+    out = oracle_mod.preprocess(q, k, g, b, qk_l2norm=False, gate_softplus=False,
+                                beta_sigmoid=False)
+    for a, e in zip(out, (q, k, g, b)):
+        assert torch.equal(a, e)
+
+
+def test_preprocess_rounds_to_input_dtype(oracle_mod):
+    """bf16 inputs come back as bf16, each value the rounding of the float64 result."""
+    import torch
+    x = torch.tensor([[[0.3, -1.7, 2.2, 0.0]]], dtype=torch.bfloat16)
+    b = torch.tensor([[0.7]], dtype=torch.bfloat16)
+    qn, kn, gn, bn = oracle_mod.preprocess(x, x, x, b)
+    assert qn.dtype == torch.bfloat16 and bn.dtype == torch.bfloat16
+    xd = x.double().numpy()[0, 0]
+    want_q = xd / np.sqrt(np.sum(xd * xd))
+    want_g = -np.log1p(np.exp(xd))
+    want_b = 1.0 / (1.0 + np.exp(-0.69921875))   # bf16(0.7)
+    assert torch.equal(qn[0, 0], torch.from_numpy(want_q).to(torch.bfloat16))
+    assert torch.equal(gn[0, 0], torch.from_numpy(want_g).to(torch.bfloat16))
+    assert bn.item() == torch.tensor(want_b).to(torch.bfloat16).item()
