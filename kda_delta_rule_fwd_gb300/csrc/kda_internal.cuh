@@ -103,9 +103,18 @@ template <> __device__ __forceinline__ float round_to<float>(float x) { return x
 template <> __device__ __forceinline__ float round_to<__nv_bfloat16>(float x) {
   return __bfloat162float(__float2bfloat16_rn(x));
 }
-// -softplus(x), with softplus(x) = x above 20 (where log(1 + e^x) rounds to x)
+// -softplus(x) from softplus(x) = max(x, 0) + log1p(y), y = e^-|x| in (0, 1], on the
+// special-function unit: y = 2^(-|x| log2 e); log1p(y) as ln 2 * log2(1 + y) for
+// y >= 1/32 and as its Taylor series y - y^2/2 + y^3/3 - y^4/4 below (truncation
+// under y^5/5, relative 2^-20; there 1 + y would lose y's low bits).  Absolute
+// error below 4e-7 before the final rounding; log1p(y) rounds away above |x| ~ 17.
 __device__ __forceinline__ float neg_softplus(float x) {
-  return -(x > 20.f ? x : log1pf(expf(x)));
+  float y, l2;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(-fabsf(x) * 1.4426950408889634f));
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(1.f + y));
+  const float series = y * fmaf(y, fmaf(y, fmaf(y, -0.25f, 1.f / 3.f), -0.5f), 1.f);
+  const float l = y < 0.03125f ? series : l2 * 0.6931471805599453f;
+  return -(fmaxf(x, 0.f) + l);
 }
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
 __device__ __forceinline__ float inv_l2(float sumsq) { return 1.f / fmaxf(sqrtf(sumsq), 1e-12f); }

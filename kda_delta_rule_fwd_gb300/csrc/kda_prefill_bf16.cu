@@ -58,13 +58,14 @@ constexpr float kRefExp2 = 100.f;  // |log2 c| is clamped here (S' and its bf16 
 // ---- shared memory map (bytes) --------------------------------------------
 constexpr uint32_t SM_IN_Q = 0;          // TMA tiles, [8-channel group][token][8] bf16
 constexpr uint32_t SM_IN_K = 16384;
-constexpr uint32_t SM_IN_G = 32768;
+constexpr uint32_t SM_NRM = 32768;       // pass A: q/k sums of squares (fused normalisation)
+constexpr uint32_t SM_GB = 40960;        // g tile, tokens 32..63: [group][32 tokens][8] bf16
 constexpr uint32_t SM_IN_V = 49152;
-// forward-substitution scratch, over the q, k and g tiles once pass A has read them
+// forward-substitution scratch, over the q and k tiles once pass A has read them
 constexpr uint32_t SV_AT = 0, SV_T32 = 17408, SV_M32 = 34304;
 constexpr int ALD = 68;  // row stride of A^T (float): fragment loads hit distinct banks
 constexpr int TLD = 66;  // row stride of T (float): 8-byte rows, few bank conflicts
-static_assert(SV_M32 + 4 * 256 * 4 <= SM_IN_V, "substitution scratch overlaps the v tile");
+static_assert(SV_M32 + 4 * 256 * 4 <= SM_GB, "substitution scratch overlaps the g tile");
 constexpr uint32_t SM_X = 65536;         // 96 KB: [R_K; R_Q] hi, lo (K-major), Ck hi, lo
 constexpr uint32_t X_R_HI = 0, X_R_LO = 32768, X_CK_HI = 65536, X_CK_LO = 81920;
 constexpr uint32_t X_OUT = 0;  // output staging for the bulk store, [64 tokens][128] (32 KB)
@@ -75,7 +76,9 @@ constexpr uint32_t SM_MISC = 212992;
 constexpr uint32_t MISC_RHO = 0, MISC_GL = 512, MISC_C = 1024, MISC_GAMC = 2048,
                    MISC_BETA = 2560, MISC_BAR = 2816, MISC_TMEM = 2848, MISC_FLAG = 2852;
 constexpr uint32_t SM_NEGI = 216064;     // -I (64 x 64 bf16, K-major): adds -V^T on the tensor core
-constexpr uint32_t SMEM_BYTES = SM_NEGI + 8192;
+constexpr uint32_t SM_GA = SM_NEGI + 8192;  // g tile, tokens 0..31 (the two halves are
+                                             // loaded a chunk ahead, outside the scratch)
+constexpr uint32_t SMEM_BYTES = SM_GA + 8192;
 static_assert(SM_MISC + 2880 <= SM_NEGI && SMEM_BYTES <= 232448, "shared memory map");
 
 // ---- tensor memory map (columns) -------------------------------------------
@@ -460,21 +463,29 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   // parts are issued from different warps so their issue latencies overlap
   // (a tile's bytes may land before the barrier is armed: the transaction count
   // only has to balance when the arrival comes)
-  // The g tile completes on its own barrier: the next chunk's cumulative sum is
-  // issued as soon as it lands, ahead of the q, k and v tiles' consumers.
+  // The g tile completes on its own barrier and travels as two 32-token halves
+  // in buffers of their own: the next chunk's tile is loaded as soon as this
+  // chunk's cumulative sum has read the previous one (a chunk ahead of the q, k
+  // and v tiles, which share their buffers with the substitution scratch).
   uint64_t* g_bar = &bars[3];
   uint32_t g_issued = 0, g_waited = 0;  // g_waited: thread 0's count
-  auto issue_tma_part = [&](int chunk, int part) {
+  auto issue_tma_part = [&](int chunk, int part) {  // 0: q, 1: k, 2: v
     const int32_t y = (int32_t)(t0 + (int64_t)chunk * C);
     const int32_t z = h * (D / 8);
-    uint64_t* bar = part == 2 ? g_bar : wt.tma_bar;
     if (part == 0) mbar_arrive_expect_tx(wt.tma_bar, 3 * 16384);
-    if (part == 2) mbar_arrive_expect_tx(g_bar, 16384);
-    const CUtensorMap* m = part == 0 ? &tm_q : part == 1 ? &tm_k : part == 2 ? &tm_g : &tm_v;
-    tma_load_3d(smem + SM_IN_Q + part * 16384, m, 0, y, z, bar);
+    const CUtensorMap* m = part == 0 ? &tm_q : part == 1 ? &tm_k : &tm_v;
+    tma_load_3d(smem + (part == 2 ? SM_IN_V : SM_IN_Q + part * 16384), m, 0, y, z, wt.tma_bar);
   };
-  if (tid == 0 && nchunks > 0)
-    for (int part = 0; part < 4; ++part) issue_tma_part(0, part);
+  auto issue_g_half = [&](int chunk, int half) {
+    const int32_t y = (int32_t)(t0 + (int64_t)chunk * C + half * (C / 2));
+    if (half == 0) mbar_arrive_expect_tx(g_bar, 16384);
+    tma_load_3d(smem + (half ? SM_GB : SM_GA), &tm_g, 0, y, h * (D / 8), g_bar);
+  };
+  if (tid == 0 && nchunks > 0) {
+    for (int part = 0; part < 3; ++part) issue_tma_part(0, part);
+    issue_g_half(0, 0);
+    issue_g_half(0, 1);
+  }
   if (nchunks > 0) {
     ++tma_issued;
     ++g_issued;
@@ -527,8 +538,9 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   // log2 of the chunk's per-channel reference c (an integer, clamped)
   auto ref_log2 = [](float rho) { return fminf(fmaxf(rintf(rho * kLog2e), -kRefExp2), kRefExp2); };
   // thread 0: once the g tile of `chunk` has landed, Gam (rows 0..63 and again
-  // 64..127) = [L; L] G with G the g tile as an MN-major B, committed to mma_bar;
-  // returns false if the wait ran out
+  // 64..127) = [L; L] G with G the g tile as an MN-major B (K steps 0, 1 on the
+  // first half, 2, 3 on the second), committed to mma_bar; returns false if the
+  // wait ran out
   auto issue_cumsum = [&](int chunk) -> bool {
     const bool ok = mbar_wait(g_bar, (uint32_t)chunk & 1u);
     ++g_waited;
@@ -537,25 +549,32 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
     for (int kk = 0; kk < C / 16; ++kk)
       mma_ss(tb + TM_ACC1, (smem_desc(sbase + SM_LL, 128, 1024) + (uint64_t)(kk * 16)),
-             (smem_desc(sbase + SM_IN_G, 128, 1024) + (uint64_t)(kk * 16)), idesc_cum, kk > 0);
+             (smem_desc(sbase + (kk < 2 ? SM_GA : SM_GB), 128, 512) + (uint64_t)((kk & 1) * 16)),
+             idesc_cum, kk > 0);
     mma_commit(wt.mma_bar);
     return true;
   };
-  // fused gate: log(alpha) = -softplus(raw) rounded to bf16, in place on the g tile of
-  // `chunk`, by every thread once the tile has landed (the cumulative sum reads it next)
-  auto activate_gate = [&](int chunk) {
+  // fused gate: log(alpha) = -softplus(raw) rounded to bf16, in place on both halves
+  // of the g tile of `chunk` (rows of 8 channels), by `nthr` threads numbered from
+  // `i`, once the tile has landed; the callers order these writes before the
+  // cumulative sum (a proxy fence and a CTA barrier)
+  auto activate_gate = [&](int chunk, int i, int nthr) {
     if (!mbar_wait(g_bar, (uint32_t)chunk & 1u)) wt.on_timeout();
-    for (int i = tid; i < (D / 8) * C; i += kThreads) {  // rows of 8 channels
+    constexpr int kHalfRows = (D / 8) * (C / 2);
+    for (; i < 2 * kHalfRows; i += nthr) {
+      uint8_t* r = smem + (i < kHalfRows ? SM_GA + i * 16 : SM_GB + (i - kHalfRows) * 16);
       float x[8];
-      ld8(smem + SM_IN_G + i * 16, x);
+      ld8(r, x);
 #pragma unroll
       for (int e = 0; e < 8; ++e) x[e] = neg_softplus(x[e]);
-      st8(smem + SM_IN_G + i * 16, x);
+      st8(r, x);
     }
+  };
+  if (kPre && p.pre.gate && nchunks > 0) {
+    activate_gate(0, tid, kThreads);
     fence_proxy_async_smem();
     __syncthreads();
-  };
-  if (kPre && p.pre.gate && nchunks > 0) activate_gate(0);
+  }
   if (tid == 0 && nchunks > 0 && !issue_cumsum(0)) wt.on_timeout();
 
 #pragma unroll 1
@@ -574,6 +593,11 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (ci + 1 < nchunks) beta_bits = load_beta_bits(ci + 1);
     if (wt.wait_tma()) break;
     if (wt.wait_mma()) break;
+    // the cumulative sum has read the g tile: load the next chunk's
+    if (ci + 1 < nchunks) {
+      if (lane == 0 && (warp == 1 || warp == 2)) issue_g_half(ci + 1, warp - 1);
+      ++g_issued;
+    }
 
     // ---- P3 (pass A): per-channel reference, the decayed key/query operands
     // (the previous chunk's output store reads X until it completes)
@@ -600,7 +624,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     // fused q/k normalisation: the 128 channels of a token are spread over NCOL * 2
     // threads; each leaves its sums of squares in a slot (in the g tile's region,
     // free once the cumulative sum has run)
-    float* s_nrm = reinterpret_cast<float*>(smem + SM_IN_G + 8192);  // [2][C][2 * NCOL]
+    float* s_nrm = reinterpret_cast<float*>(smem + SM_NRM);  // [2][C][2 * NCOL]
     const int nslot = (row >> 6) * NCOL + cq;
     if (kPre && p.pre.l2) {
       float s2k = 0.f, s2q = 0.f;
@@ -870,6 +894,9 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
         mma_commit(xo_bar);
       }
+      // the next chunk's gate, while the products with S' run (its writes are
+      // fenced for the cumulative sum at the join)
+      if (kPre && p.pre.gate && ci + 1 < nchunks) activate_gate(ci + 1, tid - 256, 256);
       // this warp: lane quarter qd, tokens h8 * 32 .. h8 * 32 + 31 of X'^T
       if (!mbar_wait(xo_bar, (xo_issued - 1) & 1u)) wt.on_timeout();
       tc_fence_after();
@@ -894,12 +921,11 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     __syncthreads();
     if (*(volatile uint32_t*)s_flag) break;
 
-    // ---- P8: prefetch chunk ci+1 (the q, k, g, v tiles are consumed; warps 1-4
+    // ---- P8: prefetch chunk ci+1 (the q, k, v tiles are consumed; warps 1-3
     // issue one tile each); U^T = X'^T (-TB)^T with split operands
     if (ci + 1 < nchunks) {
-      if (lane == 0 && warp >= 1 && warp <= 4) issue_tma_part(ci + 1, warp - 1);
+      if (lane == 0 && warp >= 1 && warp <= 3) issue_tma_part(ci + 1, warp - 1);
       ++tma_issued;
-      ++g_issued;
     }
     if (tid == 0) {
       tc_fence_after();
@@ -956,7 +982,6 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 
     // ---- P13: next chunk's cumulative log-decay (ACC1 and U are free); outputs;
     // S^T <- S'^T diag(e^Gam_last / c)
-    if (kPre && p.pre.gate && ci + 1 < nchunks) activate_gate(ci + 1);
     if (tid == 0 && ci + 1 < nchunks && !issue_cumsum(ci + 1)) wt.on_timeout();
     {
       const int j = row;
@@ -1152,12 +1177,12 @@ bool make_out_map(CUtensorMap* m, void* base, int64_t tokens, int H, bool bf16) 
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool make_map(CUtensorMap* m, const void* base, int64_t tokens, int H) {
+bool make_map(CUtensorMap* m, const void* base, int64_t tokens, int H, int box_tokens = C) {
   auto enc = get_encode();
   if (!enc) return false;
   cuuint64_t dims[3] = {8, (cuuint64_t)tokens, (cuuint64_t)H * (D / 8)};
   cuuint64_t strides[2] = {(cuuint64_t)H * D * 2, 16};
-  cuuint32_t box[3] = {8, C, D / 8};
+  cuuint32_t box[3] = {8, (cuuint32_t)box_tokens, D / 8};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -1219,7 +1244,7 @@ cudaError_t launch_prefill_bf16(const FwdArgs& a) {
   const int64_t map_tokens = tokens > 0 ? tokens : 1;
   CUtensorMap mq, mk, mg, mv, mo;
   if (!make_map(&mq, pick(a.q), map_tokens, a.H) || !make_map(&mk, pick(a.k), map_tokens, a.H) ||
-      !make_map(&mg, pick(a.g), map_tokens, a.H) || !make_map(&mv, pick(a.v), map_tokens, a.H) ||
+      !make_map(&mg, pick(a.g), map_tokens, a.H, C / 2) || !make_map(&mv, pick(a.v), map_tokens, a.H) ||
       !make_out_map(&mo, tokens > 0 ? a.out : const_cast<void*>(dummy), map_tokens, a.H,
                     tokens > 0 && a.out_dtype == KDA_BF16))
     return cudaErrorInvalidValue;

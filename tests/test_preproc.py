@@ -154,3 +154,32 @@ def test_decode_preproc_continues_prefill_preproc(kda, oracle_mod):
     o_ref, h_ref = oracle_mod.recurrent(fq, fk, x.v, fg, fb, h0=x.h0)
     assert rel_err(torch.cat(outs, 1), o_ref[:, P:]) <= TOL_BF16
     assert rel_err(hT, h_ref) <= TOL_BF16
+
+
+def test_gate_activation_precision(kda):
+    """float32 decode from h0 = I with k = 0: the state after one token is
+    diag(alpha), alpha = exp(-softplus(g)), so its diagonal shows the kernel's
+    gate activation.  Over g in [-40, 40] the relative error of alpha (= the
+    absolute error of log(alpha)) stays within the activation's 4e-7 plus the
+    float32 roundings of log(alpha) and of exp."""
+    n, H, d = 48, 4, 128
+    gen = torch.Generator().manual_seed(590)
+    graw = torch.linspace(-40.0, 40.0, n * H * d, dtype=torch.float64)
+    graw = graw[torch.randperm(graw.numel(), generator=gen)].reshape(n, 1, H, d)
+    g32 = graw.float()
+    q = torch.randn(n, 1, H, d, generator=gen)
+    v = torch.randn(n, 1, H, d, generator=gen)
+    b = torch.randn(n, 1, H, generator=gen)
+    k = torch.zeros(n, 1, H, d)
+    state = torch.eye(d).expand(n, H, d, d).contiguous().to(DEV)
+    kda.decode_preproc(q.to(DEV), k.to(DEV), v.to(DEV), g32.to(DEV), b.to(DEV), state)
+    torch.cuda.synchronize()
+    st = state.double().cpu()
+    alpha = st.diagonal(dim1=-2, dim2=-1)
+    off = st - torch.diag_embed(alpha)
+    assert torch.count_nonzero(off) == 0
+    logalpha = -torch.logaddexp(torch.zeros_like(graw), g32.double())[:, 0]
+    ref = torch.exp(logalpha)
+    rel = (alpha - ref).abs() / ref
+    bound = 7e-7 + 1.2e-7 * logalpha.abs()
+    assert torch.all(rel <= bound), float((rel / bound).max())
