@@ -116,8 +116,10 @@ __device__ __forceinline__ float neg_softplus(float x) {
   const float l = y < 0.03125f ? series : l2 * 0.6931471805599453f;
   return -(fmaxf(x, 0.f) + l);
 }
-__device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
-__device__ __forceinline__ float inv_l2(float sumsq) { return 1.f / fmaxf(sqrtf(sumsq), 1e-12f); }
+// 1 / (1 + e^-x) with the fast exponential and division (a few ulp; 0 below x ~ -87)
+__device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
+// 1 / max(||x||, 1e-12) from the sum of squares, as rsqrt(max(sumsq, 1e-24))
+__device__ __forceinline__ float inv_l2(float sumsq) { return rsqrtf(fmaxf(sumsq, 1e-24f)); }
 
 struct FwdArgs {
   const void *q, *k, *v, *g, *beta;

@@ -52,15 +52,16 @@ constexpr int SCOL = 128 / NCOL;      // state columns per thread
 constexpr int GPT = 16 / (2 * NCOL);  // 8-channel groups per thread in the elementwise passes
 static_assert(TCOL == 16 && SCOL % 16 == 0 && GPT >= 1, "thread mapping");
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kGateRowsP8 = 384;  // fused gate rows activated during the U product
 constexpr float kMaxExp2 = 115.f;  // |log2 of a decay factor| beyond this overflows it
 constexpr float kRefExp2 = 100.f;  // |log2 c| is clamped here (S' and its bf16 parts stay normal)
 
 // ---- shared memory map (bytes) --------------------------------------------
-constexpr uint32_t SM_IN_Q = 0;          // TMA tiles, [8-channel group][token][8] bf16
-constexpr uint32_t SM_IN_K = 16384;
+constexpr uint32_t SM_IN_Q = 0;          // q, k tiles: two 64-channel halves, 128-byte swizzle
+constexpr uint32_t SM_IN_K = 16384;      // (see off_sw128)
 constexpr uint32_t SM_NRM = 32768;       // pass A: q/k sums of squares (fused normalisation)
 constexpr uint32_t SM_GB = 40960;        // g tile, tokens 32..63: [group][32 tokens][8] bf16
-constexpr uint32_t SM_IN_V = 49152;
+constexpr uint32_t SM_IN_V = 49152;      // v and g tiles: [8-channel group][token][8] bf16
 // forward-substitution scratch, over the q and k tiles once pass A has read them
 constexpr uint32_t SV_AT = 0, SV_T32 = 17408, SV_M32 = 34304;
 constexpr int ALD = 68;  // row stride of A^T (float): fragment loads hit distinct banks
@@ -102,6 +103,14 @@ __device__ __forceinline__ uint32_t off_kmaj(int r, int k, int kdim) {
 }
 __device__ __forceinline__ uint32_t off_mnmaj(int r, int k, int kdim) {
   return (r >> 3) * (kdim >> 3) * 128 + (k >> 3) * 128 + (k & 7) * 16 + (r & 7) * 2;
+}
+
+// Byte offset of channels 8 cg .. 8 cg + 7 of token t in a q or k tile: each
+// 64-channel half is 64 rows of 128 bytes (one per token) whose 16-byte chunks
+// sit at chunk ^ (t & 7) (the 128-byte swizzle of the tile loads; lanes on
+// consecutive tokens then read distinct banks).
+__device__ __forceinline__ uint32_t off_sw128(int t, int cg) {
+  return (cg >> 3) * 8192 + t * 128 + (((cg & 7) ^ (t & 7)) << 4);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -370,6 +379,11 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   // starts; the value cannot change while it runs, so the test is CTA-uniform.
   if (p.status && *(volatile const unsigned int*)p.status == (unsigned)KDA_ERR_BAD_SEQLENS)
     return;
+  // the swizzled tile layout assumes a 1024-byte aligned window (CTA-uniform test)
+  if (smem_u32(smem) & 1023u) {
+    if (tid == 0) latch_status(p.status, KDA_ERR_CUDA);
+    return;
+  }
 
   const int item = blockIdx.x;
   int n, h;
@@ -469,12 +483,15 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   // and v tiles, which share their buffers with the substitution scratch).
   uint64_t* g_bar = &bars[3];
   uint32_t g_issued = 0, g_waited = 0;  // g_waited: thread 0's count
-  auto issue_tma_part = [&](int chunk, int part) {  // 0: q, 1: k, 2: v
+  // parts 0-3: the 64-channel halves of q and k (128-byte rows); 4: v
+  auto issue_tma_part = [&](int chunk, int part) {
     const int32_t y = (int32_t)(t0 + (int64_t)chunk * C);
-    const int32_t z = h * (D / 8);
     if (part == 0) mbar_arrive_expect_tx(wt.tma_bar, 3 * 16384);
-    const CUtensorMap* m = part == 0 ? &tm_q : part == 1 ? &tm_k : &tm_v;
-    tma_load_3d(smem + (part == 2 ? SM_IN_V : SM_IN_Q + part * 16384), m, 0, y, z, wt.tma_bar);
+    if (part < 4)
+      tma_load_2d(smem + SM_IN_Q + part * 8192, part < 2 ? &tm_q : &tm_k,
+                  (int32_t)(h * D + (part & 1) * 64), y, wt.tma_bar);
+    else
+      tma_load_3d(smem + SM_IN_V, &tm_v, 0, y, h * (D / 8), wt.tma_bar);
   };
   auto issue_g_half = [&](int chunk, int half) {
     const int32_t y = (int32_t)(t0 + (int64_t)chunk * C + half * (C / 2));
@@ -482,7 +499,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     tma_load_3d(smem + (half ? SM_GB : SM_GA), &tm_g, 0, y, h * (D / 8), g_bar);
   };
   if (tid == 0 && nchunks > 0) {
-    for (int part = 0; part < 3; ++part) issue_tma_part(0, part);
+    for (int part = 0; part < 5; ++part) issue_tma_part(0, part);
     issue_g_half(0, 0);
     issue_g_half(0, 1);
   }
@@ -554,14 +571,15 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     mma_commit(wt.mma_bar);
     return true;
   };
-  // fused gate: log(alpha) = -softplus(raw) rounded to bf16, in place on both halves
-  // of the g tile of `chunk` (rows of 8 channels), by `nthr` threads numbered from
-  // `i`, once the tile has landed; the callers order these writes before the
-  // cumulative sum (a proxy fence and a CTA barrier)
-  auto activate_gate = [&](int chunk, int i, int nthr) {
+  // fused gate: log(alpha) = -softplus(raw) rounded to bf16, in place on rows
+  // [i, end) of the g tile of `chunk` (16-byte rows of 8 channels; 0..511 in the
+  // first half, 512..1023 in the second), stepping by `nthr`, once the tile has
+  // landed; the callers order these writes before the cumulative sum (a proxy
+  // fence and a CTA barrier)
+  constexpr int kHalfRows = (D / 8) * (C / 2);
+  auto activate_gate = [&](int chunk, int i, int end, int nthr) {
     if (!mbar_wait(g_bar, (uint32_t)chunk & 1u)) wt.on_timeout();
-    constexpr int kHalfRows = (D / 8) * (C / 2);
-    for (; i < 2 * kHalfRows; i += nthr) {
+    for (; i < end; i += nthr) {
       uint8_t* r = smem + (i < kHalfRows ? SM_GA + i * 16 : SM_GB + (i - kHalfRows) * 16);
       float x[8];
       ld8(r, x);
@@ -570,8 +588,27 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       st8(r, x);
     }
   };
-  if (kPre && p.pre.gate && nchunks > 0) {
-    activate_gate(0, tid, kThreads);
+  // fused normalisation, warps 12-15: once the q and k tiles of `chunk` have
+  // landed, the per-token sums of squares (s_nrm[token] for k, s_nrm[C + token]
+  // for q); a lane per token (eight consecutive tokens cover all banks)
+  float* s_nrm = reinterpret_cast<float*>(smem + SM_NRM);
+  auto qk_sumsq = [&](uint32_t phase) {
+    if (!mbar_wait(wt.tma_bar, phase & 1u)) wt.on_timeout();
+    const int j = tid - 384, tt = j & (C - 1), isq = j >> 6;
+    const uint8_t* base = smem + (isq ? SM_IN_Q : SM_IN_K);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int cg = 0; cg < D / 8; ++cg) {
+      float x[8];
+      ld8(base + off_sw128(tt, cg), x);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e & 3] = fmaf(x[e], x[e], acc[e & 3]);
+    }
+    s_nrm[isq * C + tt] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+  };
+  if (kPre && nchunks > 0 && (p.pre.gate || p.pre.l2)) {
+    if (p.pre.gate) activate_gate(0, tid, 2 * kHalfRows, kThreads);
+    if (p.pre.l2 && warp >= 12) qk_sumsq(0);
     fence_proxy_async_smem();
     __syncthreads();
   }
@@ -587,7 +624,10 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     // (issued at the end of the previous chunk, or before the loop)
     if (tid < C) {
       float bt = __uint_as_float(beta_bits << 16);
-      if (kPre && p.pre.beta && tid < nv) bt = round_to<__nv_bfloat16>(sigmoid_f(bt));
+      if (kPre) {  // branch-free select
+        const float sb = round_to<__nv_bfloat16>(sigmoid_f(bt));
+        bt = p.pre.beta && tid < nv ? sb : bt;
+      }
       s_beta[tid] = bt;
     }
     if (ci + 1 < nchunks) beta_bits = load_beta_bits(ci + 1);
@@ -621,39 +661,12 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (t == nv - 1)
 #pragma unroll
       for (int e = 0; e < GPT * 8; ++e) s_gl[cg0 * 8 + e] = gam[e];
-    // fused q/k normalisation: the 128 channels of a token are spread over NCOL * 2
-    // threads; each leaves its sums of squares in a slot (in the g tile's region,
-    // free once the cumulative sum has run)
-    float* s_nrm = reinterpret_cast<float*>(smem + SM_NRM);  // [2][C][2 * NCOL]
-    const int nslot = (row >> 6) * NCOL + cq;
-    if (kPre && p.pre.l2) {
-      float s2k = 0.f, s2q = 0.f;
-#pragma unroll
-      for (int g4 = 0; g4 < GPT; ++g4) {
-        float kx[8], qx[8];
-        ld8(smem + SM_IN_K + (cg0 + g4) * 1024 + t * 16, kx);
-        ld8(smem + SM_IN_Q + (cg0 + g4) * 1024 + t * 16, qx);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          s2k = fmaf(kx[e], kx[e], s2k);
-          s2q = fmaf(qx[e], qx[e], s2q);
-        }
-      }
-      s_nrm[t * 2 * NCOL + nslot] = s2k;
-      s_nrm[(C + t) * 2 * NCOL + nslot] = s2q;
-    }
     tc_fence_before();
     __syncthreads();
     float inv_k = 1.f, inv_q = 1.f;
-    if (kPre && p.pre.l2) {
-      float s2k = 0.f, s2q = 0.f;
-#pragma unroll
-      for (int j = 0; j < 2 * NCOL; ++j) {
-        s2k += s_nrm[t * 2 * NCOL + j];
-        s2q += s_nrm[(C + t) * 2 * NCOL + j];
-      }
-      inv_k = inv_l2(s2k);
-      inv_q = inv_l2(s2q);
+    if (kPre && p.pre.l2) {  // sums of squares from the previous chunk's last products
+      inv_k = inv_l2(s_nrm[t]);
+      inv_q = inv_l2(s_nrm[C + t]);
     }
     if (tid < D) {
       const float e2 = s_rho[tid];
@@ -665,8 +678,8 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     for (int g4 = 0; g4 < GPT; ++g4) {
       const int cg = cg0 + g4;
       float kx[8], qx[8];
-      ld8(smem + SM_IN_K + cg * 1024 + t * 16, kx);
-      ld8(smem + SM_IN_Q + cg * 1024 + t * 16, qx);
+      ld8(smem + SM_IN_K + off_sw128(t, cg), kx);
+      ld8(smem + SM_IN_Q + off_sw128(t, cg), qx);
       if (kPre && p.pre.l2) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -894,9 +907,6 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
         mma_commit(xo_bar);
       }
-      // the next chunk's gate, while the products with S' run (its writes are
-      // fenced for the cumulative sum at the join)
-      if (kPre && p.pre.gate && ci + 1 < nchunks) activate_gate(ci + 1, tid - 256, 256);
       // this warp: lane quarter qd, tokens h8 * 32 .. h8 * 32 + 31 of X'^T
       if (!mbar_wait(xo_bar, (xo_issued - 1) & 1u)) wt.on_timeout();
       tc_fence_after();
@@ -921,10 +931,10 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     __syncthreads();
     if (*(volatile uint32_t*)s_flag) break;
 
-    // ---- P8: prefetch chunk ci+1 (the q, k, v tiles are consumed; warps 1-3
-    // issue one tile each); U^T = X'^T (-TB)^T with split operands
+    // ---- P8: prefetch chunk ci+1 (the q, k, v tiles are consumed; warps 1-5
+    // issue one part each); U^T = X'^T (-TB)^T with split operands
     if (ci + 1 < nchunks) {
-      if (lane == 0 && warp >= 1 && warp <= 3) issue_tma_part(ci + 1, warp - 1);
+      if (lane == 0 && warp >= 1 && warp <= 5) issue_tma_part(ci + 1, warp - 1);
       ++tma_issued;
     }
     if (tid == 0) {
@@ -938,6 +948,11 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           mma_ts(tb + TM_U, tb + xa[pr] + kk * 8,
                  (smem_desc(bt[pr], 128, 1024) + (uint64_t)(kk * 16)), idesc_sq, (pr | kk) != 0);
       mma_commit(wt.mma_bar);
+    }
+    // while U runs: rows 0..383 of the next chunk's gate (warps 4-15)
+    if (kPre && p.pre.gate && ci + 1 < nchunks && warp >= 4) {
+      activate_gate(ci + 1, tid - 128, kGateRowsP8, kThreads - 128);
+      fence_proxy_async_smem();
     }
     if (wt.wait_mma()) break;
 
@@ -977,6 +992,15 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           mma_ts(tb + TM_S, tb + ua[pr] + kk * 8,
                  (smem_desc(bk[pr], 2048, 128) + (uint64_t)(kk * 256)), idesc_s, 1);
       mma_commit(wt.mma_bar);
+    }
+    // while these (longer) products run: the rest of the next chunk's gate (warps
+    // 1-11) and its q/k sums of squares (warps 12-15; the tiles were requested in P8)
+    if (kPre && ci + 1 < nchunks) {
+      if (p.pre.gate && warp >= 1 && warp < 12) {
+        activate_gate(ci + 1, kGateRowsP8 + tid - 32, 2 * kHalfRows, 352);
+        fence_proxy_async_smem();
+      }
+      if (p.pre.l2 && warp >= 12) qk_sumsq(tma_issued - 1);
     }
     if (wt.wait_mma()) break;
 
@@ -1177,6 +1201,21 @@ bool make_out_map(CUtensorMap* m, void* base, int64_t tokens, int H, bool bf16) 
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Map over q or k [tokens, H, D] (bf16) as [tokens][H * D]: box = 64 channels x 64
+// tokens, one 128-byte row per token, 128-byte swizzle
+bool make_map_sw128(CUtensorMap* m, const void* base, int64_t tokens, int H) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)H * D, (cuuint64_t)tokens};
+  cuuint64_t strides[1] = {(cuuint64_t)H * D * 2};
+  cuuint32_t box[2] = {64, C};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map(CUtensorMap* m, const void* base, int64_t tokens, int H, int box_tokens = C) {
   auto enc = get_encode();
   if (!enc) return false;
@@ -1243,7 +1282,8 @@ cudaError_t launch_prefill_bf16(const FwdArgs& a) {
   auto pick = [&](const void* x) { return tokens > 0 ? x : dummy; };
   const int64_t map_tokens = tokens > 0 ? tokens : 1;
   CUtensorMap mq, mk, mg, mv, mo;
-  if (!make_map(&mq, pick(a.q), map_tokens, a.H) || !make_map(&mk, pick(a.k), map_tokens, a.H) ||
+  if (!make_map_sw128(&mq, pick(a.q), map_tokens, a.H) ||
+      !make_map_sw128(&mk, pick(a.k), map_tokens, a.H) ||
       !make_map(&mg, pick(a.g), map_tokens, a.H, C / 2) || !make_map(&mv, pick(a.v), map_tokens, a.H) ||
       !make_out_map(&mo, tokens > 0 ? a.out : const_cast<void*>(dummy), map_tokens, a.H,
                     tokens > 0 && a.out_dtype == KDA_BF16))
