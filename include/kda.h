@@ -145,10 +145,13 @@ kda_status kda_fwd_checkpoints(const kda_shape* s, const void* q, const void* k,
  * computed in float32 from the values passed in and rounded to in_dtype, which is
  * what a separate preprocessing pass that stores in_dtype tensors produces:
  *   qk_l2norm      q, k per (token, head):  x / max(||x||_2, 1e-12)
- *   gate_softplus  g holds the raw gate:    log(alpha) = -softplus(g), with
- *                  softplus(x) = x for x > 20, else log(1 + e^x)
+ *   gate_softplus  g holds the raw gate:    log(alpha) = -softplus(g),
+ *                  softplus(x) = log(1 + e^x) (absolute error below 4e-7
+ *                  before rounding; it equals x once log1p(e^-x) rounds away)
  *   beta_sigmoid   beta holds the raw value: beta = 1 / (1 + e^-beta)
- * A zero-initialised struct disables everything (plain kda_fwd / kda_decode).
+ *                  (a few float32 ulp)
+ * The norm uses rsqrt (a few ulp).  A zero-initialised struct disables
+ * everything (plain kda_fwd / kda_decode).
  */
 typedef struct {
   int32_t qk_l2norm;
