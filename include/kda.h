@@ -150,6 +150,14 @@ kda_status kda_fwd_checkpoints(const kda_shape* s, const void* q, const void* k,
  *                  before rounding; it equals x once log1p(e^-x) rounds away)
  *   beta_sigmoid   beta holds the raw value: beta = 1 / (1 + e^-beta)
  *                  (a few float32 ulp)
+ *   gate_scale     device float32 [H] or NULL (= 1): with gate_softplus,
+ *                  log(alpha) = -gate_scale[h] * softplus(g) (a per-head
+ *                  scale of the decay rate); non-NULL without gate_softplus
+ *                  is KDA_ERR_INVALID_ARG.  4-byte aligned.
+ *   gate_per_head  the scalar-gate (Gated DeltaNet) variant: g is [.., H], one
+ *                  gate per token and head (raw, or log(alpha) without
+ *                  gate_softplus), shared by all dk key channels; g then needs
+ *                  only in_dtype alignment.
  * The norm uses rsqrt (a few ulp).  A zero-initialised struct disables
  * everything (plain kda_fwd / kda_decode).
  */
@@ -157,6 +165,8 @@ typedef struct {
   int32_t qk_l2norm;
   int32_t gate_softplus;
   int32_t beta_sigmoid;
+  int32_t gate_per_head;
+  const float* gate_scale;
 } kda_preproc;
 
 /* kda_fwd with the preprocessing `pre` (NULL = none) applied to q, k, g, beta

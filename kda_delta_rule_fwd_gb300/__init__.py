@@ -45,7 +45,20 @@ class Shape(ctypes.Structure):
 class Preproc(ctypes.Structure):
     """Mirror of ``kda_preproc`` (fused input preprocessing flags)."""
     _fields_ = [("qk_l2norm", ctypes.c_int32), ("gate_softplus", ctypes.c_int32),
-                ("beta_sigmoid", ctypes.c_int32)]
+                ("beta_sigmoid", ctypes.c_int32), ("gate_per_head", ctypes.c_int32),
+                ("gate_scale", ctypes.c_void_p)]
+
+
+def _preproc(q, g, qk_l2norm, gate_softplus, beta_sigmoid, gate_per_head, gate_scale):
+    if gate_per_head and tuple(g.shape) != tuple(q.shape[:-1]):
+        raise ValueError("a per-head gate has the shape of q without its last dimension")
+    if not gate_per_head and g.shape != q.shape:
+        raise ValueError("g must have the shape of q")
+    if gate_scale is not None and (not gate_scale.is_cuda or gate_scale.dtype != torch.float32
+                                   or gate_scale.numel() != q.shape[2]):
+        raise ValueError("gate_scale must be a CUDA float32 tensor with one value per head")
+    return Preproc(int(qk_l2norm), int(gate_softplus), int(beta_sigmoid), int(gate_per_head),
+                   _ptr(gate_scale))
 
 
 class KDAError(RuntimeError):
@@ -218,11 +231,14 @@ def fwd_checkpoints(q, k, v, g, beta, *, interval=512, cu_seqlens=None, h0=None,
 
 
 def fwd_preproc(q, k, v, g, beta, *, qk_l2norm=True, gate_softplus=True, beta_sigmoid=True,
-                cu_seqlens=None, h0=None, scale=None, out_dtype=torch.float32, out=None, hT=None,
-                output_final_state=True, workspace=None, stream=None):
+                gate_per_head=False, gate_scale=None, cu_seqlens=None, h0=None, scale=None,
+                out_dtype=torch.float32, out=None, hT=None, output_final_state=True,
+                workspace=None, stream=None):
     """``fwd`` on raw inputs with the preprocessing fused into the kernels: q, k
-    L2-normalised per (token, head), log(alpha) = -softplus(g), beta = sigmoid(beta),
-    each computed in float32 and rounded to the input dtype (selected by the flags)."""
+    L2-normalised per (token, head), log(alpha) = -gate_scale[h] softplus(g), beta =
+    sigmoid(beta), each computed in float32 and rounded to the input dtype (selected
+    by the flags).  ``gate_per_head``: g is ``[B,T,H]``, one gate per token and head
+    shared by the key channels (the scalar-gate variant)."""
     _check_inputs(q, k, v, g, beta)
     N = q.shape[0] if cu_seqlens is None else cu_seqlens.numel() - 1
     shape = make_shape(q, v, packed_seqs=None if cu_seqlens is None else N, scale=scale,
@@ -235,7 +251,7 @@ def fwd_preproc(q, k, v, g, beta, *, qk_l2norm=True, gate_softplus=True, beta_si
         hT = torch.empty(N, H, dk, dv, dtype=torch.float32, device=q.device)
     if workspace is None:
         workspace = new_workspace(shape, q.device)
-    pre = Preproc(int(qk_l2norm), int(gate_softplus), int(beta_sigmoid))
+    pre = _preproc(q, g, qk_l2norm, gate_softplus, beta_sigmoid, gate_per_head, gate_scale)
     rc = load().kda_fwd_preproc(ctypes.byref(shape), ctypes.byref(pre), _ptr(q), _ptr(k),
                                 _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), _ptr(h0),
                                 _ptr(out), _ptr(hT), _ptr(workspace), workspace.numel(),
@@ -246,8 +262,8 @@ def fwd_preproc(q, k, v, g, beta, *, qk_l2norm=True, gate_softplus=True, beta_si
 
 
 def decode_preproc(q, k, v, g, beta, state, *, qk_l2norm=True, gate_softplus=True,
-                   beta_sigmoid=True, scale=None, out_dtype=torch.float32, out=None,
-                   workspace=None, stream=None):
+                   beta_sigmoid=True, gate_per_head=False, gate_scale=None, scale=None,
+                   out_dtype=torch.float32, out=None, workspace=None, stream=None):
     """``decode`` on raw inputs with the preprocessing of ``fwd_preproc`` fused in."""
     _check_inputs(q, k, v, g, beta)
     shape = make_shape(q, v, scale=scale, out_dtype=out_dtype)
@@ -256,7 +272,7 @@ def decode_preproc(q, k, v, g, beta, state, *, qk_l2norm=True, gate_softplus=Tru
         out = torch.empty(B, T, H, v.shape[-1], dtype=out_dtype, device=q.device)
     if workspace is None:
         workspace = new_workspace(shape, q.device)
-    pre = Preproc(int(qk_l2norm), int(gate_softplus), int(beta_sigmoid))
+    pre = _preproc(q, g, qk_l2norm, gate_softplus, beta_sigmoid, gate_per_head, gate_scale)
     rc = load().kda_decode_preproc(ctypes.byref(shape), ctypes.byref(pre), _ptr(q), _ptr(k),
                                    _ptr(v), _ptr(g), _ptr(beta), _ptr(state), _ptr(out),
                                    _ptr(workspace), workspace.numel(), _stream_ptr(stream))

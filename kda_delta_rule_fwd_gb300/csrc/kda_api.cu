@@ -57,13 +57,22 @@ size_t kda_workspace_size(const kda_shape* s) {
 namespace {
 // shared by kda_fwd and kda_fwd_checkpoints (ckpt == nullptr: no checkpoints)
 Preproc to_preproc(const kda_preproc* p) {
-  Preproc r{0, 0, 0};
+  Preproc r{0, 0, 0, 0, nullptr};
   if (p) {
     r.l2 = p->qk_l2norm != 0;
     r.gate = p->gate_softplus != 0;
     r.beta = p->beta_sigmoid != 0;
+    r.per_head = p->gate_per_head != 0;
+    r.gate_scale = p->gate_scale;
   }
   return r;
+}
+// the preprocessing's own argument rules; g's alignment follows its layout
+bool preproc_ok(const kda_preproc* p, const void* g, kda_dtype in_dtype) {
+  const bool per_head = p && p->gate_per_head;
+  if (g && !aligned(g, per_head ? dsize(in_dtype) : 16)) return false;
+  if (p && p->gate_scale && (!p->gate_softplus || !aligned(p->gate_scale, 4))) return false;
+  return true;
 }
 
 kda_status fwd_common(const kda_shape* s, const void* q, const void* k, const void* v,
@@ -78,10 +87,11 @@ kda_status fwd_common(const kda_shape* s, const void* q, const void* k, const vo
   // with no tokens the activation buffers are empty and may be NULL
   const bool any_tokens = (int64_t)s->B * s->T > 0;
   if (any_tokens && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_INVALID_ARG;
-  const void* ptrs[] = {q, k, v, g, out, h0, hT};
+  const void* ptrs[] = {q, k, v, out, h0, hT};
   for (const void* p : ptrs)
     if (p && !aligned(p, 16)) return KDA_ERR_INVALID_ARG;
-  if (!aligned(beta, dsize(s->in_dtype)) || (packed && !aligned(cu_seqlens, 4)))
+  if (!aligned(beta, dsize(s->in_dtype)) || (packed && !aligned(cu_seqlens, 4)) ||
+      !preproc_ok(pre, g, s->in_dtype))
     return KDA_ERR_INVALID_ARG;
   st = check_ws(s, workspace, workspace_bytes);
   if (st != KDA_OK) return st;
@@ -165,10 +175,11 @@ kda_status decode_common(const kda_shape* s, const void* q, const void* k, const
   if (st != KDA_OK) return st;
   if (s->T < 1 || s->T > 8) return KDA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !g || !beta || !state || (!out && !num_commit)) return KDA_ERR_INVALID_ARG;
-  const void* ptrs[] = {q, k, v, g, state, out};
+  const void* ptrs[] = {q, k, v, state, out};
   for (const void* p : ptrs)
     if (p && !aligned(p, 16)) return KDA_ERR_INVALID_ARG;
-  if (!aligned(beta, dsize(s->in_dtype))) return KDA_ERR_INVALID_ARG;
+  if (!aligned(beta, dsize(s->in_dtype)) || !preproc_ok(pre, g, s->in_dtype))
+    return KDA_ERR_INVALID_ARG;
   if (num_commit && !aligned(num_commit, 4)) return KDA_ERR_INVALID_ARG;
   st = check_ws(s, workspace, workspace_bytes);
   if (st != KDA_OK) return st;

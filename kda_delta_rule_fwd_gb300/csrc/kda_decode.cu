@@ -65,14 +65,16 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
     for (int c = 0; c < CPL; ++c) S[r][c] = xf[c];
   }
 
-  // Stage the step's inputs (Tstep tokens) in shared memory as float32.
+  // Stage the step's inputs (Tstep tokens) in shared memory as float32 (with the
+  // fused preprocessing: a scalar gate per (token, head) is shared by the channels).
+  const float gsc = kPre && pre.gate_scale ? pre.gate_scale[h] : 1.f;
   for (int i = tid; i < Tstep * D; i += kDecodeThreads) {
     const int t = i / D, c = i % D;
     const int64_t x = ((n * Tstep + t) * H + h) * D + c;
     s_k[t][c] = to_f32(k[x]);
     s_q[t][c] = to_f32(q[x]);
-    float gv = to_f32(g[x]);
-    if (kPre && pre.gate) gv = round_to<TIn>(neg_softplus(gv));
+    float gv = to_f32(g[kPre && pre.per_head ? (n * Tstep + t) * H + h : x]);
+    if (kPre && pre.gate) gv = round_to<TIn>(gsc * neg_softplus(gv));
     s_a[t][c] = expf(gv);
     s_v[t][c] = to_f32(v[x]);
   }
@@ -231,7 +233,7 @@ cudaError_t launch_pre(const DecodeArgs& a) {
 template <int D, typename TIn>
 cudaError_t launch_d_in(const DecodeArgs& a) {
   if ((int64_t)a.B * a.H == 0 || a.Tstep == 0) return cudaSuccess;
-  if (a.pre.l2 || a.pre.gate || a.pre.beta) return launch_pre<D, TIn, true>(a);
+  if (a.pre.l2 || a.pre.gate || a.pre.beta || a.pre.per_head) return launch_pre<D, TIn, true>(a);
   return launch_pre<D, TIn, false>(a);
 }
 

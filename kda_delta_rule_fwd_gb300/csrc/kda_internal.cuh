@@ -94,9 +94,11 @@ inline size_t seg_bytes(const SegPlan& pl, int64_t chains, int D) {
 // Fused input preprocessing (kda_preproc): each enabled step in float32, rounded
 // to the input dtype, as a separate pass that stores input-dtype tensors would.
 struct Preproc {
-  int l2;    // q, k: x / max(||x||, 1e-12) per (token, head)
-  int gate;  // log(alpha) = -softplus(g)
-  int beta;  // beta = sigmoid(beta)
+  int l2;                   // q, k: x / max(||x||, 1e-12) per (token, head)
+  int gate;                 // log(alpha) = -gate_scale[h] * softplus(g)
+  int beta;                 // beta = sigmoid(beta)
+  int per_head;             // g holds one gate per (token, head), shared by the key channels
+  const float* gate_scale;  // [H], or null for 1
 };
 template <typename T> __device__ __forceinline__ float round_to(float x);
 template <> __device__ __forceinline__ float round_to<float>(float x) { return x; }

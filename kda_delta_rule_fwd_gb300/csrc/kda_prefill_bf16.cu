@@ -318,6 +318,7 @@ struct Bf16Params {
   int64_t ckpt_rows;
   int64_t ckpt_interval;
   Preproc pre;           // fused input preprocessing (kPre instantiation only)
+  const __nv_bfloat16* g;  // the scalar gate [tokens, H] (pre.per_head only)
 };
 
 // The CTA's bounded waits.  Every thread waits on the barrier itself; a thread
@@ -493,6 +494,11 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     else
       tma_load_3d(smem + SM_IN_V, &tm_v, 0, y, h * (D / 8), wt.tma_bar);
   };
+  // The scalar gate (one per token and head) has no tile to load: threads write
+  // it, broadcast over the channels, into the g buffers (activate_gate below).
+  const bool g_tma = !(kPre && p.pre.per_head);
+  const bool g_fill = kPre && (p.pre.gate || p.pre.per_head);  // threads produce the g tile
+  const float gsc = kPre && p.pre.gate_scale ? p.pre.gate_scale[h] : 1.f;
   auto issue_g_half = [&](int chunk, int half) {
     const int32_t y = (int32_t)(t0 + (int64_t)chunk * C + half * (C / 2));
     if (half == 0) mbar_arrive_expect_tx(g_bar, 16384);
@@ -500,12 +506,14 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   };
   if (tid == 0 && nchunks > 0) {
     for (int part = 0; part < 5; ++part) issue_tma_part(0, part);
-    issue_g_half(0, 0);
-    issue_g_half(0, 1);
+    if (g_tma) {
+      issue_g_half(0, 0);
+      issue_g_half(0, 1);
+    }
   }
   if (nchunks > 0) {
     ++tma_issued;
-    ++g_issued;
+    if (g_tma) ++g_issued;
   }
   // raw bf16 bits of beta for a chunk, loaded a chunk ahead and converted only
   // when used (no instruction waits on the load meanwhile); tokens past the
@@ -559,8 +567,8 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   // first half, 2, 3 on the second), committed to mma_bar; returns false if the
   // wait ran out
   auto issue_cumsum = [&](int chunk) -> bool {
-    const bool ok = mbar_wait(g_bar, (uint32_t)chunk & 1u);
-    ++g_waited;
+    const bool ok = !g_tma || mbar_wait(g_bar, (uint32_t)chunk & 1u);
+    if (g_tma) ++g_waited;
     if (!ok) return false;
     tc_fence_after();
 #pragma unroll
@@ -571,20 +579,30 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     mma_commit(wt.mma_bar);
     return true;
   };
-  // fused gate: log(alpha) = -softplus(raw) rounded to bf16, in place on rows
-  // [i, end) of the g tile of `chunk` (16-byte rows of 8 channels; 0..511 in the
-  // first half, 512..1023 in the second), stepping by `nthr`, once the tile has
-  // landed; the callers order these writes before the cumulative sum (a proxy
-  // fence and a CTA barrier)
+  // fused gate: log(alpha) = -gate_scale[h] softplus(raw) rounded to bf16, in
+  // place on rows [i, end) of the g tile of `chunk` (16-byte rows of 8 channels;
+  // 0..511 in the first half, 512..1023 in the second, each half [group][32
+  // tokens]), stepping by `nthr`, once the tile has landed.  A scalar gate is
+  // read per token from global memory and written to the 8 channels of the row.
+  // The callers order these writes before the cumulative sum (a proxy fence and
+  // a CTA barrier).
   constexpr int kHalfRows = (D / 8) * (C / 2);
   auto activate_gate = [&](int chunk, int i, int end, int nthr) {
-    if (!mbar_wait(g_bar, (uint32_t)chunk & 1u)) wt.on_timeout();
+    if (g_tma && !mbar_wait(g_bar, (uint32_t)chunk & 1u)) wt.on_timeout();
     for (; i < end; i += nthr) {
       uint8_t* r = smem + (i < kHalfRows ? SM_GA + i * 16 : SM_GB + (i - kHalfRows) * 16);
       float x[8];
-      ld8(r, x);
+      if (g_tma) {
+        ld8(r, x);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = neg_softplus(x[e]);
+        for (int e = 0; e < 8; ++e) x[e] = gsc * neg_softplus(x[e]);
+      } else {
+        const int64_t tt = (int64_t)chunk * C + (i < kHalfRows ? 0 : C / 2) + (i & (C / 2 - 1));
+        float gv = tt < len ? __bfloat162float(p.g[(t0 + tt) * p.H + h]) : 0.f;
+        if (p.pre.gate) gv = gsc * neg_softplus(gv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = gv;
+      }
       st8(r, x);
     }
   };
@@ -606,8 +624,8 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     s_nrm[isq * C + tt] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
   };
-  if (kPre && nchunks > 0 && (p.pre.gate || p.pre.l2)) {
-    if (p.pre.gate) activate_gate(0, tid, 2 * kHalfRows, kThreads);
+  if (kPre && nchunks > 0 && (g_fill || p.pre.l2)) {
+    if (g_fill) activate_gate(0, tid, 2 * kHalfRows, kThreads);
     if (p.pre.l2 && warp >= 12) qk_sumsq(0);
     fence_proxy_async_smem();
     __syncthreads();
@@ -634,7 +652,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (wt.wait_tma()) break;
     if (wt.wait_mma()) break;
     // the cumulative sum has read the g tile: load the next chunk's
-    if (ci + 1 < nchunks) {
+    if (g_tma && ci + 1 < nchunks) {
       if (lane == 0 && (warp == 1 || warp == 2)) issue_g_half(ci + 1, warp - 1);
       ++g_issued;
     }
@@ -950,7 +968,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       mma_commit(wt.mma_bar);
     }
     // while U runs: rows 0..383 of the next chunk's gate (warps 4-15)
-    if (kPre && p.pre.gate && ci + 1 < nchunks && warp >= 4) {
+    if (g_fill && ci + 1 < nchunks && warp >= 4) {
       activate_gate(ci + 1, tid - 128, kGateRowsP8, kThreads - 128);
       fence_proxy_async_smem();
     }
@@ -996,7 +1014,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     // while these (longer) products run: the rest of the next chunk's gate (warps
     // 1-11) and its q/k sums of squares (warps 12-15; the tiles were requested in P8)
     if (kPre && ci + 1 < nchunks) {
-      if (p.pre.gate && warp >= 1 && warp < 12) {
+      if (g_fill && warp >= 1 && warp < 12) {
         activate_gate(ci + 1, kGateRowsP8 + tid - 32, 2 * kHalfRows, 352);
         fence_proxy_async_smem();
       }
@@ -1284,7 +1302,7 @@ cudaError_t launch_prefill_bf16(const FwdArgs& a) {
   CUtensorMap mq, mk, mg, mv, mo;
   if (!make_map_sw128(&mq, pick(a.q), map_tokens, a.H) ||
       !make_map_sw128(&mk, pick(a.k), map_tokens, a.H) ||
-      !make_map(&mg, pick(a.g), map_tokens, a.H, C / 2) || !make_map(&mv, pick(a.v), map_tokens, a.H) ||
+      !make_map(&mg, pick(a.pre.per_head ? a.q : a.g), map_tokens, a.H, C / 2) || !make_map(&mv, pick(a.v), map_tokens, a.H) ||
       !make_out_map(&mo, tokens > 0 ? a.out : const_cast<void*>(dummy), map_tokens, a.H,
                     tokens > 0 && a.out_dtype == KDA_BF16))
     return cudaErrorInvalidValue;
@@ -1309,7 +1327,8 @@ cudaError_t launch_prefill_bf16(const FwdArgs& a) {
   p.ckpt_rows = a.ckpt_rows;
   p.ckpt_interval = a.ckpt_interval > 0 ? a.ckpt_interval : 1;
   p.pre = a.pre;
-  if (a.pre.l2 || a.pre.gate || a.pre.beta) return run_bf16<true>(a, mq, mk, mg, mv, mo, p, items);
+  p.g = static_cast<const __nv_bfloat16*>(a.g);
+  if (a.pre.l2 || a.pre.gate || a.pre.beta || a.pre.per_head) return run_bf16<true>(a, mq, mk, mg, mv, mo, p, items);
   return run_bf16<false>(a, mq, mk, mg, mv, mo, p, items);
 }
 

@@ -73,6 +73,7 @@ kda_prefill_f32_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
   const int64_t ck_base =
       ckpt_base(ckpt, ckpt_off, ckpt_rows, ckpt_interval, n, len, status, tid == 0);
 
+  const float gsc = kPre && pre.gate_scale ? pre.gate_scale[h] : 1.f;
   for (int64_t cs = 0; cs < len; cs += C) {
     const int nv = (int)(len - cs < C ? len - cs : C);
     __syncthreads();  // previous chunk finished with every buffer
@@ -82,8 +83,9 @@ kda_prefill_f32_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
       float xq = 0.f, xk = 0.f, xv = 0.f, xg = 0.f;
       if (t < nv) {
         const int64_t x = ((t0 + cs + t) * H + h) * D + c;
-        xq = to_f32(q[x]); xk = to_f32(k[x]); xv = to_f32(v[x]); xg = to_f32(g[x]);
-        if (kPre && pre.gate) xg = round_to<TIn>(neg_softplus(xg));
+        xq = to_f32(q[x]); xk = to_f32(k[x]); xv = to_f32(v[x]);
+        xg = to_f32(g[kPre && pre.per_head ? (t0 + cs + t) * H + h : x]);  // scalar gate: shared
+        if (kPre && pre.gate) xg = round_to<TIn>(gsc * neg_softplus(xg));
       }
       sq[t * LD + c] = xq; sk[t * LD + c] = xk; sv[t * LD + c] = xv; sG[t * LD + c] = xg;
     }
@@ -227,7 +229,7 @@ cudaError_t launch_p(const FwdArgs& a) {
 
 template <int D, int C, typename TIn, typename TOut>
 cudaError_t launch_t(const FwdArgs& a) {
-  if (a.pre.l2 || a.pre.gate || a.pre.beta) return launch_p<D, C, TIn, TOut, true>(a);
+  if (a.pre.l2 || a.pre.gate || a.pre.beta || a.pre.per_head) return launch_p<D, C, TIn, TOut, true>(a);
   return launch_p<D, C, TIn, TOut, false>(a);
 }
 

@@ -152,14 +152,18 @@ def recurrent(q, k, v, g, beta, *, cu_seqlens=None, h0=None, scale=None, n_threa
 # chunkwise-parallel form (numpy, float64)
 # ---------------------------------------------------------------------------
 
-def preprocess(q, k, g, beta, *, qk_l2norm=True, gate_softplus=True, beta_sigmoid=True):
+def preprocess(q, k, g, beta, *, qk_l2norm=True, gate_softplus=True, beta_sigmoid=True,
+               gate_scale=None, gate_per_head=False):
     """Preprocessed (q, k, g, beta) as torch tensors of the inputs' dtype.
 
     Each enabled step follows its definition in float64 on the given values and
     is then rounded to the input dtype:
       q, k:  x / max(||x||_2, 1e-12) over the head dimension
-      g:     -softplus(g), softplus(x) = log(1 + e^x) (= x above 20)
+      g:     -a_h softplus(g), softplus(x) = log(1 + e^x) (= x above 20), a_h the
+             per-head scale (1 when gate_scale is None)
       beta:  1 / (1 + e^-beta)
+    With gate_per_head, g holds one value per (token, head) (the scalar-gate
+    variant); the result is that value repeated over the dk key channels.
     """
     import torch
     dt = q.dtype
@@ -169,11 +173,20 @@ def preprocess(q, k, g, beta, *, qk_l2norm=True, gate_softplus=True, beta_sigmoi
     if qk_l2norm:
         Q = Q / np.maximum(np.sqrt(np.sum(Q * Q, axis=-1, keepdims=True)), 1e-12)
         K = K / np.maximum(np.sqrt(np.sum(K * K, axis=-1, keepdims=True)), 1e-12)
+    if gate_per_head:
+        G = G[..., None]
     if gate_softplus:
         G = -np.where(G > 20.0, G, np.log1p(np.exp(np.minimum(G, 20.0))))
+        if gate_scale is not None:
+            a = np.asarray(gate_scale.detach().double().cpu().numpy()
+                           if hasattr(gate_scale, "detach") else gate_scale, dtype=np.float64)
+            G = G * a[:, None]
     if beta_sigmoid:
         Bt = 1.0 / (1.0 + np.exp(-Bt))
-    return back(Q), back(K), back(G), back(Bt)
+    Gr = back(G)
+    if gate_per_head:
+        Gr = Gr.expand(*G.shape[:-1], Q.shape[-1]).contiguous()
+    return back(Q), back(K), Gr, back(Bt)
 
 
 def _tri_inv_unit_lower(A):

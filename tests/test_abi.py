@@ -185,3 +185,35 @@ def test_workspace_size_long_chain_split(lib):
     # the split is optional: the minimum workspace is still accepted
     if not torch.cuda.is_available():  # would launch on fake pointers otherwise
         assert _fwd(L, _shape(m, B=1, T=1 << 20, H=32), ws_bytes=256) == m.KDA_ERR_CUDA
+
+
+def _fwd_pre(L, m, shape, pre, *, g=FAKE):
+    vp = ctypes.c_void_p
+    L.kda_fwd_preproc.restype = ctypes.c_int
+    return L.kda_fwd_preproc(ctypes.byref(shape), ctypes.byref(pre) if pre else None, vp(FAKE),
+                             vp(FAKE), vp(FAKE), vp(g), vp(FAKE), None, None, vp(FAKE),
+                             vp(FAKE), vp(FAKE), ctypes.c_size_t(1 << 20), None)
+
+
+def _dec_pre(L, m, shape, pre, *, g=FAKE):
+    vp = ctypes.c_void_p
+    L.kda_decode_preproc.restype = ctypes.c_int
+    return L.kda_decode_preproc(ctypes.byref(shape), ctypes.byref(pre) if pre else None,
+                                vp(FAKE), vp(FAKE), vp(FAKE), vp(g), vp(FAKE), vp(FAKE),
+                                vp(FAKE), vp(FAKE), ctypes.c_size_t(1 << 20), None)
+
+
+def test_preproc_argument_errors(lib):
+    """A per-head gate scale needs the softplus step and 4-byte alignment; a
+    per-channel g needs 16-byte alignment, a per-head g only its dtype's."""
+    m, L = lib
+    P = m.Preproc
+    for call, shp in ((_fwd_pre, _shape(m)), (_dec_pre, _shape(m, T=2))):
+        assert call(L, m, shp, P(1, 0, 1, 0, FAKE)) == m.KDA_ERR_INVALID_ARG  # scale, no softplus
+        assert call(L, m, shp, P(1, 1, 1, 0, FAKE + 2)) == m.KDA_ERR_INVALID_ARG
+        assert call(L, m, shp, P(0, 1, 0, 0, None), g=FAKE + 2) == m.KDA_ERR_INVALID_ARG
+        assert call(L, m, shp, None, g=FAKE + 2) == m.KDA_ERR_INVALID_ARG
+        assert call(L, m, shp, P(0, 1, 0, 1, None), g=FAKE + 1) == m.KDA_ERR_INVALID_ARG
+        if not torch.cuda.is_available():  # valid arguments reach the (absent) device
+            assert call(L, m, shp, P(0, 1, 0, 1, FAKE), g=FAKE + 2) == m.KDA_ERR_CUDA
+            assert call(L, m, shp, P(1, 1, 1, 0, FAKE + 4)) == m.KDA_ERR_CUDA

@@ -377,3 +377,39 @@ def test_preprocess_rounds_to_input_dtype(oracle_mod):
     assert torch.equal(qn[0, 0], torch.from_numpy(want_q).to(torch.bfloat16))
     assert torch.equal(gn[0, 0], torch.from_numpy(want_g).to(torch.bfloat16))
     assert bn.item() == torch.tensor(want_b).to(torch.bfloat16).item()
+
+
+def test_preprocess_gate_scale_and_per_head(oracle_mod):
+    """A per-head scale multiplies -softplus (scale 1 is the unscaled gate, scale 2
+    doubles it); a per-head gate equals the per-channel gate with that value on
+    every channel, and it turns KDA into the scalar-gate (GDN) recurrence: the
+    decay of every key channel is the same."""
+    import torch
+    rng = np.random.default_rng(62)
+    L, H, d = 7, 3, 5
+    q = torch.from_numpy(rng.standard_normal((L, H, d)))
+    k = torch.from_numpy(rng.standard_normal((L, H, d)))
+    g1 = torch.from_numpy(rng.standard_normal((L, H)))
+    b = torch.from_numpy(rng.standard_normal((L, H)))
+    ones = np.ones(H)
+    base = oracle_mod.preprocess(q, k, g1[..., None].expand(L, H, d).contiguous(), b)
+    per_head = oracle_mod.preprocess(q, k, g1, b, gate_per_head=True)
+    for x, y in zip(base, per_head):
+        assert torch.equal(x, y)
+    scaled1 = oracle_mod.preprocess(q, k, g1, b, gate_per_head=True, gate_scale=ones)
+    assert torch.equal(scaled1[2], per_head[2])
+    sc = np.array([2.0, 0.5, 0.0])
+    scaled = oracle_mod.preprocess(q, k, g1, b, gate_per_head=True, gate_scale=sc)[2]
+    np.testing.assert_allclose(scaled.numpy(), per_head[2].numpy() * sc[None, :, None],
+                               rtol=1e-15, atol=0)
+    assert torch.all(scaled[:, 2] == 0)  # scale 0: no decay
+    # every channel of a head decays alike: the state's column norms keep their ratios
+    # when beta = 0 (pure decay), as in the scalar-gate recurrence
+    qn, kn, gn, _ = per_head
+    v = rng.standard_normal((L, H, d))
+    h0 = rng.standard_normal((1, H, d, d))
+    _, hT = oracle_mod.recurrent(qn.numpy(), kn.numpy(), v, gn.numpy(), np.zeros((L, H)),
+                                 cu_seqlens=np.array([0, L]), h0=h0)
+    decay = np.exp(gn.numpy().sum(axis=0))          # [H, d], equal over d
+    np.testing.assert_allclose(decay, decay[:, :1].repeat(d, axis=1), rtol=1e-15)
+    np.testing.assert_allclose(hT[0], decay[:, :, None] * h0[0], rtol=1e-12, atol=1e-14)

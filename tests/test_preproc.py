@@ -183,3 +183,80 @@ def test_gate_activation_precision(kda):
     rel = (alpha - ref).abs() / ref
     bound = 7e-7 + 1.2e-7 * logalpha.abs()
     assert torch.all(rel <= bound), float((rel / bound).max())
+
+
+def _gate_scale(H, seed):
+    gen = torch.Generator().manual_seed(seed)
+    return (torch.rand(H, generator=gen) * 1.5 + 0.25).to(DEV)
+
+
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 128),
+                                     (torch.float32, 64), (torch.bfloat16, 64)],
+                         ids=["bf16-128", "f32-128", "f32-64", "bf16-64"])
+@pytest.mark.parametrize("per_head", [False, True], ids=["per-channel", "per-head"])
+def test_prefill_gate_scale_and_scalar_gate(kda, oracle_mod, dtype, d, per_head):
+    """log(alpha) = -a_h softplus(g) with a per-head scale a_h, per channel and in the
+    scalar-gate variant (g [B, T, H] shared by the key channels), packed."""
+    x = _raw_packed([1, 64, 0, 130, 77], 3, d, dtype, seed=600 + d)
+    if per_head:
+        x.g = x.g[..., 0].contiguous()
+    a = _gate_scale(3, 601)
+    o, hT = kda.fwd_preproc(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens, h0=x.h0,
+                            gate_per_head=per_head, gate_scale=a)
+    torch.cuda.synchronize()
+    fq, fk, fg, fb = oracle_mod.preprocess(x.q, x.k, x.g, x.beta, gate_per_head=per_head,
+                                           gate_scale=a)
+    o_ref, h_ref = oracle_mod.recurrent(fq, fk, x.v, fg, fb, cu_seqlens=x.cu_seqlens, h0=x.h0)
+    assert rel_err(o, o_ref) <= TOL[dtype]
+    assert rel_err(hT, h_ref) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_prefill_scalar_log_decay_without_softplus(kda, oracle_mod, dtype):
+    """A per-head gate given directly as log(alpha) (no activation) is broadcast over
+    the key channels: the scalar-gate (GDN) recurrence, several chunks."""
+    x = _raw_fixed(2, 200, 2, 128, dtype, seed=610)
+    graw = x.g[..., 0].contiguous()
+    lg = oracle_mod.preprocess(x.q, x.k, graw, x.beta, qk_l2norm=False, beta_sigmoid=False,
+                               gate_per_head=True)[2][..., 0].contiguous().to(DEV)
+    o, hT = kda.fwd_preproc(x.q, x.k, x.v, lg, x.beta, h0=x.h0, gate_softplus=False,
+                            gate_per_head=True)
+    torch.cuda.synchronize()
+    fq, fk, fg, fb = oracle_mod.preprocess(x.q, x.k, lg, x.beta, gate_softplus=False,
+                                           gate_per_head=True)
+    o_ref, h_ref = oracle_mod.recurrent(fq, fk, x.v, fg, fb, h0=x.h0)
+    assert rel_err(o, o_ref) <= TOL[dtype]
+    assert rel_err(hT, h_ref) <= TOL[dtype]
+
+
+def test_prefill_scalar_gate_long_chain_split(kda, oracle_mod):
+    x = _raw_fixed(1, 64 * 257 + 37, 1, 128, torch.bfloat16, seed=620)
+    x.g = x.g[..., 0].contiguous()
+    a = _gate_scale(1, 621)
+    o, hT = kda.fwd_preproc(x.q, x.k, x.v, x.g, x.beta, h0=x.h0, gate_per_head=True,
+                            gate_scale=a)
+    torch.cuda.synchronize()
+    fq, fk, fg, fb = oracle_mod.preprocess(x.q, x.k, x.g, x.beta, gate_per_head=True,
+                                           gate_scale=a)
+    o_ref, h_ref = oracle_mod.recurrent(fq, fk, x.v, fg, fb, h0=x.h0)
+    assert rel_err(o, o_ref) <= TOL_BF16
+    assert rel_err(hT, h_ref) <= TOL_BF16
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("per_head", [False, True], ids=["per-channel", "per-head"])
+def test_decode_gate_scale_and_scalar_gate(kda, oracle_mod, dtype, per_head):
+    x = kda_inputs.draw_raw((5, 8), 3, 128, 128, dtype=dtype, device=DEV, seed=630,
+                            num_states=5, h0_std=0.1)
+    if per_head:
+        x.g = x.g[..., 0].contiguous()
+    a = _gate_scale(3, 631)
+    state = x.h0.clone()
+    o = kda.decode_preproc(x.q, x.k, x.v, x.g, x.beta, state, gate_per_head=per_head,
+                           gate_scale=a)
+    torch.cuda.synchronize()
+    fq, fk, fg, fb = oracle_mod.preprocess(x.q, x.k, x.g, x.beta, gate_per_head=per_head,
+                                           gate_scale=a)
+    o_ref, h_ref = oracle_mod.recurrent(fq, fk, x.v, fg, fb, h0=x.h0)
+    assert rel_err(o, o_ref) <= TOL[dtype]
+    assert rel_err(state, h_ref) <= TOL[dtype]
