@@ -20,6 +20,12 @@ Three forms are provided, each citing the passage it follows:
   decomposition that KDA context parallelism rests on ("Kimi K3 模型结构（7）：
   结构决定系统", section 上下文并行: each segment contributes a local transition
   matrix and a zero-start state; a prefix scan combines them).
+* :func:`recurrent_grad` -- the gradients of the forward's outputs (o and the
+  final state) with respect to q, k, v, g, beta and h0: reverse-mode automatic
+  differentiation (torch autograd, float64, CPU) of the token recurrence written
+  out step by step.  The backward is one of the KDA training operators on "Kimi
+  K3 NPU Training" (section 结论, item 1; section NPU 算子支持度, row KDA 反向:
+  dq, dk, dv, dbeta, dgate and dstate).
 * :func:`preprocess` -- the input preprocessing that the fused entry points
   apply ("Kimi K3 NPU Training", section 模型结构, steps 1 and 3: q/k L2
   normalisation, channel-wise decay and beta from the gate inputs), evaluated
@@ -151,6 +157,66 @@ def recurrent(q, k, v, g, beta, *, cu_seqlens=None, h0=None, scale=None, n_threa
 # ---------------------------------------------------------------------------
 # chunkwise-parallel form (numpy, float64)
 # ---------------------------------------------------------------------------
+
+def recurrent_grad(q, k, v, g, beta, do, *, cu_seqlens=None, h0=None, dhT=None, scale=None):
+    """Gradients of L = sum(o * do) + sum(hT * dhT) (dhT None: no state term).
+
+    Shapes as in :func:`recurrent`; ``do`` is shaped like ``v``.  The forward
+    is the recurrence itself, one token at a time, vectorised over heads only:
+      S <- diag(e^g_t) S;  u = beta_t (v_t - S^T k_t);  S <- S + k_t u^T;
+      o_t = scale S^T q_t
+    and the gradients are torch autograd's, in float64.  Returns numpy float64
+    ``(dq, dk, dv, dg, dbeta, dh0)`` shaped like the inputs (dh0 [N,H,dk,dv],
+    also when h0 is None, i.e. zero).
+    """
+    import torch
+
+    def t64(x):
+        if x is None:
+            return None
+        if hasattr(x, "detach"):
+            x = x.detach().double().cpu().numpy()
+        return torch.from_numpy(np.array(x, dtype=np.float64))
+
+    Q, K, V, G, Bt, dO = (t64(x) for x in (q, k, v, g, beta, do))
+    shapes = [x.shape for x in (Q, K, V, G, Bt)]
+    if cu_seqlens is None:
+        B, T = Q.shape[0], Q.shape[1]
+        cu = [b * T for b in range(B + 1)]
+    else:
+        cu = [int(c) for c in (cu_seqlens.detach().cpu().numpy()
+                               if hasattr(cu_seqlens, "detach") else cu_seqlens)]
+    H, dk = Q.shape[-2], Q.shape[-1]
+    dv = V.shape[-1]
+    N = len(cu) - 1
+    if scale is None:
+        scale = dk ** -0.5
+    H0 = t64(h0) if h0 is not None else torch.zeros(N, H, dk, dv, dtype=torch.float64)
+    leaves = [Q, K, V, G, Bt, H0]
+    for x in leaves:
+        x.requires_grad_(True)
+    Qf, Kf, Gf = (x.reshape(-1, H, dk) for x in (Q, K, G))
+    Vf = V.reshape(-1, H, dv)
+    Bf = Bt.reshape(-1, H)
+    outs, finals = [], []
+    for n in range(N):
+        S = H0[n]
+        for t in range(cu[n], cu[n + 1]):
+            S = S * torch.exp(Gf[t])[:, :, None]
+            pred = torch.einsum("hkv,hk->hv", S, Kf[t])
+            u = Bf[t][:, None] * (Vf[t] - pred)
+            S = S + Kf[t][:, :, None] * u[:, None, :]
+            outs.append(scale * torch.einsum("hkv,hk->hv", S, Qf[t]))
+        finals.append(S)
+    loss = (torch.stack(outs) * dO.reshape(-1, H, dv)).sum() if outs else Q.sum() * 0.0
+    if dhT is not None:
+        loss = loss + (torch.stack(finals) * t64(dhT)).sum()
+    grads = torch.autograd.grad(loss, leaves, allow_unused=True)
+    res = []
+    for x, gr, shp in zip(leaves, grads, shapes + [H0.shape]):
+        res.append(np.zeros(tuple(shp)) if gr is None else gr.numpy().reshape(shp))
+    return tuple(res)
+
 
 def preprocess(q, k, g, beta, *, qk_l2norm=True, gate_softplus=True, beta_sigmoid=True,
                gate_scale=None, gate_per_head=False):

@@ -413,3 +413,77 @@ def test_preprocess_gate_scale_and_per_head(oracle_mod):
     decay = np.exp(gn.numpy().sum(axis=0))          # [H, d], equal over d
     np.testing.assert_allclose(decay, decay[:, :1].repeat(d, axis=1), rtol=1e-15)
     np.testing.assert_allclose(hT[0], decay[:, :, None] * h0[0], rtol=1e-12, atol=1e-14)
+
+
+# 7. gradients ----------------------------------------------------------------------
+def _loss(oracle_mod, q, k, v, g, beta, h0, do, dhT, cu):
+    o, hT = oracle_mod.recurrent(q, k, v, g, beta, cu_seqlens=cu, h0=h0)
+    return float(np.sum(o * do) + np.sum(hT * dhT))
+
+
+def test_grad_matches_central_differences(oracle_mod):
+    """Every gradient of the autograd oracle equals the central difference of the
+    C oracle's loss (a separate implementation of the forward) on a tiny packed
+    batch with a start state and a final-state cotangent."""
+    rng = np.random.default_rng(70)
+    cu = np.array([0, 3, 3, 5])
+    L, H, dk, dv = 5, 2, 3, 2
+    q, k, v, g, beta = _rand_inputs(rng, L, H, dk, dv, decay=(0.4, 0.95))
+    h0 = rng.standard_normal((3, H, dk, dv))
+    do = rng.standard_normal((L, H, dv))
+    dhT = rng.standard_normal((3, H, dk, dv))
+    grads = oracle_mod.recurrent_grad(q, k, v, g, beta, do, cu_seqlens=cu, h0=h0, dhT=dhT)
+    args = [q, k, v, g, beta, h0]
+    eps = 1e-6
+    for i, (x, gr) in enumerate(zip(args, grads)):
+        assert gr.shape == x.shape
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            ap, am = list(args), list(args)
+            ap[i], am[i] = xp, xm
+            fd[idx] = (_loss(oracle_mod, *ap, do, dhT, cu) - _loss(oracle_mod, *am, do, dhT, cu)) \
+                / (2 * eps)
+        np.testing.assert_allclose(gr, fd, rtol=1e-6, atol=1e-8)
+
+
+def test_grad_single_token_closed_form(oracle_mod):
+    """One token from a zero state: o = scale beta (k.q) v, so dv = scale beta (k.q) do,
+    dq = scale beta (v.do) k, dk = scale beta (v.do) q, dbeta = scale (k.q)(v.do), and
+    the gate has no effect (dg = 0)."""
+    rng = np.random.default_rng(71)
+    q, k, v, g, beta = _rand_inputs(rng, 1, 1, 4, 3)
+    do = rng.standard_normal((1, 1, 3))
+    s = 0.7
+    dq, dk, dv, dg, db, dh0 = oracle_mod.recurrent_grad(q, k, v, g, beta, do,
+                                                        cu_seqlens=np.array([0, 1]), scale=s)
+    kq = float(k[0, 0] @ q[0, 0])
+    vd = float(v[0, 0] @ do[0, 0])
+    b = beta[0, 0]
+    np.testing.assert_allclose(dv[0, 0], s * b * kq * do[0, 0], rtol=1e-13)
+    np.testing.assert_allclose(dq[0, 0], s * b * vd * k[0, 0], rtol=1e-13)
+    np.testing.assert_allclose(dk[0, 0], s * b * vd * q[0, 0], rtol=1e-13)
+    np.testing.assert_allclose(db[0, 0], s * kq * vd, rtol=1e-13)
+    assert np.all(dg == 0)
+    # the start state's gradient: dh0 = diag(alpha) (I - beta k k^T) (scale q do^T)
+    alpha = np.exp(g[0, 0])
+    kk = k[0, 0]
+    want = alpha[:, None] * ((np.eye(4) - b * np.outer(kk, kk)) @ (s * np.outer(q[0, 0], do[0, 0])))
+    np.testing.assert_allclose(dh0[0, 0], want, rtol=1e-12, atol=1e-14)
+
+
+def test_grad_is_linear_in_the_cotangents(oracle_mod):
+    rng = np.random.default_rng(72)
+    q, k, v, g, beta = _rand_inputs(rng, 6, 1, 3, 3, decay=(0.5, 1.0))
+    h0 = rng.standard_normal((1, 1, 3, 3))
+    do1, do2 = rng.standard_normal((2, 6, 1, 3))
+    dh1, dh2 = rng.standard_normal((2, 1, 1, 3, 3))
+    cu = np.array([0, 6])
+    g1 = oracle_mod.recurrent_grad(q, k, v, g, beta, do1, cu_seqlens=cu, h0=h0, dhT=dh1)
+    g2 = oracle_mod.recurrent_grad(q, k, v, g, beta, do2, cu_seqlens=cu, h0=h0, dhT=dh2)
+    g12 = oracle_mod.recurrent_grad(q, k, v, g, beta, 2 * do1 - do2, cu_seqlens=cu, h0=h0,
+                                    dhT=2 * dh1 - dh2)
+    for a, b, c in zip(g1, g2, g12):
+        np.testing.assert_allclose(c, 2 * a - b, rtol=1e-11, atol=1e-12)
