@@ -184,6 +184,32 @@ kda_status kda_decode_preproc(const kda_shape* s, const kda_preproc* pre, const 
                               void* stream);
 
 /*
+ * Backward of kda_fwd: the gradients of L = sum(o * dout) + sum(hT * dhT) with
+ * respect to q, k, v, g (= log alpha), beta and h0 ("Kimi K3 NPU Training",
+ * section NPU 算子支持度, row KDA 反向: dq, dk, dv, dbeta, dgate and dstate).
+ * Shapes, dtypes and cu_seqlens as kda_fwd (scale included; out_dtype is not
+ * used), and:
+ *   dout     device float32 [B,T,H,dv]   cotangent of o
+ *   dhT      device float32 [N,H,dk,dv]  cotangent of the final states, or NULL (0)
+ *   h0       device float32 [N,H,dk,dv]  start states, or NULL (zeros)
+ *   dq, dk, dg  device float32 [B,T,H,dk];  dv device float32 [B,T,H,dv];
+ *   dbeta    device float32 [B,T,H];  dh0 device float32 [N,H,dk,dv] or NULL
+ *   workspace   device, 256-byte aligned, at least kda_bwd_workspace_size(s)
+ *               bytes: it holds the state at every 16-token sub-chunk start
+ *               (one dk x dv float32 matrix per sub-chunk and head).
+ * Everything is computed in float32 (inputs converted exactly).  The forward
+ * is recomputed inside the call, so the o and hT of a previous kda_fwd are not
+ * needed.  Gates must be finite.  Device-detected errors (malformed
+ * cu_seqlens) are latched as in kda_fwd.
+ */
+size_t kda_bwd_workspace_size(const kda_shape* s);
+kda_status kda_bwd(const kda_shape* s, const void* q, const void* k, const void* v,
+                   const void* g, const void* beta, const int32_t* cu_seqlens, const float* h0,
+                   const float* dout, const float* dhT, float* dq, float* dk, float* dv,
+                   float* dg, float* dbeta, float* dh0, void* workspace, size_t workspace_bytes,
+                   void* stream);
+
+/*
  * Decode step: T_step = s->T tokens (1..8) per sequence applied in order to a
  * state pool resident in device memory, updated in place (the replay form of
  * speculative-decode rollback: the cached inputs of the accepted tokens are

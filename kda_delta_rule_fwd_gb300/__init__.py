@@ -100,6 +100,10 @@ def load(path: str | None = None):
         lib.kda_decode.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         lib.kda_decode_commit.restype = ctypes.c_int
         lib.kda_decode_commit.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        lib.kda_bwd_workspace_size.restype = sz
+        lib.kda_bwd_workspace_size.argtypes = [sp]
+        lib.kda_bwd.restype = ctypes.c_int
+        lib.kda_bwd.argtypes = [sp] + [vp] * 16 + [sz, vp]
         lib.kda_read_device_status.restype = ctypes.c_int
         lib.kda_read_device_status.argtypes = [vp, vp]
         lib.kda_status_string.restype = ctypes.c_char_p
@@ -259,6 +263,36 @@ def fwd_preproc(q, k, v, g, beta, *, qk_l2norm=True, gate_softplus=True, beta_si
     if rc != KDA_OK:
         raise KDAError(rc, "kda_fwd_preproc")
     return out, hT
+
+
+def bwd_workspace_size(shape: Shape) -> int:
+    return int(load().kda_bwd_workspace_size(ctypes.byref(shape)))
+
+
+def bwd(q, k, v, g, beta, dout, *, cu_seqlens=None, h0=None, dhT=None, scale=None,
+        want_dh0=True, workspace=None, stream=None):
+    """Gradients of ``sum(o * dout) + sum(hT * dhT)`` for ``fwd``'s inputs.  Returns
+    ``(dq, dk, dv, dg, dbeta, dh0)``, float32 (``dh0`` None unless ``want_dh0``)."""
+    _check_inputs(q, k, v, g, beta)
+    if dout.dtype != torch.float32 or not dout.is_contiguous() or dout.shape != v.shape:
+        raise ValueError("dout must be a contiguous float32 tensor shaped like v")
+    N = q.shape[0] if cu_seqlens is None else cu_seqlens.numel() - 1
+    shape = make_shape(q, v, packed_seqs=None if cu_seqlens is None else N, scale=scale)
+    B, T, H, dk = q.shape
+    f32 = dict(dtype=torch.float32, device=q.device)
+    dq, dk_, dg = (torch.empty(B, T, H, dk, **f32) for _ in range(3))
+    dv = torch.empty(B, T, H, v.shape[-1], **f32)
+    dbeta = torch.empty(B, T, H, **f32)
+    dh0 = torch.empty(N, H, dk, v.shape[-1], **f32) if want_dh0 else None
+    if workspace is None:
+        workspace = torch.empty(bwd_workspace_size(shape), dtype=torch.uint8, device=q.device)
+    rc = load().kda_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                        _ptr(cu_seqlens), _ptr(h0), _ptr(dout), _ptr(dhT), _ptr(dq), _ptr(dk_),
+                        _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(dh0), _ptr(workspace),
+                        workspace.numel(), _stream_ptr(stream))
+    if rc != KDA_OK:
+        raise KDAError(rc, "kda_bwd")
+    return dq, dk_, dv, dg, dbeta, dh0
 
 
 def decode_preproc(q, k, v, g, beta, state, *, qk_l2norm=True, gate_softplus=True,

@@ -254,6 +254,85 @@ const char* kda_status_string(kda_status st) {
   return "unknown status";
 }
 
+// Backward workspace: status header, the packed order list, the packed state-row
+// offsets, then one float32 dk x dv state per (16-token sub-chunk, head).
+namespace {
+size_t bwd_off_bytes(int64_t N) { return (size_t)((N * 8 + 255) / 256) * 256; }
+size_t bwd_ws_bytes(const kda_shape* s) {
+  const bool packed = s->num_seqs > 0;
+  const int64_t N = packed ? s->num_seqs : s->B;
+  size_t b = kWsHeader;
+  if (packed) b += ws_order_bytes(N) + bwd_off_bytes(N);
+  b = (b + 255) / 256 * 256;
+  b += kda::bwd_state_rows(packed, N, s->T) * (size_t)s->H * s->dk * s->dv * sizeof(float);
+  return b;
+}
+}  // namespace
+
+size_t kda_bwd_workspace_size(const kda_shape* s) {
+  if (!s || s->B < 0 || s->T < 0 || s->H < 0 || s->num_seqs < 0 || s->dk < 0 || s->dv < 0)
+    return 0;
+  return bwd_ws_bytes(s);
+}
+
+kda_status kda_bwd(const kda_shape* s, const void* q, const void* k, const void* v,
+                   const void* g, const void* beta, const int32_t* cu_seqlens, const float* h0,
+                   const float* dout, const float* dhT, float* dq, float* dk, float* dv,
+                   float* dg, float* dbeta, float* dh0, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+  const bool packed = cu_seqlens != nullptr;
+  kda_status st = check_shape(s, packed);
+  if (st != KDA_OK) return st;
+  const bool any_tokens = (int64_t)s->B * s->T > 0;
+  if (any_tokens && (!q || !k || !v || !g || !beta || !dout || !dq || !dk || !dv || !dg ||
+                     !dbeta))
+    return KDA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, g, dout, h0, dhT, dq, dk, dv, dg, dh0};
+  for (const void* p : ptrs)
+    if (p && !aligned(p, 16)) return KDA_ERR_INVALID_ARG;
+  if (!aligned(beta, dsize(s->in_dtype)) || !aligned(dbeta, 4) ||
+      (packed && !aligned(cu_seqlens, 4)))
+    return KDA_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256)) return KDA_ERR_WORKSPACE;
+  if (workspace_bytes < bwd_ws_bytes(s)) return KDA_ERR_WORKSPACE;
+
+  kda::BwdArgs a{};
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
+  a.dout = dout; a.dhT = dhT; a.h0 = h0;
+  a.cu = cu_seqlens;
+  a.T = s->T;
+  a.N = packed ? s->num_seqs : s->B;
+  a.H = s->H;
+  a.D = s->dk;
+  a.scale = s->scale;
+  a.bf16 = s->in_dtype == KDA_BF16;
+  a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg; a.dbeta = dbeta; a.dh0 = dh0;
+  a.status = static_cast<unsigned int*>(workspace);
+  a.stream = static_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(workspace);
+  size_t at = kWsHeader;
+  if (cudaMemsetAsync(workspace, 0, kWsHeader, a.stream) != cudaSuccess) return KDA_ERR_CUDA;
+  if (packed) {
+    int32_t* order = reinterpret_cast<int32_t*>(w + at);
+    at += ws_order_bytes(a.N);
+    int64_t* off = reinterpret_cast<int64_t*>(w + at);
+    at += bwd_off_bytes(a.N);
+    kda::FwdArgs f{};
+    f.cu = cu_seqlens;
+    f.T = s->T;
+    f.N = a.N;
+    f.status = a.status;
+    f.stream = a.stream;
+    if (kda::launch_schedule(f, order) != cudaSuccess) return KDA_ERR_CUDA;
+    if (kda::launch_bwd_offsets(a, off) != cudaSuccess) return KDA_ERR_CUDA;
+    a.order = order;
+    a.sub_off = off;
+  }
+  at = (at + 255) / 256 * 256;
+  a.states = reinterpret_cast<float*>(w + at);
+  return kda::launch_backward(a) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 const char* kda_version(void) { return "kda-gb300 0.1"; }
 
 }  // extern "C"

@@ -1,0 +1,594 @@
+// KDA backward: the gradients of L = sum(o * do) + sum(hT * dhT) with respect to
+// q, k, v, g (log alpha), beta and h0, for the forward of kda_fwd ("Kimi K3 NPU
+// Training", section NPU 算子支持度, row KDA 反向: dq, dk, dv, dbeta, dgate and
+// dstate).
+//
+// One CTA of 512 threads per (sequence, head) chain, float32 throughout, in
+// sub-chunks of C = 16 tokens (the M of the warp-level m16n8k8 products).
+//   1. Forward sweep: the state at the start of every sub-chunk is recomputed
+//      and stored in the workspace.
+//   2. Backward sweep, last sub-chunk first, carrying dS = dL/dS at the current
+//      sub-chunk's end (dhT at the start of the sweep).
+//
+// Per sub-chunk, with S its start state, Gam the in-sub-chunk prefix sum of g,
+// Gl = Gam[C-1] (tokens past the sequence end carry zeros, so Gl is the last
+// valid token's), Kb = K e^Gam, Qb = Q e^Gam, Kh = K e^(Gl - Gam),
+//   P[i][j] = sum_c K_ic K_jc e^(Gam_ic - Gam_jc)  (j < i),  M likewise with Q_i
+//   (j <= i),  T = (I + diag(beta) P)^-1,  X = V - Kb S,  U = T diag(beta) X,
+//   O = scale (Qb S + M U),  S_end = diag(e^Gl) S + Kh^T U
+// (the token recurrence unrolled over the sub-chunk; u_t are the rows of U).
+// The backward applies the chain rule to these steps:
+//   dU = scale M^T dO + Kh dS;  dY = T^T dU, dX = diag(beta) dY, dV = dX,
+//   dbeta += rowsum(dY . X);  dT = dU (diag(beta) X)^T, dA = -T^T dT T^T
+//   (strictly lower), dbeta_i += sum_j dA_ij P_ij, dP = diag(beta) dA;
+//   dM = scale dO U^T (lower);  dKh = U dS^T, dQb = scale dO S^T, dKb = -dX S^T;
+//   per channel, the pairwise factors give dq, dk and dGam; the elementwise
+//   factors add dQb e^Gam, dKb e^Gam, dKh e^(Gl - Gam) and their dGam terms;
+//   dGl = e^Gl rowsum(dS . S) + colsum(Kh . dKh);  dg = reverse prefix sum of dGam
+//   (dGl added at the last row);  dS <- diag(e^Gl) dS + scale Qb^T dO - Kb^T dX.
+// Pairwise factors are exponentials of differences (each at most 1), so finite
+// gates of any size stay finite; a gate of -inf is not supported here.
+//
+// The seven products with S, dS or a 16 x d operand on both sides run on the
+// warp-level tensor-core path with the three-way tf32 split (float32
+// accuracy); the 16 x 16 pieces and the per-channel exponentials run on the
+// CUDA cores.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kda_internal.cuh"
+#include "kda_mma_sync.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kBT = 512;  // threads per CTA
+constexpr int kBC = 16;   // sub-chunk length
+constexpr int kSL = 17;   // row stride of the 16 x 16 matrices
+
+// shared-memory layout in floats
+template <int D>
+struct BwdLayout {
+  static constexpr int SLD = D + 4;  // D x D state matrices
+  static constexpr int CLD = D + 4;  // 16 x D sub-chunk matrices
+  static constexpr int CM = kBC * CLD;
+  static constexpr int S = 0;
+  static constexpr int DS = S + D * SLD;
+  static constexpr int Q = DS + D * SLD;
+  static constexpr int K = Q + CM;
+  static constexpr int G = K + CM;    // g, then Gam
+  static constexpr int KB = G + CM;
+  static constexpr int QB = KB + CM;
+  static constexpr int KH = QB + CM;  // Kh, then dk
+  static constexpr int X = KH + CM;   // v, then X, then dX
+  static constexpr int DO = X + CM;
+  static constexpr int U = DO + CM;   // U, then dq
+  static constexpr int DU = U + CM;   // dU, then dGam
+  static constexpr int TM = DU + CM;  // T
+  static constexpr int PM = TM + kBC * kSL;
+  static constexpr int MM = PM + kBC * kSL;
+  static constexpr int DT = MM + kBC * kSL;  // dT, then dP
+  static constexpr int DM = DT + kBC * kSL;
+  static constexpr int WM = DM + kBC * kSL;  // dT T^T
+  static constexpr int BETA = WM + kBC * kSL;
+  static constexpr int DB = BETA + kBC;     // dbeta
+  static constexpr int GL = DB + kBC;       // Gl
+  static constexpr int EGL = GL + D;        // e^Gl
+  static constexpr int DGL = EGL + D;       // dGl
+  static constexpr int TOTAL = DGL + D;
+  static constexpr size_t BYTES = (size_t)TOTAL * sizeof(float);
+};
+static_assert(BwdLayout<128>::BYTES <= 232448, "backward shared memory");
+
+template <typename TIn>
+struct BwdParams {
+  const TIn *q, *k, *v, *g, *beta;
+  const float* dout;
+  const float* dhT;
+  const float* h0;
+  SeqView seqs;
+  const int32_t* order;    // packed: longest first
+  const int64_t* sub_off;  // packed: first sub-chunk state row of each sequence
+  int H;
+  float scale;
+  float *dq, *dk, *dv, *dg, *dbeta, *dh0;
+  float* states;  // [rows][H][D][D]
+  unsigned int* status;
+};
+
+// acc += A(m0.., 0..Kd) B(0..Kd, n0..) for one m16n8 tile, with A(r, k) =
+// A[r * ars + k * acs] and B(k, n) = B[k * bks + n * bns] in shared memory
+template <int Kd>
+__device__ __forceinline__ void tile_mma(float (&acc)[3][4], const float* A, int ars, int acs,
+                                         int m0, const float* B, int bks, int bns, int n0,
+                                         int g, int t4, float ascale) {
+#pragma unroll 4
+  for (int k0 = 0; k0 < Kd; k0 += 8) {
+    float a[4], b[2];
+    a[0] = ascale * A[(m0 + g) * ars + (k0 + t4) * acs];
+    a[1] = ascale * A[(m0 + g + 8) * ars + (k0 + t4) * acs];
+    a[2] = ascale * A[(m0 + g) * ars + (k0 + t4 + 4) * acs];
+    a[3] = ascale * A[(m0 + g + 8) * ars + (k0 + t4 + 4) * acs];
+    b[0] = B[(k0 + t4) * bks + (n0 + g) * bns];
+    b[1] = B[(k0 + t4 + 4) * bks + (n0 + g) * bns];
+    mma_tf32x3(acc, a, b);
+  }
+}
+__device__ __forceinline__ void acc_zero(float (&acc)[3][4]) {
+#pragma unroll
+  for (int q = 0; q < 3; ++q)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) acc[q][r] = 0.f;
+}
+// element e of the C fragment: row g + 8 (e >> 1), column 2 t4 + (e & 1)
+__device__ __forceinline__ float acc_sum(const float (&acc)[3][4], int e) {
+  return acc[0][e] + acc[1][e] + acc[2][e];
+}
+
+template <int D, typename TIn>
+__global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p) {
+  using L = BwdLayout<D>;
+  constexpr int CLD = L::CLD, SLD = L::SLD;
+  extern __shared__ __align__(16) float sm[];
+  float* S = sm + L::S;
+  float* dS = sm + L::DS;
+  float* Q = sm + L::Q;
+  float* K = sm + L::K;
+  float* G = sm + L::G;
+  float* KB = sm + L::KB;
+  float* QB = sm + L::QB;
+  float* KH = sm + L::KH;
+  float* X = sm + L::X;
+  float* DO = sm + L::DO;
+  float* U = sm + L::U;
+  float* DU = sm + L::DU;
+  float* Tm = sm + L::TM;
+  float* Pm = sm + L::PM;
+  float* Mm = sm + L::MM;
+  float* dTm = sm + L::DT;
+  float* dMm = sm + L::DM;
+  float* Wm = sm + L::WM;
+  float* sbeta = sm + L::BETA;
+  float* sdb = sm + L::DB;
+  float* gl = sm + L::GL;
+  float* egl = sm + L::EGL;
+  float* dgl = sm + L::DGL;
+  float* dK = KH;   // aliases (see the layout)
+  float* dQ = U;
+  float* dG = DU;
+
+  // a malformed cu_seqlens is latched by the validation before this kernel
+  if (p.status && *(volatile const unsigned int*)p.status == (unsigned)KDA_ERR_BAD_SEQLENS) return;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g8 = lane >> 2, t4 = lane & 3;
+  const int H = p.H;
+  const int n = p.order ? p.order[blockIdx.x / H] : (int)(blockIdx.x / H);
+  const int h = blockIdx.x % H;
+  int64_t t0, len;
+  p.seqs.get(n, t0, len);
+  const int64_t nsub = (len + kBC - 1) / kBC;
+  const int64_t row0 = p.sub_off ? p.sub_off[n] : (int64_t)n * ((p.seqs.T + kBC - 1) / kBC);
+  auto state_row = [&](int64_t s) { return p.states + ((row0 + s) * H + h) * (int64_t)D * D; };
+  const int64_t sbase = ((int64_t)n * H + h) * D * D;
+
+  auto load_rows = [&](float* dst, const auto* src, int64_t cs, int nv) {
+    for (int i = tid; i < kBC * D; i += kBT) {
+      const int t = i / D, c = i % D;
+      dst[t * CLD + c] = t < nv ? to_f32(src[((t0 + cs + t) * H + h) * D + c]) : 0.f;
+    }
+  };
+  auto load_chunk = [&](int64_t cs, int nv, bool bwd) {
+    load_rows(K, p.k, cs, nv);
+    load_rows(G, p.g, cs, nv);
+    load_rows(X, p.v, cs, nv);
+    if (bwd) {
+      load_rows(Q, p.q, cs, nv);
+      load_rows(DO, p.dout, cs, nv);
+    }
+    if (tid < kBC) {
+      sbeta[tid] = tid < nv ? to_f32(p.beta[(t0 + cs + tid) * H + h]) : 0.f;
+      sdb[tid] = 0.f;
+    }
+  };
+
+  // Gam, the decayed operands, P (and M), T, X = V - Kb S and U = T diag(beta) X
+  auto prepare = [&](bool bwd) {
+    if (tid < D) {
+      float run = 0.f;
+#pragma unroll
+      for (int t = 0; t < kBC; ++t) {
+        run += G[t * CLD + tid];
+        G[t * CLD + tid] = run;
+      }
+      gl[tid] = run;
+      egl[tid] = expf(run);
+    }
+    __syncthreads();
+    for (int i = tid; i < kBC * D; i += kBT) {
+      const int t = i / D, c = i % D, o = t * CLD + c;
+      const float gm = G[o], e = expf(gm);
+      KB[o] = K[o] * e;
+      if (bwd) QB[o] = Q[o] * e;
+      KH[o] = K[o] * expf(gl[c] - gm);
+    }
+    {  // threads 0..255: P (j < i); 256..511: M (j <= i, backward only)
+      const int pi = (tid & 255) >> 4, pj = tid & 15;
+      const bool isM = tid >= 256;
+      float acc = 0.f;
+      if (isM ? (bwd && pj <= pi) : pj < pi) {
+        const float* A = isM ? Q : K;
+        for (int cc = 0; cc < D; ++cc) {
+          const int c = (cc + lane) & (D - 1);  // rotated so the lanes hit distinct banks
+          acc = fmaf(A[pi * CLD + c] * K[pj * CLD + c], expf(G[pi * CLD + c] - G[pj * CLD + c]),
+                     acc);
+        }
+      }
+      (isM ? Mm : Pm)[pi * kSL + pj] = acc;
+    }
+    __syncthreads();
+    if (warp == 0 && lane < kBC) {  // T = (I + diag(beta) P)^-1, column jj per lane
+      const int jj = lane;
+      float x[kBC];
+#pragma unroll
+      for (int m = 0; m < kBC; ++m) {
+        float vv = m == jj ? 1.f : 0.f;
+#pragma unroll
+        for (int l = 0; l < m; ++l)
+          if (l >= jj) vv = fmaf(-sbeta[m] * Pm[m * kSL + l], x[l], vv);
+        x[m] = m < jj ? 0.f : vv;
+      }
+#pragma unroll
+      for (int m = 0; m < kBC; ++m) Tm[m * kSL + jj] = x[m];
+    }
+    // X = V - Kb S (one n-tile of 8 columns per warp)
+    for (int nt = warp; nt < D / 8; nt += kBT / 32) {
+      float acc[3][4];
+      acc_zero(acc);
+      tile_mma<D>(acc, KB, CLD, 1, 0, S, SLD, 1, nt * 8, g8, t4, 1.f);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = g8 + 8 * (e >> 1), c = nt * 8 + 2 * t4 + (e & 1);
+        X[r * CLD + c] -= acc_sum(acc, e);
+      }
+    }
+    __syncthreads();
+    for (int i = tid; i < kBC * D; i += kBT) {  // U = T diag(beta) X
+      const int t = i / D, j = i % D;
+      float acc = 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < kBC; ++s2)
+        if (s2 <= t) acc = fmaf(Tm[t * kSL + s2] * sbeta[s2], X[s2 * CLD + j], acc);
+      U[t * CLD + j] = acc;
+    }
+    __syncthreads();
+  };
+
+  // ---- 1. forward sweep: the start state of every sub-chunk
+  for (int i = tid; i < D * D; i += kBT)
+    S[(i / D) * SLD + i % D] = p.h0 ? p.h0[sbase + i] : 0.f;
+  __syncthreads();
+  for (int64_t s = 0; s < nsub; ++s) {
+    const int64_t cs = s * kBC;
+    const int nv = (int)(len - cs < kBC ? len - cs : kBC);
+    float* st = state_row(s);
+    for (int i = tid; i < D * D; i += kBT) st[i] = S[(i / D) * SLD + i % D];
+    load_chunk(cs, nv, false);
+    __syncthreads();
+    prepare(false);
+    // S <- diag(e^Gl) S + Kh^T U
+    for (int tile = warp; tile < (D / 16) * (D / 8); tile += kBT / 32) {
+      const int m0 = (tile / (D / 8)) * 16, n0 = (tile % (D / 8)) * 8;
+      float acc[3][4];
+      acc_zero(acc);
+      tile_mma<kBC>(acc, KH, 1, CLD, m0, U, CLD, 1, n0, g8, t4, 1.f);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = m0 + g8 + 8 * (e >> 1), c = n0 + 2 * t4 + (e & 1);
+        S[r * SLD + c] = fmaf(egl[r], S[r * SLD + c], acc_sum(acc, e));
+      }
+    }
+    __syncthreads();
+  }
+
+  // ---- 2. backward sweep
+  for (int i = tid; i < D * D; i += kBT)
+    dS[(i / D) * SLD + i % D] = p.dhT ? p.dhT[sbase + i] : 0.f;
+  for (int64_t s = nsub - 1; s >= 0; --s) {
+    const int64_t cs = s * kBC;
+    const int nv = (int)(len - cs < kBC ? len - cs : kBC);
+    const float* st = state_row(s);
+    for (int i = tid; i < D * D; i += kBT) S[(i / D) * SLD + i % D] = st[i];
+    load_chunk(cs, nv, true);
+    __syncthreads();
+    prepare(true);
+
+    // dU = scale M^T dO + Kh dS
+    for (int nt = warp; nt < D / 8; nt += kBT / 32) {
+      float acc[3][4];
+      acc_zero(acc);
+      tile_mma<kBC>(acc, Mm, 1, kSL, 0, DO, CLD, 1, nt * 8, g8, t4, p.scale);
+      tile_mma<D>(acc, KH, CLD, 1, 0, dS, SLD, 1, nt * 8, g8, t4, 1.f);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = g8 + 8 * (e >> 1), c = nt * 8 + 2 * t4 + (e & 1);
+        DU[r * CLD + c] = acc_sum(acc, e);
+      }
+    }
+    if (tid < D) {  // dGl from the decay of the start state: e^Gl rowsum(dS . S)
+      float acc = 0.f;
+      for (int j = 0; j < D; ++j) acc = fmaf(dS[tid * SLD + j], S[tid * SLD + j], acc);
+      dgl[tid] = egl[tid] * acc;
+    }
+    __syncthreads();
+    {  // dT = dU (diag(beta) X)^T (threads 0..255), dM = scale dO U^T, lower (256..511)
+      const int pi = (tid & 255) >> 4, pj = tid & 15;
+      const bool isM = tid >= 256;
+      float acc = 0.f;
+      if (!isM || pj <= pi) {
+        const float* A = isM ? DO : DU;
+        const float* B = isM ? U : X;
+        for (int cc = 0; cc < D; ++cc) {
+          const int c = (cc + lane) & (D - 1);
+          acc = fmaf(A[pi * CLD + c], B[pj * CLD + c], acc);
+        }
+        acc *= isM ? p.scale : sbeta[pj];
+      }
+      (isM ? dMm : dTm)[pi * kSL + pj] = acc;
+    }
+    __syncthreads();
+    // dY = T^T dU; dbeta += rowsum(dY . X); dX = diag(beta) dY in place of X (each
+    // thread reads and writes only its own elements of X)
+    for (int i = tid; i < kBC * D; i += kBT) {
+      const int t = i / D, j = i % D;
+      float dy = 0.f;
+#pragma unroll
+      for (int i2 = 0; i2 < kBC; ++i2)
+        if (i2 >= t) dy = fmaf(Tm[i2 * kSL + t], DU[i2 * CLD + j], dy);
+      float part = dy * X[t * CLD + j];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+      if (lane == 0) atomicAdd(&sdb[t], part);
+      const float dx = sbeta[t] * dy;
+      X[t * CLD + j] = dx;
+      if (t < nv) p.dv[((t0 + cs + t) * H + h) * D + j] = dx;
+    }
+    // W = dT T^T (threads 0..255)
+    if (tid < 256) {
+      const int wi = tid >> 4, wj = tid & 15;
+      float acc = 0.f;
+#pragma unroll
+      for (int l = 0; l < kBC; ++l)
+        if (l <= wj) acc = fmaf(dTm[wi * kSL + l], Tm[wj * kSL + l], acc);
+      Wm[wi * kSL + wj] = acc;
+    }
+    __syncthreads();  // dU is consumed: dG may take its buffer
+    // dKh = U dS^T: dk = dKh e^(Gl - Gam); dGam = -Kh dKh; dGl += colsum(Kh dKh)
+    for (int nt = warp; nt < D / 8; nt += kBT / 32) {
+      float acc[3][4];
+      acc_zero(acc);
+      tile_mma<D>(acc, U, CLD, 1, 0, dS, 1, SLD, nt * 8, g8, t4, 1.f);
+      float col[2] = {0.f, 0.f};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = g8 + 8 * (e >> 1), c = nt * 8 + 2 * t4 + (e & 1), o = r * CLD + c;
+        const float d = acc_sum(acc, e), kh = KH[o];
+        col[e & 1] = fmaf(kh, d, col[e & 1]);
+        dG[o] = -kh * d;
+        dK[o] = d * expf(gl[c] - G[o]);
+      }
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        col[0] += __shfl_xor_sync(0xffffffffu, col[0], o);
+        col[1] += __shfl_xor_sync(0xffffffffu, col[1], o);
+      }
+      if (g8 == 0) {
+        dgl[nt * 8 + 2 * t4] += col[0];
+        dgl[nt * 8 + 2 * t4 + 1] += col[1];
+      }
+    }
+    // dA = -T^T W, strictly lower; dbeta_i += sum_j dA_ij P_ij; dP = diag(beta) dA
+    if (tid < 256) {
+      const int ai = tid >> 4, aj = tid & 15;
+      float acc = 0.f;
+      if (aj < ai) {
+#pragma unroll
+        for (int m = 0; m < kBC; ++m)
+          if (m >= ai) acc = fmaf(-Tm[m * kSL + ai], Wm[m * kSL + aj], acc);
+      }
+      float part = acc * Pm[ai * kSL + aj];
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+      if ((tid & 15) == 0) atomicAdd(&sdb[ai], part);
+      dTm[ai * kSL + aj] = sbeta[ai] * acc;  // dP (dT is consumed by W)
+    }
+    __syncthreads();
+    // dQb = scale dO S^T: dq = dQb e^Gam; dGam += Qb dQb   (U is consumed: dq takes it)
+    for (int nt = warp; nt < D / 8; nt += kBT / 32) {
+      float acc[3][4];
+      acc_zero(acc);
+      tile_mma<D>(acc, DO, CLD, 1, 0, S, 1, SLD, nt * 8, g8, t4, p.scale);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = g8 + 8 * (e >> 1), c = nt * 8 + 2 * t4 + (e & 1), o = r * CLD + c;
+        const float d = acc_sum(acc, e);
+        dQ[o] = d * expf(G[o]);
+        dG[o] = fmaf(QB[o], d, dG[o]);
+      }
+    }
+    // dKb = -dX S^T: dk += dKb e^Gam; dGam += Kb dKb
+    for (int nt = warp; nt < D / 8; nt += kBT / 32) {
+      float acc[3][4];
+      acc_zero(acc);
+      tile_mma<D>(acc, X, CLD, 1, 0, S, 1, SLD, nt * 8, g8, t4, -1.f);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = g8 + 8 * (e >> 1), c = nt * 8 + 2 * t4 + (e & 1), o = r * CLD + c;
+        const float d = acc_sum(acc, e);
+        dK[o] = fmaf(d, expf(G[o]), dK[o]);
+        dG[o] = fmaf(KB[o], d, dG[o]);
+      }
+    }
+    __syncthreads();
+    // pairwise factors, per (token t, channel c):
+    //   RK = sum_{j<t} dP_tj K_jc E_tj, RQ = sum_{j<=t} dM_tj K_jc E_tj,
+    //   CK = sum_{i>t} dP_it K_ic E_it, CQ = sum_{i>=t} dM_it Q_ic E_it,
+    //   E_ij = e^(Gam_ic - Gam_jc);  dq += RQ, dk += RK + CK + CQ,
+    //   dGam += K RK + Q RQ - K CK - K CQ
+    for (int i = tid; i < kBC * D; i += kBT) {
+      const int t = i / D, c = i % D, o = t * CLD + c;
+      const float gt = G[o], kt = K[o], qt = Q[o];
+      float rk = 0.f, rq = 0.f, ck = 0.f, cq = 0.f;
+#pragma unroll
+      for (int j = 0; j < kBC; ++j) {
+        const int oj = j * CLD + c;
+        if (j <= t) {
+          const float e = expf(gt - G[oj]) * K[oj];
+          rq = fmaf(dMm[t * kSL + j], e, rq);
+          if (j < t) rk = fmaf(dTm[t * kSL + j], e, rk);
+        }
+        if (j >= t) {
+          const float e = expf(G[oj] - gt);
+          cq = fmaf(dMm[j * kSL + t] * Q[oj], e, cq);
+          if (j > t) ck = fmaf(dTm[j * kSL + t] * K[oj], e, ck);
+        }
+      }
+      dQ[o] += rq;
+      dK[o] += rk + ck + cq;
+      dG[o] += kt * (rk - ck - cq) + qt * rq;
+    }
+    __syncthreads();
+    // outputs of the sub-chunk; dS <- diag(e^Gl) dS + scale Qb^T dO - Kb^T dX
+    for (int i = tid; i < kBC * D; i += kBT) {
+      const int t = i / D, c = i % D;
+      if (t < nv) {
+        const int64_t go = ((t0 + cs + t) * H + h) * D + c;
+        p.dq[go] = dQ[t * CLD + c];
+        p.dk[go] = dK[t * CLD + c];
+      }
+    }
+    if (tid < D) {  // dg: reverse prefix sum of dGam, dGl entering at the last row
+      float run = dgl[tid];
+#pragma unroll
+      for (int t = kBC - 1; t >= 0; --t) {
+        run += dG[t * CLD + tid];
+        if (t < nv) p.dg[((t0 + cs + t) * H + h) * D + tid] = run;
+      }
+    }
+    if (tid < nv) p.dbeta[(t0 + cs + tid) * H + h] = sdb[tid];
+    for (int tile = warp; tile < (D / 16) * (D / 8); tile += kBT / 32) {
+      const int m0 = (tile / (D / 8)) * 16, n0 = (tile % (D / 8)) * 8;
+      float acc[3][4];
+      acc_zero(acc);
+      tile_mma<kBC>(acc, QB, 1, CLD, m0, DO, CLD, 1, n0, g8, t4, p.scale);
+      tile_mma<kBC>(acc, KB, 1, CLD, m0, X, CLD, 1, n0, g8, t4, -1.f);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = m0 + g8 + 8 * (e >> 1), c = n0 + 2 * t4 + (e & 1);
+        dS[r * SLD + c] = fmaf(egl[r], dS[r * SLD + c], acc_sum(acc, e));
+      }
+    }
+    __syncthreads();
+  }
+  if (p.dh0)
+    for (int i = tid; i < D * D; i += kBT) p.dh0[sbase + i] = dS[(i / D) * SLD + i % D];
+}
+
+// first state row of each packed sequence: exclusive prefix sum of
+// ceil(len / 16), one block of 1024 threads stepping through the sequences
+__global__ void __launch_bounds__(1024) kda_bwd_offsets(const int32_t* cu, int N, int64_t T,
+                                                        int64_t* off) {
+  __shared__ int64_t warp_tot[32];
+  __shared__ int64_t carry;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  const SeqView sv{cu, T};
+  for (int base = 0; base < N; base += 1024) {
+    const int n = base + tid;
+    int64_t x = 0;
+    if (n < N) {
+      int64_t a, l;
+      sv.get(n, a, l);
+      x = (l + kBC - 1) / kBC;
+    }
+    int64_t incl = x;  // inclusive scan within the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_tot[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+      int64_t wt = warp_tot[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, wt, o);
+        if (lane >= o) wt += y;
+      }
+      warp_tot[lane] = wt;  // inclusive over warps
+    }
+    __syncthreads();
+    const int64_t before = carry + (w > 0 ? warp_tot[w - 1] : 0);
+    if (n < N) off[n] = before + incl - x;
+    __syncthreads();
+    if (tid == 1023) carry = before + incl;
+    __syncthreads();
+  }
+}
+
+template <int D, typename TIn>
+cudaError_t launch_bwd_t(const BwdArgs& a) {
+  using L = BwdLayout<D>;
+  BwdParams<TIn> p;
+  p.q = static_cast<const TIn*>(a.q);
+  p.k = static_cast<const TIn*>(a.k);
+  p.v = static_cast<const TIn*>(a.v);
+  p.g = static_cast<const TIn*>(a.g);
+  p.beta = static_cast<const TIn*>(a.beta);
+  p.dout = a.dout;
+  p.dhT = a.dhT;
+  p.h0 = a.h0;
+  p.seqs = SeqView{a.cu, a.T};
+  p.order = a.order;
+  p.sub_off = a.sub_off;
+  p.H = a.H;
+  p.scale = a.scale;
+  p.dq = a.dq;
+  p.dk = a.dk;
+  p.dv = a.dv;
+  p.dg = a.dg;
+  p.dbeta = a.dbeta;
+  p.dh0 = a.dh0;
+  p.states = a.states;
+  p.status = a.status;
+  auto kern = kda_bwd_kernel<D, TIn>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)L::BYTES);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)((int64_t)a.N * a.H), kBT, L::BYTES, a.stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t bwd_state_rows(bool packed, int64_t N, int64_t T) {
+  return packed ? (size_t)((T + kBC - 1) / kBC + N) : (size_t)(N * ((T + kBC - 1) / kBC));
+}
+
+cudaError_t launch_bwd_offsets(const BwdArgs& a, int64_t* off) {
+  if (a.N == 0) return cudaSuccess;
+  kda_bwd_offsets<<<1, 1024, 0, a.stream>>>(a.cu, a.N, a.T, off);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_backward(const BwdArgs& a) {
+  if ((int64_t)a.N * a.H == 0) return cudaSuccess;
+  if (a.bf16)
+    return a.D == 128 ? launch_bwd_t<128, __nv_bfloat16>(a) : launch_bwd_t<64, __nv_bfloat16>(a);
+  return a.D == 128 ? launch_bwd_t<128, float>(a) : launch_bwd_t<64, float>(a);
+}
+
+}  // namespace kda

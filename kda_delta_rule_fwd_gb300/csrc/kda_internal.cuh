@@ -182,4 +182,28 @@ struct DecodeArgs {
 
 cudaError_t launch_decode(const DecodeArgs& a);
 
+// Backward (kda_bwd): gradients of sum(o * dout) + sum(hT * dhT).
+struct BwdArgs {
+  const void *q, *k, *v, *g, *beta;
+  const float* dout;
+  const float* dhT;
+  const float* h0;
+  const int32_t* cu;
+  int64_t T;
+  int N, H, D;
+  float scale;
+  bool bf16;
+  const int32_t* order;
+  const int64_t* sub_off;
+  float *dq, *dk, *dv, *dg, *dbeta, *dh0;
+  float* states;
+  unsigned int* status;
+  cudaStream_t stream;
+};
+// state rows the backward keeps in the workspace (one per 16-token sub-chunk of
+// every sequence, for each head)
+size_t bwd_state_rows(bool packed, int64_t N, int64_t T);
+cudaError_t launch_bwd_offsets(const BwdArgs& a, int64_t* off);
+cudaError_t launch_backward(const BwdArgs& a);
+
 }  // namespace kda

@@ -36,6 +36,7 @@
 #include <mutex>
 
 #include "kda_internal.cuh"
+#include "kda_mma_sync.cuh"
 #include "kda_sm100.cuh"
 
 namespace kda {
@@ -158,44 +159,6 @@ __device__ __forceinline__ void st8_split(unsigned char* phi, unsigned char* plo
   *reinterpret_cast<uint4*>(phi) = h;
   *reinterpret_cast<uint4*>(plo) = l;
 }
-// Warp-level m16n8k8 tf32 product with fp32 accumulation, split three ways
-// for float32 accuracy: acc[0] += hi(a) hi(b), acc[1] += hi(a) lo(b),
-// acc[2] += lo(a) hi(b), with hi = tf32 rounding and lo = x - hi rounded again.
-// Fragments: a = (row g, col t), (g+8, t), (g, t+4), (g+8, t+4);
-// b = (row t, col g), (t+4, g); c = (g, 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1)
-// with g = lane/4, t = lane%4.  Used for the 16 x 16 blocks of the triangular
-// inverse, which are below the tensor-memory MMA's minimum M.
-__device__ __forceinline__ uint32_t tf32_rn(float x) {
-  uint32_t y;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4],
-                                         const uint32_t (&b)[2]) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-__device__ __forceinline__ void mma_tf32x3(float (&acc)[3][4], const float (&a)[4],
-                                           const float (&b)[2]) {
-  uint32_t ah[4], al[4], bh[2], bl[2];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    ah[i] = tf32_rn(a[i]);
-    al[i] = tf32_rn(a[i] - __uint_as_float(ah[i]));
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    bh[i] = tf32_rn(b[i]);
-    bl[i] = tf32_rn(b[i] - __uint_as_float(bh[i]));
-  }
-  mma_tf32(acc[0], ah, bh);
-  mma_tf32(acc[1], ah, bl);
-  mma_tf32(acc[2], al, bh);
-}
-
 // CTA-local named barrier over the first `count` threads (warps 0..count/32-1)
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

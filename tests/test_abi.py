@@ -217,3 +217,41 @@ def test_preproc_argument_errors(lib):
         if not torch.cuda.is_available():  # valid arguments reach the (absent) device
             assert call(L, m, shp, P(0, 1, 0, 1, FAKE), g=FAKE + 2) == m.KDA_ERR_CUDA
             assert call(L, m, shp, P(1, 1, 1, 0, FAKE + 4)) == m.KDA_ERR_CUDA
+
+
+def _bwd(L, shape, *, dout=FAKE, dq=FAKE, dbeta=FAKE, dh0=None, ws_bytes=None, cu=None):
+    vp = ctypes.c_void_p
+    L.kda_bwd.restype = ctypes.c_int
+    L.kda_bwd_workspace_size.restype = ctypes.c_size_t
+    L.kda_bwd_workspace_size.argtypes = [ctypes.c_void_p]
+    if ws_bytes is None:
+        ws_bytes = L.kda_bwd_workspace_size(ctypes.byref(shape))
+    return L.kda_bwd(ctypes.byref(shape), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE),
+                     vp(cu), None, vp(dout), None, vp(dq), vp(FAKE), vp(FAKE), vp(FAKE),
+                     vp(dbeta), vp(dh0), vp(FAKE), ctypes.c_size_t(ws_bytes), None)
+
+
+def test_bwd_workspace_and_argument_errors(lib):
+    """The backward keeps one dk x dv float32 state per 16-token sub-chunk and head:
+    the workspace size says so, and a smaller workspace, a missing or misaligned
+    gradient buffer or an unsupported head size is refused before any launch."""
+    m, L = lib
+    shp = _shape(m, B=2, T=100, H=4)
+    L.kda_bwd_workspace_size.restype = ctypes.c_size_t
+    L.kda_bwd_workspace_size.argtypes = [ctypes.c_void_p]
+    need = L.kda_bwd_workspace_size(ctypes.byref(shp))
+    assert need >= 2 * 7 * 4 * 128 * 128 * 4          # ceil(100 / 16) = 7 sub-chunks
+    assert need < 2 * 7 * 4 * 128 * 128 * 4 + 4096
+    packed = _shape(m, B=1, T=100, H=4, num_seqs=3)
+    assert L.kda_bwd_workspace_size(ctypes.byref(packed)) >= (7 + 3) * 4 * 128 * 128 * 4
+    assert _bwd(L, shp, ws_bytes=need - 1) == m.KDA_ERR_WORKSPACE
+    assert _bwd(L, shp, dout=0) == m.KDA_ERR_INVALID_ARG
+    assert _bwd(L, shp, dq=0) == m.KDA_ERR_INVALID_ARG
+    assert _bwd(L, shp, dq=FAKE + 4) == m.KDA_ERR_INVALID_ARG
+    assert _bwd(L, shp, dbeta=FAKE + 2) == m.KDA_ERR_INVALID_ARG
+    assert _bwd(L, shp, dh0=FAKE + 8) == m.KDA_ERR_INVALID_ARG
+    assert _bwd(L, _shape(m, dk=96, dv=96)) == m.KDA_ERR_UNSUPPORTED
+    assert _bwd(L, packed, cu=FAKE + 2) == m.KDA_ERR_INVALID_ARG
+    if not torch.cuda.is_available():  # valid arguments reach the (absent) device
+        assert _bwd(L, shp) == m.KDA_ERR_CUDA
+        assert _bwd(L, packed, cu=FAKE) == m.KDA_ERR_CUDA
