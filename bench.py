@@ -35,6 +35,8 @@ FLOP_PER_TOKEN_HEAD = 10 * CHUNK * D + 6 * D * D          # 180,224
 # minimum HBM bytes per token per head: q, k, v, g bf16 + beta bf16 + o float32
 BYTES_PER_TOKEN_HEAD = 4 * D * 2 + 2 + D * 4               # 1,538
 STATE_BYTES = D * D * 4                                    # one head's float32 state
+# backward: q, k, v, g bf16 + beta bf16 + dout fp32 in; dq, dk, dv, dg, dbeta fp32 out
+BWD_BYTES_PER_TOKEN_HEAD = 4 * D * 2 + 2 + D * 4 + 4 * D * 4 + 4   # 3,590
 WORKLOAD = "KDA prefill, fixed length: B=4, T=4096, H=32, dk=dv=128, bf16 in, fp32 state/out, chunk 64"
 METRIC = "KDA fwd tokens/s at H=32,d=128 (prefill+decode); % of tensor/HBM roofline"
 
@@ -327,7 +329,20 @@ def run_ours(args):
     qms = _time_steps(qfn, max(5, args.steps), max(3, args.warmup), stream, dist_on)
     qbytes = 1024 * H * (2 * STATE_BYTES + BYTES_PER_TOKEN_HEAD)
     del y, out_d
-    cms, kms, rms, ums, qms = max_over_ranks([cms, kms, rms, ums, qms], dev)
+    # backward on the fixed-length batch: gradients of sum(o * dout), dout ~ N(0, 1)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1005 + 13 * rank)
+    dout = torch.randn(B, T, H, D, generator=gen, device=dev)
+    bshape = kda.make_shape(x.q, x.v)
+    bws = torch.empty(kda.bwd_workspace_size(bshape), dtype=torch.uint8, device=dev)
+    bfn = lambda: kda.bwd(x.q, x.k, x.v, x.g, x.beta, dout, want_dh0=False, workspace=bws)
+    bms = _time_steps(bfn, max(3, args.steps // 4), 2, stream, dist_on)
+    st = kda.read_device_status(bws)
+    if st != kda.KDA_OK:
+        raise RuntimeError(f"device status {kda.status_string(st)}")
+    del dout, bws
+    bbytes = B * T * H * BWD_BYTES_PER_TOKEN_HEAD
+    cms, kms, rms, ums, qms, bms = max_over_ranks([cms, kms, rms, ums, qms, bms], dev)
     fbytes = B * T * H * BYTES_PER_TOKEN_HEAD + B * H * STATE_BYTES
     next_rows = {
         "prefill_checkpoints_512": {
@@ -351,6 +366,16 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "achieved": fbytes / (rms * 1e-3) / 1e9,
                          "peak": hbm_peak, "unit": "GB/s",
                          "frac": fbytes / (rms * 1e-3) / 1e9 / hbm_peak}},
+        "backward": {
+            "workload": WORKLOAD + "; gradients dq, dk, dv, dg, dbeta of sum(o * dout), "
+            "dout float32",
+            "ms_per_step": bms, "vs_prefill": bms / ms,
+            "tokens_per_s": B * T * H * world / H / (bms * 1e-3),
+            "roofline": {"bound": "hbm", "achieved": bbytes / (bms * 1e-3) / 1e9,
+                         "peak": hbm_peak, "unit": "GB/s",
+                         "frac": bbytes / (bms * 1e-3) / 1e9 / hbm_peak,
+                         "note": "algorithmic bytes (inputs, dout, gradients); the sub-chunk "
+                                 "states add 8 KB per token and head of workspace traffic"}},
         "decode_preproc_T1": {
             "workload": "decode pool 1024 x 32 heads, T_step=1, raw inputs, preprocessing fused",
             "ms_per_step": qms, "tokens_per_s": 1024 * world / (qms * 1e-3),

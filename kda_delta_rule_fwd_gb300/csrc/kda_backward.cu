@@ -58,7 +58,7 @@ struct BwdLayout {
   static constexpr int DS = S + D * SLD;
   static constexpr int Q = DS + D * SLD;
   static constexpr int K = Q + CM;
-  static constexpr int G = K + CM;    // g, then Gam
+  static constexpr int G = K + CM;    // g, then Gam log2(e)
   static constexpr int KB = G + CM;
   static constexpr int QB = KB + CM;
   static constexpr int KH = QB + CM;  // Kh, then dk
@@ -77,7 +77,8 @@ struct BwdLayout {
   static constexpr int GL = DB + kBC;       // Gl
   static constexpr int EGL = GL + D;        // e^Gl
   static constexpr int DGL = EGL + D;       // dGl
-  static constexpr int TOTAL = DGL + D;
+  static constexpr int FLAG = DGL + D;      // nonzero: a pairwise factor too large to split
+  static constexpr int TOTAL = FLAG + 4;
   static constexpr size_t BYTES = (size_t)TOTAL * sizeof(float);
 };
 static_assert(BwdLayout<128>::BYTES <= 232448, "backward shared memory");
@@ -98,6 +99,15 @@ struct BwdParams {
   unsigned int* status;
 };
 
+constexpr float kLog2e = 1.4426950408889634f;
+// 2^x on the special-function unit (relative error about 2^-22; results below
+// 2^-126 flush to zero, where they only drop terms far below the others)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // acc += A(m0.., 0..Kd) B(0..Kd, n0..) for one m16n8 tile, with A(r, k) =
 // A[r * ars + k * acs] and B(k, n) = B[k * bks + n * bns] in shared memory
 template <int Kd>
@@ -116,12 +126,44 @@ __device__ __forceinline__ void tile_mma(float (&acc)[3][4], const float* A, int
     mma_tf32x3(acc, a, b);
   }
 }
+// as tile_mma, with A and B scaled by ks[k] at their K index (KS) and B by
+// ns[n] at its column (NS)
+template <int Kd, bool KS, bool NS>
+__device__ __forceinline__ void tile_mma_sc(float (&acc)[3][4], const float* A, int ars, int acs,
+                                            int m0, const float* B, int bks, int bns, int n0,
+                                            int g, int t4, float ascale, const float* ks,
+                                            const float* ns) {
+  const float nsv = NS ? ns[n0 + g] : 1.f;
+#pragma unroll 4
+  for (int k0 = 0; k0 < Kd; k0 += 8) {
+    const float k1 = KS ? ks[k0 + t4] : 1.f, k2 = KS ? ks[k0 + t4 + 4] : 1.f;
+    float a[4], b[2];
+    a[0] = ascale * k1 * A[(m0 + g) * ars + (k0 + t4) * acs];
+    a[1] = ascale * k1 * A[(m0 + g + 8) * ars + (k0 + t4) * acs];
+    a[2] = ascale * k2 * A[(m0 + g) * ars + (k0 + t4 + 4) * acs];
+    a[3] = ascale * k2 * A[(m0 + g + 8) * ars + (k0 + t4 + 4) * acs];
+    b[0] = nsv * k1 * B[(k0 + t4) * bks + (n0 + g) * bns];
+    b[1] = nsv * k2 * B[(k0 + t4 + 4) * bks + (n0 + g) * bns];
+    mma_tf32x3(acc, a, b);
+  }
+}
 __device__ __forceinline__ void acc_zero(float (&acc)[3][4]) {
 #pragma unroll
   for (int q = 0; q < 3; ++q)
 #pragma unroll
     for (int r = 0; r < 4; ++r) acc[q][r] = 0.f;
 }
+// four consecutive elements as float32 (8-byte bf16 or 16-byte float loads)
+__device__ __forceinline__ float4 ld4f(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 ld4f(const __nv_bfloat16* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+}
+__device__ __forceinline__ void st4(float* p, const float4& v) {
+  p[0] = v.x; p[1] = v.y; p[2] = v.z; p[3] = v.w;
+}
+
 // element e of the C fragment: row g + 8 (e >> 1), column 2 t4 + (e & 1)
 __device__ __forceinline__ float acc_sum(const float (&acc)[3][4], int e) {
   return acc[0][e] + acc[1][e] + acc[2][e];
@@ -155,6 +197,7 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
   float* gl = sm + L::GL;
   float* egl = sm + L::EGL;
   float* dgl = sm + L::DGL;
+  int* s_wide = reinterpret_cast<int*>(sm + L::FLAG);
   float* dK = KH;   // aliases (see the layout)
   float* dQ = U;
   float* dG = DU;
@@ -173,59 +216,136 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
   auto state_row = [&](int64_t s) { return p.states + ((row0 + s) * H + h) * (int64_t)D * D; };
   const int64_t sbase = ((int64_t)n * H + h) * D * D;
 
-  auto load_rows = [&](float* dst, const auto* src, int64_t cs, int nv) {
-    for (int i = tid; i < kBC * D; i += kBT) {
-      const int t = i / D, c = i % D;
-      dst[t * CLD + c] = t < nv ? to_f32(src[((t0 + cs + t) * H + h) * D + c]) : 0.f;
-    }
-  };
+  // the sub-chunk's inputs, four channels per thread, every load issued before
+  // the first store (rows past the sequence end are zero)
   auto load_chunk = [&](int64_t cs, int nv, bool bwd) {
-    load_rows(K, p.k, cs, nv);
-    load_rows(G, p.g, cs, nv);
-    load_rows(X, p.v, cs, nv);
-    if (bwd) {
-      load_rows(Q, p.q, cs, nv);
-      load_rows(DO, p.dout, cs, nv);
+    constexpr int G4 = D / 4;
+    if (tid < kBC * G4) {
+      const int t = tid / G4, c = (tid % G4) * 4;
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 fk = z, fg = z, fv = z, fq = z, fo = z;
+      if (t < nv) {
+        const int64_t go = ((t0 + cs + t) * H + h) * D + c;
+        fk = ld4f(p.k + go);
+        fg = ld4f(p.g + go);
+        fv = ld4f(p.v + go);
+        if (bwd) {
+          fq = ld4f(p.q + go);
+          fo = ld4f(p.dout + go);
+        }
+      }
+      st4(K + t * CLD + c, fk);
+      st4(G + t * CLD + c, fg);
+      st4(X + t * CLD + c, fv);
+      if (bwd) {
+        st4(Q + t * CLD + c, fq);
+        st4(DO + t * CLD + c, fo);
+      }
     }
     if (tid < kBC) {
       sbeta[tid] = tid < nv ? to_f32(p.beta[(t0 + cs + tid) * H + h]) : 0.f;
       sdb[tid] = 0.f;
     }
   };
+  // a D x D state between global memory (dense) and shared memory (row stride SLD),
+  // 16 bytes per access, all loads issued before the stores
+  auto state_in = [&](float* dst, const float* src) {
+    constexpr int NV = D * D / 4 / kBT;
+    float4 r[NV];
+#pragma unroll
+    for (int m = 0; m < NV; ++m) r[m] = src ? ld4f(src + 4 * (tid + m * kBT)) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < NV; ++m) {
+      const int i = 4 * (tid + m * kBT);
+      *reinterpret_cast<float4*>(dst + (i / D) * SLD + i % D) = r[m];
+    }
+  };
+  auto state_out = [&](float* dst, const float* src) {
+#pragma unroll 4
+    for (int m = 0; m < D * D / 4 / kBT; ++m) {
+      const int i = 4 * (tid + m * kBT);
+      *reinterpret_cast<float4*>(dst + i) = *reinterpret_cast<const float4*>(src + (i / D) * SLD + i % D);
+    }
+  };
 
-  // Gam, the decayed operands, P (and M), T, X = V - Kb S and U = T diag(beta) X
+  bool split = true;  // the pairwise factors of this sub-chunk are split (see prepare)
+  // Gam (kept as Gam log2 e, so every factor is one ex2), the decayed operands,
+  // P (and M), T, X = V - Kb S and U = T diag(beta) X
   auto prepare = [&](bool bwd) {
+    if (tid == 0) *s_wide = 0;
+    __syncthreads();
     if (tid < D) {
       float run = 0.f;
 #pragma unroll
       for (int t = 0; t < kBC; ++t) {
         run += G[t * CLD + tid];
-        G[t * CLD + tid] = run;
+        G[t * CLD + tid] = run * kLog2e;
       }
-      gl[tid] = run;
-      egl[tid] = expf(run);
+      gl[tid] = run * kLog2e;
+      egl[tid] = ex2(run * kLog2e);
+      // e^(Gam_i - Gam_j) = e^(Gam_i - h) e^(h - Gam_j), h = Gl / 2; where some
+      // factor would pass 2^86 the sub-chunk takes the explicit form instead
+      const float h2 = 0.5f * run * kLog2e;
+      bool ok = true;
+#pragma unroll
+      for (int t = 0; t < kBC; ++t) ok = ok && fabsf(G[t * CLD + tid] - h2) <= 86.f;
+      if (!ok) atomicOr(s_wide, 1);
     }
     __syncthreads();
+    split = *(volatile int*)s_wide == 0;
     for (int i = tid; i < kBC * D; i += kBT) {
       const int t = i / D, c = i % D, o = t * CLD + c;
-      const float gm = G[o], e = expf(gm);
+      const float gm = G[o], e = ex2(gm);
       KB[o] = K[o] * e;
       if (bwd) QB[o] = Q[o] * e;
-      KH[o] = K[o] * expf(gl[c] - gm);
+      KH[o] = K[o] * ex2(gl[c] - gm);
     }
-    {  // threads 0..255: P (j < i); 256..511: M (j <= i, backward only)
-      const int pi = (tid & 255) >> 4, pj = tid & 15;
-      const bool isM = tid >= 256;
-      float acc = 0.f;
-      if (isM ? (bwd && pj <= pi) : pj < pi) {
+    __syncthreads();  // the split products below read Kb, Qb and Kh
+    if (split) {
+      // P = (K a)(K b)^T (warps 0, 1), M = (Q a)(K b)^T (warps 2, 3), with the factors
+      // a = e^(Gam - h), b = e^(h - Gam) formed directly (not from Kb, which may
+      // have underflowed)
+      if (warp < (bwd ? 4 : 2)) {
+        const bool isM = warp >= 2;
         const float* A = isM ? Q : K;
-        for (int cc = 0; cc < D; ++cc) {
-          const int c = (cc + lane) & (D - 1);  // rotated so the lanes hit distinct banks
-          acc = fmaf(A[pi * CLD + c] * K[pj * CLD + c], expf(G[pi * CLD + c] - G[pj * CLD + c]),
-                     acc);
+        const int n0 = (warp & 1) * 8;
+        float acc[3][4];
+        acc_zero(acc);
+#pragma unroll 4
+        for (int k0 = 0; k0 < D; k0 += 8) {
+          float a[4], b[2];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = k0 + t4 + 4 * (e >> 1), o = (g8 + 8 * (e & 1)) * CLD + c;
+            a[e] = A[o] * ex2(G[o] - 0.5f * gl[c]);
+          }
+#pragma unroll
+          for (int q2 = 0; q2 < 2; ++q2) {
+            const int c = k0 + t4 + 4 * q2, o = (n0 + g8) * CLD + c;
+            b[q2] = K[o] * ex2(0.5f * gl[c] - G[o]);
+          }
+          mma_tf32x3(acc, a, b);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = g8 + 8 * (e >> 1), c = n0 + 2 * t4 + (e & 1);
+          (isM ? Mm : Pm)[r * kSL + c] = (isM ? c <= r : c < r) ? acc_sum(acc, e) : 0.f;
         }
       }
-      (isM ? Mm : Pm)[pi * kSL + pj] = acc;
+    } else {  // explicit differences: threads 0..255 P (j < i), 256..511 M (j <= i)
+      const int pi = (tid & 255) >> 4, pj = tid & 15;
+      const bool isM = tid >= 256;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      if (isM ? (bwd && pj <= pi) : pj < pi) {
+        const float* A = isM ? Q : K;
+#pragma unroll 4
+        for (int cc = 0; cc < D; ++cc) {
+          const int c = (cc + lane) & (D - 1);  // rotated so the lanes hit distinct banks
+          acc[cc & 3] = fmaf(A[pi * CLD + c] * K[pj * CLD + c],
+                             ex2(G[pi * CLD + c] - G[pj * CLD + c]), acc[cc & 3]);
+        }
+      }
+      (isM ? Mm : Pm)[pi * kSL + pj] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
     }
     __syncthreads();
     if (warp == 0 && lane < kBC) {  // T = (I + diag(beta) P)^-1, column jj per lane
@@ -266,14 +386,12 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
   };
 
   // ---- 1. forward sweep: the start state of every sub-chunk
-  for (int i = tid; i < D * D; i += kBT)
-    S[(i / D) * SLD + i % D] = p.h0 ? p.h0[sbase + i] : 0.f;
+  state_in(S, p.h0 ? p.h0 + sbase : nullptr);
   __syncthreads();
   for (int64_t s = 0; s < nsub; ++s) {
     const int64_t cs = s * kBC;
     const int nv = (int)(len - cs < kBC ? len - cs : kBC);
-    float* st = state_row(s);
-    for (int i = tid; i < D * D; i += kBT) st[i] = S[(i / D) * SLD + i % D];
+    state_out(state_row(s), S);
     load_chunk(cs, nv, false);
     __syncthreads();
     prepare(false);
@@ -293,13 +411,11 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
   }
 
   // ---- 2. backward sweep
-  for (int i = tid; i < D * D; i += kBT)
-    dS[(i / D) * SLD + i % D] = p.dhT ? p.dhT[sbase + i] : 0.f;
+  state_in(dS, p.dhT ? p.dhT + sbase : nullptr);
   for (int64_t s = nsub - 1; s >= 0; --s) {
     const int64_t cs = s * kBC;
     const int nv = (int)(len - cs < kBC ? len - cs : kBC);
-    const float* st = state_row(s);
-    for (int i = tid; i < D * D; i += kBT) S[(i / D) * SLD + i % D] = st[i];
+    state_in(S, state_row(s));
     load_chunk(cs, nv, true);
     __syncthreads();
     prepare(true);
@@ -322,20 +438,22 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
       dgl[tid] = egl[tid] * acc;
     }
     __syncthreads();
-    {  // dT = dU (diag(beta) X)^T (threads 0..255), dM = scale dO U^T, lower (256..511)
-      const int pi = (tid & 255) >> 4, pj = tid & 15;
-      const bool isM = tid >= 256;
-      float acc = 0.f;
-      if (!isM || pj <= pi) {
-        const float* A = isM ? DO : DU;
-        const float* B = isM ? U : X;
-        for (int cc = 0; cc < D; ++cc) {
-          const int c = (cc + lane) & (D - 1);
-          acc = fmaf(A[pi * CLD + c], B[pj * CLD + c], acc);
-        }
-        acc *= isM ? p.scale : sbeta[pj];
+    if (warp < 4) {  // dT = dU (diag(beta) X)^T (warps 0, 1); dM = scale dO U^T, lower (2, 3)
+      const bool isM = warp >= 2;
+      const int n0 = (warp & 1) * 8;
+      float acc[3][4];
+      acc_zero(acc);
+      if (isM)
+        tile_mma_sc<D, false, false>(acc, DO, CLD, 1, 0, U, 1, CLD, n0, g8, t4, p.scale, nullptr,
+                                     nullptr);
+      else
+        tile_mma_sc<D, false, true>(acc, DU, CLD, 1, 0, X, 1, CLD, n0, g8, t4, 1.f, nullptr,
+                                    sbeta);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = g8 + 8 * (e >> 1), c = n0 + 2 * t4 + (e & 1);
+        (isM ? dMm : dTm)[r * kSL + c] = (!isM || c <= r) ? acc_sum(acc, e) : 0.f;
       }
-      (isM ? dMm : dTm)[pi * kSL + pj] = acc;
     }
     __syncthreads();
     // dY = T^T dU; dbeta += rowsum(dY . X); dX = diag(beta) dY in place of X (each
@@ -376,7 +494,7 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
         const float d = acc_sum(acc, e), kh = KH[o];
         col[e & 1] = fmaf(kh, d, col[e & 1]);
         dG[o] = -kh * d;
-        dK[o] = d * expf(gl[c] - G[o]);
+        dK[o] = d * ex2(gl[c] - G[o]);
       }
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) {
@@ -413,7 +531,7 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
       for (int e = 0; e < 4; ++e) {
         const int r = g8 + 8 * (e >> 1), c = nt * 8 + 2 * t4 + (e & 1), o = r * CLD + c;
         const float d = acc_sum(acc, e);
-        dQ[o] = d * expf(G[o]);
+        dQ[o] = d * ex2(G[o]);
         dG[o] = fmaf(QB[o], d, dG[o]);
       }
     }
@@ -426,7 +544,7 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
       for (int e = 0; e < 4; ++e) {
         const int r = g8 + 8 * (e >> 1), c = nt * 8 + 2 * t4 + (e & 1), o = r * CLD + c;
         const float d = acc_sum(acc, e);
-        dK[o] = fmaf(d, expf(G[o]), dK[o]);
+        dK[o] = fmaf(d, ex2(G[o]), dK[o]);
         dG[o] = fmaf(KB[o], d, dG[o]);
       }
     }
@@ -436,6 +554,56 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
     //   CK = sum_{i>t} dP_it K_ic E_it, CQ = sum_{i>=t} dM_it Q_ic E_it,
     //   E_ij = e^(Gam_ic - Gam_jc);  dq += RQ, dk += RK + CK + CQ,
     //   dGam += K RK + Q RQ - K CK - K CQ
+    // Split (E_ij = a_i b_j, a = e^(Gam - h), b = e^(h - Gam)): RK = a (dP (K b)),
+    // RQ = a (dM (K b)), CK = b (dP^T (K a)), CQ = b (dM^T (Q a)), the factors formed
+    // from Gam directly; dP and dM are zero outside their triangles.
+    if (split) {
+      for (int nt = warp; nt < D / 8; nt += kBT / 32) {
+        const int n0 = nt * 8;
+        float rk[3][4], rq[3][4], ck[3][4], cq[3][4];
+        acc_zero(rk);
+        acc_zero(rq);
+        acc_zero(ck);
+        acc_zero(cq);
+        const float hb = 0.5f * gl[n0 + g8];
+#pragma unroll
+        for (int k0 = 0; k0 < kBC; k0 += 8) {
+          float kb[2], ka[2], qa[2], ap[4], am[4], apt[4], amt[4];
+#pragma unroll
+          for (int q2 = 0; q2 < 2; ++q2) {
+            const int o = (k0 + t4 + 4 * q2) * CLD + n0 + g8;
+            const float x = G[o] - hb;
+            kb[q2] = K[o] * ex2(-x);
+            ka[q2] = K[o] * ex2(x);
+            qa[q2] = Q[o] * ex2(x);
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int r = g8 + 8 * (e & 1), k = k0 + t4 + 4 * (e >> 1);
+            ap[e] = dTm[r * kSL + k];
+            am[e] = dMm[r * kSL + k];
+            apt[e] = dTm[k * kSL + r];
+            amt[e] = dMm[k * kSL + r];
+          }
+          mma_tf32x3(rk, ap, kb);
+          mma_tf32x3(rq, am, kb);
+          mma_tf32x3(ck, apt, ka);
+          mma_tf32x3(cq, amt, qa);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = g8 + 8 * (e >> 1), c = n0 + 2 * t4 + (e & 1), o = t * CLD + c;
+          const float h2 = 0.5f * gl[c];
+          const float a = ex2(G[o] - h2), b = ex2(h2 - G[o]);
+          const float vrk = a * acc_sum(rk, e), vrq = a * acc_sum(rq, e);
+          const float vck = b * acc_sum(ck, e), vcq = b * acc_sum(cq, e);
+          const float kt = K[o];
+          dQ[o] += vrq;
+          dK[o] += vrk + vck + vcq;
+          dG[o] += kt * (vrk - vck - vcq) + Q[o] * vrq;
+        }
+      }
+    } else
     for (int i = tid; i < kBC * D; i += kBT) {
       const int t = i / D, c = i % D, o = t * CLD + c;
       const float gt = G[o], kt = K[o], qt = Q[o];
@@ -444,12 +612,12 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
       for (int j = 0; j < kBC; ++j) {
         const int oj = j * CLD + c;
         if (j <= t) {
-          const float e = expf(gt - G[oj]) * K[oj];
+          const float e = ex2(gt - G[oj]) * K[oj];
           rq = fmaf(dMm[t * kSL + j], e, rq);
           if (j < t) rk = fmaf(dTm[t * kSL + j], e, rk);
         }
         if (j >= t) {
-          const float e = expf(G[oj] - gt);
+          const float e = ex2(G[oj] - gt);
           cq = fmaf(dMm[j * kSL + t] * Q[oj], e, cq);
           if (j > t) ck = fmaf(dTm[j * kSL + t] * K[oj], e, ck);
         }
@@ -491,8 +659,7 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
     }
     __syncthreads();
   }
-  if (p.dh0)
-    for (int i = tid; i < D * D; i += kBT) p.dh0[sbase + i] = dS[(i / D) * SLD + i % D];
+  if (p.dh0) state_out(p.dh0 + sbase, dS);
 }
 
 // first state row of each packed sequence: exclusive prefix sum of

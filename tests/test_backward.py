@@ -91,11 +91,13 @@ def test_state_cotangent_alone(kda, oracle_mod):
 
 
 def test_strong_gates(kda, oracle_mod):
-    """Gates of -30 on some channels and tokens: every pairwise factor is an
-    exponential of a difference, so nothing overflows."""
-    x = kda_inputs.fixed(1, 40, 2, 64, dtype=torch.float32, device=DEV, seed=740, h0_std=0.1)
+    """Gates of -30 on some channels and tokens.  Tokens 20-22 of head 1 stay within
+    the range where the pairwise factors are split; tokens 33-38 of head 0 (-180
+    nats in one sub-chunk) take the explicit exponentials of differences."""
+    x = kda_inputs.fixed(1, 50, 2, 64, dtype=torch.float32, device=DEV, seed=740, h0_std=0.1)
     x.g[0, 5, 0, :10] = -30.0
     x.g[0, 20:23, 1, 3] = -30.0
+    x.g[0, 33:39, 0, :4] = -30.0
     do, dh = _cotangents(x, 741)
     _check(kda, oracle_mod, x, do, dh)
 
