@@ -71,8 +71,9 @@ struct BwdLayout {
   static constexpr int MM = PM + kBC * kSL;
   static constexpr int DT = MM + kBC * kSL;  // dT, then dP
   static constexpr int DM = DT + kBC * kSL;
-  static constexpr int WM = DM + kBC * kSL;  // dT T^T
-  static constexpr int BETA = WM + kBC * kSL;
+  static constexpr int SCR = DM + kBC * kSL;  // partial dT / dM tiles (8 x 16 x 8)
+  static constexpr int SCG = SCR + 1024;      // partial row sums for dGl (2 x D)
+  static constexpr int BETA = SCG + 2 * D;
   static constexpr int DB = BETA + kBC;     // dbeta
   static constexpr int GL = DB + kBC;       // Gl
   static constexpr int EGL = GL + D;        // e^Gl
@@ -191,7 +192,9 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
   float* Mm = sm + L::MM;
   float* dTm = sm + L::DT;
   float* dMm = sm + L::DM;
-  float* Wm = sm + L::WM;
+  float* Wm = Mm;  // dT T^T, once M is consumed
+  float* scr = sm + L::SCR;
+  float* scg = sm + L::SCG;
   float* sbeta = sm + L::BETA;
   float* sdb = sm + L::DB;
   float* gl = sm + L::GL;
@@ -305,14 +308,18 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
       // P = (K a)(K b)^T (warps 0, 1), M = (Q a)(K b)^T (warps 2, 3), with the factors
       // a = e^(Gam - h), b = e^(h - Gam) formed directly (not from Kb, which may
       // have underflowed)
-      if (warp < (bwd ? 4 : 2)) {
-        const bool isM = warp >= 2;
+      // every warp takes one (matrix, 8-column tile) over a slice of the channels;
+      // the partial tiles meet in the U buffer (U is formed further down)
+      {
+        const int nw = bwd ? 4 : 2, parts = (kBT / 32) / nw;
+        const int combo = warp % nw;
+        const bool isM = combo >= 2;
         const float* A = isM ? Q : K;
-        const int n0 = (warp & 1) * 8;
+        const int n0 = (combo & 1) * 8, kc = D / parts, kb = (warp / nw) * kc;
         float acc[3][4];
         acc_zero(acc);
-#pragma unroll 4
-        for (int k0 = 0; k0 < D; k0 += 8) {
+#pragma unroll 2
+        for (int k0 = kb; k0 < kb + kc; k0 += 8) {
           float a[4], b[2];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -327,9 +334,15 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
           mma_tf32x3(acc, a, b);
         }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int r = g8 + 8 * (e >> 1), c = n0 + 2 * t4 + (e & 1);
-          (isM ? Mm : Pm)[r * kSL + c] = (isM ? c <= r : c < r) ? acc_sum(acc, e) : 0.f;
+        for (int e = 0; e < 4; ++e)
+          U[warp * 128 + (g8 + 8 * (e >> 1)) * 8 + 2 * t4 + (e & 1)] = acc_sum(acc, e);
+        __syncthreads();
+        for (int i = tid; i < nw * 128; i += kBT) {
+          const int cb = i >> 7, w = i & 127, r = w >> 3, c = (cb & 1) * 8 + (w & 7);
+          float v = 0.f;
+          for (int pp = 0; pp < parts; ++pp) v += U[(pp * nw + cb) * 128 + w];
+          const bool m2 = cb >= 2;
+          (m2 ? Mm : Pm)[r * kSL + c] = (m2 ? c <= r : c < r) ? v : 0.f;
         }
       }
     } else {  // explicit differences: threads 0..255 P (j < i), 256..511 M (j <= i)
@@ -432,30 +445,41 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
         DU[r * CLD + c] = acc_sum(acc, e);
       }
     }
-    if (tid < D) {  // dGl from the decay of the start state: e^Gl rowsum(dS . S)
-      float acc = 0.f;
-      for (int j = 0; j < D; ++j) acc = fmaf(dS[tid * SLD + j], S[tid * SLD + j], acc);
-      dgl[tid] = egl[tid] * acc;
+    if (tid < 2 * D) {  // dGl from the decay of the start state: e^Gl rowsum(dS . S), by halves
+      const int c = tid % D, j0 = (tid / D) * (D / 2);
+      float acc[2] = {0.f, 0.f};
+#pragma unroll 4
+      for (int j = 0; j < D / 2; ++j)
+        acc[j & 1] = fmaf(dS[c * SLD + j0 + j], S[c * SLD + j0 + j], acc[j & 1]);
+      scg[tid] = acc[0] + acc[1];
     }
     __syncthreads();
-    if (warp < 4) {  // dT = dU (diag(beta) X)^T (warps 0, 1); dM = scale dO U^T, lower (2, 3)
-      const bool isM = warp >= 2;
-      const int n0 = (warp & 1) * 8;
+    // dT = dU (diag(beta) X)^T, dM = scale dO U^T (lower): warps 0..7 each take one
+    // (matrix, 8-column tile) over half of the value channels
+    if (warp < 8) {
+      const int cb = warp & 3, kb = (warp >> 2) * (D / 2);
+      const bool isM = cb >= 2;
+      const int n0 = (cb & 1) * 8;
       float acc[3][4];
       acc_zero(acc);
       if (isM)
-        tile_mma_sc<D, false, false>(acc, DO, CLD, 1, 0, U, 1, CLD, n0, g8, t4, p.scale, nullptr,
-                                     nullptr);
+        tile_mma_sc<D / 2, false, false>(acc, DO + kb, CLD, 1, 0, U + kb, 1, CLD, n0, g8, t4,
+                                         p.scale, nullptr, nullptr);
       else
-        tile_mma_sc<D, false, true>(acc, DU, CLD, 1, 0, X, 1, CLD, n0, g8, t4, 1.f, nullptr,
-                                    sbeta);
+        tile_mma_sc<D / 2, false, true>(acc, DU + kb, CLD, 1, 0, X + kb, 1, CLD, n0, g8, t4, 1.f,
+                                        nullptr, sbeta);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = g8 + 8 * (e >> 1), c = n0 + 2 * t4 + (e & 1);
-        (isM ? dMm : dTm)[r * kSL + c] = (!isM || c <= r) ? acc_sum(acc, e) : 0.f;
-      }
+      for (int e = 0; e < 4; ++e)
+        scr[warp * 128 + (g8 + 8 * (e >> 1)) * 8 + 2 * t4 + (e & 1)] = acc_sum(acc, e);
     }
     __syncthreads();
+    {  // the two halves of dT and dM; dGl's first term
+      const int cb = tid >> 7, w = tid & 127, r = w >> 3, c = (cb & 1) * 8 + (w & 7);
+      const float v = scr[cb * 128 + w] + scr[(4 + cb) * 128 + w];
+      const bool isM = cb >= 2;
+      (isM ? dMm : dTm)[r * kSL + c] = (!isM || c <= r) ? v : 0.f;
+    }
+    if (tid < D) dgl[tid] = egl[tid] * (scg[tid] + scg[D + tid]);
     // dY = T^T dU; dbeta += rowsum(dY . X); dX = diag(beta) dY in place of X (each
     // thread reads and writes only its own elements of X)
     for (int i = tid; i < kBC * D; i += kBT) {
@@ -472,7 +496,8 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
       X[t * CLD + j] = dx;
       if (t < nv) p.dv[((t0 + cs + t) * H + h) * D + j] = dx;
     }
-    // W = dT T^T (threads 0..255)
+    __syncthreads();  // dU is consumed: dG may take its buffer; dT and dM are complete
+    // W = dT T^T (threads 0..255; M is consumed, so W takes its place)
     if (tid < 256) {
       const int wi = tid >> 4, wj = tid & 15;
       float acc = 0.f;
@@ -481,7 +506,6 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
         if (l <= wj) acc = fmaf(dTm[wi * kSL + l], Tm[wj * kSL + l], acc);
       Wm[wi * kSL + wj] = acc;
     }
-    __syncthreads();  // dU is consumed: dG may take its buffer
     // dKh = U dS^T: dk = dKh e^(Gl - Gam); dGam = -Kh dKh; dGl += colsum(Kh dKh)
     for (int nt = warp; nt < D / 8; nt += kBT / 32) {
       float acc[3][4];
@@ -506,6 +530,7 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
         dgl[nt * 8 + 2 * t4 + 1] += col[1];
       }
     }
+    __syncthreads();
     // dA = -T^T W, strictly lower; dbeta_i += sum_j dA_ij P_ij; dP = diag(beta) dA
     if (tid < 256) {
       const int ai = tid >> 4, aj = tid & 15;
@@ -521,7 +546,6 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
       if ((tid & 15) == 0) atomicAdd(&sdb[ai], part);
       dTm[ai * kSL + aj] = sbeta[ai] * acc;  // dP (dT is consumed by W)
     }
-    __syncthreads();
     // dQb = scale dO S^T: dq = dQb e^Gam; dGam += Qb dQb   (U is consumed: dq takes it)
     for (int nt = warp; nt < D / 8; nt += kBT / 32) {
       float acc[3][4];
