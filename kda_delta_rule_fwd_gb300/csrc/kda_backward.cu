@@ -115,7 +115,7 @@ template <int Kd>
 __device__ __forceinline__ void tile_mma(float (&acc)[3][4], const float* A, int ars, int acs,
                                          int m0, const float* B, int bks, int bns, int n0,
                                          int g, int t4, float ascale) {
-#pragma unroll 4
+#pragma unroll
   for (int k0 = 0; k0 < Kd; k0 += 8) {
     float a[4], b[2];
     a[0] = ascale * A[(m0 + g) * ars + (k0 + t4) * acs];
@@ -146,6 +146,95 @@ __device__ __forceinline__ void tile_mma_sc(float (&acc)[3][4], const float* A, 
     b[0] = nsv * k1 * B[(k0 + t4) * bks + (n0 + g) * bns];
     b[1] = nsv * k2 * B[(k0 + t4 + 4) * bks + (n0 + g) * bns];
     mma_tf32x3(acc, a, b);
+  }
+}
+// two products sharing B: acc1 += s1 A1 B and acc2 += s2 A2 B (A1, A2 row-major with
+// row stride ars; B(k, n) = B[k * bks + n * bns]); B is split once per K step
+template <int Kd>
+__device__ __forceinline__ void tile_mma2(float (&acc1)[3][4], float (&acc2)[3][4],
+                                          const float* A1, float s1, const float* A2, float s2,
+                                          int ars, const float* B, int bks, int bns, int n0,
+                                          int g, int t4) {
+#pragma unroll
+  for (int k0 = 0; k0 < Kd; k0 += 8) {
+    uint32_t bh[2], bl[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const float x = B[(k0 + t4 + 4 * q) * bks + (n0 + g) * bns];
+      bh[q] = tf32_rn(x);
+      bl[q] = tf32_rn(x - __uint_as_float(bh[q]));
+    }
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      const float* A = which ? A2 : A1;
+      const float sc = which ? s2 : s1;
+      uint32_t ah[4], al[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float x = sc * A[(g + 8 * (e & 1)) * ars + k0 + t4 + 4 * (e >> 1)];
+        ah[e] = tf32_rn(x);
+        al[e] = tf32_rn(x - __uint_as_float(ah[e]));
+      }
+      float (&acc)[3][4] = which ? acc2 : acc1;
+      mma_tf32(acc[0], ah, bh);
+      mma_tf32(acc[1], ah, bl);
+      mma_tf32(acc[2], al, bh);
+    }
+  }
+}
+// Dm[rows, n0..n0+7] = egl[row] Dm + sum over the products p < NP of s_p A_p^T B_p, for
+// every 16-row tile this warp owns (K = the 16 tokens; A_p(c, t) = A_p[t * CLD + c],
+// B_p(t, n) = B_p[t * CLD + n]); the B fragments, the same for all of the warp's
+// tiles, are split once
+template <int D, int NP>
+__device__ __forceinline__ void dd_update(float* Dm, int sld, const float* egl, int cld,
+                                          const float* A1, float s1, const float* B1,
+                                          const float* A2, float s2, const float* B2, int warp,
+                                          int g, int t4) {
+  constexpr int NT = D / 8;  // 8-column tiles per row of tiles
+  const int n0 = (warp % NT) * 8;
+  uint32_t bh[NP][2][2], bl[NP][2][2];
+#pragma unroll
+  for (int pp = 0; pp < NP; ++pp)
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const float x = (pp ? B2 : B1)[(ks * 8 + t4 + 4 * q) * cld + n0 + g];
+        bh[pp][ks][q] = tf32_rn(x);
+        bl[pp][ks][q] = tf32_rn(x - __uint_as_float(bh[pp][ks][q]));
+      }
+  for (int tile = warp; tile < (D / 16) * NT; tile += kBT / 32) {
+    const int m0 = (tile / NT) * 16;
+    float acc[3][4];
+#pragma unroll
+    for (int q = 0; q < 3; ++q)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) acc[q][r] = 0.f;
+#pragma unroll
+    for (int pp = 0; pp < NP; ++pp)
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+        const float* A = pp ? A2 : A1;
+        const float sc = pp ? s2 : s1;
+        uint32_t ah[4], al[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float x = sc * A[(ks * 8 + t4 + 4 * (e >> 1)) * cld + m0 + g + 8 * (e & 1)];
+          ah[e] = tf32_rn(x);
+          al[e] = tf32_rn(x - __uint_as_float(ah[e]));
+        }
+        const uint32_t bhh[2] = {bh[pp][ks][0], bh[pp][ks][1]};
+        const uint32_t bll[2] = {bl[pp][ks][0], bl[pp][ks][1]};
+        mma_tf32(acc[0], ah, bhh);
+        mma_tf32(acc[1], ah, bll);
+        mma_tf32(acc[2], al, bhh);
+      }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int r = m0 + g + 8 * (e >> 1), c = n0 + 2 * t4 + (e & 1);
+      Dm[r * sld + c] = fmaf(egl[r], Dm[r * sld + c], acc[0][e] + acc[1][e] + acc[2][e]);
+    }
   }
 }
 __device__ __forceinline__ void acc_zero(float (&acc)[3][4]) {
@@ -409,17 +498,7 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
     __syncthreads();
     prepare(false);
     // S <- diag(e^Gl) S + Kh^T U
-    for (int tile = warp; tile < (D / 16) * (D / 8); tile += kBT / 32) {
-      const int m0 = (tile / (D / 8)) * 16, n0 = (tile % (D / 8)) * 8;
-      float acc[3][4];
-      acc_zero(acc);
-      tile_mma<kBC>(acc, KH, 1, CLD, m0, U, CLD, 1, n0, g8, t4, 1.f);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = m0 + g8 + 8 * (e >> 1), c = n0 + 2 * t4 + (e & 1);
-        S[r * SLD + c] = fmaf(egl[r], S[r * SLD + c], acc_sum(acc, e));
-      }
-    }
+    dd_update<D, 1>(S, SLD, egl, CLD, KH, 1.f, U, nullptr, 0.f, nullptr, warp, g8, t4);
     __syncthreads();
   }
 
@@ -547,29 +626,19 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
       dTm[ai * kSL + aj] = sbeta[ai] * acc;  // dP (dT is consumed by W)
     }
     // dQb = scale dO S^T: dq = dQb e^Gam; dGam += Qb dQb   (U is consumed: dq takes it)
+    // dKb = -dX S^T: dk += dKb e^Gam; dGam += Kb dKb   (one pass: both read S^T)
     for (int nt = warp; nt < D / 8; nt += kBT / 32) {
-      float acc[3][4];
-      acc_zero(acc);
-      tile_mma<D>(acc, DO, CLD, 1, 0, S, 1, SLD, nt * 8, g8, t4, p.scale);
+      float aq[3][4], ak[3][4];
+      acc_zero(aq);
+      acc_zero(ak);
+      tile_mma2<D>(aq, ak, DO, p.scale, X, -1.f, CLD, S, 1, SLD, nt * 8, g8, t4);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int r = g8 + 8 * (e >> 1), c = nt * 8 + 2 * t4 + (e & 1), o = r * CLD + c;
-        const float d = acc_sum(acc, e);
-        dQ[o] = d * ex2(G[o]);
-        dG[o] = fmaf(QB[o], d, dG[o]);
-      }
-    }
-    // dKb = -dX S^T: dk += dKb e^Gam; dGam += Kb dKb
-    for (int nt = warp; nt < D / 8; nt += kBT / 32) {
-      float acc[3][4];
-      acc_zero(acc);
-      tile_mma<D>(acc, X, CLD, 1, 0, S, 1, SLD, nt * 8, g8, t4, -1.f);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = g8 + 8 * (e >> 1), c = nt * 8 + 2 * t4 + (e & 1), o = r * CLD + c;
-        const float d = acc_sum(acc, e);
-        dK[o] = fmaf(d, ex2(G[o]), dK[o]);
-        dG[o] = fmaf(KB[o], d, dG[o]);
+        const float dqb = acc_sum(aq, e), dkb = acc_sum(ak, e), eg = ex2(G[o]);
+        dQ[o] = dqb * eg;
+        dK[o] = fmaf(dkb, eg, dK[o]);
+        dG[o] = fmaf(QB[o], dqb, fmaf(KB[o], dkb, dG[o]));
       }
     }
     __syncthreads();
@@ -669,18 +738,7 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
       }
     }
     if (tid < nv) p.dbeta[(t0 + cs + tid) * H + h] = sdb[tid];
-    for (int tile = warp; tile < (D / 16) * (D / 8); tile += kBT / 32) {
-      const int m0 = (tile / (D / 8)) * 16, n0 = (tile % (D / 8)) * 8;
-      float acc[3][4];
-      acc_zero(acc);
-      tile_mma<kBC>(acc, QB, 1, CLD, m0, DO, CLD, 1, n0, g8, t4, p.scale);
-      tile_mma<kBC>(acc, KB, 1, CLD, m0, X, CLD, 1, n0, g8, t4, -1.f);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = m0 + g8 + 8 * (e >> 1), c = n0 + 2 * t4 + (e & 1);
-        dS[r * SLD + c] = fmaf(egl[r], dS[r * SLD + c], acc_sum(acc, e));
-      }
-    }
+    dd_update<D, 2>(dS, SLD, egl, CLD, QB, p.scale, DO, KB, -1.f, X, warp, g8, t4);
     __syncthreads();
   }
   if (p.dh0) state_out(p.dh0 + sbase, dS);
