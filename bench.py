@@ -156,14 +156,20 @@ def _cpu_baseline(x, budget_s=20.0):
     rate1 = 1024 / (time.perf_counter() - t0)          # token-heads/s on one core
     heads = max(1, min(H, int(budget_s * rate1 * cores / (B * T))))
     sub = lambda a: a[:, :, :heads].contiguous()
-    t0 = time.perf_counter()
-    oracle.recurrent(sub(x.q), sub(x.k), sub(x.v), sub(x.g), x.beta[:, :, :heads].contiguous(),
-                     n_threads=cores)
-    dt = time.perf_counter() - t0
-    head_tokens_per_s = B * T * heads / dt
+    args = (sub(x.q), sub(x.k), sub(x.v), sub(x.g), x.beta[:, :, :heads].contiguous())
+    # whole passes over the sample until at least half the budget has elapsed (the
+    # oracle may finish all heads well inside it), at most 30
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        oracle.recurrent(*args, n_threads=cores)
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= 0.5 * budget_s or passes >= 30:
+            break
+    head_tokens_per_s = passes * B * T * heads / dt
     return {"value": head_tokens_per_s / H, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"B={B}, T={T}, {heads} of {H} heads, all tokens ({dt:.1f} s); "
-                      f"tokens/s = head-tokens/s / H"}
+            "sample": f"B={B}, T={T}, {heads} of {H} heads, all tokens, {passes} passes "
+                      f"({dt:.1f} s); tokens/s = head-tokens/s / H"}
 
 
 def _time_steps(fn, steps, warmup, stream, dist_on):
