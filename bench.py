@@ -51,14 +51,19 @@ def _peaks():
 
 def profiled_traffic():
     """DRAM bytes per prefill launch from the committed ncu summary, or None when
-    the kernel source has changed since those counters were taken."""
+    the kernel source (with its headers) has changed since those counters were taken."""
     import hashlib
     import re
-    src = os.path.join(ROOT, "kda_delta_rule_fwd_gb300", "csrc", "kda_prefill_bf16.cu")
+    csrc = os.path.join(ROOT, "kda_delta_rule_fwd_gb300", "csrc")
+    srcs = [os.path.join(csrc, f) for f in ("kda_prefill_bf16.cu", "kda_internal.cuh",
+                                            "kda_mma_sync.cuh", "kda_sm100.cuh")]
     prof = os.path.join(ROOT, "profiles", "prefill_bf16_B4_T4096_H32.txt")
     try:
         txt = open(prof).read()
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        h = hashlib.sha256()
+        for f in srcs:  # the kernel's source and the headers it includes
+            h.update(open(f, "rb").read())
+        digest = h.hexdigest()[:16]
     except OSError:
         return None
     m = re.search(r"kernel_source_sha256_16: (\w+)", txt)

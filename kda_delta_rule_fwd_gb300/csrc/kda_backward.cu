@@ -109,30 +109,6 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// tf32 parts of x by truncation: hi keeps sign, exponent and the top 10 mantissa
-// bits, lo = x - hi (exact) truncated the same way; hi lo + lo hi + hi hi then
-// carries x y to about 2^-20 relative, float32-level accuracy for these sums
-__device__ __forceinline__ uint32_t tf32_hi(float x) { return __float_as_uint(x) & 0xffffe000u; }
-__device__ __forceinline__ uint32_t tf32_lo(float x, uint32_t hi) {
-  return __float_as_uint(x - __uint_as_float(hi)) & 0xffffe000u;
-}
-__device__ __forceinline__ void mma3(float (&acc)[3][4], const float (&a)[4], const float (&b)[2]) {
-  uint32_t ah[4], al[4], bh[2], bl[2];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    ah[i] = tf32_hi(a[i]);
-    al[i] = tf32_lo(a[i], ah[i]);
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    bh[i] = tf32_hi(b[i]);
-    bl[i] = tf32_lo(b[i], bh[i]);
-  }
-  mma_tf32(acc[0], ah, bh);
-  mma_tf32(acc[1], ah, bl);
-  mma_tf32(acc[2], al, bh);
-}
-
 // acc += A(m0.., 0..Kd) B(0..Kd, n0..) for one m16n8 tile, with A(r, k) =
 // A[r * ars + k * acs] and B(k, n) = B[k * bks + n * bns] in shared memory
 template <int Kd>
@@ -148,7 +124,7 @@ __device__ __forceinline__ void tile_mma(float (&acc)[3][4], const float* A, int
     a[3] = ascale * A[(m0 + g + 8) * ars + (k0 + t4 + 4) * acs];
     b[0] = B[(k0 + t4) * bks + (n0 + g) * bns];
     b[1] = B[(k0 + t4 + 4) * bks + (n0 + g) * bns];
-    mma3(acc, a, b);
+    mma_tf32x3(acc, a, b);
   }
 }
 // as tile_mma, with A and B scaled by ks[k] at their K index (KS) and B by
@@ -169,7 +145,7 @@ __device__ __forceinline__ void tile_mma_sc(float (&acc)[3][4], const float* A, 
     a[3] = ascale * k2 * A[(m0 + g + 8) * ars + (k0 + t4 + 4) * acs];
     b[0] = nsv * k1 * B[(k0 + t4) * bks + (n0 + g) * bns];
     b[1] = nsv * k2 * B[(k0 + t4 + 4) * bks + (n0 + g) * bns];
-    mma3(acc, a, b);
+    mma_tf32x3(acc, a, b);
   }
 }
 // two products sharing B: acc1 += s1 A1 B and acc2 += s2 A2 B (A1, A2 row-major with
@@ -444,7 +420,7 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
             const int c = k0 + t4 + 4 * q2, o = (n0 + g8) * CLD + c;
             b[q2] = K[o] * ex2(0.5f * gl[c] - G[o]);
           }
-          mma3(acc, a, b);
+          mma_tf32x3(acc, a, b);
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e)
@@ -702,10 +678,10 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
             apt[e] = dTm[k * kSL + r];
             amt[e] = dMm[k * kSL + r];
           }
-          mma3(rk, ap, kb);
-          mma3(rq, am, kb);
-          mma3(ck, apt, ka);
-          mma3(cq, amt, qa);
+          mma_tf32x3(rk, ap, kb);
+          mma_tf32x3(rq, am, kb);
+          mma_tf32x3(ck, apt, ka);
+          mma_tf32x3(cq, amt, qa);
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
