@@ -142,8 +142,10 @@ kda_status kda_fwd_checkpoints(const kda_shape* s, const void* q, const void* k,
  * Input preprocessing fused into the kernels ("Kimi K3 NPU Training", section
  * 模型结构, steps 1 and 3: q/k are L2 normalised and the channel-wise decay and
  * beta are built from the projected gate inputs).  Each enabled step is
- * computed in float32 from the values passed in and rounded to in_dtype, which is
- * what a separate preprocessing pass that stores in_dtype tensors produces:
+ * computed in float32 from the values passed in.  The gate and beta are then
+ * rounded to in_dtype, as a separate pass that stores in_dtype tensors would
+ * (the bf16 path's cumulative sum takes a bf16 gate); the normalised q and k
+ * enter the float32 products unrounded:
  *   qk_l2norm      q, k per (token, head):  x / max(||x||_2, 1e-12)
  *   gate_softplus  g holds the raw gate:    log(alpha) = -softplus(g),
  *                  softplus(x) = log(1 + e^x) (absolute error below 4e-7

@@ -100,8 +100,8 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
       }
       const float ik = inv_l2(sk), iq = inv_l2(sq);
       for (int c = lane; c < D; c += 32) {
-        s_k[warp][c] = round_to<TIn>(s_k[warp][c] * ik);
-        s_q[warp][c] = round_to<TIn>(s_q[warp][c] * iq);
+        s_k[warp][c] *= ik;  // kept in float32 (the products take float32)
+        s_q[warp][c] *= iq;
       }
     }
     float acc = 0.f;

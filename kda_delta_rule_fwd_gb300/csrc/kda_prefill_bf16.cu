@@ -664,8 +664,8 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (kPre && p.pre.l2) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          kx[e] = round_to<__nv_bfloat16>(kx[e] * inv_k);
-          qx[e] = round_to<__nv_bfloat16>(qx[e] * inv_q);
+          kx[e] *= inv_k;  // kept in float32 into the decayed operands
+          qx[e] *= inv_q;
         }
       }
       const float4 e2a = *reinterpret_cast<const float4*>(s_rho + cg * 8);

@@ -110,8 +110,8 @@ kda_prefill_f32_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
         }
         const float ik = inv_l2(s2k), iq = inv_l2(s2q);
         for (int c = lane; c < D; c += 32) {
-          sk[t * LD + c] = round_to<TIn>(sk[t * LD + c] * ik);
-          sq[t * LD + c] = round_to<TIn>(sq[t * LD + c] * iq);
+          sk[t * LD + c] *= ik;  // kept in float32
+          sq[t * LD + c] *= iq;
         }
       }
       __syncthreads();

@@ -29,7 +29,8 @@ Three forms are provided, each citing the passage it follows:
 * :func:`preprocess` -- the input preprocessing that the fused entry points
   apply ("Kimi K3 NPU Training", section 模型结构, steps 1 and 3: q/k L2
   normalisation, channel-wise decay and beta from the gate inputs), evaluated
-  in float64 and rounded to the input dtype.
+  in float64; the gate and beta are rounded to the input dtype, the normalised
+  q and k are not.
 
 Parity status: every function here is pinned by ``tests/test_oracle.py``
 against closed forms, special cases and a brute-force Kronecker formulation.
@@ -93,9 +94,14 @@ def max_threads() -> int:
 def _as_host(x, f64):
     if x is None:
         return None
-    if hasattr(x, "detach"):  # a torch tensor: take an exact float32 copy
-        x = x.detach().to("cpu").float().numpy()
+    if hasattr(x, "detach"):  # a torch tensor: an exact float32 (or float64) copy
+        x = x.detach().to("cpu")
+        x = (x.double() if f64 else x.float()).numpy()
     return np.ascontiguousarray(x, dtype=np.float64 if f64 else np.float32)
+
+
+def _is_f64(x):
+    return x is not None and str(getattr(x, "dtype", "")) in ("float64", "torch.float64")
 
 
 def _ptr(a):
@@ -110,13 +116,13 @@ def recurrent(q, k, v, g, beta, *, cu_seqlens=None, h0=None, scale=None, n_threa
     or packed ``[T,H,d]`` / ``[T,H]`` with ``cu_seqlens`` (N+1 offsets).
     ``g`` is log(alpha).  ``h0`` is ``[N,H,dk,dv]`` or None (zeros).
     ``scale`` defaults to dk**-0.5.  Inputs may be numpy arrays or torch
-    tensors (copied to host float32, which is exact for bf16 and fp32 data);
-    float64 numpy inputs are used as they are.
+    tensors; they are copied to host float32 (exact for bf16 and fp32 data), or
+    to float64 when any activation is float64.
     ``lib`` overrides the compiled library (used by the mutation tests).
     Returns ``(o, hT)`` as float64 arrays with ``o`` shaped like ``v``.
     """
-    f64 = all(isinstance(x, np.ndarray) and x.dtype == np.float64
-              for x in (q, k, v, g, beta) )
+    # float64 buffers when any activation is float64 (exact for the others too)
+    f64 = any(_is_f64(x) for x in (q, k, v, g, beta))
     q, k, v, g, beta = (_as_host(x, f64) for x in (q, k, v, g, beta))
     h0 = _as_host(h0, f64)
     out_shape = v.shape
@@ -155,7 +161,7 @@ def recurrent(q, k, v, g, beta, *, cu_seqlens=None, h0=None, scale=None, n_threa
 
 
 # ---------------------------------------------------------------------------
-# chunkwise-parallel form (numpy, float64)
+# gradients (torch autograd, float64)
 # ---------------------------------------------------------------------------
 
 def recurrent_grad(q, k, v, g, beta, do, *, cu_seqlens=None, h0=None, dhT=None, scale=None):
@@ -218,12 +224,18 @@ def recurrent_grad(q, k, v, g, beta, do, *, cu_seqlens=None, h0=None, dhT=None, 
     return tuple(res)
 
 
+# ---------------------------------------------------------------------------
+# input preprocessing (numpy, float64)
+# ---------------------------------------------------------------------------
+
 def preprocess(q, k, g, beta, *, qk_l2norm=True, gate_softplus=True, beta_sigmoid=True,
                gate_scale=None, gate_per_head=False):
-    """Preprocessed (q, k, g, beta) as torch tensors of the inputs' dtype.
+    """Preprocessed (q, k, g, beta) as torch tensors.
 
-    Each enabled step follows its definition in float64 on the given values and
-    is then rounded to the input dtype:
+    Each enabled step follows its definition in float64 on the given values.  The
+    gate and beta are then rounded to the input dtype (the kernels round them
+    there too); normalised q and k stay float64 (the kernels carry them in
+    float32, unrounded):
       q, k:  x / max(||x||_2, 1e-12) over the head dimension
       g:     -a_h softplus(g), softplus(x) = log(1 + e^x) (= x above 20), a_h the
              per-head scale (1 when gate_scale is None)
@@ -252,8 +264,14 @@ def preprocess(q, k, g, beta, *, qk_l2norm=True, gate_softplus=True, beta_sigmoi
     Gr = back(G)
     if gate_per_head:
         Gr = Gr.expand(*G.shape[:-1], Q.shape[-1]).contiguous()
-    return back(Q), back(K), Gr, back(Bt)
+    exact = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    qk = exact if qk_l2norm else back
+    return qk(Q), qk(K), Gr, back(Bt)
 
+
+# ---------------------------------------------------------------------------
+# chunkwise-parallel form (numpy, float64)
+# ---------------------------------------------------------------------------
 
 def _tri_inv_unit_lower(A):
     """(I + A)^-1 for strictly lower-triangular A, by forward substitution."""

@@ -363,20 +363,25 @@ def test_preprocess_l2_norm(oracle_mod):
         assert torch.equal(a, e)
 
 
-def test_preprocess_rounds_to_input_dtype(oracle_mod):
-    """bf16 inputs come back as bf16, each value the rounding of the float64 result."""
+def test_preprocess_rounds_gate_and_beta_to_input_dtype(oracle_mod):
+    """bf16 inputs: the gate and beta come back as bf16, each value the rounding of
+    the float64 result; normalised q and k come back unrounded (float64), and with
+    the norm step off q and k keep their dtype."""
     import torch
     x = torch.tensor([[[0.3, -1.7, 2.2, 0.0]]], dtype=torch.bfloat16)
     b = torch.tensor([[0.7]], dtype=torch.bfloat16)
     qn, kn, gn, bn = oracle_mod.preprocess(x, x, x, b)
-    assert qn.dtype == torch.bfloat16 and bn.dtype == torch.bfloat16
+    assert gn.dtype == torch.bfloat16 and bn.dtype == torch.bfloat16
+    assert qn.dtype == torch.float64 and kn.dtype == torch.float64
     xd = x.double().numpy()[0, 0]
     want_q = xd / np.sqrt(np.sum(xd * xd))
     want_g = -np.log1p(np.exp(xd))
     want_b = 1.0 / (1.0 + np.exp(-0.69921875))   # bf16(0.7)
-    assert torch.equal(qn[0, 0], torch.from_numpy(want_q).to(torch.bfloat16))
+    np.testing.assert_allclose(qn[0, 0].numpy(), want_q, rtol=1e-15, atol=0)
     assert torch.equal(gn[0, 0], torch.from_numpy(want_g).to(torch.bfloat16))
     assert bn.item() == torch.tensor(want_b).to(torch.bfloat16).item()
+    q2, k2, _, _ = oracle_mod.preprocess(x, x, x, b, qk_l2norm=False)
+    assert q2.dtype == torch.bfloat16 and torch.equal(q2, x)
 
 
 def test_preprocess_gate_scale_and_per_head(oracle_mod):

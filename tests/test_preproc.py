@@ -33,10 +33,12 @@ def _raw_packed(lengths, H, d, dtype, seed):
 
 def _split(oracle_mod, x, on):
     """Kernel inputs that leave exactly the steps in ``on`` to the kernel (the
-    others applied beforehand by the oracle) and the oracle's fully
-    preprocessed inputs."""
+    others applied beforehand by the oracle, the results cast to the input dtype
+    as a caller would store them) and the oracle's fully preprocessed inputs from
+    those same values."""
     off = {s: s not in on for s in STEPS}
-    kq, kk, kg, kb = oracle_mod.preprocess(x.q, x.k, x.g, x.beta, **off)
+    pre = oracle_mod.preprocess(x.q, x.k, x.g, x.beta, **off)
+    kq, kk, kg, kb = (t.to(x.q.dtype).contiguous() for t in pre)
     full = oracle_mod.preprocess(kq, kk, kg, kb, **{s: s in on for s in STEPS})
     dev = lambda t: t.to(DEV).contiguous()
     return (dev(kq), dev(kk), dev(kg), dev(kb)), full

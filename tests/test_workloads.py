@@ -4,7 +4,10 @@ benchmark uses, against the float64 oracle:
 * fixed-length prefill B=4, T=4096, H=32, d=128 (bf16): every element;
 * packed prefill, 16 sequences of 128..8192 tokens with h0 ~ N(0, 0.1^2): every element;
 * long context B=1, T=1,048,576, H=32: two seeded, sampled heads over the full length;
-* decode pool of 1024 sequences (T_step 1 and 8): a seeded sample of 64 sequences.
+* decode pool of 1024 sequences (T_step 1 and 8): a seeded sample of 64 sequences;
+* the fused preprocessing on the fixed-length batch: every element;
+* the backward of the fixed-length batch: exact zeros past the cotangent's support and
+  two sampled (sequence, head) chains (tolerance 1e-4, float32 throughout).
 
 Tolerance: max|err| / rms(ref) <= 1e-2 for bf16 inputs with float32 state,
 per output tensor.
@@ -77,3 +80,44 @@ def test_decode_pool_sampled_sequences(kda, oracle_mod, T_step):
     eo, eh = rel_err(pick(o), o_ref), rel_err(pick(state), h_ref)
     _report(f"decode T_step={T_step} (64 of 1024 sequences)", eo, eh)
     assert eo <= TOL_BF16 and eh <= TOL_BF16
+
+
+def test_fused_preprocessing_full(kda, oracle_mod):
+    """The fixed-length batch on raw inputs with all three preprocessing steps fused,
+    the bench's launch: every element against the oracle's preprocessing and
+    recurrence."""
+    r = kda_inputs.draw_raw((4, 4096), 32, 128, 128, device=DEV, seed=1001)
+    o, hT = kda.fwd_preproc(r.q, r.k, r.v, r.g, r.beta)
+    torch.cuda.synchronize()
+    fq, fk, fg, fb = oracle_mod.preprocess(r.q, r.k, r.g, r.beta)
+    o_ref, h_ref = oracle_mod.recurrent(fq, fk, r.v, fg, fb)
+    eo, eh = rel_err(o, o_ref), rel_err(hT, h_ref)
+    _report("fused preprocessing B=4 T=4096 H=32", eo, eh)
+    assert eo <= TOL_BF16 and eh <= TOL_BF16
+
+
+def test_backward_full_sampled(kda, oracle_mod):
+    """The backward on the full B=4, T=4096, H=32 batch (the bench's launch) with
+    dout nonzero on the first 512 tokens only.  Every gradient past token 512 must
+    then be exactly zero, and on two seeded (sequence, head) samples the first 512
+    tokens' gradients match the oracle's autograd (which needs only those tokens)."""
+    x = kda_inputs.workload(1, device=DEV)
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(1005)
+    do = torch.randn(x.v.shape, generator=gen, device=DEV)
+    do[:, 512:] = 0
+    grads = kda.bwd(x.q, x.k, x.v, x.g, x.beta, do)
+    torch.cuda.synchronize()
+    for gr in grads[:5]:
+        assert torch.count_nonzero(gr[:, 512:]) == 0
+    pick = torch.Generator().manual_seed(1006)
+    for _ in range(2):
+        b = int(torch.randint(0, 4, (1,), generator=pick))
+        h = int(torch.randint(0, 32, (1,), generator=pick))
+        sl = lambda t: t[b:b + 1, :512, h:h + 1].contiguous().cpu()
+        ref = oracle_mod.recurrent_grad(sl(x.q), sl(x.k), sl(x.v), sl(x.g), sl(x.beta), sl(do))
+        for name, a, e in zip(("dq", "dk", "dv", "dg", "dbeta"), grads[:5], ref[:5]):
+            err = rel_err(a[b:b + 1, :512, h:h + 1], e)
+            print(f"backward B=4 T=4096 H=32, sample ({b}, {h}) {name}: {err:.3e}")
+            assert err <= 1e-4, (name, b, h, err)
+        assert rel_err(grads[5][b:b + 1, h:h + 1], ref[5]) <= 1e-4  # that chain's dh0
