@@ -197,8 +197,8 @@ kda_status kda_decode_preproc(const kda_shape* s, const kda_preproc* pre, const 
  *   dq, dk, dg  device float32 [B,T,H,dk];  dv device float32 [B,T,H,dv];
  *   dbeta    device float32 [B,T,H];  dh0 device float32 [N,H,dk,dv] or NULL
  *   workspace   device, 256-byte aligned, at least kda_bwd_workspace_size(s)
- *               bytes: it holds the state at every 16-token sub-chunk start
- *               (one dk x dv float32 matrix per sub-chunk and head).
+ *               bytes: per 16-token sub-chunk and head it holds the start state
+ *               (dk x dv), X and U (16 x dv) and T and P (16 x 16), float32.
  * Everything is computed in float32 (inputs converted exactly).  The forward
  * is recomputed inside the call, so the o and hT of a previous kda_fwd are not
  * needed.  Gates must be finite.  Device-detected errors (malformed

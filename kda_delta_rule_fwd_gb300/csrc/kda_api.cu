@@ -264,7 +264,8 @@ size_t bwd_ws_bytes(const kda_shape* s) {
   size_t b = kWsHeader;
   if (packed) b += ws_order_bytes(N) + bwd_off_bytes(N);
   b = (b + 255) / 256 * 256;
-  b += kda::bwd_state_rows(packed, N, s->T) * (size_t)s->H * s->dk * s->dv * sizeof(float);
+  b += kda::bwd_state_rows(packed, N, s->T) * (size_t)s->H * kda::bwd_row_floats(s->dk) *
+       sizeof(float);
   return b;
 }
 }  // namespace

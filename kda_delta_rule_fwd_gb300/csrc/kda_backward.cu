@@ -305,7 +305,10 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
   p.seqs.get(n, t0, len);
   const int64_t nsub = (len + kBC - 1) / kBC;
   const int64_t row0 = p.sub_off ? p.sub_off[n] : (int64_t)n * ((p.seqs.T + kBC - 1) / kBC);
-  auto state_row = [&](int64_t s) { return p.states + ((row0 + s) * H + h) * (int64_t)D * D; };
+  // workspace row of sub-chunk s: its start state S [D][D], then X and U [16][D],
+  // T and P [16][16], all written by the forward sweep
+  constexpr int64_t RF = (int64_t)D * D + 2 * kBC * D + 2 * kBC * kBC;
+  auto state_row = [&](int64_t s) { return p.states + ((row0 + s) * H + h) * RF; };
   const int64_t sbase = ((int64_t)n * H + h) * D * D;
 
   // the sub-chunk's inputs, four channels per thread, every load issued before
@@ -320,15 +323,16 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
         const int64_t go = ((t0 + cs + t) * H + h) * D + c;
         fk = ld4f(p.k + go);
         fg = ld4f(p.g + go);
-        fv = ld4f(p.v + go);
         if (bwd) {
           fq = ld4f(p.q + go);
           fo = ld4f(p.dout + go);
+        } else {
+          fv = ld4f(p.v + go);
         }
       }
       st4(K + t * CLD + c, fk);
       st4(G + t * CLD + c, fg);
-      st4(X + t * CLD + c, fv);
+      if (!bwd) st4(X + t * CLD + c, fv);  // the backward sweep reads X itself
       if (bwd) {
         st4(Q + t * CLD + c, fq);
         st4(DO + t * CLD + c, fo);
@@ -352,6 +356,54 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
       *reinterpret_cast<float4*>(dst + (i / D) * SLD + i % D) = r[m];
     }
   };
+  // the forward sweep's X, U, T and P of a sub-chunk, after its state in the row
+  auto row_out = [&](float* row) {
+    float* xr = row + D * D;
+    float* ur = xr + kBC * D;
+    float* tr = ur + kBC * D;
+    float* pr = tr + kBC * kBC;
+    for (int i = 4 * tid; i < kBC * D; i += 4 * kBT) {
+      const int o = (i / D) * CLD + i % D;
+      *reinterpret_cast<float4*>(xr + i) = *reinterpret_cast<const float4*>(X + o);
+      *reinterpret_cast<float4*>(ur + i) = *reinterpret_cast<const float4*>(U + o);
+    }
+    if (tid < kBC * kBC) {
+      tr[tid] = Tm[(tid >> 4) * kSL + (tid & 15)];
+      pr[tid] = Pm[(tid >> 4) * kSL + (tid & 15)];
+    }
+  };
+  // the backward sweep's start: S, X, U, T and P of sub-chunk s, every load issued
+  // before the first store
+  auto row_in = [&](const float* row) {
+    constexpr int NV = D * D / 4 / kBT;
+    constexpr int NX = kBC * D / 4;  // float4 per 16 x D matrix
+    float4 r[NV], rx = make_float4(0.f, 0.f, 0.f, 0.f), ru = rx;
+    float vt = 0.f, vp = 0.f;
+#pragma unroll
+    for (int m = 0; m < NV; ++m) r[m] = ld4f(row + 4 * (tid + m * kBT));
+    if (tid < NX) {
+      rx = ld4f(row + D * D + 4 * tid);
+      ru = ld4f(row + D * D + kBC * D + 4 * tid);
+    }
+    if (tid < kBC * kBC) {
+      vt = row[D * D + 2 * kBC * D + tid];
+      vp = row[D * D + 2 * kBC * D + kBC * kBC + tid];
+    }
+#pragma unroll
+    for (int m = 0; m < NV; ++m) {
+      const int i = 4 * (tid + m * kBT);
+      *reinterpret_cast<float4*>(S + (i / D) * SLD + i % D) = r[m];
+    }
+    if (tid < NX) {
+      const int i = 4 * tid, o = (i / D) * CLD + i % D;
+      *reinterpret_cast<float4*>(X + o) = rx;
+      *reinterpret_cast<float4*>(U + o) = ru;
+    }
+    if (tid < kBC * kBC) {
+      Tm[(tid >> 4) * kSL + (tid & 15)] = vt;
+      Pm[(tid >> 4) * kSL + (tid & 15)] = vp;
+    }
+  };
   auto state_out = [&](float* dst, const float* src) {
 #pragma unroll 4
     for (int m = 0; m < D * D / 4 / kBT; ++m) {
@@ -361,8 +413,9 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
   };
 
   bool split = true;  // the pairwise factors of this sub-chunk are split (see prepare)
-  // Gam (kept as Gam log2 e, so every factor is one ex2), the decayed operands,
-  // P (and M), T, X = V - Kb S and U = T diag(beta) X
+  // Gam (kept as Gam log2 e, so every factor is one ex2) and the decayed operands;
+  // forward sweep: P, T, X = V - Kb S and U = T diag(beta) X; backward sweep: M
+  // (P, T, X and U come back from the forward sweep's workspace row)
   auto prepare = [&](bool bwd) {
     if (tid == 0) *s_wide = 0;
     __syncthreads();
@@ -393,18 +446,21 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
       KH[o] = K[o] * ex2(gl[c] - gm);
     }
     __syncthreads();  // the split products below read Kb, Qb and Kh
+    float* Pt = bwd ? Mm : Pm;  // the pairwise matrix this sweep forms
     if (split) {
-      // P = (K a)(K b)^T (warps 0, 1), M = (Q a)(K b)^T (warps 2, 3), with the factors
-      // a = e^(Gam - h), b = e^(h - Gam) formed directly (not from Kb, which may
-      // have underflowed)
-      // every warp takes one (matrix, 8-column tile) over a slice of the channels;
-      // the partial tiles meet in the U buffer (U is formed further down)
-      {
-        const int nw = bwd ? 4 : 2, parts = (kBT / 32) / nw;
-        const int combo = warp % nw;
-        const bool isM = combo >= 2;
+      // P = (K a)(K b)^T or M = (Q a)(K b)^T, with the factors a = e^(Gam - h),
+      // b = e^(h - Gam) formed directly (not from Kb, which may have underflowed);
+      // each of the first nw * parts warps takes one 8-column tile over a slice of
+      // the channels, and the partial tiles meet in a 16 x D buffer that is free at
+      // this point (parts is bounded by that buffer: 8 at D = 128, 4 at D = 64)
+      constexpr int nw = 2;
+      constexpr int parts = L::CM / (nw * 128) < 8 ? L::CM / (nw * 128) : 8;
+      static_assert(nw * parts * 128 <= L::CM && D % (8 * parts) == 0, "partial tiles");
+      const bool isM = bwd;
+      float* part = bwd ? DU : U;
+      if (warp < nw * parts) {
         const float* A = isM ? Q : K;
-        const int n0 = (combo & 1) * 8, kc = D / parts, kb = (warp / nw) * kc;
+        const int n0 = (warp % nw) * 8, kc = D / parts, kb = (warp / nw) * kc;
         float acc[3][4];
         acc_zero(acc);
 #pragma unroll 2
@@ -424,21 +480,23 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          U[warp * 128 + (g8 + 8 * (e >> 1)) * 8 + 2 * t4 + (e & 1)] = acc_sum(acc, e);
-        __syncthreads();
-        for (int i = tid; i < nw * 128; i += kBT) {
-          const int cb = i >> 7, w = i & 127, r = w >> 3, c = (cb & 1) * 8 + (w & 7);
+          part[warp * 128 + (g8 + 8 * (e >> 1)) * 8 + 2 * t4 + (e & 1)] = acc_sum(acc, e);
+      }
+      __syncthreads();
+      {
+        if (tid < nw * 128) {
+          const int cb = tid >> 7, w = tid & 127, r = w >> 3, c = cb * 8 + (w & 7);
           float v = 0.f;
-          for (int pp = 0; pp < parts; ++pp) v += U[(pp * nw + cb) * 128 + w];
-          const bool m2 = cb >= 2;
-          (m2 ? Mm : Pm)[r * kSL + c] = (m2 ? c <= r : c < r) ? v : 0.f;
+#pragma unroll
+          for (int pp = 0; pp < parts; ++pp) v += part[(pp * nw + cb) * 128 + w];
+          Pt[r * kSL + c] = (isM ? c <= r : c < r) ? v : 0.f;
         }
       }
-    } else {  // explicit differences: threads 0..255 P (j < i), 256..511 M (j <= i)
-      const int pi = (tid & 255) >> 4, pj = tid & 15;
-      const bool isM = tid >= 256;
+    } else if (tid < 256) {  // explicit differences: P (j < i) or M (j <= i)
+      const int pi = tid >> 4, pj = tid & 15;
+      const bool isM = bwd;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      if (isM ? (bwd && pj <= pi) : pj < pi) {
+      if (isM ? pj <= pi : pj < pi) {
         const float* A = isM ? Q : K;
 #pragma unroll 4
         for (int cc = 0; cc < D; ++cc) {
@@ -447,9 +505,10 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
                              ex2(G[pi * CLD + c] - G[pj * CLD + c]), acc[cc & 3]);
         }
       }
-      (isM ? Mm : Pm)[pi * kSL + pj] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+      Pt[pi * kSL + pj] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
     }
     __syncthreads();
+    if (bwd) return;
     if (warp == 0 && lane < kBC) {  // T = (I + diag(beta) P)^-1, column jj per lane
       const int jj = lane;
       float x[kBC];
@@ -497,6 +556,7 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
     load_chunk(cs, nv, false);
     __syncthreads();
     prepare(false);
+    row_out(state_row(s));
     // S <- diag(e^Gl) S + Kh^T U
     dd_update<D, 1>(S, SLD, egl, CLD, KH, 1.f, U, nullptr, 0.f, nullptr, warp, g8, t4);
     __syncthreads();
@@ -507,7 +567,7 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
   for (int64_t s = nsub - 1; s >= 0; --s) {
     const int64_t cs = s * kBC;
     const int nv = (int)(len - cs < kBC ? len - cs : kBC);
-    state_in(S, state_row(s));
+    row_in(state_row(s));
     load_chunk(cs, nv, true);
     __syncthreads();
     prepare(true);

@@ -203,6 +203,8 @@ struct BwdArgs {
 // state rows the backward keeps in the workspace (one per 16-token sub-chunk of
 // every sequence, for each head)
 size_t bwd_state_rows(bool packed, int64_t N, int64_t T);
+// floats per row (state, then X and U [16][d], T and P [16][16] of the sub-chunk)
+inline size_t bwd_row_floats(int d) { return (size_t)d * d + 2 * 16 * d + 2 * 16 * 16; }
 cudaError_t launch_bwd_offsets(const BwdArgs& a, int64_t* off);
 cudaError_t launch_backward(const BwdArgs& a);
 

@@ -232,18 +232,20 @@ def _bwd(L, shape, *, dout=FAKE, dq=FAKE, dbeta=FAKE, dh0=None, ws_bytes=None, c
 
 
 def test_bwd_workspace_and_argument_errors(lib):
-    """The backward keeps one dk x dv float32 state per 16-token sub-chunk and head:
-    the workspace size says so, and a smaller workspace, a missing or misaligned
+    """The backward keeps, per 16-token sub-chunk and head, the float32 start state
+    (dk x dv) with the sub-chunk's X and U (16 x dv) and T and P (16 x 16): the
+    workspace size says so, and a smaller workspace, a missing or misaligned
     gradient buffer or an unsupported head size is refused before any launch."""
     m, L = lib
     shp = _shape(m, B=2, T=100, H=4)
     L.kda_bwd_workspace_size.restype = ctypes.c_size_t
     L.kda_bwd_workspace_size.argtypes = [ctypes.c_void_p]
     need = L.kda_bwd_workspace_size(ctypes.byref(shp))
-    assert need >= 2 * 7 * 4 * 128 * 128 * 4          # ceil(100 / 16) = 7 sub-chunks
-    assert need < 2 * 7 * 4 * 128 * 128 * 4 + 4096
+    row = (128 * 128 + 2 * 16 * 128 + 2 * 16 * 16) * 4
+    assert need >= 2 * 7 * 4 * row                     # ceil(100 / 16) = 7 sub-chunks
+    assert need < 2 * 7 * 4 * row + 4096
     packed = _shape(m, B=1, T=100, H=4, num_seqs=3)
-    assert L.kda_bwd_workspace_size(ctypes.byref(packed)) >= (7 + 3) * 4 * 128 * 128 * 4
+    assert L.kda_bwd_workspace_size(ctypes.byref(packed)) >= (7 + 3) * 4 * row
     assert _bwd(L, shp, ws_bytes=need - 1) == m.KDA_ERR_WORKSPACE
     assert _bwd(L, shp, dout=0) == m.KDA_ERR_INVALID_ARG
     assert _bwd(L, shp, dq=0) == m.KDA_ERR_INVALID_ARG
