@@ -254,6 +254,18 @@ __device__ __forceinline__ void st4(float* p, const float4& v) {
   p[0] = v.x; p[1] = v.y; p[2] = v.z; p[3] = v.w;
 }
 
+// 16-byte asynchronous global -> shared copies (completion waited with cp_async_wait)
+__device__ __forceinline__ void cp_async16(float* dst, const float* src) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
 // element e of the C fragment: row g + 8 (e >> 1), column 2 t4 + (e & 1)
 __device__ __forceinline__ float acc_sum(const float (&acc)[3][4], int e) {
   return acc[0][e] + acc[1][e] + acc[2][e];
@@ -372,15 +384,16 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
       pr[tid] = Pm[(tid >> 4) * kSL + (tid & 15)];
     }
   };
-  // the backward sweep's start: S, X, U, T and P of sub-chunk s, every load issued
-  // before the first store
-  auto row_in = [&](const float* row) {
+  // the backward sweep's start: S (unless it is already on its way, see below), X,
+  // U, T and P of sub-chunk s, every load issued before the first store
+  auto row_in = [&](const float* row, bool with_s) {
     constexpr int NV = D * D / 4 / kBT;
     constexpr int NX = kBC * D / 4;  // float4 per 16 x D matrix
     float4 r[NV], rx = make_float4(0.f, 0.f, 0.f, 0.f), ru = rx;
     float vt = 0.f, vp = 0.f;
 #pragma unroll
-    for (int m = 0; m < NV; ++m) r[m] = ld4f(row + 4 * (tid + m * kBT));
+    for (int m = 0; m < NV; ++m)
+      r[m] = with_s ? ld4f(row + 4 * (tid + m * kBT)) : make_float4(0.f, 0.f, 0.f, 0.f);
     if (tid < NX) {
       rx = ld4f(row + D * D + 4 * tid);
       ru = ld4f(row + D * D + kBC * D + 4 * tid);
@@ -389,10 +402,14 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
       vt = row[D * D + 2 * kBC * D + tid];
       vp = row[D * D + 2 * kBC * D + kBC * kBC + tid];
     }
+    if (with_s) {
 #pragma unroll
-    for (int m = 0; m < NV; ++m) {
-      const int i = 4 * (tid + m * kBT);
-      *reinterpret_cast<float4*>(S + (i / D) * SLD + i % D) = r[m];
+      for (int m = 0; m < NV; ++m) {
+        const int i = 4 * (tid + m * kBT);
+        *reinterpret_cast<float4*>(S + (i / D) * SLD + i % D) = r[m];
+      }
+    } else {
+      cp_async_wait();  // this thread's part of S, requested during the previous step
     }
     if (tid < NX) {
       const int i = 4 * tid, o = (i / D) * CLD + i % D;
@@ -403,6 +420,15 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
       Tm[(tid >> 4) * kSL + (tid & 15)] = vt;
       Pm[(tid >> 4) * kSL + (tid & 15)] = vp;
     }
+  };
+  // the next (earlier) sub-chunk's state into S once this step is done with it
+  auto s_prefetch = [&](const float* row) {
+#pragma unroll
+    for (int m = 0; m < D * D / 4 / kBT; ++m) {
+      const int i = 4 * (tid + m * kBT);
+      cp_async16(S + (i / D) * SLD + i % D, row + i);
+    }
+    cp_async_commit();
   };
   auto state_out = [&](float* dst, const float* src) {
 #pragma unroll 4
@@ -567,7 +593,7 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
   for (int64_t s = nsub - 1; s >= 0; --s) {
     const int64_t cs = s * kBC;
     const int nv = (int)(len - cs < kBC ? len - cs : kBC);
-    row_in(state_row(s));
+    row_in(state_row(s), s == nsub - 1);
     load_chunk(cs, nv, true);
     __syncthreads();
     prepare(true);
@@ -702,6 +728,7 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
       }
     }
     __syncthreads();
+    if (s > 0) s_prefetch(state_row(s - 1));  // S is not read again in this step
     // pairwise factors, per (token t, channel c):
     //   RK = sum_{j<t} dP_tj K_jc E_tj, RQ = sum_{j<=t} dM_tj K_jc E_tj,
     //   CK = sum_{i>t} dP_it K_ic E_it, CQ = sum_{i>=t} dM_it Q_ic E_it,
