@@ -205,6 +205,28 @@ def test_decode(kda, oracle_mod, dtype, d, T_step):
     assert rel_err(state, h_ref) <= tol
 
 
+@pytest.mark.parametrize("T_step", [2, 4, 5, 6, 7])
+def test_decode_every_step_count(kda, oracle_mod, T_step):
+    """d=128 steps of every other token count (the staging of a step's inputs
+    covers 1 to 4 rounds of the block): each matches the oracle at the float32
+    bound, and the same step taken one token at a time agrees to 1e-5."""
+    x = kda_inputs.decode_pool(num_seqs=6, H=4, d=128, T_step=T_step, dtype=torch.float32,
+                               device=DEV, seed=400 + T_step)
+    state = x.h0.clone()
+    o = kda.decode(x.q, x.k, x.v, x.g, x.beta, state)
+    s1 = x.h0.clone()
+    o1 = torch.cat([kda.decode(x.q[:, t:t + 1].contiguous(), x.k[:, t:t + 1].contiguous(),
+                               x.v[:, t:t + 1].contiguous(), x.g[:, t:t + 1].contiguous(),
+                               x.beta[:, t:t + 1].contiguous(), s1) for t in range(T_step)],
+                   dim=1)
+    torch.cuda.synchronize()
+    o_ref, h_ref = oracle_mod.recurrent(x.q, x.k, x.v, x.g, x.beta, h0=x.h0)
+    assert rel_err(o, o_ref) <= TOL_F32
+    assert rel_err(state, h_ref) <= TOL_F32
+    assert rel_err(o, o1.double().cpu().numpy()) <= 1e-5
+    assert rel_err(state, s1.double().cpu().numpy()) <= 1e-5
+
+
 @pytest.mark.parametrize("d", [64, 128])
 def test_decode_extreme_gates(kda, oracle_mod, d):
     """Gates strong enough that the product of alpha over the step underflows
@@ -259,6 +281,26 @@ def test_decode_commit_counts(kda, oracle_mod, dtype, d):
             assert torch.equal(state[n], x.h0[n])  # untouched
         else:
             assert rel_err(state[n], ref) <= tol
+
+
+@pytest.mark.parametrize("T_step", [2, 5, 8])
+def test_decode_commit_every_count(kda, oracle_mod, T_step):
+    """Commit counts 0..T_step on one batch (bf16 inputs, bf16 outputs): outputs of
+    all tokens, and each sequence's kept state after its accepted prefix."""
+    counts = list(range(T_step + 1))
+    x = kda_inputs.decode_pool(num_seqs=len(counts), H=2, d=128, T_step=T_step,
+                               dtype=torch.bfloat16, device=DEV, seed=500 + T_step)
+    state = x.h0.clone()
+    o = kda.decode_commit(x.q, x.k, x.v, x.g, x.beta, state,
+                          torch.tensor(counts, dtype=torch.int32, device=DEV))
+    torch.cuda.synchronize()
+    o_ref, _ = oracle_mod.recurrent(x.q, x.k, x.v, x.g, x.beta, h0=x.h0)
+    assert rel_err(o, o_ref) <= TOL_BF16
+    for n, ref in enumerate(_commit_refs(oracle_mod, x, counts)):
+        if counts[n] == 0:
+            assert torch.equal(state[n], x.h0[n])
+        else:
+            assert rel_err(state[n], ref) <= TOL_BF16
 
 
 def test_decode_commit_verify_then_replay(kda):
