@@ -26,6 +26,23 @@ template <int N> struct VecF;
 template <> struct VecF<2> { using T = float2; };
 template <> struct VecF<4> { using T = float4; };
 
+// Two float32 lanes per instruction (packed f32x2, IEEE round-to-nearest in each
+// lane: the same results as two scalar operations, in half the issue slots).
+union F2 {
+  float2 f;
+  unsigned long long u;
+};
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  F2 x{a}, y{b}, d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d.u) : "l"(x.u), "l"(y.u));
+  return d.f;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {  // a * b + c
+  F2 x{a}, y{b}, z{c}, d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d.u) : "l"(x.u), "l"(y.u), "l"(z.u));
+  return d.f;
+}
+
 // kCommit: per-sequence commit counts (num_commit) decide which state is written
 // back; otherwise the state after all Tstep tokens is.
 // kPre: the fused input preprocessing `pre` is applied while the inputs are staged.
@@ -39,6 +56,7 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                   Preproc pre) {
   constexpr int R = D / 8;     // state rows per warp
   constexpr int CPL = D / 32;  // state columns per lane
+  constexpr int P = CPL / 2;   // column pairs per lane (packed arithmetic)
   using Vec = typename VecF<CPL>::T;
 
   __shared__ __align__(16) float s_k[kMaxTstep][D];
@@ -56,13 +74,13 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
 
   // Issue the state loads first: they are the HBM traffic that matters.
   float* Sg = state + nh * (int64_t)D * D;
-  float S[R][CPL];
+  float2 S[R][P];
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     const Vec x = *reinterpret_cast<const Vec*>(Sg + (int64_t)(warp * R + r) * D + lane * CPL);
-    const float* xf = reinterpret_cast<const float*>(&x);
+    const float2* xf = reinterpret_cast<const float2*>(&x);
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) S[r][c] = xf[c];
+    for (int c = 0; c < P; ++c) S[r][c] = xf[c];
   }
 
   // Stage the step's inputs (Tstep tokens) in shared memory as float32 (with the
@@ -127,9 +145,9 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       Vec x;
-      float* xf = reinterpret_cast<float*>(&x);
+      float2* xf = reinterpret_cast<float2*>(&x);
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) xf[c] = S[r][c];
+      for (int c = 0; c < P; ++c) xf[c] = S[r][c];
       *reinterpret_cast<Vec*>(Sg + (int64_t)(warp * R + r) * D + lane * CPL) = x;
     }
   };
@@ -146,25 +164,27 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
       kr[4 * r4] = kv.x; kr[4 * r4 + 1] = kv.y; kr[4 * r4 + 2] = kv.z; kr[4 * r4 + 3] = kv.w;
       qr[4 * r4] = qv.x; qr[4 * r4 + 1] = qv.y; qr[4 * r4 + 2] = qv.z; qr[4 * r4 + 3] = qv.w;
     }
-    // decay and partial reductions over this warp's rows
-    float pk[CPL], pq[CPL];
+    // decay and partial reductions over this warp's rows, two columns at a time
+    float2 pk[P], pq[P];
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) pk[c] = pq[c] = 0.f;
+    for (int c = 0; c < P; ++c) pk[c] = pq[c] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int r = 0; r < R; ++r) {
+      const float2 a2 = make_float2(a[r], a[r]), k2 = make_float2(kr[r], kr[r]);
+      const float2 q2 = make_float2(qr[r], qr[r]);
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) {
-        S[r][c] *= a[r];
-        pk[c] = fmaf(S[r][c], kr[r], pk[c]);
-        pq[c] = fmaf(S[r][c], qr[r], pq[c]);
+      for (int c = 0; c < P; ++c) {
+        S[r][c] = mul2(S[r][c], a2);
+        pk[c] = fma2(S[r][c], k2, pk[c]);
+        pq[c] = fma2(S[r][c], q2, pq[c]);
       }
     }
     {
       Vec vk, vq;
-      float* fk = reinterpret_cast<float*>(&vk);
-      float* fq = reinterpret_cast<float*>(&vq);
+      float2* fk = reinterpret_cast<float2*>(&vk);
+      float2* fq = reinterpret_cast<float2*>(&vq);
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) { fk[c] = pk[c]; fq[c] = pq[c]; }
+      for (int c = 0; c < P; ++c) { fk[c] = pk[c]; fq[c] = pq[c]; }
       *reinterpret_cast<Vec*>(&s_red[warp][0][lane * CPL]) = vk;
       *reinterpret_cast<Vec*>(&s_red[warp][1][lane * CPL]) = vq;
     }
@@ -183,17 +203,18 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
     }
     __syncthreads();
     // rank-1 write S <- S + k u^T
-    float u[CPL];
+    float2 u[P];
     {
       const Vec uv = *reinterpret_cast<const Vec*>(&s_u[lane * CPL]);
-      const float* uf = reinterpret_cast<const float*>(&uv);
+      const float2* uf = reinterpret_cast<const float2*>(&uv);
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) u[c] = uf[c];
+      for (int c = 0; c < P; ++c) u[c] = uf[c];
     }
 #pragma unroll
     for (int r = 0; r < R; ++r) {
+      const float2 k2 = make_float2(kr[r], kr[r]);
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) S[r][c] = fmaf(kr[r], u[c], S[r][c]);
+      for (int c = 0; c < P; ++c) S[r][c] = fma2(k2, u[c], S[r][c]);
     }
     if (kCommit && t + 1 == commit) store_state();
   }
