@@ -3,7 +3,8 @@
 ``python -m kda_delta_rule_fwd_gb300.cases bwd`` runs the backward twice (a
 warm-up launch, then the one to capture) on B=1, T=512, H=4, d=128, bf16
 inputs with a start state; ``prefill`` does the same for the forward on
-B=1, T=4096, H=8; ``decode8`` the 8-token decode on 256 sequences x 32 heads.
+B=1, T=4096, H=8; ``decode1`` and ``decode8`` the 1- and 8-token decode on 256
+sequences x 32 heads.
 Inputs are seeded and synthetic.
 """
 from __future__ import annotations
@@ -37,9 +38,10 @@ def prefill_case(device="cuda:0"):
     return o, hT
 
 
-def decode8_case(device="cuda:0"):
-    """8-token decode on a pool of 256 sequences x 32 heads (512 MB of state)."""
-    x = kda_inputs.decode_pool(num_seqs=256, H=32, d=128, T_step=8, device=device, seed=15)
+def decode_case(T_step, device="cuda:0"):
+    """T_step-token decode on a pool of 256 sequences x 32 heads (512 MB of state)."""
+    x = kda_inputs.decode_pool(num_seqs=256, H=32, d=128, T_step=T_step, device=device,
+                               seed=15)
     state = x.h0.clone()
     for _ in range(2):
         o = kda.decode(x.q, x.k, x.v, x.g, x.beta, state)
@@ -49,5 +51,6 @@ def decode8_case(device="cuda:0"):
 
 if __name__ == "__main__":
     which = sys.argv[1] if len(sys.argv) > 1 else "bwd"
-    out = {"bwd": bwd_case, "prefill": prefill_case, "decode8": decode8_case}[which]()
+    out = {"bwd": bwd_case, "prefill": prefill_case, "decode1": lambda: decode_case(1),
+           "decode8": lambda: decode_case(8)}[which]()
     print(which, "ok", float(out[0].abs().sum()))
