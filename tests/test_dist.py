@@ -4,7 +4,6 @@ ranks; nothing else crosses ranks."""
 import os
 import socket
 
-import pytest
 import torch
 import torch.distributed as td
 import torch.multiprocessing as mp
