@@ -72,9 +72,11 @@ typedef struct {
 
 /* Bytes of workspace that let kda_fwd / kda_decode use every path for `s`
  * (always >= 256: the first 256 bytes hold the device status word).  For a
- * fixed-length bf16 batch of a few very long sequences this includes the
- * segment states of the long-chain split (chains of (sequence, head) cut into
- * up to 16 segments joined through their affine state maps).  The minimum a
+ * fixed-length bf16 batch with fewer (sequence, head) chains than SMs and long
+ * sequences this includes the segment states of the long-chain split: each chain
+ * is cut into up to 64 segments joined through their affine state maps, as many
+ * as a model of the waves of CTAs on a GB300's 152 SMs favours, and 3 * nseg - 2
+ * float32 dk x dv states per chain are reserved.  The minimum a
  * call accepts is 256 bytes plus, for packed batches, 4 bytes per sequence
  * rounded up to 64 sequences; with less than kda_workspace_size the split is
  * skipped.  Returns 0 if `s` is NULL. */

@@ -59,27 +59,45 @@ inline size_t ws_order_bytes(int64_t n) { return (size_t)((n + 63) / 64) * 64 * 
 // device has enough independent work (the segments are joined exactly through
 // their affine state transitions).  A pure function of the shape, so that the
 // workspace size can be computed without a device.
+//
+// The plan minimises a model of the critical path in chunk-steps (one 64-token
+// chunk of one chain on one SM), counting waves of one CTA per SM on the 152
+// SMs of a GB300: a split runs 2 (nseg - 1) transition CTAs per chain, then
+// nseg output CTAs per chain, each over seg_len / 64 chunks, plus the scan
+// (about half a chunk-step per segment); no split runs every chain whole.  A
+// split is taken only when the model saves at least 10%.  On a device with
+// fewer SMs the plan is still exact, only its choice may be less good.
 struct SegPlan {
   int nseg = 1;
   int64_t seg_len = 0;
 };
-constexpr int kSegMaxChains = 64;       // split only when chains leave most SMs idle
-constexpr int64_t kSegMinChunks = 64;   // at least this many 64-token chunks per segment
-constexpr int kSegMaxSegs = 16;
-constexpr int kSegTargetChains = 512;
+constexpr int64_t kPlanSms = 152;      // SMs the plan counts waves on
+constexpr int64_t kSegMinChunks = 64;  // at least this many 64-token chunks per segment
+constexpr int64_t kSegMaxSegs = 64;
+inline int64_t plan_waves(int64_t ctas) { return (ctas + kPlanSms - 1) / kPlanSms; }
+inline double plan_cost(int64_t chains, int64_t chunks, int64_t seg_chunks, int64_t nseg) {
+  if (nseg < 2) return (double)plan_waves(chains) * (double)chunks;
+  return (double)seg_chunks *
+             (double)(plan_waves(2 * chains * (nseg - 1)) + plan_waves(chains * nseg)) +
+         0.5 * (double)nseg;
+}
 inline SegPlan seg_plan(bool packed, bool bf16_d128, int64_t chains, int64_t T) {
   SegPlan pl;
   const int64_t chunks = (T + 63) / 64;
-  if (packed || !bf16_d128 || chains <= 0 || chains > kSegMaxChains ||
-      chunks < 4 * kSegMinChunks)
+  if (packed || !bf16_d128 || chains <= 0 || chains >= kPlanSms || chunks < 2 * kSegMinChunks)
     return pl;
-  int64_t ns = kSegTargetChains / chains;
-  if (ns > kSegMaxSegs) ns = kSegMaxSegs;
-  if (ns > chunks / kSegMinChunks) ns = chunks / kSegMinChunks;
-  if (ns < 2) return pl;
-  pl.seg_len = ((chunks + ns - 1) / ns) * 64;
-  pl.nseg = (int)((T + pl.seg_len - 1) / pl.seg_len);
-  if (pl.nseg < 2) pl = SegPlan{};
+  double best = 0.9 * plan_cost(chains, chunks, chunks, 1);
+  const int64_t max_ns = chunks / kSegMinChunks < kSegMaxSegs ? chunks / kSegMinChunks
+                                                              : kSegMaxSegs;
+  for (int64_t ns = 2; ns <= max_ns; ++ns) {
+    const int64_t seg = (chunks + ns - 1) / ns, nseg = (chunks + seg - 1) / seg;
+    const double c = plan_cost(chains, chunks, seg, nseg);
+    if (c < best) {
+      best = c;
+      pl.nseg = (int)nseg;
+      pl.seg_len = seg * 64;
+    }
+  }
   return pl;
 }
 // bytes of segment states: b and M for segments 0..nseg-2, start states for 0..nseg-1

@@ -174,14 +174,20 @@ def test_binding_refuses_to_run_without_library(tmp_path):
 
 
 def test_workspace_size_long_chain_split(lib):
-    """A fixed-length bf16 batch of few, very long chains reserves segment states:
-    B=1, T=2^20, H=32 -> 16 segments per chain, (3*16 - 2) states of 128x128 fp32."""
+    """A fixed-length bf16 batch of few, very long chains reserves (3 nseg - 2)
+    segment states of 128x128 fp32 per chain.  The segment count minimises the
+    waves of CTAs on 152 SMs: B=1, T=2^20, H=32 (16384 chunks) -> 8 segments
+    (448 transition CTAs in 3 waves, 256 output CTAs in 2, of 2048 chunks each,
+    against 11 waves of 1024 chunks for 16 segments); B=1, T=64*255, H=2 -> 3."""
     m, L = lib
-    assert m.workspace_size(_shape(m, B=1, T=1 << 20, H=32)) == 256 + 32 * 46 * 128 * 128 * 4
-    # float32 inputs, many chains or short chains never split
+    assert m.workspace_size(_shape(m, B=1, T=1 << 20, H=32)) == 256 + 32 * 22 * 128 * 128 * 4
+    assert m.workspace_size(_shape(m, B=1, T=64 * 255, H=2)) == 256 + 2 * 7 * 128 * 128 * 4
+    # float32 inputs, many chains or short chains never split; at 64 chains no split
+    # saves 10% (two waves of half-length segments cost what one unsplit wave does)
     assert m.workspace_size(_shape(m, B=1, T=1 << 20, H=32, in_dtype=m.KDA_F32)) == 256
+    assert m.workspace_size(_shape(m, B=2, T=1 << 20, H=32)) == 256
     assert m.workspace_size(_shape(m, B=4, T=4096, H=32)) == 256
-    assert m.workspace_size(_shape(m, B=1, T=64 * 255, H=2)) == 256
+    assert m.workspace_size(_shape(m, B=1, T=64 * 127, H=2)) == 256
     # the split is optional: the minimum workspace is still accepted
     if not torch.cuda.is_available():  # would launch on fake pointers otherwise
         assert _fwd(L, _shape(m, B=1, T=1 << 20, H=32), ws_bytes=256) == m.KDA_ERR_CUDA
