@@ -182,6 +182,13 @@ def test_workspace_size_long_chain_split(lib):
     m, L = lib
     assert m.workspace_size(_shape(m, B=1, T=1 << 20, H=32)) == 256 + 32 * 22 * 128 * 128 * 4
     assert m.workspace_size(_shape(m, B=1, T=64 * 255, H=2)) == 256 + 2 * 7 * 128 * 128 * 4
+    # one chain: every split is two single waves, so more segments always model
+    # faster and the cap of 64 applies (190 states)
+    assert m.workspace_size(_shape(m, B=1, T=1 << 20, H=1)) == 256 + 190 * 128 * 128 * 4
+    # 8 chains of 1024 chunks: at most 16 segments of >= 64 chunks, which take 2 + 1
+    # waves of 64 chunks (192 chunk-steps + 8 of scan); every smaller count models
+    # more (the closest, 10 segments: 1 + 1 waves of 103 chunks + 5 = 211)
+    assert m.workspace_size(_shape(m, B=8, T=1 << 16, H=1)) == 256 + 8 * 46 * 128 * 128 * 4
     # float32 inputs, many chains or short chains never split; at 64 chains no split
     # saves 10% (two waves of half-length segments cost what one unsplit wave does)
     assert m.workspace_size(_shape(m, B=1, T=1 << 20, H=32, in_dtype=m.KDA_F32)) == 256
