@@ -381,6 +381,24 @@ def test_long_chain_split_matches_oracle_and_unsplit_run(kda, oracle_mod):
         assert rel_err(h, h_ref) <= TOL_BF16
 
 
+def test_long_chain_split_many_segments(kda, oracle_mod):
+    """One chain of 2561 chunks (ragged last chunk): the plan cuts it into 40
+    segments of 65 chunks, composed by 39 steps of the segment scan; split and
+    unsplit runs both match the oracle."""
+    x = kda_inputs.fixed(1, 64 * 64 * 40 + 17, 1, 128, dtype=torch.bfloat16, device=DEV,
+                         seed=78, h0_std=0.1)
+    shape = kda.make_shape(x.q, x.v)
+    assert kda.workspace_size(shape) == 256 + (3 * 40 - 2) * 128 * 128 * 4
+    o_s, h_s = kda.fwd(x.q, x.k, x.v, x.g, x.beta, h0=x.h0)
+    small = torch.empty(256, dtype=torch.uint8, device=DEV)
+    o_u, h_u = kda.fwd(x.q, x.k, x.v, x.g, x.beta, h0=x.h0, workspace=small)
+    torch.cuda.synchronize()
+    o_ref, h_ref = oracle_mod.recurrent(x.q, x.k, x.v, x.g, x.beta, h0=x.h0)
+    for o, h in ((o_s, h_s), (o_u, h_u)):
+        assert rel_err(o, o_ref) <= TOL_BF16
+        assert rel_err(h, h_ref) <= TOL_BF16
+
+
 def test_bounded_wait_runs_out_and_is_reported(kda, oracle_mod):
     """A device wait that can never complete gives up after its budget, latches
     KDA_ERR_DEVICE_TIMEOUT, and leaves the context usable for the next call."""
