@@ -13,7 +13,9 @@
 // state S [D x D] (row = key channel, dv contiguous) lives in registers: warp w
 // owns rows [w*D/8, (w+1)*D/8) and lane l owns columns [l*D/32, (l+1)*D/32), so
 // every warp load/store of a state row is one contiguous, vectorised access.
-// The kernel is HBM-bound: each head reads and writes 4*D*D bytes of state.
+// The token loop works on pairs of a lane's columns with packed f32x2 arithmetic.
+// One head-step reads and writes 4*D*D bytes of state: HBM-bound at T_step = 1,
+// and bound by the per-token arithmetic and barriers as T_step grows.
 #include "kda_internal.cuh"
 
 namespace kda {
