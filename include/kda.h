@@ -19,8 +19,10 @@
  * sequence boundary; cu_seqlens).  g carries log(alpha) in natural-log units.
  *
  * Conventions shared by every entry point:
- *   - The caller owns every buffer.  The library allocates no memory and
- *     keeps no global state; calls are reentrant.
+ *   - The caller owns every buffer.  The library allocates no memory.  Every
+ *     entry point except kda_fwd_noalloc keeps no global state and is
+ *     reentrant; kda_fwd_noalloc keeps its scratch in one fixed array per
+ *     device (see there).
  *   - Tensor pointers are DEVICE pointers, 16-byte aligned, dense and
  *     row-major with the innermost dimension contiguous.  Activations are
  *     token-major [B, T, H, d]; a packed batch is [1, T_total, H, d] with
@@ -30,9 +32,8 @@
  *     kda_read_device_status().
  *   - Host-checkable argument errors return before anything is launched.
  *     Launch failures return KDA_ERR_CUDA.  Errors found on the device
- *     (malformed cu_seqlens, a bounded wait that ran out, a decay outside
- *     the supported range) are latched in the workspace status word; read
- *     them with kda_read_device_status().
+ *     (malformed cu_seqlens, a bounded wait that ran out) are latched in the
+ *     workspace status word; read them with kda_read_device_status().
  *   - `out` must not alias any input.  `hT` may alias `h0`.
  */
 #ifndef KDA_H_
@@ -53,7 +54,8 @@ typedef enum {
   KDA_ERR_CUDA = 4,           /* a CUDA call or kernel launch failed */
   KDA_ERR_BAD_SEQLENS = 5,    /* device: cu_seqlens not non-decreasing from 0 to T */
   KDA_ERR_DEVICE_TIMEOUT = 6, /* device: a bounded wait inside a kernel ran out */
-  KDA_ERR_DECAY_RANGE = 7     /* device: a decay factor left the range the bf16 path supports */
+  KDA_ERR_DECAY_RANGE = 7     /* not raised: kept for compatibility (every gate in [-inf, 0]
+                                 is supported; see kda_fwd) */
 } kda_status;
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
@@ -71,22 +73,24 @@ typedef struct {
 } kda_shape;
 
 /* Bytes of workspace that let kda_fwd / kda_decode use every path for `s`
- * (always >= 256: the first 256 bytes hold the device status word).  For a
- * fixed-length bf16 batch with fewer (sequence, head) chains than SMs and long
- * sequences this includes the segment states of the long-chain split: each chain
- * is cut into up to 64 segments joined through their affine state maps, as many
- * as a model of the waves of CTAs on a GB300's 152 SMs favours, and 3 * nseg - 2
- * float32 dk x dv states per chain are reserved.  The minimum a
- * call accepts is 256 bytes plus, for packed batches, 4 bytes per sequence
- * rounded up to 64 sequences; with less than kda_workspace_size the split is
- * skipped.  Returns 0 if `s` is NULL. */
+ * (always >= 256: the first 256 bytes hold the device status word; num_seqs > 0
+ * counts as a packed call, which for a fixed-length call only over-estimates).
+ * For a fixed-length bf16 batch with fewer (sequence, head) chains than SMs and
+ * long sequences this includes the segment states of the long-chain split: each
+ * chain is cut into up to 64 segments joined through their affine state maps, as
+ * many as a model of the waves of CTAs on the current device's SMs favours (152,
+ * a GB300's count, when no device can be queried), and 3 * nseg - 2 float32
+ * dk x dv states per chain are reserved.  The minimum a call accepts is 256
+ * bytes plus, for packed batches, 4 bytes per sequence rounded up to 64
+ * sequences; with less than kda_workspace_size the split is skipped.  Returns 0
+ * if `s` is NULL. */
 size_t kda_workspace_size(const kda_shape* s);
 
 /*
  * Chunkwise prefill over fixed-length or packed variable-length sequences.
  *
  *   q, k, g  [B,T,H,dk]   in_dtype.  q and k L2-normalised per (token, head);
- *                         g = log(alpha) <= 0.
+ *                         g = log(alpha) <= 0; -inf (alpha = 0) is allowed.
  *   v        [B,T,H,dv]   in_dtype.
  *   beta     [B,T,H]      in_dtype, in [0, 1].
  *   cu_seqlens  device int32 [num_seqs+1] or NULL (fixed length, N = B).
@@ -101,7 +105,10 @@ size_t kda_workspace_size(const kda_shape* s);
  * sequence may be partial.  A zero-length sequence writes hT = h0 (or 0).
  * The float32 path (in_dtype KDA_F32) evaluates every product in float32;
  * the bf16 path uses tensor cores with split bf16 operands and float32
- * accumulation.
+ * accumulation.  A 64-token chunk in which some key channel decays by more
+ * than about 160 nats (alpha near 0) cannot be factorised within float32's
+ * exponent range; the bf16 path runs such a chunk token by token on the CUDA
+ * cores (same results, about four times the time of a tensor-core chunk).
  */
 kda_status kda_fwd(const kda_shape* s, const void* q, const void* k, const void* v,
                    const void* g, const void* beta, const int32_t* cu_seqlens,
@@ -275,6 +282,13 @@ kda_status kda_decode_commit(const kda_shape* s, const void* q, const void* k, c
  *     status word it needs when it starts; calls whose work overlaps on the GPU
  *     (other streams, or other host threads) race on the array, so serialise
  *     them;
+ *   - the array's address is looked up once per device and kept for the life
+ *     of the process; do not use this entry point on a device after
+ *     cudaDeviceReset (or any other teardown of its primary context);
+ *   - a fixed-length batch whose few long chains kda_fwd would cut into
+ *     segments (the segment states need a workspace of kda_workspace_size)
+ *     runs every chain whole here: same results, but a batch like B=1,
+ *     T=2^20, H=32 takes several times longer than through kda_fwd;
  *   - status_out: optional DEVICE pointer to one unsigned int; when non-NULL,
  *     the call's device status (KDA_OK or a device error code) is copied there
  *     in stream order after the kernels.

@@ -29,14 +29,35 @@ kda_status check_shape(const kda_shape* s, bool packed) {
   return KDA_OK;
 }
 
-// The minimum workspace: status header plus the packed-batch order list.  The
-// long-chain segment states are optional (the split is skipped without them).
-kda_status check_ws(const kda_shape* s, void* ws, size_t bytes) {
+// The minimum workspace: status header plus, for a packed call, the order list
+// (num_seqs is ignored otherwise).  The long-chain segment states are optional
+// (the split is skipped without them).
+kda_status check_ws(const kda_shape* s, void* ws, size_t bytes, bool packed) {
   if (!ws || !aligned(ws, 256)) return KDA_ERR_WORKSPACE;
   size_t need = kWsHeader;
-  if (s->num_seqs > 0) need += ws_order_bytes(s->num_seqs);
+  if (packed && s->num_seqs > 0) need += ws_order_bytes(s->num_seqs);
   if (bytes < need) return KDA_ERR_WORKSPACE;
   return KDA_OK;
+}
+
+// SMs of the current device for the segment plan, looked up once per device;
+// 152 (a GB300) when there is no device to ask, so sizes computed without a
+// GPU match a GB300's.
+int64_t device_sms() {
+  constexpr int kMaxDev = 64;
+  static int64_t cache[kMaxDev] = {};
+  int dev = -1, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+    cudaGetLastError();  // clear the error a device-less host leaves behind
+    return kGb300Sms;
+  }
+  if (dev < kMaxDev && cache[dev] > 0) return cache[dev];
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return kGb300Sms;
+  }
+  if (dev < kMaxDev) cache[dev] = n;
+  return n;
 }
 
 }  // namespace
@@ -50,7 +71,7 @@ size_t kda_workspace_size(const kda_shape* s) {
   // fixed-length batches of a few very long chains also keep segment states
   const bool bf16_d128 = s->in_dtype == KDA_BF16 && s->dk == 128 && s->dv == 128;
   const int64_t chains = (int64_t)(s->B > 0 ? s->B : 0) * (s->H > 0 ? s->H : 0);
-  b += seg_bytes(seg_plan(false, bf16_d128, chains, s->T), chains, s->dk);
+  b += seg_bytes(seg_plan(false, bf16_d128, chains, s->T, device_sms()), chains, s->dk);
   return b;
 }
 
@@ -93,7 +114,7 @@ kda_status fwd_common(const kda_shape* s, const void* q, const void* k, const vo
   if (!aligned(beta, dsize(s->in_dtype)) || (packed && !aligned(cu_seqlens, 4)) ||
       !preproc_ok(pre, g, s->in_dtype))
     return KDA_ERR_INVALID_ARG;
-  st = check_ws(s, workspace, workspace_bytes);
+  st = check_ws(s, workspace, workspace_bytes, packed);
   if (st != KDA_OK) return st;
 
   FwdArgs a{};
@@ -122,10 +143,12 @@ kda_status fwd_common(const kda_shape* s, const void* q, const void* k, const vo
   } else {
     // long-chain split: segment states follow the header when the plan asks for them
     const bool bf16_d128 = s->in_dtype == KDA_BF16 && s->dk == 128;
-    const SegPlan pl = seg_plan(false, bf16_d128, (int64_t)s->B * s->H, s->T);
+    const SegPlan pl = seg_plan(false, bf16_d128, (int64_t)s->B * s->H, s->T, device_sms());
     const size_t need = kWsHeader + seg_bytes(pl, (int64_t)s->B * s->H, s->dk);
-    if (pl.nseg > 1 && workspace_bytes >= need)
+    if (pl.nseg > 1 && workspace_bytes >= need) {
       a.seg_ws = reinterpret_cast<float*>(static_cast<char*>(workspace) + kWsHeader);
+      a.plan = pl;
+    }
   }
   cudaError_t e;
   if (s->in_dtype == KDA_BF16 && s->dk == 128)
@@ -181,7 +204,7 @@ kda_status decode_common(const kda_shape* s, const void* q, const void* k, const
   if (!aligned(beta, dsize(s->in_dtype)) || !preproc_ok(pre, g, s->in_dtype))
     return KDA_ERR_INVALID_ARG;
   if (num_commit && !aligned(num_commit, 4)) return KDA_ERR_INVALID_ARG;
-  st = check_ws(s, workspace, workspace_bytes);
+  st = check_ws(s, workspace, workspace_bytes, false);
   if (st != KDA_OK) return st;
 
   DecodeArgs a{};
@@ -249,7 +272,7 @@ const char* kda_status_string(kda_status st) {
     case KDA_ERR_CUDA: return "CUDA call or kernel launch failed";
     case KDA_ERR_BAD_SEQLENS: return "cu_seqlens is not non-decreasing from 0 to T";
     case KDA_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel ran out";
-    case KDA_ERR_DECAY_RANGE: return "a decay factor left the range the bf16 path supports";
+    case KDA_ERR_DECAY_RANGE: return "decay range (not raised by this version)";
   }
   return "unknown status";
 }

@@ -28,22 +28,6 @@ template <int N> struct VecF;
 template <> struct VecF<2> { using T = float2; };
 template <> struct VecF<4> { using T = float4; };
 
-// Two float32 lanes per instruction (packed f32x2, IEEE round-to-nearest in each
-// lane: the same results as two scalar operations, in half the issue slots).
-union F2 {
-  float2 f;
-  unsigned long long u;
-};
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-  F2 x{a}, y{b}, d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d.u) : "l"(x.u), "l"(y.u));
-  return d.f;
-}
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {  // a * b + c
-  F2 x{a}, y{b}, z{c}, d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d.u) : "l"(x.u), "l"(y.u), "l"(z.u));
-  return d.f;
-}
 
 // kCommit: per-sequence commit counts (num_commit) decide which state is written
 // back; otherwise the state after all Tstep tokens is.

@@ -22,6 +22,23 @@ __device__ __forceinline__ void latch_status(unsigned int* status, unsigned int 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 
+// Two float32 lanes per instruction (packed f32x2, IEEE round-to-nearest in each
+// lane: the same results as two scalar operations, in half the issue slots).
+union F2 {
+  float2 f;
+  unsigned long long u;
+};
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  F2 x{a}, y{b}, d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d.u) : "l"(x.u), "l"(y.u));
+  return d.f;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {  // a * b + c
+  F2 x{a}, y{b}, z{c}, d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d.u) : "l"(x.u), "l"(y.u), "l"(z.u));
+  return d.f;
+}
+
 template <typename T> __device__ __forceinline__ T from_f32(float x);
 template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
@@ -61,37 +78,38 @@ inline size_t ws_order_bytes(int64_t n) { return (size_t)((n + 63) / 64) * 64 * 
 // workspace size can be computed without a device.
 //
 // The plan minimises a model of the critical path in chunk-steps (one 64-token
-// chunk of one chain on one SM), counting waves of one CTA per SM on the 152
-// SMs of a GB300: a split runs 2 (nseg - 1) transition CTAs per chain, then
+// chunk of one chain on one SM), counting waves of one CTA per SM on the
+// device's `sms` SMs: a split runs 2 (nseg - 1) transition CTAs per chain, then
 // nseg output CTAs per chain, each over seg_len / 64 chunks, plus the scan
 // (about half a chunk-step per segment); no split runs every chain whole.  A
-// split is taken only when the model saves at least 10%.  On a device with
-// fewer SMs the plan is still exact, only its choice may be less good.
+// split is taken only when the model saves at least 10%.
 struct SegPlan {
   int nseg = 1;
   int64_t seg_len = 0;
 };
-constexpr int64_t kPlanSms = 152;      // SMs the plan counts waves on
+constexpr int64_t kGb300Sms = 152;     // the plan's SM count when no device can be queried
 constexpr int64_t kSegMinChunks = 64;  // at least this many 64-token chunks per segment
 constexpr int64_t kSegMaxSegs = 64;
-inline int64_t plan_waves(int64_t ctas) { return (ctas + kPlanSms - 1) / kPlanSms; }
-inline double plan_cost(int64_t chains, int64_t chunks, int64_t seg_chunks, int64_t nseg) {
-  if (nseg < 2) return (double)plan_waves(chains) * (double)chunks;
-  return (double)seg_chunks *
-             (double)(plan_waves(2 * chains * (nseg - 1)) + plan_waves(chains * nseg)) +
+inline int64_t plan_waves(int64_t ctas, int64_t sms) { return (ctas + sms - 1) / sms; }
+inline double plan_cost(int64_t chains, int64_t chunks, int64_t seg_chunks, int64_t nseg,
+                        int64_t sms) {
+  if (nseg < 2) return (double)plan_waves(chains, sms) * (double)chunks;
+  return (double)seg_chunks * (double)(plan_waves(2 * chains * (nseg - 1), sms) +
+                                       plan_waves(chains * nseg, sms)) +
          0.5 * (double)nseg;
 }
-inline SegPlan seg_plan(bool packed, bool bf16_d128, int64_t chains, int64_t T) {
+inline SegPlan seg_plan(bool packed, bool bf16_d128, int64_t chains, int64_t T, int64_t sms) {
   SegPlan pl;
   const int64_t chunks = (T + 63) / 64;
-  if (packed || !bf16_d128 || chains <= 0 || chains >= kPlanSms || chunks < 2 * kSegMinChunks)
+  if (sms < 1) sms = kGb300Sms;
+  if (packed || !bf16_d128 || chains <= 0 || chains >= sms || chunks < 2 * kSegMinChunks)
     return pl;
-  double best = 0.9 * plan_cost(chains, chunks, chunks, 1);
+  double best = 0.9 * plan_cost(chains, chunks, chunks, 1, sms);
   const int64_t max_ns = chunks / kSegMinChunks < kSegMaxSegs ? chunks / kSegMinChunks
                                                               : kSegMaxSegs;
   for (int64_t ns = 2; ns <= max_ns; ++ns) {
     const int64_t seg = (chunks + ns - 1) / ns, nseg = (chunks + seg - 1) / seg;
-    const double c = plan_cost(chains, chunks, seg, nseg);
+    const double c = plan_cost(chains, chunks, seg, nseg, sms);
     if (c < best) {
       best = c;
       pl.nseg = (int)nseg;
@@ -154,6 +172,7 @@ struct FwdArgs {
   unsigned int* status;
   const int32_t* order;  // scheduler output: sequences longest first (packed), or nullptr
   float* seg_ws;         // segment-state area of the workspace (long-chain split), or nullptr
+  SegPlan plan;          // the split seg_ws was sized for (nseg 1: none)
   // prefix-cache checkpoints (state after every ckpt_interval tokens), or ckpt == nullptr
   float* ckpt;              // [ckpt_rows, H, D, D]
   const int32_t* ckpt_off;  // [N+1] row offsets (packed batches), or nullptr (fixed length)

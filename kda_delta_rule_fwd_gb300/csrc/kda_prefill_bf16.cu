@@ -54,7 +54,7 @@ constexpr int GPT = 16 / (2 * NCOL);  // 8-channel groups per thread in the elem
 static_assert(TCOL == 16 && SCOL % 16 == 0 && GPT >= 1, "thread mapping");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kGateRowsP8 = 384;  // fused gate rows activated during the U product
-constexpr float kMaxExp2 = 115.f;  // |log2 of a decay factor| beyond this overflows it
+constexpr float kMaxExp2 = 115.f;  // |log2 of a decay factor| beyond this: the exact token path
 constexpr float kRefExp2 = 100.f;  // |log2 c| is clamped here (S' and its bf16 parts stay normal)
 
 // ---- shared memory map (bytes) --------------------------------------------
@@ -71,8 +71,11 @@ static_assert(SV_M32 + 4 * 256 * 4 <= SM_GB, "substitution scratch overlaps the 
 constexpr uint32_t SM_X = 65536;         // 96 KB: [R_K; R_Q] hi, lo (K-major), Ck hi, lo
 constexpr uint32_t X_R_HI = 0, X_R_LO = 32768, X_CK_HI = 65536, X_CK_LO = 81920;
 constexpr uint32_t X_OUT = 0;  // output staging for the bulk store, [64 tokens][128] (32 KB)
+constexpr uint32_t X_ALPHA = 32768;  // token path: alpha [64 tokens][128] float32
 constexpr uint32_t SM_Y = 163840;        // 32 KB
 constexpr uint32_t Y_TB_HI = 0, Y_TB_LO = 8192, Y_AQK_HI = 16384, Y_AQK_LO = 24576;
+// token path scratch over the Aqk parts (rewritten in full by every tensor-core chunk)
+constexpr uint32_t Y_RED = 16384, Y_KQ = 16384 + 8192;
 constexpr uint32_t SM_LL = 196608;       // [L; L] 128 x 64 bf16 (lower-triangular ones)
 constexpr uint32_t SM_MISC = 212992;
 constexpr uint32_t MISC_RHO = 0, MISC_GL = 512, MISC_C = 1024, MISC_GAMC = 2048,
@@ -517,7 +520,6 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   const uint32_t sbase = smem_u32(smem);
   uint64_t* xo_bar = &bars[2];  // completion of the products with S'
   uint32_t xo_issued = 0;
-  bool range_err = false;
   // prefix-cache checkpoints of this chain (output items only)
   const int64_t ck_base =
       want_o ? ckpt_base(p.ckpt, p.ckpt_off, p.ckpt_rows, p.ckpt_interval, n, seq_len, p.status,
@@ -587,6 +589,194 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     s_nrm[isq * C + tt] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
   };
+  // The exact token path for a chunk whose in-chunk decay span overflows the
+  // factorisation (see pass A): the recurrence itself on the CUDA cores, with
+  // the state read from and written back to TMEM, so the tensor-core path
+  // continues from it.  Per token, for value channel j = row and key channels
+  // cq*32 .. cq*32+31 of this thread:
+  //   S <- diag(alpha) S;  p = S^T k, r = S^T q (one cross-warp sum);
+  //   u = beta (v - p);    S <- S + k u^T;   o = scale (r + u (k . q))
+  // alpha = e^g comes from global memory (the g tile buffers already hold the
+  // next chunk's gate), activated exactly as the fused path does.  Costs about
+  // four tensor-core chunks; ends with the same hand-over to chunk ci + 1.
+  auto token_chunk = [&](int ci, int64_t cs, int nv) {
+    float* s_al = reinterpret_cast<float*>(smem + SM_X + X_ALPHA);
+    float2* s_red = reinterpret_cast<float2*>(smem + SM_Y + Y_RED);
+    float* s_kq = reinterpret_cast<float*>(smem + SM_Y + Y_KQ);
+    {  // alpha for (token tid / 8, channels 16 (tid % 8) ..); 1 past the sequence end
+      const int tt = tid >> 3, c0 = (tid & 7) * 16;
+      float a[16];
+      if (tt < nv) {
+        const int64_t tok = t0 + cs + tt;
+        if (kPre && p.pre.per_head) {
+          float gv = __bfloat162float(p.g[tok * p.H + h]);
+          if (p.pre.gate) gv = round_to<__nv_bfloat16>(gsc * neg_softplus(gv));
+#pragma unroll
+          for (int e = 0; e < 16; ++e) a[e] = gv;
+        } else {
+          const uint4* src = reinterpret_cast<const uint4*>(p.g + (tok * p.H + h) * D + c0);
+          const uint4 u0 = src[0], u1 = src[1];
+          const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            a[2 * e] = bf16_lo(w[e]);
+            a[2 * e + 1] = bf16_hi(w[e]);
+          }
+          if (kPre && p.pre.gate)
+#pragma unroll
+            for (int e = 0; e < 16; ++e) a[e] = round_to<__nv_bfloat16>(gsc * neg_softplus(a[e]));
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) a[e] = ex2(a[e] * kLog2e);  // e^-inf = 0
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) a[e] = 1.f;
+      }
+      float4* dst = reinterpret_cast<float4*>(s_al + tt * D + c0);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dst[e] = make_float4(a[4 * e], a[4 * e + 1], a[4 * e + 2], a[4 * e + 3]);
+    }
+    {  // k . q per token: 16 lanes per token, two tokens per warp and pass
+      const int half = lane >> 4, cg = lane & 15;
+#pragma unroll
+      for (int it = 0; it < 2; ++it) {
+        const int tt = warp * 4 + it * 2 + half;
+        float kx[8], qx[8];
+        ld8(smem + SM_IN_K + off_sw128(tt, cg), kx);
+        ld8(smem + SM_IN_Q + off_sw128(tt, cg), qx);
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc = fmaf(kx[e], qx[e], acc);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (kPre && p.pre.l2) acc *= inv_l2(s_nrm[tt]) * inv_l2(s_nrm[C + tt]);
+        if (cg == 0) s_kq[tt] = acc;
+      }
+    }
+    float sv[SCOL];  // S^T row j, key channels cq*32 ..
+    {
+      float a0[16], a1[16];
+      tmem_ld16(tb + lane_base + TM_S + cq * SCOL, a0);
+      tmem_ld16(tb + lane_base + TM_S + cq * SCOL + 16, a1);
+      tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        sv[e] = a0[e];
+        sv[16 + e] = a1[e];
+      }
+    }
+    __syncthreads();  // alpha and k . q in place
+    const int j = row;
+    const uint8_t* vcol = smem + SM_IN_V + (j >> 3) * (C * 16) + (j & 7) * 2;
+    const int64_t obase = ((t0 + cs) * p.H + h) * D + j, ostride = (int64_t)p.H * D;
+#pragma unroll 1
+    for (int tt = 0; tt < nv; ++tt) {
+      float ik = 1.f, iq = 1.f;
+      if (kPre && p.pre.l2) {
+        ik = inv_l2(s_nrm[tt]);
+        iq = inv_l2(s_nrm[C + tt]);
+      }
+      const float4* al4 = reinterpret_cast<const float4*>(s_al + tt * D + cq * SCOL);
+      float2 pk = make_float2(0.f, 0.f), pq = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int g4 = 0; g4 < SCOL / 8; ++g4) {
+        float kx[8], qx[8];
+        ld8(smem + SM_IN_K + off_sw128(tt, cq * (SCOL / 8) + g4), kx);
+        ld8(smem + SM_IN_Q + off_sw128(tt, cq * (SCOL / 8) + g4), qx);
+        const float4 a0 = al4[2 * g4], a1 = al4[2 * g4 + 1];
+        const float al[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          float2 s2 = mul2(make_float2(sv[g4 * 8 + e], sv[g4 * 8 + e + 1]),
+                           make_float2(al[e], al[e + 1]));
+          sv[g4 * 8 + e] = s2.x;
+          sv[g4 * 8 + e + 1] = s2.y;
+          pk = fma2(s2, make_float2(kx[e] * ik, kx[e + 1] * ik), pk);
+          pq = fma2(s2, make_float2(qx[e] * iq, qx[e + 1] * iq), pq);
+        }
+      }
+      const int buf = tt & 1;
+      s_red[(buf * NCOL + cq) * 128 + j] = make_float2(pk.x + pk.y, pq.x + pq.y);
+      __syncthreads();  // double-buffered partial sums: one barrier per token
+      float P = 0.f, Q = 0.f;
+#pragma unroll
+      for (int c = 0; c < NCOL; ++c) {
+        const float2 r = s_red[(buf * NCOL + c) * 128 + j];
+        P += r.x;
+        Q += r.y;
+      }
+      const float vj = zero_v ? 0.f
+                              : __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                                    vcol + tt * 16));
+      const float u = s_beta[tt] * (vj - P);
+      const float2 u2 = make_float2(u, u);
+#pragma unroll
+      for (int g4 = 0; g4 < SCOL / 8; ++g4) {
+        float kx[8];
+        ld8(smem + SM_IN_K + off_sw128(tt, cq * (SCOL / 8) + g4), kx);
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          const float2 s2 = fma2(make_float2(kx[e] * ik, kx[e + 1] * ik), u2,
+                                 make_float2(sv[g4 * 8 + e], sv[g4 * 8 + e + 1]));
+          sv[g4 * 8 + e] = s2.x;
+          sv[g4 * 8 + e + 1] = s2.y;
+        }
+      }
+      if (want_o && cq == 0) {
+        const float o = p.scale * fmaf(u, s_kq[tt], Q);
+        if (nv == C) {  // staged for the bulk store, as the tensor-core chunk does
+          if (p.out_bf16)
+            reinterpret_cast<__nv_bfloat16*>(smem + SM_X + X_OUT)[tt * D + j] =
+                __float2bfloat16_rn(o);
+          else
+            reinterpret_cast<float*>(smem + SM_X + X_OUT)[tt * D + j] = o;
+        } else if (p.out_bf16) {
+          static_cast<__nv_bfloat16*>(p.out)[obase + tt * ostride] = __float2bfloat16_rn(o);
+        } else {
+          static_cast<float*>(p.out)[obase + tt * ostride] = o;
+        }
+      }
+    }
+    {  // the state back to TMEM, and the chunk's checkpoint
+      uint32_t w0[16], w1[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        w0[e] = __float_as_uint(sv[e]);
+        w1[e] = __float_as_uint(sv[16 + e]);
+      }
+      tmem_st16(tb + lane_base + TM_S + cq * SCOL, w0);
+      tmem_st16(tb + lane_base + TM_S + cq * SCOL + 16, w1);
+      const int64_t done = rel0 + cs + C;
+      if (ck_base >= 0 && nv == C && done % p.ckpt_interval == 0) {
+        float* ck = p.ckpt + ((ck_base + done / p.ckpt_interval - 1) * p.H + h) * D * D + j;
+#pragma unroll
+        for (int e = 0; e < SCOL; ++e) ck[(int64_t)(cq * SCOL + e) * D] = sv[e];
+      }
+      tmem_wait_st();
+    }
+    fence_proxy_async_smem();  // staged outputs are read by the bulk store
+    tc_fence_before();
+    __syncthreads();  // every thread is done with the q, k, v tiles and the staging
+    // hand-over to chunk ci + 1, as the tensor-core chunk does it: its q, k, v
+    // tiles, this chunk's outputs, the fused preprocessing, its cumulative sum
+    if (ci + 1 < nchunks) {
+      if (lane == 0 && warp >= 1 && warp <= 5) issue_tma_part(ci + 1, warp - 1);
+      ++tma_issued;
+    }
+    if (tid == 0 && want_o && nv == C) {
+      tma_store_2d(&tm_o, h * D, (int32_t)(t0 + cs), smem + SM_X + X_OUT);
+      bulk_commit();
+    }
+    if (kPre && ci + 1 < nchunks && (g_fill || p.pre.l2)) {
+      if (g_fill) {
+        activate_gate(ci + 1, tid, 2 * kHalfRows, kThreads);
+        fence_proxy_async_smem();
+      }
+      if (p.pre.l2 && warp >= 12) qk_sumsq(tma_issued - 1);
+      __syncthreads();
+    }
+    if (tid == 0 && ci + 1 < nchunks && !issue_cumsum(ci + 1)) wt.on_timeout();
+  };
   if (kPre && nchunks > 0 && (g_fill || p.pre.l2)) {
     if (g_fill) activate_gate(0, tid, 2 * kHalfRows, kThreads);
     if (p.pre.l2 && warp >= 12) qk_sumsq(0);
@@ -654,7 +844,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       s_c[tid] = ldexpf(1.f, (int)e2);
       s_gamc[tid] = ex2(s_gl[tid] * kLog2e - e2);  // e^Gam_last / c
     }
-    float dmin = 0.f, dmax = 0.f;
+    bool wide = false;  // a factor of this thread's slice leaves the exponent range (or is NaN)
 #pragma unroll
     for (int g4 = 0; g4 < GPT; ++g4) {
       const int cg = cg0 + g4;
@@ -676,9 +866,8 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       for (int e = 0; e < 8; ++e) {
         // log2(e^Gam / c); rows past the sequence end take 0 (their k and q are 0)
         float d = valid ? fmaf(gam[g4 * 8 + e], kLog2e, -e2[e]) : 0.f;
-        dmin = fminf(dmin, d);
-        dmax = fmaxf(dmax, d);
-        d = fminf(fmaxf(d, -kMaxExp2), kMaxExp2);  // keeps results finite when latched
+        wide |= !(fabsf(d) <= kMaxExp2);
+        d = fminf(fmaxf(d, -kMaxExp2), kMaxExp2);  // finite operands (unused if wide)
         const float er = ex2(d), ec = ex2(-d);
         const float kv = valid ? kx[e] : 0.f, qv = valid ? qx[e] : 0.f;
         rk[e] = kv * er;
@@ -692,10 +881,15 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       st8_split(smem + SM_X + X_CK_HI + off_kmaj(t, cg * 8, 128),
                 smem + SM_X + X_CK_LO + off_kmaj(t, cg * 8, 128), ck);
     }
-    // a factor beyond 2^+-115 overflows the factorisation: latched (clamped above)
-    if (dmin < -kMaxExp2 || dmax > kMaxExp2) range_err = true;
     fence_proxy_async_smem();
-    __syncthreads();
+    // A factor beyond 2^+-115 (an in-chunk decay span of more than about 160
+    // nats on some channel, alpha = 0 included) would overflow the
+    // factorisation: the whole chunk then runs the recurrence token by token.
+    // (A wait that ran out there is seen after the next chunk's first barrier.)
+    if (__syncthreads_or(wide)) {
+      token_chunk(ci, cs, nv);
+      continue;
+    }
 
     // ---- P4: [Akk; Aqk] = R Ck^T with split operands, while every thread
     // rescales its slice of the state: S' = S diag(c) (transposed), bf16 parts
@@ -1059,7 +1253,6 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   }
 
   if (tid == 0) bulk_wait_all();  // outputs complete before shared memory is released
-  if (range_err) latch_status(p.status, KDA_ERR_DECAY_RANGE);
   const bool aborted = *(volatile uint32_t*)s_flag != 0;
   if (!aborted && s_out) {
     const int j = row;
@@ -1220,7 +1413,7 @@ cudaError_t run_bf16(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap&
   cudaError_t e = cudaFuncSetAttribute(kda_prefill_bf16_kernel<kPre>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const SegPlan pl = seg_plan(a.cu != nullptr, true, items, a.T);
+  const SegPlan pl = a.plan;
   if (pl.nseg < 2 || !a.seg_ws) {
     kda_prefill_bf16_kernel<kPre><<<(unsigned)items, kThreads, SMEM_BYTES, a.stream>>>(
         mq, mk, mg, mv, mo, p);

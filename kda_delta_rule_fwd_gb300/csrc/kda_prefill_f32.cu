@@ -10,9 +10,13 @@
 //   O  = scale ((Q * e^Gam) S + Aqk U)
 //   S <- diag(e^Gam_last) S + (K * e^(Gam_last - Gam))^T U
 // The decayed products use exp of differences, which never exceed 1, so this
-// path has no range limit on g.  One CTA (256 threads) per (sequence, head)
-// chain, state S in shared memory.  Chunk: 64 tokens at d = 64, 32 at d = 128
-// (the rearrangement is exact for any chunk length).
+// path has no range limit on g.  Gam is summed in float64 and kept as a float
+// hi + lo pair, so a difference of two nearby prefix sums stays exact even
+// after a run of very large gates (g is floored at -1e4, where e^g is already
+// 0 in float32; g = -inf, alpha = 0, is taken as that floor).  One CTA (256
+// threads) per (sequence, head) chain, state S in shared memory.  Chunk: 64
+// tokens at d = 64, 32 at d = 128 (the rearrangement is exact for any chunk
+// length).
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -25,9 +29,9 @@ struct F32Smem {
   static constexpr int LD = D + 1;  // padded row stride: row-per-thread reads hit distinct banks
   static constexpr size_t floats =
       (size_t)D * D                 // S
-      + 7 * (size_t)C * LD          // q(->Qhat), k(->Khat), v, Gam, Kb, W, U
+      + 8 * (size_t)C * LD          // q(->Qhat), k(->Khat), v, Gam (hi, lo), Kb, W, U
       + 3 * (size_t)C * C           // A, Aqk, T
-      + C + D;                      // beta, Gam_last
+      + C + 2 * D;                  // beta, Gam_last (hi, lo)
   static constexpr size_t bytes = floats * sizeof(float);
 };
 
@@ -50,7 +54,8 @@ kda_prefill_f32_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
   float* sk = sq + C * LD;
   float* sv = sk + C * LD;
   float* sG = sv + C * LD;
-  float* sKb = sG + C * LD;
+  float* sGlo = sG + C * LD;
+  float* sKb = sGlo + C * LD;
   float* sW = sKb + C * LD;
   float* sU = sW + C * LD;
   float* sA = sU + C * LD;
@@ -58,6 +63,7 @@ kda_prefill_f32_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
   float* sT = sAqk + C * C;
   float* sb = sT + C * C;
   float* sGl = sb + C;
+  float* sGllo = sGl + D;
 
   // a malformed cu_seqlens is latched by the scheduler before this kernel starts
   if (status && *(volatile const unsigned int*)status == (unsigned)KDA_ERR_BAD_SEQLENS) return;
@@ -86,6 +92,7 @@ kda_prefill_f32_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
         xq = to_f32(q[x]); xk = to_f32(k[x]); xv = to_f32(v[x]);
         xg = to_f32(g[kPre && pre.per_head ? (t0 + cs + t) * H + h : x]);  // scalar gate: shared
         if (kPre && pre.gate) xg = round_to<TIn>(gsc * neg_softplus(xg));
+        xg = fmaxf(xg, -1e4f);
       }
       sq[t * LD + c] = xq; sk[t * LD + c] = xk; sv[t * LD + c] = xv; sG[t * LD + c] = xg;
     }
@@ -116,11 +123,18 @@ kda_prefill_f32_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
       }
       __syncthreads();
     }
-    // 2. inclusive log-decay prefix sums per channel
+    // 2. inclusive log-decay prefix sums per channel (float64, kept as hi + lo)
     for (int c = tid; c < D; c += kThreads) {
-      float run = 0.f;
-      for (int t = 0; t < C; ++t) { run += sG[t * LD + c]; sG[t * LD + c] = run; }
-      sGl[c] = run;
+      double run = 0.0;
+      for (int t = 0; t < C; ++t) {
+        run += (double)sG[t * LD + c];
+        const float hi = (float)run;
+        sG[t * LD + c] = hi;
+        sGlo[t * LD + c] = (float)(run - (double)hi);
+      }
+      const float hi = (float)run;
+      sGl[c] = hi;
+      sGllo[c] = (float)(run - (double)hi);
     }
     __syncthreads();
     // 3. decayed key-key and query-key products (lower triangle)
@@ -129,7 +143,8 @@ kda_prefill_f32_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
       float ak = 0.f, aq = 0.f;
       if (j <= i) {
         for (int c = 0; c < D; ++c) {
-          const float e = expf(sG[i * LD + c] - sG[j * LD + c]);
+          const float e = expf((sG[i * LD + c] - sG[j * LD + c]) +
+                               (sGlo[i * LD + c] - sGlo[j * LD + c]));
           const float kj = sk[j * LD + c] * e;
           ak = fmaf(sk[i * LD + c], kj, ak);
           aq = fmaf(sq[i * LD + c], kj, aq);
@@ -147,7 +162,7 @@ kda_prefill_f32_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
       const float e = expf(G);
       sKb[t * LD + c] = sb[t] * sk[t * LD + c] * e;
       sq[t * LD + c] *= e;
-      sk[t * LD + c] *= expf(sGl[c] - G);
+      sk[t * LD + c] *= expf((sGl[c] - G) + (sGllo[c] - sGlo[t * LD + c]));
     }
     // 5. T = (I + A)^-1 by forward substitution, one row at a time
     for (int i = 0; i < C; ++i) {

@@ -418,23 +418,91 @@ def test_bounded_wait_runs_out_and_is_reported(kda, oracle_mod):
     assert rel_err(o, o_ref) <= TOL_BF16
 
 
-def test_decay_outside_bf16_range_is_reported(kda):
-    """A per-chunk log-decay span beyond what the bf16 factorisation holds
-    (|Gam - rho| > 80 within a chunk) is latched as KDA_ERR_DECAY_RANGE; the
-    kernel clamps the factors, stays finite and does not fault."""
-    x = kda_inputs.fixed(1, 128, 2, 128, dtype=torch.bfloat16, device=DEV, seed=9)
-    g = x.g.clone()
-    g[:, 40:44] = -30.0  # 4 tokens of -30 per channel: a span of 120 inside the chunk
-    shape = kda.make_shape(x.q, x.v)
-    ws = kda.new_workspace(shape, DEV)
-    o, hT = kda.fwd(x.q, x.k, x.v, g, x.beta, workspace=ws)
-    assert kda.read_device_status(ws) == kda.KDA_ERR_DECAY_RANGE
-    assert torch.isfinite(hT).all()
-    # the float32 path has no such limit
-    o32, h32 = kda.fwd(x.q.float(), x.k.float(), x.v.float(), g.float(), x.beta.float(),
-                       workspace=ws)
+# strong gates: decay beyond the range one chunk's factorisation holds -----------------
+# The gate is per channel in (0, 1) ("Kimi K3 NPU Training", section 模型结构), so any
+# log(alpha) <= 0 is valid, alpha = 0 (g = -inf) included.  The bf16 tensor-core path
+# runs a chunk whose in-chunk decay span leaves its factor range token by token; the
+# float32 path takes exponentials of differences.  Both must match the oracle.
+
+def _strong_gates(g, pattern):
+    """g (token axis 1) with a few channels pushed far past the workload's range."""
+    g = g.clone()
+    if pattern == "g-3":        # e^-3 per token on four channels: 192 nats per chunk
+        g[..., 5:9] = -3.0
+    elif pattern == "g-25":     # e^-25 per token on two channels
+        g[..., 40:42] = -25.0
+    elif pattern == "alpha0":   # alpha = 0 at two tokens of one channel (chunks 1 and 2)
+        g[:, 70, :, 3] = float("-inf")
+        g[:, 150, :, 3] = float("-inf")
+    elif pattern == "burst":    # every channel at -30 for four tokens (chunk 0 only)
+        g[:, 40:44] = -30.0
+    return g
+
+
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 128),
+                                     (torch.float32, 64), (torch.bfloat16, 64)],
+                         ids=["bf16-128", "f32-128", "f32-64", "bf16-64"])
+@pytest.mark.parametrize("pattern", ["g-3", "g-25", "alpha0", "burst"])
+def test_strong_gates_match_oracle(kda, oracle_mod, dtype, d, pattern):
+    x = kda_inputs.fixed(2, 200, 2, d, dtype=dtype, device=DEV, seed=900 + d, h0_std=0.1)
+    x.g = _strong_gates(x.g, pattern)
+    ws = kda.new_workspace(kda.make_shape(x.q, x.v), DEV)
+    o, hT = kda.fwd(x.q, x.k, x.v, x.g, x.beta, h0=x.h0, workspace=ws)
     assert kda.read_device_status(ws) == kda.KDA_OK
-    assert torch.isfinite(o32).all() and torch.isfinite(h32).all()
+    o_ref, h_ref = oracle_mod.recurrent(x.q, x.k, x.v, x.g, x.beta, h0=x.h0)
+    assert rel_err(o, o_ref) <= TOL[dtype]
+    assert rel_err(hT, h_ref) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["o32", "o16"])
+def test_strong_gates_packed(kda, oracle_mod, dtype, out_dtype):
+    """Packed sequences (an empty and a one-token one included) with alpha = 0, -25 and
+    -4 runs crossing sequence boundaries, beside chunks of ordinary gates."""
+    x = kda_inputs.packed([1, 64, 0, 130, 77, 200], 2, 128, dtype=dtype, device=DEV, seed=910,
+                          h0_std=0.1)
+    g = x.g.clone()
+    g[:, 60:70, :, 7] = float("-inf")
+    g[:, 100:110, :, :4] = -25.0
+    g[:, 300:330, :, 50:60] = -4.0
+    x.g = g
+    _check_fwd(kda, oracle_mod, x, dtype, out_dtype=out_dtype)
+
+
+def test_strong_gates_long_chain_split(kda, oracle_mod):
+    """A chain long enough for the segment split, with strong decay inside some
+    segments: the transition passes (identity start, v = 0) and the output pass run
+    those chunks token by token too."""
+    T = 64 * 257 + 37
+    x = kda_inputs.fixed(1, T, 2, 128, dtype=torch.bfloat16, device=DEV, seed=920, h0_std=0.1)
+    g = x.g.clone()
+    g[:, 5000:9000, :, 5:9] = -3.0
+    g[:, 12000, :, 3] = float("-inf")
+    g[:, 15000:15004] = -30.0
+    x.g = g
+    shape = kda.make_shape(x.q, x.v)
+    assert kda.workspace_size(shape) > 256  # the split is planned
+    o, hT = kda.fwd(x.q, x.k, x.v, x.g, x.beta, h0=x.h0)
+    torch.cuda.synchronize()
+    o_ref, h_ref = oracle_mod.recurrent(x.q, x.k, x.v, x.g, x.beta, h0=x.h0)
+    assert rel_err(o, o_ref) <= TOL_BF16
+    assert rel_err(hT, h_ref) <= TOL_BF16
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_strong_gates_checkpoints(kda, oracle_mod, dtype):
+    """Checkpoints written by chunks that ran token by token."""
+    x = kda_inputs.fixed(2, 200, 2, 128, dtype=dtype, device=DEV, seed=930, h0_std=0.1)
+    g = _strong_gates(x.g, "alpha0")
+    g[:, :64, :, 40:42] = -25.0
+    x.g = g
+    o, hT, ck, _ = kda.fwd_checkpoints(x.q, x.k, x.v, x.g, x.beta, interval=64, h0=x.h0)
+    torch.cuda.synchronize()
+    refs = _ckpt_refs(oracle_mod, x, [(b, 0, 200, b) for b in range(2)], 64)
+    _check_ckpts(ck, refs, TOL[dtype])
+    o_ref, h_ref = oracle_mod.recurrent(x.q, x.k, x.v, x.g, x.beta, h0=x.h0)
+    assert rel_err(o, o_ref) <= TOL[dtype]
+    assert rel_err(hT, h_ref) <= TOL[dtype]
 
 
 @pytest.mark.parametrize("T", [200, 64 * 257 + 37], ids=["chain", "segment-split"])

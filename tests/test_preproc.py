@@ -213,6 +213,40 @@ def test_prefill_gate_scale_and_scalar_gate(kda, oracle_mod, dtype, d, per_head)
     assert rel_err(hT, h_ref) <= TOL[dtype]
 
 
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 128),
+                                     (torch.float32, 64)], ids=["bf16-128", "f32-128", "f32-64"])
+@pytest.mark.parametrize("per_head", [False, True], ids=["per-channel", "per-head"])
+def test_prefill_gate_scale_8(kda, oracle_mod, dtype, d, per_head):
+    """A per-head decay-rate scale of 8: log(alpha) = -8 softplus(g), about 6.5 nats
+    per token on average, so most chunks exceed the span one factorisation holds and
+    the bf16 path runs them token by token.  Packed, with an empty sequence."""
+    x = _raw_packed([1, 64, 0, 130, 77, 200], 2, d, dtype, seed=640 + d)
+    if per_head:
+        x.g = x.g[..., 0].contiguous()
+    a = torch.full((2,), 8.0, device=DEV)
+    o, hT = kda.fwd_preproc(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens, h0=x.h0,
+                            gate_per_head=per_head, gate_scale=a)
+    torch.cuda.synchronize()
+    fq, fk, fg, fb = oracle_mod.preprocess(x.q, x.k, x.g, x.beta, gate_per_head=per_head,
+                                           gate_scale=a)
+    o_ref, h_ref = oracle_mod.recurrent(fq, fk, x.v, fg, fb, cu_seqlens=x.cu_seqlens, h0=x.h0)
+    assert rel_err(o, o_ref) <= TOL[dtype]
+    assert rel_err(hT, h_ref) <= TOL[dtype]
+
+
+def test_decode_gate_scale_8(kda, oracle_mod):
+    x = kda_inputs.draw_raw((5, 8), 3, 128, 128, dtype=torch.bfloat16, device=DEV, seed=650,
+                            num_states=5, h0_std=0.1)
+    a = torch.full((3,), 8.0, device=DEV)
+    state = x.h0.clone()
+    o = kda.decode_preproc(x.q, x.k, x.v, x.g, x.beta, state, gate_scale=a)
+    torch.cuda.synchronize()
+    fq, fk, fg, fb = oracle_mod.preprocess(x.q, x.k, x.g, x.beta, gate_scale=a)
+    o_ref, h_ref = oracle_mod.recurrent(fq, fk, x.v, fg, fb, h0=x.h0)
+    assert rel_err(o, o_ref) <= TOL_BF16
+    assert rel_err(state, h_ref) <= TOL_BF16
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
 def test_prefill_scalar_log_decay_without_softplus(kda, oracle_mod, dtype):
     """A per-head gate given directly as log(alpha) (no activation) is broadcast over

@@ -4,7 +4,7 @@ benchmark uses, against the float64 oracle:
 * fixed-length prefill B=4, T=4096, H=32, d=128 (bf16): every element;
 * packed prefill, 16 sequences of 128..8192 tokens with h0 ~ N(0, 0.1^2): every element;
 * long context B=1, T=1,048,576, H=32: two seeded, sampled heads over the full length;
-* decode pool of 1024 sequences (T_step 1 and 8): a seeded sample of 64 sequences;
+* decode pool of 1024 sequences (T_step 1 and 8): every element;
 * the fused preprocessing on the fixed-length batch: every element;
 * the backward of the fixed-length batch: exact zeros past the cotangent's support and
   two sampled (sequence, head) chains (tolerance 1e-4, float32 throughout).
@@ -67,18 +67,33 @@ def test_long_context_prefill_sampled_heads(kda, oracle_mod):
 
 
 @pytest.mark.parametrize("T_step", [1, 8])
-def test_decode_pool_sampled_sequences(kda, oracle_mod, T_step):
+def test_decode_pool_full(kda, oracle_mod, T_step):
+    """Every element of o and of the updated state, all 1024 sequences x 32 heads.  The
+    oracle runs 128 sequences at a time (host memory); max|err| and the rms of the
+    reference are accumulated over the whole pool, so the metric is the pool's."""
     x = kda_inputs.decode_pool(num_seqs=1024, H=32, d=128, T_step=T_step, device=DEV)
     state = x.h0.clone()
     o = kda.decode(x.q, x.k, x.v, x.g, x.beta, state)
     torch.cuda.synchronize()
-    gen = torch.Generator().manual_seed(2000 + T_step)
-    seqs = torch.randperm(1024, generator=gen)[:64].sort().values
-    pick = lambda t: t[seqs.to(t.device)].contiguous().cpu()
-    o_ref, h_ref = oracle_mod.recurrent(pick(x.q), pick(x.k), pick(x.v), pick(x.g),
-                                        pick(x.beta), h0=pick(x.h0))
-    eo, eh = rel_err(pick(o), o_ref), rel_err(pick(state), h_ref)
-    _report(f"decode T_step={T_step} (64 of 1024 sequences)", eo, eh)
+    acc = {"o": [0.0, 0.0, 0], "h": [0.0, 0.0, 0]}  # max|err|, sum ref^2, count
+
+    def add(key, got, ref):
+        got = got.double().cpu().numpy()
+        assert np.all(np.isfinite(got))
+        a = acc[key]
+        a[0] = max(a[0], float(np.max(np.abs(got - ref))))
+        a[1] += float(np.sum(ref * ref))
+        a[2] += ref.size
+
+    for s0 in range(0, 1024, 128):
+        sl = lambda t: t[s0:s0 + 128].contiguous().cpu()
+        o_ref, h_ref = oracle_mod.recurrent(sl(x.q), sl(x.k), sl(x.v), sl(x.g), sl(x.beta),
+                                            h0=sl(x.h0))
+        add("o", o[s0:s0 + 128], o_ref)
+        add("h", state[s0:s0 + 128], h_ref)
+        del o_ref, h_ref
+    eo, eh = (acc[k][0] / np.sqrt(acc[k][1] / acc[k][2]) for k in ("o", "h"))
+    _report(f"decode T_step={T_step} (all 1024 sequences)", eo, eh)
     assert eo <= TOL_BF16 and eh <= TOL_BF16
 
 

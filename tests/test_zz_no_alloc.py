@@ -2,8 +2,8 @@
 device memory (their memory is planned in full by a host framework, or their
 bindings cannot reach a device allocator).  It keeps its scratch in a fixed
 array inside the library instead of a caller workspace.  Checked through the
-C ABI against kda_fwd on two calls in a row, since every call reuses the same
-array."""
+C ABI against kda_fwd, bit for bit, on two calls in a row, since every call
+reuses the same array."""
 import ctypes
 
 import pytest
@@ -40,6 +40,9 @@ def _call(kda, f, x, status):
 
 @pytest.mark.parametrize("packed", [True, False], ids=["packed", "fixed"])
 def test_noalloc_matches_kda_fwd_on_two_calls(kda, packed):
+    """Two calls in a row: each equals kda_fwd bit for bit (the same kernels run;
+    only the scratch's home differs), although the second finds the first's
+    contents in the shared array."""
     f = _entry(kda)
     status = torch.full((1,), 12345, dtype=torch.int32, device=DEV)
     for call in range(2):
@@ -55,8 +58,45 @@ def test_noalloc_matches_kda_fwd_on_two_calls(kda, packed):
         torch.cuda.synchronize()
         assert rc == kda.KDA_OK, kda.status_string(rc)
         assert int(status.item()) == kda.KDA_OK
-        assert rel_err(o, ref_o.double().cpu().numpy()) <= TOL_BF16
-        assert rel_err(hT, ref_h.double().cpu().numpy()) <= TOL_BF16
+        assert torch.equal(o, ref_o)
+        assert torch.equal(hT, ref_h)
+
+
+def test_noalloc_fixed_length_ignores_num_seqs(kda):
+    """num_seqs only describes packed batches: a fixed-length call carrying a stale
+    value beyond the array's sequence limit still runs."""
+    f = _entry(kda)
+    x = kda_inputs.fixed(2, 100, 2, 128, dtype=torch.bfloat16, device=DEV, seed=55)
+    shape = kda.make_shape(x.q, x.v)
+    shape.num_seqs = 100000
+    o = torch.empty_like(x.v, dtype=torch.float32)
+    hT = torch.empty(2, 2, 128, 128, device=DEV)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    rc = f(ctypes.byref(shape), p(x.q), p(x.k), p(x.v), p(x.g), p(x.beta), None, None, p(o),
+           p(hT), None, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    assert rc == kda.KDA_OK, kda.status_string(rc)
+    ref_o, ref_h = kda.fwd(x.q, x.k, x.v, x.g, x.beta)
+    assert torch.equal(o, ref_o) and torch.equal(hT, ref_h)
+
+
+def test_noalloc_long_chain_runs_unsplit(kda, oracle_mod):
+    """A chain kda_fwd cuts into segments (that needs its workspace) runs whole
+    through the fixed array, with the same results within the tolerance."""
+    f = _entry(kda)
+    x = kda_inputs.fixed(1, 64 * 257 + 37, 2, 128, dtype=torch.bfloat16, device=DEV, seed=57,
+                         h0_std=0.1)
+    assert kda.workspace_size(kda.make_shape(x.q, x.v)) > 256  # kda_fwd would split it
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    rc, o, hT = _call(kda, f, x, status)
+    torch.cuda.synchronize()
+    assert rc == kda.KDA_OK and int(status.item()) == kda.KDA_OK
+    small = torch.empty(256, dtype=torch.uint8, device=DEV)  # kda_fwd without the split
+    o_u, h_u = kda.fwd(x.q, x.k, x.v, x.g, x.beta, h0=x.h0, workspace=small)
+    assert torch.equal(o, o_u) and torch.equal(hT, h_u)
+    o_ref, h_ref = oracle_mod.recurrent(x.q, x.k, x.v, x.g, x.beta, h0=x.h0)
+    assert rel_err(o, o_ref) <= TOL_BF16
+    assert rel_err(hT, h_ref) <= TOL_BF16
 
 
 def test_noalloc_reports_device_errors_and_limits(kda):
