@@ -3,17 +3,21 @@
 Default workload (one "step" = one kda_fwd call over the whole batch):
     fixed-length prefill, B=4, T=4096, H=32, dk=dv=128, bf16 q/k/v/g/beta,
     float32 state and output, chunk 64, h0 = 0.
-The decode pool (1024 sequences, H=32, d=128, float32 states resident in HBM;
-T_step = 1 and an 8-token replay step) is timed in the same run and reported
-under "decode".
+Timed in the same run and reported in sub-objects: the decode pool (1024
+sequences, H=32, d=128, float32 states resident in HBM; T_step = 1 and an
+8-token replay step) under "decode", the packed 16-sequence prefill under
+"prefill_packed", the 1,048,576-token prefill (B=1, H=32) under "prefill_long",
+and the rows beyond the hot path under "next_rows".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py --case NAME     (one kernel's workload, for an ncu capture)
 
-Prints one JSON line.  Under torchrun every rank runs its own batch (weak
-scaling, no data-path collective); the barrier and the max over ranks of the
-timed region are the only communication.  ``--impl reference`` times the
-float64 CPU oracle on the host's cores on a bounded sample of the same
-workload.
+Prints one JSON line.  Under torchrun every rank runs its own batch of the
+headline workload (weak scaling, no data-path collective); the packed batch is
+also partitioned across the ranks by sequence, longest first, and timed as one
+job ("prefill_packed_sharded").  The barrier and the max over ranks of the
+timed regions are the only communication.  ``--impl reference`` times the
+float64 CPU oracle on the host's cores on a bounded sample of the workload.
 """
 from __future__ import annotations
 
@@ -198,6 +202,124 @@ def _time_steps(fn, steps, warmup, stream, dist_on):
     return e0.elapsed_time(e1) / steps
 
 
+def _hbm_line(nbytes, ms, peak):
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak}
+
+
+E2E_PARTS = 4  # sequences of the headline batch pipelined through the host copies
+
+
+def make_e2e_step(kda, x, dev, parts=E2E_PARTS):
+    """One end-to-end step through the public API with HOST buffers: pinned host
+    inputs in, o and hT back to pinned host memory.  The batch is cut by sequence
+    into `parts`: every part's inputs go down in turn on one copy stream, each
+    part's kda_fwd runs on a stream of its own as soon as its inputs have landed,
+    and its o and hT come back on a third stream, so the copies overlap the
+    kernels and each other (the two directions of the link are independent).
+    Returns (step, h2d_bytes, d2h_bytes)."""
+    import torch
+    pin = lambda t: t.cpu().pin_memory()
+    hin = [pin(t) for t in (x.q, x.k, x.v, x.g, x.beta)]
+    din = [torch.empty_like(t) for t in (x.q, x.k, x.v, x.g, x.beta)]
+    o = torch.empty(B, T, H, D, device=dev)
+    hT = torch.empty(B, H, D, D, device=dev)
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hh = torch.empty(hT.shape, dtype=hT.dtype).pin_memory()
+    per = B // parts
+    shape = kda.make_shape(x.q[:per], x.v[:per])
+    wss = [kda.new_workspace(shape, dev) for _ in range(parts)]
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    s_run = [torch.cuda.Stream(device=dev) for _ in range(parts)]
+
+    def step():
+        cur = torch.cuda.current_stream()
+        start = torch.cuda.Event()
+        start.record(cur)
+        s_in.wait_event(start)
+        s_out.wait_event(start)
+        for i in range(parts):
+            sl = slice(i * per, (i + 1) * per)
+            landed, done = torch.cuda.Event(), torch.cuda.Event()
+            with torch.cuda.stream(s_in):
+                for d_, h_ in zip(din, hin):
+                    d_[sl].copy_(h_[sl], non_blocking=True)
+                landed.record(s_in)
+            s_run[i].wait_event(landed)
+            with torch.cuda.stream(s_run[i]):
+                kda.fwd(*(d_[sl] for d_ in din), out=o[sl], hT=hT[sl], workspace=wss[i])
+                done.record(s_run[i])
+            s_out.wait_event(done)
+            with torch.cuda.stream(s_out):
+                ho[sl].copy_(o[sl], non_blocking=True)
+                hh[sl].copy_(hT[sl], non_blocking=True)
+        cur.wait_stream(s_out)
+
+    h2d = sum(t.numel() * t.element_size() for t in hin)
+    d2h = ho.numel() * ho.element_size() + hh.numel() * hh.element_size()
+    return step, h2d, d2h, (o, hT, ho, hh)
+
+
+def bench_long(kda, args, dev, stream, dist_on, hbm_peak):
+    """The 1,048,576-token prefill (B=1, H=32): one step is the whole call (the
+    long-chain split's transition, scan and output passes included)."""
+    import torch
+    import kda_inputs
+    x = kda_inputs.workload(3, device=dev)
+    shape = kda.make_shape(x.q, x.v)
+    ws = kda.new_workspace(shape, dev)
+    o = torch.empty_like(x.v, dtype=torch.float32)
+    hT = torch.empty(1, H, D, D, device=dev)
+    fn = lambda: kda.fwd(x.q, x.k, x.v, x.g, x.beta, out=o, hT=hT, workspace=ws)
+    ms = _time_steps(fn, max(3, args.steps // 4), 2, stream, dist_on)
+    st = kda.read_device_status(ws)
+    if st != kda.KDA_OK:
+        raise RuntimeError(f"device status {kda.status_string(st)}")
+    tok = x.q.shape[1]
+    nbytes = tok * H * BYTES_PER_TOKEN_HEAD + H * STATE_BYTES
+    del x, o, hT, ws
+    torch.cuda.empty_cache()
+    ms = max_over_ranks([ms], dev)[0]
+    return {
+        "workload": "KDA prefill, long context: B=1, T=1,048,576, H=32, dk=dv=128, bf16 in, "
+                    "fp32 state/out, chunk 64, h0 = 0",
+        "tokens": tok, "ms_per_step": ms, "tokens_per_s": tok * _dist()[1] / (ms * 1e-3),
+        "workspace_bytes": int(kda.workspace_size(shape)),
+        "roofline": _hbm_line(nbytes, ms, hbm_peak),
+    }
+
+
+def bench_packed_sharded(kda, args, dev, stream, dist_on, hbm_peak):
+    """The packed 16-sequence batch partitioned across the ranks by sequence,
+    longest first: each rank runs only its own sequences; the job's time is the
+    slowest rank's and its tokens are the whole batch's (one batch, strong
+    scaling)."""
+    import torch
+    import kda_inputs
+    from kda_delta_rule_fwd_gb300 import shard
+    rank, world, _ = _dist()
+    y = kda_inputs.workload(2, device=dev)
+    lens = (y.cu_seqlens[1:] - y.cu_seqlens[:-1]).tolist()
+    mine = shard.take_sequences(y, shard.lpt_by_sequence(lens, world)[rank])
+    n = len(mine.seqs)
+    if n:
+        ws = kda.new_workspace(kda.make_shape(mine.q, mine.v, packed_seqs=n), dev)
+        o = torch.empty_like(mine.v, dtype=torch.float32)
+        hT = torch.empty(n, H, D, D, device=dev)
+        fn = lambda: kda.fwd(mine.q, mine.k, mine.v, mine.g, mine.beta,
+                             cu_seqlens=mine.cu_seqlens, h0=mine.h0, out=o, hT=hT, workspace=ws)
+    else:
+        fn = lambda: None
+    ms = _time_steps(fn, max(5, args.steps), max(3, args.warmup), stream, dist_on)
+    ms = max_over_ranks([ms], dev)[0]
+    tok = y.q.shape[1]
+    nbytes = tok * H * BYTES_PER_TOKEN_HEAD + len(lens) * H * 2 * STATE_BYTES
+    return {"workload": "16 packed sequences (as prefill_packed) split across the ranks by "
+                        "sequence, longest first", "ranks": world, "tokens": tok,
+            "ms_per_step": ms, "tokens_per_s": tok / (ms * 1e-3),
+            "roofline_per_job": _hbm_line(nbytes, ms, hbm_peak * world)}
+
+
 def run_ours(args):
     import torch
     import kda_inputs
@@ -231,23 +353,13 @@ def run_ours(args):
     if st != kda.KDA_OK:
         raise RuntimeError(f"device status {kda.status_string(st)}")
 
-    # end to end through the public API: pinned host inputs in, o and hT back to host
-    pin = lambda t: t.cpu().pin_memory()
-    hq, hk, hv, hg, hb = (pin(t) for t in (x.q, x.k, x.v, x.g, x.beta))
-    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    hh = torch.empty(hT.shape, dtype=hT.dtype).pin_memory()
-    dq, dk_, dv, dg, db = (torch.empty_like(t) for t in (x.q, x.k, x.v, x.g, x.beta))
-
-    def e2e_step():
-        for d_, h_ in ((dq, hq), (dk_, hk), (dv, hv), (dg, hg), (db, hb)):
-            d_.copy_(h_, non_blocking=True)
-        kda.fwd(dq, dk_, dv, dg, db, out=o, hT=hT, workspace=ws)
-        ho.copy_(o, non_blocking=True)
-        hh.copy_(hT, non_blocking=True)
-
+    # end to end through the public API with host buffers (pipelined by sequence)
+    e2e_step, h2d, d2h, keep = make_e2e_step(kda, x, dev)
     ms_e2e = _time_steps(e2e_step, max(3, args.steps // 4), 2, stream, dist_on)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg, hb))
-    d2h = ho.numel() * ho.element_size() + hh.numel() * hh.element_size()
+    # the same with one part: copies in, kernel, copies out in sequence
+    e2e_serial, _, _, keep1 = make_e2e_step(kda, x, dev, parts=1)
+    ms_e2e1 = _time_steps(e2e_serial, max(3, args.steps // 4), 2, stream, dist_on)
+    del keep, keep1, e2e_step, e2e_serial
 
     # decode pool: T_step = 1 and 8, states resident in HBM (updated in place)
     dec = {}
@@ -261,13 +373,9 @@ def run_ours(args):
         fn = lambda: kda.decode(y.q, y.k, y.v, y.g, y.beta, state, out=out_d, workspace=dws)
         dms = _time_steps(fn, max(5, args.steps), max(3, args.warmup), stream, dist_on)
         nbytes = 1024 * H * (2 * STATE_BYTES + T_step * BYTES_PER_TOKEN_HEAD)
-        dec[f"T{T_step}"] = {
-            "tokens_per_s": 1024 * T_step * world / (dms * 1e-3),
-            "ms_per_step": dms,
-            "roofline": {"bound": "hbm", "achieved": nbytes / (dms * 1e-3) / 1e9,
-                         "peak": hbm_peak, "unit": "GB/s",
-                         "frac": nbytes / (dms * 1e-3) / 1e9 / hbm_peak, "traffic": None},
-        }
+        dec[f"T{T_step}"] = {"tokens_per_s": 1024 * T_step * world / (dms * 1e-3),
+                             "ms_per_step": dms, "roofline": _hbm_line(nbytes, dms, hbm_peak)}
+        dec[f"T{T_step}"]["roofline"]["traffic"] = None
         del y, state, out_d
 
     # packed prefill: 16 sequences of 128..8192 tokens with h0 (a second prefill workload)
@@ -287,10 +395,13 @@ def run_ours(args):
     packed_line = {
         "workload": "16 packed sequences, lengths uniform in [128, 8192], H=32, d=128, bf16, h0",
         "tokens": ptok, "ms_per_step": pms, "tokens_per_s": ptok * world / (pms * 1e-3),
-        "roofline": {"bound": "hbm", "achieved": pbytes / (pms * 1e-3) / 1e9, "peak": hbm_peak,
-                     "unit": "GB/s", "frac": pbytes / (pms * 1e-3) / 1e9 / hbm_peak},
+        "roofline": _hbm_line(pbytes, pms, hbm_peak),
     }
     del y, py_o, py_h
+
+    long_line = None if args.no_long else bench_long(kda, args, dev, stream, dist_on, hbm_peak)
+    sharded_line = bench_packed_sharded(kda, args, dev, stream, dist_on, hbm_peak) \
+        if dist_on else None
 
     # rows beyond the hot path: prefix-cache checkpoints every 512 tokens on the
     # fixed-length batch, and the decode step with per-sequence commit counts
@@ -359,44 +470,34 @@ def run_ours(args):
         "prefill_checkpoints_512": {
             "workload": WORKLOAD + "; state checkpoint every 512 tokens (32 per chain)",
             "ms_per_step": cms, "overhead_vs_prefill": cms / ms - 1.0,
-            "roofline": {"bound": "hbm", "achieved": cbytes / (cms * 1e-3) / 1e9,
-                         "peak": hbm_peak, "unit": "GB/s",
-                         "frac": cbytes / (cms * 1e-3) / 1e9 / hbm_peak}},
+            "roofline": _hbm_line(cbytes, cms, hbm_peak)},
         "decode_commit_T8": {
             "workload": "decode pool 1024 x 32 heads, T_step=8, commit counts uniform 0..8",
             "ms_per_step": kms, "tokens_per_s": 1024 * 8 * world / (kms * 1e-3),
-            "roofline": {"bound": "hbm", "achieved": kbytes / (kms * 1e-3) / 1e9,
-                         "peak": hbm_peak, "unit": "GB/s",
-                         "frac": kbytes / (kms * 1e-3) / 1e9 / hbm_peak,
-                         "note": "bytes counted as if every sequence commits"}},
+            "roofline": dict(_hbm_line(kbytes, kms, hbm_peak),
+                             note="bytes counted as if every sequence commits")},
         "prefill_preproc": {
             "workload": WORKLOAD.replace("bf16", "bf16 raw") +
             "; q/k L2 norm, -softplus gate, sigmoid beta fused",
             "ms_per_step": rms, "overhead_vs_prefill": rms / ms - 1.0,
             "unfused_ms_per_step": ums,
-            "roofline": {"bound": "hbm", "achieved": fbytes / (rms * 1e-3) / 1e9,
-                         "peak": hbm_peak, "unit": "GB/s",
-                         "frac": fbytes / (rms * 1e-3) / 1e9 / hbm_peak}},
+            "roofline": _hbm_line(fbytes, rms, hbm_peak)},
         "backward": {
             "workload": WORKLOAD + "; gradients dq, dk, dv, dg, dbeta of sum(o * dout), "
             "dout float32",
             "ms_per_step": bms, "vs_prefill": bms / ms,
             "tokens_per_s": B * T * H * world / H / (bms * 1e-3),
-            "roofline": {"bound": "hbm", "achieved": bbytes / (bms * 1e-3) / 1e9,
-                         "peak": hbm_peak, "unit": "GB/s",
-                         "frac": bbytes / (bms * 1e-3) / 1e9 / hbm_peak,
-                         "note": "algorithmic bytes (inputs, dout, gradients); the sub-chunk "
-                                 "states add 8 KB per token and head of workspace traffic"}},
+            "roofline": dict(_hbm_line(bbytes, bms, hbm_peak),
+                             note="algorithmic bytes (inputs, dout, gradients); the sub-chunk "
+                                  "states add 8 KB per token and head of workspace traffic")},
         "decode_preproc_T1": {
             "workload": "decode pool 1024 x 32 heads, T_step=1, raw inputs, preprocessing fused",
             "ms_per_step": qms, "tokens_per_s": 1024 * world / (qms * 1e-3),
-            "roofline": {"bound": "hbm", "achieved": qbytes / (qms * 1e-3) / 1e9,
-                         "peak": hbm_peak, "unit": "GB/s",
-                         "frac": qbytes / (qms * 1e-3) / 1e9 / hbm_peak}},
+            "roofline": _hbm_line(qbytes, qms, hbm_peak)},
     }
     clk = clocks.stop()
 
-    ms, ms_e2e = max_over_ranks([ms, ms_e2e], dev)
+    ms, ms_e2e, ms_e2e1 = max_over_ranks([ms, ms_e2e, ms_e2e1], dev)
     for key in dec:
         dec[key]["ms_per_step"] = max_over_ranks([dec[key]["ms_per_step"]], dev)[0]
 
@@ -429,19 +530,67 @@ def run_ours(args):
                      "tensor_tflops_algorithmic": alg_flops / (ms * 1e-3) / 1e12,
                      "tensor_frac_of_bf16_peak": alg_flops / (ms * 1e-3) / 1e12 / bf16_peak},
         "e2e": {"value": tokens / (ms_e2e * 1e-3), "unit": "tokens/s", "ms_per_step": ms_e2e,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "how": f"pinned host inputs -> device -> kda_fwd -> o, hT to pinned host, "
+                       f"pipelined in {E2E_PARTS} parts by sequence (copies in on one stream, "
+                       f"a stream per part's kernel, copies out on another)",
+                "serial_ms_per_step": ms_e2e1},
         "gpu_launches": args.steps,
         "clocks": clk,
         "decode": dec,
         "prefill_packed": packed_line,
         "next_rows": next_rows,
     }
+    if long_line is not None:
+        result["prefill_long"] = long_line
+    if sharded_line is not None:
+        result["prefill_packed_sharded"] = sharded_line
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = _cpu_baseline(kda_inputs.workload(1, device=dev))
     if dist_on:
         td.destroy_process_group()
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def run_case(name):
+    """One kernel's workload, run twice (a warm-up launch, then the one to
+    capture: ``ncu -s 1 -c 1``), seeded and synthetic:
+
+      prefill   the headline batch, B=4, T=4096, H=32, d=128, bf16
+      packed    the 16-sequence packed batch with h0
+      long      B=1, T=65,536, H=32 (one chain per head split into segments)
+      decode1   1-token decode on a pool of 256 sequences x 32 heads
+      decode8   8-token decode on the same pool
+      bwd       the backward on B=1, T=512, H=4, d=128, bf16, with h0
+    """
+    import torch
+    import kda_inputs
+    import kda_delta_rule_fwd_gb300 as kda
+    dev = torch.device("cuda:0")
+    if name in ("prefill", "packed", "long"):
+        x = (kda_inputs.workload(1, device=dev) if name == "prefill" else
+             kda_inputs.workload(2, device=dev) if name == "packed" else
+             kda_inputs.fixed(1, 1 << 16, H, D, device=dev, seed=1003))
+        for _ in range(2):
+            out = kda.fwd(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens, h0=x.h0)
+    elif name in ("decode1", "decode8"):
+        x = kda_inputs.decode_pool(num_seqs=256, H=H, d=D, T_step=int(name[-1]), device=dev,
+                                   seed=15)
+        state = x.h0.clone()
+        for _ in range(2):
+            out = (kda.decode(x.q, x.k, x.v, x.g, x.beta, state), state)
+    elif name == "bwd":
+        x = kda_inputs.fixed(1, 512, 4, D, dtype=torch.bfloat16, device=dev, seed=5, h0_std=0.1)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(6)
+        dout = torch.randn(x.v.shape, generator=gen, device=dev)
+        for _ in range(2):
+            out = kda.bwd(x.q, x.k, x.v, x.g, x.beta, dout, h0=x.h0)
+    else:
+        raise SystemExit(f"unknown case {name}")
+    torch.cuda.synchronize()
+    print(name, "ok", float(out[0].float().abs().sum()))
 
 
 def run_reference(args):
@@ -492,10 +641,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-long", action="store_true", help="skip the 1M-token prefill")
+    ap.add_argument("--case", help="run one kernel's workload (see run_case) and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.case:
+        run_case(args.case)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

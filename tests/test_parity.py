@@ -530,3 +530,32 @@ def test_nondefault_scale_single_head_bf16_output_packed(kda, oracle_mod):
     d = np.abs(o.float().cpu().numpy() - o_ref)
     assert np.all(d <= TOL_BF16 * np.sqrt(np.mean(o_ref ** 2)) + np.abs(o_ref) * 2.0 ** -8)
     assert rel_err(hT, h_ref) <= TOL_BF16
+
+
+# one batch partitioned across ranks, the shards run one after another on one GPU ------
+
+@pytest.mark.parametrize("by", ["sequence", "head"])
+def test_sharded_batch_equals_unsharded(kda, by):
+    """Every chain is independent, so a batch computed shard by shard (the sequence
+    partition of 3 ranks, longest first, or the head partition) and put back in place
+    equals the whole batch's result bit for bit."""
+    from kda_delta_rule_fwd_gb300 import shard
+    lens = [700, 0, 65, 1, 300, 64, 1030, 9]
+    x = kda_inputs.packed(lens, 5, 128, dtype=torch.bfloat16, device=DEV, seed=950,
+                          h0_std=0.1)
+    o_ref, h_ref = kda.fwd(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens, h0=x.h0)
+    if by == "sequence":
+        shards = [shard.take_sequences(x, idx) for idx in shard.lpt_by_sequence(lens, 3)]
+    else:
+        shards = [shard.take_heads(x, h0, h1) for h0, h1 in shard.heads_by_rank(5, 3)]
+    outs, states = [], []
+    for s in shards:
+        o, h = kda.fwd(s.q, s.k, s.v, s.g, s.beta, cu_seqlens=s.cu_seqlens, h0=s.h0)
+        outs.append(o)
+        states.append(h)
+    torch.cuda.synchronize()
+    if by == "sequence":
+        o, h = shard.place_sequences(x.q.shape[1], x.cu_seqlens.tolist(), shards, outs, states)
+    else:
+        o, h = torch.cat(outs, dim=2), torch.cat(states, dim=1)
+    assert torch.equal(o, o_ref) and torch.equal(h, h_ref)
