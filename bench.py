@@ -7,7 +7,8 @@ Timed in the same run and reported in sub-objects: the decode pool (1024
 sequences, H=32, d=128, float32 states resident in HBM; T_step = 1 and an
 8-token replay step) under "decode", the packed 16-sequence prefill under
 "prefill_packed", the 1,048,576-token prefill (B=1, H=32) under "prefill_long",
-and the rows beyond the hot path under "next_rows".
+a packed batch holding one 2^18-token sequence under "prefill_packed_long", and
+the rows beyond the hot path under "next_rows".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
     python bench.py --case NAME     (one kernel's workload, for an ncu capture)
@@ -289,6 +290,45 @@ def bench_long(kda, args, dev, stream, dist_on, hbm_peak):
     }
 
 
+def bench_packed_long(kda, args, dev, stream, dist_on, hbm_peak):
+    """A packed batch holding one long sequence, [2^18, 300, 1, 5000] tokens at H=32
+    (the device-planned split cuts the long sequence into segments), beside the
+    fixed-length B=1, T=2^18 batch of that length alone (the host-planned split)."""
+    import torch
+    import kda_inputs
+    lens = [1 << 18, 300, 1, 5000]
+    out = {}
+    for name, x in (("packed", lambda: kda_inputs.packed(lens, H, D, device=dev, seed=1006,
+                                                        h0_std=0.1)),
+                    ("fixed", lambda: kda_inputs.fixed(1, 1 << 18, H, D, device=dev,
+                                                      seed=1006))):
+        x = x()
+        n = 4 if name == "packed" else 1
+        shape = kda.make_shape(x.q, x.v, packed_seqs=n if name == "packed" else None)
+        ws = kda.new_workspace(shape, dev)
+        o = torch.empty_like(x.v, dtype=torch.float32)
+        hT = torch.empty(n, H, D, D, device=dev)
+        fn = lambda: kda.fwd(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens, h0=x.h0,
+                             out=o, hT=hT, workspace=ws)
+        ms = _time_steps(fn, max(3, args.steps // 4), 3, stream, dist_on)
+        st = kda.read_device_status(ws)
+        if st != kda.KDA_OK:
+            raise RuntimeError(f"device status {kda.status_string(st)}")
+        tok = x.q.shape[1]
+        nbytes = tok * H * BYTES_PER_TOKEN_HEAD + n * H * 2 * STATE_BYTES
+        ms = max_over_ranks([ms], dev)[0]
+        out[name] = {"tokens": tok, "ms_per_step": ms, "tokens_per_s": tok / (ms * 1e-3),
+                     "roofline": _hbm_line(nbytes, ms, hbm_peak)}
+        del x, o, hT, ws
+        torch.cuda.empty_cache()
+    out["workload"] = ("packed [2^18, 300, 1, 5000] tokens, H=32, d=128, bf16, h0; against "
+                       "fixed-length B=1, T=2^18, H=32")
+    out["time_per_token_packed_over_fixed"] = (
+        out["packed"]["ms_per_step"] / out["packed"]["tokens"]) / (
+        out["fixed"]["ms_per_step"] / out["fixed"]["tokens"])
+    return out
+
+
 def bench_packed_sharded(kda, args, dev, stream, dist_on, hbm_peak):
     """The packed 16-sequence batch partitioned across the ranks by sequence,
     longest first: each rank runs only its own sequences; the job's time is the
@@ -400,6 +440,8 @@ def run_ours(args):
     del y, py_o, py_h
 
     long_line = None if args.no_long else bench_long(kda, args, dev, stream, dist_on, hbm_peak)
+    plong_line = None if args.no_long else bench_packed_long(kda, args, dev, stream, dist_on,
+                                                             hbm_peak)
     sharded_line = bench_packed_sharded(kda, args, dev, stream, dist_on, hbm_peak) \
         if dist_on else None
 
@@ -543,6 +585,8 @@ def run_ours(args):
     }
     if long_line is not None:
         result["prefill_long"] = long_line
+    if plong_line is not None:
+        result["prefill_packed_long"] = plong_line
     if sharded_line is not None:
         result["prefill_packed_sharded"] = sharded_line
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -67,9 +67,17 @@ extern "C" {
 size_t kda_workspace_size(const kda_shape* s) {
   if (!s) return 0;
   size_t b = kWsHeader;
-  if (s->num_seqs > 0) b += ws_order_bytes(s->num_seqs);
-  // fixed-length batches of a few very long chains also keep segment states
   const bool bf16_d128 = s->in_dtype == KDA_BF16 && s->dk == 128 && s->dv == 128;
+  if (s->num_seqs > 0) {
+    // packed: the order list, then (long enough batches) the split plan and states
+    b += ws_order_bytes(s->num_seqs);
+    if (s->H > 0 && packed_split_possible(bf16_d128, s->T)) {
+      const int64_t nsx = packed_ns_max(s->T);
+      b += packed_plan_bytes(s->num_seqs, nsx) + packed_state_bytes(nsx, s->H, s->dk);
+    }
+    return b;
+  }
+  // fixed-length batches of a few very long chains also keep segment states
   const int64_t chains = (int64_t)(s->B > 0 ? s->B : 0) * (s->H > 0 ? s->H : 0);
   b += seg_bytes(seg_plan(false, bf16_d128, chains, s->T, device_sms()), chains, s->dk);
   return b;
@@ -137,9 +145,25 @@ kda_status fwd_common(const kda_shape* s, const void* q, const void* k, const vo
 
   if (cudaMemsetAsync(workspace, 0, kWsHeader, a.stream) != cudaSuccess) return KDA_ERR_CUDA;
   if (packed) {
-    int32_t* order = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + kWsHeader);
+    char* w = static_cast<char*>(workspace);
+    int32_t* order = reinterpret_cast<int32_t*>(w + kWsHeader);
     if (launch_schedule(a, order) != cudaSuccess) return KDA_ERR_CUDA;
     a.order = order;
+    // long-chain split of the longest sequences, planned on the device, when the
+    // workspace holds the plan and the segment states
+    const bool bf16_d128 = s->in_dtype == KDA_BF16 && s->dk == 128;
+    if (packed_split_possible(bf16_d128, s->T)) {
+      const int64_t nsx = packed_ns_max(s->T);
+      const size_t at = kWsHeader + ws_order_bytes(s->num_seqs);
+      const size_t plan = packed_plan_bytes(s->num_seqs, nsx);
+      if (workspace_bytes >= at + plan + packed_state_bytes(nsx, s->H, s->dk)) {
+        a.pplan = w + at;
+        a.ns_max = nsx;
+        a.seg_ws = reinterpret_cast<float*>(w + at + plan);
+        a.sms = device_sms();
+        if (launch_plan_packed(a) != cudaSuccess) return KDA_ERR_CUDA;
+      }
+    }
   } else {
     // long-chain split: segment states follow the header when the plan asks for them
     const bool bf16_d128 = s->in_dtype == KDA_BF16 && s->dk == 128;

@@ -124,6 +124,74 @@ inline size_t seg_bytes(const SegPlan& pl, int64_t chains, int D) {
   return (size_t)chains * (size_t)(3 * pl.nseg - 2) * (size_t)D * D * sizeof(float);
 }
 
+// Long-chain split for packed bf16 batches.  The lengths are only on the
+// device, so a planner kernel (one CTA) reads the validated cu_seqlens, picks a
+// segment length S (64-token chunks) from a cost model, and writes the plan
+// into the workspace: every sequence of at least 2 S chunks is cut into
+// floor(chunks / S) segments of equal length (up to 64), the others run whole.
+// The passes (transitions, scan, outputs) launch over grids sized by an upper
+// bound; CTAs past the plan's counts leave at once.
+//
+// Cost model, in chunk-steps on `sms` SMs with one CTA each: a pass whose
+// items (chains or segments) total W chunks, the longest L, takes about
+// max(L, W / sms + L / 2); the scan about half a chunk-step per segment.  The
+// split is taken when it saves at least 10% against running every chain
+// whole.
+struct PackedPlan {
+  int32_t n_trans;   // transition items (sequence, segment < nseg - 1)
+  int32_t n_split;   // split sequences
+  int32_t n_out;     // output items (sequence, segment), longest first
+  int32_t seg_chunks;  // S, or 0 when nothing is split
+};
+struct PlanItem {
+  int32_t n, seg;
+};
+// Bound on the segments of all split sequences together: each split sequence
+// is at least 2 S >= 128 chunks long and its segments at least S >= 64 chunks.
+inline int64_t packed_ns_max(int64_t T) { return T / 4096 + T / 524288 + 2; }
+// packed split possible at all: some sequence may reach 2 * 64 chunks
+inline bool packed_split_possible(bool bf16_d128, int64_t T) {
+  return bf16_d128 && T >= 2 * 64 * 64;
+}
+// workspace bytes after the order list: the plan (header, per-sequence
+// arrays, item tables; 256-byte aligned), then the segment states
+inline size_t packed_plan_bytes(int64_t N, int64_t ns_max) {
+  const size_t b = sizeof(PackedPlan) + (size_t)N * 3 * sizeof(int32_t) +
+                   (size_t)ns_max * sizeof(PlanItem)            // transitions
+                   + (size_t)ns_max * sizeof(int32_t)           // split sequences
+                   + (size_t)(N + ns_max) * sizeof(PlanItem);   // outputs
+  return (b + 255) / 256 * 256;
+}
+inline size_t packed_state_bytes(int64_t ns_max, int64_t H, int D) {
+  return (size_t)(3 * ns_max) * (size_t)H * (size_t)D * D * sizeof(float);
+}
+// Views of the plan area (laid out in the order packed_plan_bytes counts it).
+struct PlanView {
+  PackedPlan* hdr;
+  int32_t* nseg;      // [N] segments per sequence (1: whole)
+  int32_t* seglen;    // [N] tokens per segment (split sequences)
+  int32_t* slot;      // [N] first state slot of a split sequence (x H heads)
+  PlanItem* trans;    // [ns_max]
+  int32_t* split;     // [ns_max]
+  PlanItem* out;      // [N + ns_max]
+  __host__ __device__ static PlanView at(void* base, int64_t N, int64_t ns_max) {
+    PlanView v;
+    char* p = static_cast<char*>(base);
+    v.hdr = reinterpret_cast<PackedPlan*>(p);
+    p += sizeof(PackedPlan);
+    v.nseg = reinterpret_cast<int32_t*>(p);
+    v.seglen = v.nseg + N;
+    v.slot = v.seglen + N;
+    p += (size_t)N * 3 * sizeof(int32_t);
+    v.trans = reinterpret_cast<PlanItem*>(p);
+    p += (size_t)ns_max * sizeof(PlanItem);
+    v.split = reinterpret_cast<int32_t*>(p);
+    p += (size_t)ns_max * sizeof(int32_t);
+    v.out = reinterpret_cast<PlanItem*>(p);
+    return v;
+  }
+};
+
 // ---------------------------------------------------------------------------
 // launchers (each returns cudaSuccess or the launch error)
 // ---------------------------------------------------------------------------
@@ -173,6 +241,9 @@ struct FwdArgs {
   const int32_t* order;  // scheduler output: sequences longest first (packed), or nullptr
   float* seg_ws;         // segment-state area of the workspace (long-chain split), or nullptr
   SegPlan plan;          // the split seg_ws was sized for (nseg 1: none)
+  void* pplan;           // packed batches: the plan area (long-chain split), or nullptr
+  int64_t ns_max;        // packed batches: bound on the split sequences' segments
+  int64_t sms;           // SMs of the device (the planner's cost model)
   // prefix-cache checkpoints (state after every ckpt_interval tokens), or ckpt == nullptr
   float* ckpt;              // [ckpt_rows, H, D, D]
   const int32_t* ckpt_off;  // [N+1] row offsets (packed batches), or nullptr (fixed length)
@@ -201,6 +272,7 @@ __device__ __forceinline__ int64_t ckpt_base(const float* ckpt, const int32_t* o
 }
 
 cudaError_t launch_schedule(const FwdArgs& a, int32_t* order_out);
+cudaError_t launch_plan_packed(const FwdArgs& a);
 cudaError_t launch_prefill_f32(const FwdArgs& a);
 cudaError_t launch_prefill_bf16(const FwdArgs& a);
 

@@ -260,7 +260,16 @@ __device__ __forceinline__ void pack_split16(const float (&x)[16], uint32_t (&hi
 //   SEG_OUTPUT:     per (chain, segment) one CTA from the segment's true start
 //                   state (computed by the scan kernel); writes o, and hT from
 //                   the last segment.
-enum ItemMode { MODE_CHAIN = 0, MODE_SEG_TRANSITION = 1, MODE_SEG_OUTPUT = 2 };
+// The two PSEG modes do the same for packed batches, item by item from the
+// device-written plan (PackedPlan): a CTA past the plan's count leaves at once;
+// an output item of a sequence that is not split runs it whole (as CHAIN).
+enum ItemMode {
+  MODE_CHAIN = 0,
+  MODE_SEG_TRANSITION = 1,
+  MODE_SEG_OUTPUT = 2,
+  MODE_PSEG_TRANSITION = 3,
+  MODE_PSEG_OUTPUT = 4
+};
 
 struct Bf16Params {
   const __nv_bfloat16* beta;
@@ -284,7 +293,9 @@ struct Bf16Params {
   int64_t ckpt_rows;
   int64_t ckpt_interval;
   Preproc pre;           // fused input preprocessing (kPre instantiation only)
-  const __nv_bfloat16* g;  // the scalar gate [tokens, H] (pre.per_head only)
+  const __nv_bfloat16* g;  // the gate: [tokens, H, D], or [tokens, H] with pre.per_head
+  PlanView pv;           // packed long-chain split: the plan (PSEG modes)
+  float* pstates;        // packed long-chain split: segment states (PSEG modes)
 };
 
 // The CTA's bounded waits.  Every thread waits on the barrier itself; a thread
@@ -367,6 +378,39 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     seq_len = len;
     s_in = p.h0 ? p.h0 + (((int64_t)n * p.H + h) * D) * D : nullptr;
     s_out = p.hT ? p.hT + (((int64_t)n * p.H + h) * D) * D : nullptr;
+  } else if (p.mode == MODE_PSEG_TRANSITION || p.mode == MODE_PSEG_OUTPUT) {
+    // (CTA-uniform: the plan was written by an earlier launch on the stream)
+    const bool trans = p.mode == MODE_PSEG_TRANSITION;
+    const int kind = trans ? (item & 1) : 0, rest = trans ? (item >> 1) : item;
+    h = rest % p.H;
+    const int it = rest / p.H;
+    if (it >= (trans ? p.pv.hdr->n_trans : p.pv.hdr->n_out)) return;
+    const PlanItem pi = trans ? p.pv.trans[it] : p.pv.out[it];
+    n = pi.n;
+    p.seqs.get(n, t0, len);
+    seq_len = len;
+    const int nseg = p.pv.nseg[n];
+    if (nseg < 2) {  // an output item of a whole sequence
+      s_in = p.h0 ? p.h0 + (((int64_t)n * p.H + h) * D) * D : nullptr;
+      s_out = p.hT ? p.hT + (((int64_t)n * p.H + h) * D) * D : nullptr;
+    } else {
+      // this chain's states: b (segments 0..nseg-2), M (same), start states (0..nseg-1)
+      float* base = p.pstates +
+                    ((int64_t)p.pv.slot[n] * p.H + (int64_t)h * (3 * nseg - 2)) * D * D;
+      const int64_t sl = p.pv.seglen[n], a0 = (int64_t)pi.seg * sl;
+      if (trans) {
+        ident = zero_v = kind == 1;
+        want_o = false;
+        s_out = base + (int64_t)(kind ? (nseg - 1) + pi.seg : pi.seg) * D * D;
+      } else {
+        s_in = base + (int64_t)(2 * (nseg - 1) + pi.seg) * D * D;
+        if (pi.seg == nseg - 1 && p.hT) s_out = p.hT + (((int64_t)n * p.H + h) * D) * D;
+      }
+      rel0 = a0;
+      t0 += a0;
+      len = len - a0 < sl ? len - a0 : sl;
+      if (len < 0) len = 0;
+    }
   } else {
     int seg, chain;
     if (p.mode == MODE_SEG_TRANSITION) {
@@ -1290,24 +1334,23 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 constexpr int kScanThreads = 256;
 constexpr size_t kScanSmem = 2 * (size_t)D * D * sizeof(float);
 
-__global__ void __launch_bounds__(kScanThreads, 1)
-kda_segment_scan_kernel(const float* __restrict__ h0, const float* __restrict__ seg_m,
-                        const float* __restrict__ seg_b, float* __restrict__ seg_s, int nseg) {
-  extern __shared__ __align__(16) float sc[];
+// One chain's scan: S_0 = h0 (or 0), written to Sp[0]; S_{p+1} = M_p S_p + b_p
+// to Sp[p+1], with M_p = Mp + p D^2, b_p = bp + p D^2, S_p = Sp + p D^2.
+__device__ void scan_chain(const float* __restrict__ h0c, const float* __restrict__ Mp,
+                           const float* __restrict__ bp, float* __restrict__ Sp, int nseg,
+                           float* sc) {
   float* S = sc;            // current start state S_p [D][D]
   float* MT = sc + D * D;   // M_p transposed: MT[k][i] = M_p[i][k]
-  const int tid = threadIdx.x, chain = blockIdx.x;
+  const int tid = threadIdx.x;
   const int i0 = (tid >> 4) * 8, j0 = (tid & 15) * 8;
-  const float* h0c = h0 ? h0 + (int64_t)chain * D * D : nullptr;
-  float* s0 = seg_s + (int64_t)chain * nseg * D * D;  // slot 0: copy of the start state
   for (int x = tid; x < D * D; x += kScanThreads) {
     const float v = h0c ? h0c[x] : 0.f;
     S[x] = v;
-    s0[x] = v;
+    Sp[x] = v;
   }
   for (int sp = 0; sp + 1 < nseg; ++sp) {
-    const float* M = seg_m + ((int64_t)chain * (nseg - 1) + sp) * D * D;
-    const float* b = seg_b + ((int64_t)chain * (nseg - 1) + sp) * D * D;
+    const float* M = Mp + (int64_t)sp * D * D;
+    const float* b = bp + (int64_t)sp * D * D;
     for (int x = tid; x < D * D; x += kScanThreads) MT[(x % D) * D + x / D] = M[x];
     __syncthreads();
     float acc[8][8];
@@ -1329,7 +1372,7 @@ kda_segment_scan_kernel(const float* __restrict__ h0, const float* __restrict__ 
         for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(mv[r], sv[c], acc[r][c]);
     }
     __syncthreads();  // every thread is done reading S and MT
-    float* out = seg_s + ((int64_t)chain * nseg + sp + 1) * D * D;
+    float* out = Sp + (int64_t)(sp + 1) * D * D;
 #pragma unroll
     for (int r = 0; r < 8; ++r)
 #pragma unroll
@@ -1339,6 +1382,31 @@ kda_segment_scan_kernel(const float* __restrict__ h0, const float* __restrict__ 
       }
     __syncthreads();
   }
+}
+
+// Fixed-length batches: one CTA per chain, every chain nseg segments; b for all
+// chains, then M, then the start states (slot 0 a copy of h0).
+__global__ void __launch_bounds__(kScanThreads, 1)
+kda_segment_scan_kernel(const float* __restrict__ h0, const float* __restrict__ seg_m,
+                        const float* __restrict__ seg_b, float* __restrict__ seg_s, int nseg) {
+  extern __shared__ __align__(16) float sc[];
+  const int64_t chain = blockIdx.x;
+  scan_chain(h0 ? h0 + chain * D * D : nullptr, seg_m + chain * (nseg - 1) * D * D,
+             seg_b + chain * (nseg - 1) * D * D, seg_s + chain * nseg * D * D, nseg, sc);
+}
+
+// Packed batches: one CTA per (split sequence, head) of the plan; a CTA past
+// the plan's count leaves at once.
+__global__ void __launch_bounds__(kScanThreads, 1)
+kda_segment_scan_packed_kernel(const float* __restrict__ h0, PlanView pv,
+                               float* __restrict__ states, int H) {
+  extern __shared__ __align__(16) float sc[];
+  const int h = blockIdx.x % H, si = blockIdx.x / H;
+  if (si >= pv.hdr->n_split) return;
+  const int n = pv.split[si], nseg = pv.nseg[n];
+  float* base = states + ((int64_t)pv.slot[n] * H + (int64_t)h * (3 * nseg - 2)) * D * D;
+  scan_chain(h0 ? h0 + ((int64_t)n * H + h) * D * D : nullptr, base + (int64_t)(nseg - 1) * D * D,
+             base, base + (int64_t)2 * (nseg - 1) * D * D, nseg, sc);
 }
 
 // ---------------------------------------------------------------------------
@@ -1413,6 +1481,30 @@ cudaError_t run_bf16(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap&
   cudaError_t e = cudaFuncSetAttribute(kda_prefill_bf16_kernel<kPre>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(kda_segment_scan_kernel,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kScanSmem)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(kda_segment_scan_packed_kernel,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kScanSmem)) != cudaSuccess)
+    return e;
+  if (a.pplan) {
+    // packed batch with the device-written plan: transitions, scan, outputs, each
+    // over a grid bounded by ns_max (surplus CTAs leave at once)
+    p.pv = PlanView::at(a.pplan, a.N, a.ns_max);
+    p.pstates = a.seg_ws;
+    p.mode = MODE_PSEG_TRANSITION;
+    kda_prefill_bf16_kernel<kPre><<<(unsigned)(2 * a.H * a.ns_max), kThreads, SMEM_BYTES,
+                              a.stream>>>(mq, mk, mg, mv, mo, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    kda_segment_scan_packed_kernel<<<(unsigned)(a.H * a.ns_max), kScanThreads, kScanSmem,
+                                     a.stream>>>(a.h0, p.pv, a.seg_ws, a.H);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    p.mode = MODE_PSEG_OUTPUT;
+    kda_prefill_bf16_kernel<kPre><<<(unsigned)(a.H * (a.N + a.ns_max)), kThreads, SMEM_BYTES,
+                              a.stream>>>(mq, mk, mg, mv, mo, p);
+    return cudaGetLastError();
+  }
   const SegPlan pl = a.plan;
   if (pl.nseg < 2 || !a.seg_ws) {
     kda_prefill_bf16_kernel<kPre><<<(unsigned)items, kThreads, SMEM_BYTES, a.stream>>>(
@@ -1431,10 +1523,6 @@ cudaError_t run_bf16(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap&
   kda_prefill_bf16_kernel<kPre><<<(unsigned)(items * (pl.nseg - 1) * 2), kThreads, SMEM_BYTES,
                             a.stream>>>(mq, mk, mg, mv, mo, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if ((e = cudaFuncSetAttribute(kda_segment_scan_kernel,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)kScanSmem)) != cudaSuccess)
-    return e;
   kda_segment_scan_kernel<<<(unsigned)items, kScanThreads, kScanSmem, a.stream>>>(
       a.h0, p.seg_m, p.seg_b, seg_s, pl.nseg);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -1484,6 +1572,8 @@ cudaError_t launch_prefill_bf16(const FwdArgs& a) {
   p.ckpt_interval = a.ckpt_interval > 0 ? a.ckpt_interval : 1;
   p.pre = a.pre;
   p.g = static_cast<const __nv_bfloat16*>(a.g);
+  p.pv = PlanView{};
+  p.pstates = nullptr;
   if (a.pre.l2 || a.pre.gate || a.pre.beta || a.pre.per_head) return run_bf16<true>(a, mq, mk, mg, mv, mo, p, items);
   return run_bf16<false>(a, mq, mk, mg, mv, mo, p, items);
 }

@@ -9,6 +9,10 @@
 // A malformed cu_seqlens (cu[0] != 0, decreasing, or cu[N] != T) latches
 // KDA_ERR_BAD_SEQLENS in the status word; the prefill kernels then skip all
 // work, so no out-of-range token is ever read.
+//
+// For bf16 batches long enough, a planner then cuts the longest sequences into
+// segments joined through their affine state maps (the long-chain split of
+// fixed-length batches, applied per sequence): kda_plan_packed_split.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -42,7 +46,156 @@ __global__ void kda_order_by_length(const int32_t* __restrict__ cu, int N,
   order[rank] = n;
 }
 
+// Block-wide reductions of the planner (kPlanThreads threads).
+constexpr int kPlanThreads = 256;
+__device__ __forceinline__ int64_t block_sum(int64_t x, int64_t* sh) {
+  sh[threadIdx.x] = x;
+  __syncthreads();
+  for (int o = kPlanThreads / 2; o > 0; o >>= 1) {
+    if ((int)threadIdx.x < o) sh[threadIdx.x] += sh[threadIdx.x + o];
+    __syncthreads();
+  }
+  const int64_t r = sh[0];
+  __syncthreads();
+  return r;
+}
+__device__ __forceinline__ int64_t block_max(int64_t x, int64_t* sh) {
+  sh[threadIdx.x] = x;
+  __syncthreads();
+  for (int o = kPlanThreads / 2; o > 0; o >>= 1) {
+    if ((int)threadIdx.x < o && sh[threadIdx.x + o] > sh[threadIdx.x])
+      sh[threadIdx.x] = sh[threadIdx.x + o];
+    __syncthreads();
+  }
+  const int64_t r = sh[0];
+  __syncthreads();
+  return r;
+}
+// makespan estimate of one pass (chunk-steps): total work W, longest item L
+__device__ __forceinline__ double pass_cost(int64_t W, int64_t L, int64_t sms) {
+  const double lpt = (double)W / (double)sms + 0.5 * (double)L;
+  return lpt > (double)L ? lpt : (double)L;
+}
+__device__ __forceinline__ int64_t seq_chunks(const int32_t* cu, int n) {
+  return ((int64_t)cu[n + 1] - cu[n] + 63) / 64;
+}
+
+// The long-chain split plan of a packed batch (see PackedPlan).  One CTA.
+// `order` holds the sequences longest first (kda_order_by_length).
+__global__ void __launch_bounds__(kPlanThreads)
+kda_plan_packed_split(const int32_t* __restrict__ cu, const int32_t* __restrict__ order, int N,
+                      int H, int64_t sms, int64_t ns_max, void* plan_base,
+                      unsigned int* __restrict__ status) {
+  __shared__ int64_t sh[kPlanThreads];
+  const int tid = threadIdx.x;
+  PlanView pv = PlanView::at(plan_base, N, ns_max);
+  if (status && *(volatile const unsigned int*)status == (unsigned)KDA_ERR_BAD_SEQLENS) {
+    if (tid == 0) *pv.hdr = PackedPlan{0, 0, 0, 0};  // every pass leaves at once
+    return;
+  }
+  int64_t mc = 0, w = 0;
+  for (int n = tid; n < N; n += kPlanThreads) {
+    const int64_t c = seq_chunks(cu, n);
+    mc = c > mc ? c : mc;
+    w += c;
+  }
+  const int64_t maxc = block_max(mc, sh), W0 = block_sum(w, sh) * H;
+  const double cost0 = pass_cost(W0, maxc, sms);
+  // candidate segment lengths 64, 80, 96, 128, 160, 192, ... while 2 S <= maxc
+  double best = 0.9 * cost0;
+  int64_t bestS = 0;
+  for (int i = 0;; ++i) {
+    const int64_t S = (int64_t)(64 + 16 * (i % 3)) << (i / 3);
+    if (2 * S > maxc) break;
+    int64_t w1 = 0, l1 = 0, w2 = 0, l2 = 0, nsm = 0, tot = 0;
+    for (int n = tid; n < N; n += kPlanThreads) {
+      const int64_t c = seq_chunks(cu, n);
+      if (c >= 2 * S) {
+        int64_t ns = c / S;
+        ns = ns < kSegMaxSegs ? ns : kSegMaxSegs;
+        const int64_t sl = (c + ns - 1) / ns;
+        w1 += 2 * (ns - 1) * sl;
+        w2 += ns * sl;
+        l1 = sl > l1 ? sl : l1;
+        l2 = sl > l2 ? sl : l2;
+        nsm = ns > nsm ? ns : nsm;
+        tot += ns;
+      } else {
+        w2 += c;
+        l2 = c > l2 ? c : l2;
+      }
+    }
+    w1 = block_sum(w1, sh) * H;
+    w2 = block_sum(w2, sh) * H;
+    tot = block_sum(tot, sh);
+    l1 = block_max(l1, sh);
+    l2 = block_max(l2, sh);
+    nsm = block_max(nsm, sh);
+    const double c = pass_cost(w1, l1, sms) + 0.5 * (double)nsm + pass_cost(w2, l2, sms);
+    if (tot <= ns_max && c < best) {  // (uniform across the CTA: reduced values)
+      best = c;
+      bestS = S;
+    }
+  }
+  // per-sequence segments; thread 0 then builds the tables (few split sequences)
+  for (int n = tid; n < N; n += kPlanThreads) {
+    const int64_t c = seq_chunks(cu, n);
+    int64_t ns = 1, sl = 0;
+    if (bestS > 0 && c >= 2 * bestS) {
+      ns = c / bestS;
+      ns = ns < kSegMaxSegs ? ns : kSegMaxSegs;
+      sl = (c + ns - 1) / ns;
+    }
+    pv.nseg[n] = (int32_t)ns;
+    pv.seglen[n] = (int32_t)(sl * 64);
+  }
+  __syncthreads();
+  if (tid != 0) return;
+  // split sequences in order of decreasing segment length (insertion into the
+  // split list; the sequences arrive longest first)
+  int32_t n_split = 0, n_trans = 0, n_out = 0, slot = 0;
+  for (int r = 0; r < N; ++r) {
+    const int32_t n = order[r];
+    if (pv.nseg[n] < 2) continue;
+    int32_t j = n_split++;
+    while (j > 0 && pv.seglen[pv.split[j - 1]] < pv.seglen[n]) {
+      pv.split[j] = pv.split[j - 1];
+      --j;
+    }
+    pv.split[j] = n;
+  }
+  for (int i = 0; i < n_split; ++i) {
+    const int32_t n = pv.split[i];
+    pv.slot[n] = slot;
+    slot += 3 * pv.nseg[n] - 2;
+    for (int32_t sg = 0; sg + 1 < pv.nseg[n]; ++sg) pv.trans[n_trans++] = PlanItem{n, sg};
+  }
+  // outputs longest first: merge the split sequences' segments with the whole
+  // sequences (both lists already in decreasing length)
+  int i = 0, r = 0;
+  while (true) {
+    while (r < N && pv.nseg[order[r]] >= 2) ++r;  // split ones come from the other list
+    const bool has_seg = i < n_split, has_seq = r < N;
+    if (!has_seg && !has_seq) break;
+    const int64_t lseg = has_seg ? pv.seglen[pv.split[i]] : -1;
+    const int64_t lseq = has_seq ? (int64_t)cu[order[r] + 1] - cu[order[r]] : -1;
+    if (has_seg && lseg >= lseq) {
+      const int32_t n = pv.split[i++];
+      for (int32_t sg = 0; sg < pv.nseg[n]; ++sg) pv.out[n_out++] = PlanItem{n, sg};
+    } else {
+      pv.out[n_out++] = PlanItem{order[r++], 0};
+    }
+  }
+  *pv.hdr = PackedPlan{n_trans, n_split, n_out, (int32_t)bestS};
+}
+
 }  // namespace
+
+cudaError_t launch_plan_packed(const FwdArgs& a) {
+  kda_plan_packed_split<<<1, kPlanThreads, 0, a.stream>>>(a.cu, a.order, a.N, a.H, a.sms,
+                                                          a.ns_max, a.pplan, a.status);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_schedule(const FwdArgs& a, int32_t* order_out) {
   const int N = a.N;

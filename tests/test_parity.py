@@ -559,3 +559,79 @@ def test_sharded_batch_equals_unsharded(kda, by):
     else:
         o, h = torch.cat(outs, dim=2), torch.cat(states, dim=1)
     assert torch.equal(o, o_ref) and torch.equal(h, h_ref)
+
+
+# long sequences inside packed batches: the device-planned segment split ------------
+
+def _packed_plan(ws, N):
+    """The plan the device wrote into the workspace after the order list:
+    (transition items, split sequences, output items, segment length in chunks)."""
+    at = 256 + (N + 63) // 64 * 256
+    return ws[at:at + 16].view(torch.int32).tolist()
+
+
+def test_packed_long_chain_split(kda, oracle_mod):
+    """[2^18, 300, 1, 5000] tokens, H=2: the planner cuts the 4096-chunk sequence
+    into 64 segments of 64 chunks and leaves the others whole; the split run and
+    a run without the split (minimum workspace) both match the oracle."""
+    lens = [1 << 18, 300, 1, 5000]
+    x = kda_inputs.packed(lens, 2, 128, dtype=torch.bfloat16, device=DEV, seed=960, h0_std=0.1)
+    shape = kda.make_shape(x.q, x.v, packed_seqs=4)
+    ws = kda.new_workspace(shape, DEV)
+    o, hT = kda.fwd(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens, h0=x.h0, workspace=ws)
+    assert kda.read_device_status(ws) == kda.KDA_OK
+    assert _packed_plan(ws, 4) == [63, 1, 64 + 3, 64]
+    small = torch.empty(512, dtype=torch.uint8, device=DEV)
+    o_u, h_u = kda.fwd(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens, h0=x.h0,
+                       workspace=small)
+    torch.cuda.synchronize()
+    o_ref, h_ref = oracle_mod.recurrent(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens,
+                                        h0=x.h0)
+    for oo, hh in ((o, hT), (o_u, h_u)):
+        assert rel_err(oo, o_ref) <= TOL_BF16
+        assert rel_err(hh, h_ref) <= TOL_BF16
+
+
+def test_packed_split_mixed_with_checkpoints(kda, oracle_mod):
+    """Two split sequences of different segment lengths, an empty and short ones,
+    strong gates inside a split sequence (token path in the transition passes),
+    checkpoints every 512 tokens at positions relative to each sequence."""
+    lens = [20000, 0, 9000, 64, 129]
+    x = kda_inputs.packed(lens, 2, 128, dtype=torch.bfloat16, device=DEV, seed=970, h0_std=0.1)
+    g = x.g.clone()
+    g[:, 7000:7100, :, 5:9] = -25.0
+    g[:, 12345, :, 3] = float("-inf")
+    x.g = g
+    shape = kda.make_shape(x.q, x.v, packed_seqs=5)
+    ws = kda.new_workspace(shape, DEV)
+    o, hT, ck, off = kda.fwd_checkpoints(x.q, x.k, x.v, x.g, x.beta, interval=512,
+                                         cu_seqlens=x.cu_seqlens, h0=x.h0, workspace=ws)
+    torch.cuda.synchronize()
+    n_trans, n_split, n_out, S = _packed_plan(ws, 5)
+    assert n_split == 2 and S >= 64
+    starts = [sum(lens[:i]) for i in range(len(lens))]
+    refs = _ckpt_refs(oracle_mod, x, [(0, starts[i], lens[i], i) for i in range(len(lens))], 512)
+    _check_ckpts(ck, refs, TOL_BF16)
+    o_ref, h_ref = oracle_mod.recurrent(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens,
+                                        h0=x.h0)
+    assert rel_err(o, o_ref) <= TOL_BF16
+    assert rel_err(hT, h_ref) <= TOL_BF16
+
+
+def test_packed_split_fused_preprocessing(kda, oracle_mod):
+    """The packed split under the fused preprocessing (raw q, k, gate and beta)."""
+    lens = [40000, 300]
+    cu = torch.tensor([0, 40000, 40300], dtype=torch.int32)
+    x = kda_inputs.draw_raw((1, 40300), 2, 128, 128, device=DEV, seed=980, num_states=2,
+                            h0_std=0.1)
+    x.cu_seqlens = cu.to(DEV)
+    shape = kda.make_shape(x.q, x.v, packed_seqs=2)
+    ws = kda.new_workspace(shape, DEV)
+    o, hT = kda.fwd_preproc(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens, h0=x.h0,
+                            workspace=ws)
+    torch.cuda.synchronize()
+    assert _packed_plan(ws, 2)[1] == 1
+    fq, fk, fg, fb = oracle_mod.preprocess(x.q, x.k, x.g, x.beta)
+    o_ref, h_ref = oracle_mod.recurrent(fq, fk, x.v, fg, fb, cu_seqlens=x.cu_seqlens, h0=x.h0)
+    assert rel_err(o, o_ref) <= TOL_BF16
+    assert rel_err(hT, h_ref) <= TOL_BF16
