@@ -142,7 +142,9 @@ kda_status fwd_common(const kda_shape* s, const void* q, const void* k, const vo
   a.ckpt_interval = ckpt_interval;
   a.pre = to_preproc(pre);
   a.stream = static_cast<cudaStream_t>(stream);
+  a.sms = device_sms();
 
+  // the status word and the kernels' work counters start at zero
   if (cudaMemsetAsync(workspace, 0, kWsHeader, a.stream) != cudaSuccess) return KDA_ERR_CUDA;
   if (packed) {
     char* w = static_cast<char*>(workspace);
@@ -160,7 +162,6 @@ kda_status fwd_common(const kda_shape* s, const void* q, const void* k, const vo
         a.pplan = w + at;
         a.ns_max = nsx;
         a.seg_ws = reinterpret_cast<float*>(w + at + plan);
-        a.sms = device_sms();
         if (launch_plan_packed(a) != cudaSuccess) return KDA_ERR_CUDA;
       }
     }

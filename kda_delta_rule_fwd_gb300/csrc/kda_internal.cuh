@@ -66,7 +66,8 @@ struct SeqView {
 };
 
 // Workspace layout (bytes):
-//   [0, 256)            status word and counters
+//   [0, 256)            status word (bytes 0-3) and the prefill launches' work
+//                       counters (bytes 64-83), zeroed by every call
 //   [256, 256 + 4*Npad) sequence order for the packed-batch scheduler
 constexpr size_t kWsHeader = 256;
 inline size_t ws_order_bytes(int64_t n) { return (size_t)((n + 63) / 64) * 64 * 4; }

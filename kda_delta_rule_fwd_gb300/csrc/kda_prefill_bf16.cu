@@ -80,6 +80,7 @@ constexpr uint32_t SM_LL = 196608;       // [L; L] 128 x 64 bf16 (lower-triangul
 constexpr uint32_t SM_MISC = 212992;
 constexpr uint32_t MISC_RHO = 0, MISC_GL = 512, MISC_C = 1024, MISC_GAMC = 2048,
                    MISC_BETA = 2560, MISC_BAR = 2816, MISC_TMEM = 2848, MISC_FLAG = 2852;
+// (MISC_FLAG + 4: the current work item, broadcast by thread 0)
 constexpr uint32_t SM_NEGI = 216064;     // -I (64 x 64 bf16, K-major): adds -V^T on the tensor core
 constexpr uint32_t SM_GA = SM_NEGI + 8192;  // g tile, tokens 0..31 (the two halves are
                                              // loaded a chunk ahead, outside the scratch)
@@ -279,9 +280,10 @@ struct Bf16Params {
   void* out;
   float* hT;
   int H;
+  int nchains;           // (sequence, head) chains of the batch
   float scale;
   int out_bf16;
-  unsigned int* status;
+  unsigned int* status;  // status word; words 16 + mode count each launch's taken items
   int mode;
   int nseg;
   int64_t seg_len;       // tokens per segment (multiple of the chunk length)
@@ -363,82 +365,97 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     return;
   }
 
-  const int item = blockIdx.x;
-  int n, h;
-  int64_t t0, len;
+  // The current work item: (sequence, head) chain, or a segment of one.
+  int n = 0, h = 0;
+  int64_t t0 = 0, len = 0;
   int64_t rel0 = 0, seq_len = 0;  // start of this item within its sequence; sequence length
   // start state (nullptr = zeros), identity start, end-state destination, flags
   const float* s_in = nullptr;
   float* s_out = nullptr;
   bool ident = false, zero_v = false, want_o = true;
-  if (p.mode == MODE_CHAIN) {
-    n = p.order ? p.order[item / p.H] : item / p.H;
-    h = item % p.H;
-    p.seqs.get(n, t0, len);
-    seq_len = len;
-    s_in = p.h0 ? p.h0 + (((int64_t)n * p.H + h) * D) * D : nullptr;
-    s_out = p.hT ? p.hT + (((int64_t)n * p.H + h) * D) * D : nullptr;
-  } else if (p.mode == MODE_PSEG_TRANSITION || p.mode == MODE_PSEG_OUTPUT) {
-    // (CTA-uniform: the plan was written by an earlier launch on the stream)
-    const bool trans = p.mode == MODE_PSEG_TRANSITION;
-    const int kind = trans ? (item & 1) : 0, rest = trans ? (item >> 1) : item;
-    h = rest % p.H;
-    const int it = rest / p.H;
-    if (it >= (trans ? p.pv.hdr->n_trans : p.pv.hdr->n_out)) return;
-    const PlanItem pi = trans ? p.pv.trans[it] : p.pv.out[it];
-    n = pi.n;
-    p.seqs.get(n, t0, len);
-    seq_len = len;
-    const int nseg = p.pv.nseg[n];
-    if (nseg < 2) {  // an output item of a whole sequence
+  // Work items of this launch, and decoding of one (all threads, same item)
+  const int64_t n_items =
+      p.mode == MODE_CHAIN ? (int64_t)p.nchains
+      : p.mode == MODE_SEG_TRANSITION ? (int64_t)p.nchains * (p.nseg - 1) * 2
+      : p.mode == MODE_SEG_OUTPUT ? (int64_t)p.nchains * p.nseg
+      : p.mode == MODE_PSEG_TRANSITION ? 2 * (int64_t)p.H * p.pv.hdr->n_trans
+                                       : (int64_t)p.H * p.pv.hdr->n_out;
+  auto decode_item = [&](int item) {
+    rel0 = 0;
+    s_in = nullptr;
+    s_out = nullptr;
+    ident = zero_v = false;
+    want_o = true;
+    if (p.mode == MODE_CHAIN) {
+      n = p.order ? p.order[item / p.H] : item / p.H;
+      h = item % p.H;
+      p.seqs.get(n, t0, len);
+      seq_len = len;
       s_in = p.h0 ? p.h0 + (((int64_t)n * p.H + h) * D) * D : nullptr;
       s_out = p.hT ? p.hT + (((int64_t)n * p.H + h) * D) * D : nullptr;
+    } else if (p.mode == MODE_PSEG_TRANSITION || p.mode == MODE_PSEG_OUTPUT) {
+      const bool trans = p.mode == MODE_PSEG_TRANSITION;
+      const int kind = trans ? (item & 1) : 0, rest = trans ? (item >> 1) : item;
+      h = rest % p.H;
+      const int it = rest / p.H;
+      const PlanItem pi = trans ? p.pv.trans[it] : p.pv.out[it];
+      n = pi.n;
+      p.seqs.get(n, t0, len);
+      seq_len = len;
+      const int nseg = p.pv.nseg[n];
+      if (nseg < 2) {  // an output item of a whole sequence
+        s_in = p.h0 ? p.h0 + (((int64_t)n * p.H + h) * D) * D : nullptr;
+        s_out = p.hT ? p.hT + (((int64_t)n * p.H + h) * D) * D : nullptr;
+      } else {
+        // this chain's states: b (segments 0..nseg-2), M (same), start states (0..nseg-1)
+        float* base = p.pstates +
+                      ((int64_t)p.pv.slot[n] * p.H + (int64_t)h * (3 * nseg - 2)) * D * D;
+        const int64_t sl = p.pv.seglen[n], a0 = (int64_t)pi.seg * sl;
+        if (trans) {
+          ident = zero_v = kind == 1;
+          want_o = false;
+          s_out = base + (int64_t)(kind ? (nseg - 1) + pi.seg : pi.seg) * D * D;
+        } else {
+          s_in = base + (int64_t)(2 * (nseg - 1) + pi.seg) * D * D;
+          if (pi.seg == nseg - 1 && p.hT) s_out = p.hT + (((int64_t)n * p.H + h) * D) * D;
+        }
+        rel0 = a0;
+        t0 += a0;
+        len = len - a0 < sl ? len - a0 : sl;
+        if (len < 0) len = 0;
+      }
     } else {
-      // this chain's states: b (segments 0..nseg-2), M (same), start states (0..nseg-1)
-      float* base = p.pstates +
-                    ((int64_t)p.pv.slot[n] * p.H + (int64_t)h * (3 * nseg - 2)) * D * D;
-      const int64_t sl = p.pv.seglen[n], a0 = (int64_t)pi.seg * sl;
-      if (trans) {
+      int seg, chain;
+      if (p.mode == MODE_SEG_TRANSITION) {
+        const int kind = item & 1, rest = item >> 1;
+        seg = rest % (p.nseg - 1);
+        chain = rest / (p.nseg - 1);
         ident = zero_v = kind == 1;
         want_o = false;
-        s_out = base + (int64_t)(kind ? (nseg - 1) + pi.seg : pi.seg) * D * D;
+        s_out = (kind ? p.seg_m : p.seg_b) + ((int64_t)chain * (p.nseg - 1) + seg) * D * D;
       } else {
-        s_in = base + (int64_t)(2 * (nseg - 1) + pi.seg) * D * D;
-        if (pi.seg == nseg - 1 && p.hT) s_out = p.hT + (((int64_t)n * p.H + h) * D) * D;
+        seg = item % p.nseg;
+        chain = item / p.nseg;
+        // every segment, the first included, starts from the scan's copy: hT may
+        // alias h0 and the last segment's CTA writes hT while others still run
+        s_in = p.seg_s + ((int64_t)chain * p.nseg + seg) * D * D;
+        if (seg == p.nseg - 1 && p.hT) s_out = p.hT + (int64_t)chain * D * D;
       }
-      rel0 = a0;
-      t0 += a0;
-      len = len - a0 < sl ? len - a0 : sl;
+      n = chain / p.H;
+      h = chain % p.H;
+      int64_t st, ln;
+      p.seqs.get(n, st, ln);
+      const int64_t a = (int64_t)seg * p.seg_len;
+      rel0 = a;
+      seq_len = ln;
+      t0 = st + a;
+      len = ln - a < p.seg_len ? ln - a : p.seg_len;
       if (len < 0) len = 0;
     }
-  } else {
-    int seg, chain;
-    if (p.mode == MODE_SEG_TRANSITION) {
-      const int kind = item & 1, rest = item >> 1;
-      seg = rest % (p.nseg - 1);
-      chain = rest / (p.nseg - 1);
-      ident = zero_v = kind == 1;
-      want_o = false;
-      s_out = (kind ? p.seg_m : p.seg_b) + ((int64_t)chain * (p.nseg - 1) + seg) * D * D;
-    } else {
-      seg = item % p.nseg;
-      chain = item / p.nseg;
-      // every segment, the first included, starts from the scan's copy: hT may
-      // alias h0 and the last segment's CTA writes hT while others still run
-      s_in = p.seg_s + ((int64_t)chain * p.nseg + seg) * D * D;
-      if (seg == p.nseg - 1 && p.hT) s_out = p.hT + (int64_t)chain * D * D;
-    }
-    n = chain / p.H;
-    h = chain % p.H;
-    int64_t st, ln;
-    p.seqs.get(n, st, ln);
-    const int64_t a = (int64_t)seg * p.seg_len;
-    rel0 = a;
-    seq_len = ln;
-    t0 = st + a;
-    len = ln - a < p.seg_len ? ln - a : p.seg_len;
-    if (len < 0) len = 0;
-  }
+  };
+  // nothing to do for this launch (a surplus pass of the packed split): leave
+  // before any setup (CTA-uniform: the plan was written by an earlier launch)
+  if ((int64_t)blockIdx.x >= n_items) return;
 
   if (tid == 0) {
     mbar_init(&bars[0], 1);
@@ -481,7 +498,26 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   const uint32_t tb = *s_tmem;
   const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
   Waits wt{&bars[0], &bars[1], 0u, 0u, s_flag, p.status};
+  // Phase bookkeeping of the CTA's barriers carries over from item to item:
+  // within an item every copy and product issued is also waited for.
   uint32_t tma_issued = 0;
+  uint64_t* g_bar = &bars[3];
+  uint32_t g_issued = 0, g_waited = 0;  // g_waited: thread 0's count
+  uint64_t* xo_bar = &bars[2];          // completion of the products with S'
+  uint32_t xo_issued = 0;
+  uint32_t* s_item = s_flag + 1;
+  unsigned int* next_item = p.status + 16 + p.mode;  // zeroed with the status word
+
+  // Persistent loop: the CTA takes items from the launch's counter, in order
+  // (longest first where the items have different lengths), until none is left.
+#pragma unroll 1
+  for (;;) {
+  if (tid == 0) *s_item = atomicAdd(next_item, 1u);
+  __syncthreads();
+  const int64_t item = *(volatile uint32_t*)s_item;
+  __syncthreads();  // every thread has read it before thread 0 may fetch again
+  if (item >= n_items) break;
+  decode_item((int)item);
 
   const int nchunks = (int)((len + C - 1) / C);
   // one of the four tiles of a chunk (part 0 also arms the barrier); the four
@@ -492,8 +528,6 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   // in buffers of their own: the next chunk's tile is loaded as soon as this
   // chunk's cumulative sum has read the previous one (a chunk ahead of the q, k
   // and v tiles, which share their buffers with the substitution scratch).
-  uint64_t* g_bar = &bars[3];
-  uint32_t g_issued = 0, g_waited = 0;  // g_waited: thread 0's count
   // parts 0-3: the 64-channel halves of q and k (128-byte rows); 4: v
   auto issue_tma_part = [&](int chunk, int part) {
     const int32_t y = (int32_t)(t0 + (int64_t)chunk * C);
@@ -514,6 +548,8 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (half == 0) mbar_arrive_expect_tx(g_bar, 16384);
     tma_load_3d(smem + (half ? SM_GB : SM_GA), &tm_g, 0, y, h * (D / 8), g_bar);
   };
+  // the g barrier's phase of this item's chunk c is g_base + c
+  const uint32_t g_base = g_issued;
   if (tid == 0 && nchunks > 0) {
     for (int part = 0; part < 5; ++part) issue_tma_part(0, part);
     if (g_tma) {
@@ -562,8 +598,6 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   const uint32_t idesc_sq = idesc_bf16(128, 64, 0, 0);
   const uint32_t idesc_s = idesc_bf16(128, 128, 0, 1);
   const uint32_t sbase = smem_u32(smem);
-  uint64_t* xo_bar = &bars[2];  // completion of the products with S'
-  uint32_t xo_issued = 0;
   // prefix-cache checkpoints of this chain (output items only)
   const int64_t ck_base =
       want_o ? ckpt_base(p.ckpt, p.ckpt_off, p.ckpt_rows, p.ckpt_interval, n, seq_len, p.status,
@@ -576,7 +610,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   // first half, 2, 3 on the second), committed to mma_bar; returns false if the
   // wait ran out
   auto issue_cumsum = [&](int chunk) -> bool {
-    const bool ok = !g_tma || mbar_wait(g_bar, (uint32_t)chunk & 1u);
+    const bool ok = !g_tma || mbar_wait(g_bar, (g_base + (uint32_t)chunk) & 1u);
     if (g_tma) ++g_waited;
     if (!ok) return false;
     tc_fence_after();
@@ -597,7 +631,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   // a CTA barrier).
   constexpr int kHalfRows = (D / 8) * (C / 2);
   auto activate_gate = [&](int chunk, int i, int end, int nthr) {
-    if (g_tma && !mbar_wait(g_bar, (uint32_t)chunk & 1u)) wt.on_timeout();
+    if (g_tma && !mbar_wait(g_bar, (g_base + (uint32_t)chunk) & 1u)) wt.on_timeout();
     for (; i < end; i += nthr) {
       uint8_t* r = smem + (i < kHalfRows ? SM_GA + i * 16 : SM_GB + (i - kHalfRows) * 16);
       float x[8];
@@ -823,7 +857,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   };
   if (kPre && nchunks > 0 && (g_fill || p.pre.l2)) {
     if (g_fill) activate_gate(0, tid, 2 * kHalfRows, kThreads);
-    if (p.pre.l2 && warp >= 12) qk_sumsq(0);
+    if (p.pre.l2 && warp >= 12) qk_sumsq(tma_issued - 1);  // chunk 0's tiles
     fence_proxy_async_smem();
     __syncthreads();
   }
@@ -1296,7 +1330,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
   }
 
-  if (tid == 0) bulk_wait_all();  // outputs complete before shared memory is released
+  if (tid == 0) bulk_wait_all();  // this item's outputs are complete
   const bool aborted = *(volatile uint32_t*)s_flag != 0;
   if (!aborted && s_out) {
     const int j = row;
@@ -1321,6 +1355,8 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   }
   tc_fence_before();
   __syncthreads();
+  if (aborted) break;
+  }  // items
   if (warp == 0) tmem_dealloc(tb, TM_COLS);
 }
 
@@ -1401,12 +1437,16 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 kda_segment_scan_packed_kernel(const float* __restrict__ h0, PlanView pv,
                                float* __restrict__ states, int H) {
   extern __shared__ __align__(16) float sc[];
-  const int h = blockIdx.x % H, si = blockIdx.x / H;
-  if (si >= pv.hdr->n_split) return;
-  const int n = pv.split[si], nseg = pv.nseg[n];
-  float* base = states + ((int64_t)pv.slot[n] * H + (int64_t)h * (3 * nseg - 2)) * D * D;
-  scan_chain(h0 ? h0 + ((int64_t)n * H + h) * D * D : nullptr, base + (int64_t)(nseg - 1) * D * D,
-             base, base + (int64_t)2 * (nseg - 1) * D * D, nseg, sc);
+  const int chains = pv.hdr->n_split * H;
+  for (int c = blockIdx.x; c < chains; c += gridDim.x) {
+    const int h = c % H, si = c / H;
+    const int n = pv.split[si], nseg = pv.nseg[n];
+    float* base = states + ((int64_t)pv.slot[n] * H + (int64_t)h * (3 * nseg - 2)) * D * D;
+    scan_chain(h0 ? h0 + ((int64_t)n * H + h) * D * D : nullptr,
+               base + (int64_t)(nseg - 1) * D * D, base, base + (int64_t)2 * (nseg - 1) * D * D,
+               nseg, sc);
+    __syncthreads();  // shared memory is reused by the next chain
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1488,26 +1528,30 @@ cudaError_t run_bf16(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap&
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)kScanSmem)) != cudaSuccess)
     return e;
+  // Persistent CTAs, one per SM at most: each takes work items from its launch's
+  // counter until none is left.
+  const int64_t sms = a.sms > 0 ? a.sms : kGb300Sms;
+  auto grid = [&](int64_t work) { return (unsigned)(work < sms ? work : sms); };
   if (a.pplan) {
-    // packed batch with the device-written plan: transitions, scan, outputs, each
-    // over a grid bounded by ns_max (surplus CTAs leave at once)
+    // packed batch with the device-written plan: transitions, scan, outputs (the
+    // counts are on the device; a launch with nothing to do leaves at once)
     p.pv = PlanView::at(a.pplan, a.N, a.ns_max);
     p.pstates = a.seg_ws;
     p.mode = MODE_PSEG_TRANSITION;
-    kda_prefill_bf16_kernel<kPre><<<(unsigned)(2 * a.H * a.ns_max), kThreads, SMEM_BYTES,
-                              a.stream>>>(mq, mk, mg, mv, mo, p);
+    kda_prefill_bf16_kernel<kPre><<<grid(2 * a.H * a.ns_max), kThreads, SMEM_BYTES, a.stream>>>(
+        mq, mk, mg, mv, mo, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    kda_segment_scan_packed_kernel<<<(unsigned)(a.H * a.ns_max), kScanThreads, kScanSmem,
-                                     a.stream>>>(a.h0, p.pv, a.seg_ws, a.H);
+    kda_segment_scan_packed_kernel<<<grid(a.H * a.ns_max), kScanThreads, kScanSmem, a.stream>>>(
+        a.h0, p.pv, a.seg_ws, a.H);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     p.mode = MODE_PSEG_OUTPUT;
-    kda_prefill_bf16_kernel<kPre><<<(unsigned)(a.H * (a.N + a.ns_max)), kThreads, SMEM_BYTES,
+    kda_prefill_bf16_kernel<kPre><<<grid(a.H * (a.N + a.ns_max)), kThreads, SMEM_BYTES,
                               a.stream>>>(mq, mk, mg, mv, mo, p);
     return cudaGetLastError();
   }
   const SegPlan pl = a.plan;
   if (pl.nseg < 2 || !a.seg_ws) {
-    kda_prefill_bf16_kernel<kPre><<<(unsigned)items, kThreads, SMEM_BYTES, a.stream>>>(
+    kda_prefill_bf16_kernel<kPre><<<grid(items), kThreads, SMEM_BYTES, a.stream>>>(
         mq, mk, mg, mv, mo, p);
     return cudaGetLastError();
   }
@@ -1520,14 +1564,14 @@ cudaError_t run_bf16(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap&
   float* seg_s = a.seg_ws + 2 * items * (pl.nseg - 1) * per;
   p.seg_s = seg_s;
   p.mode = MODE_SEG_TRANSITION;
-  kda_prefill_bf16_kernel<kPre><<<(unsigned)(items * (pl.nseg - 1) * 2), kThreads, SMEM_BYTES,
+  kda_prefill_bf16_kernel<kPre><<<grid(items * (pl.nseg - 1) * 2), kThreads, SMEM_BYTES,
                             a.stream>>>(mq, mk, mg, mv, mo, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   kda_segment_scan_kernel<<<(unsigned)items, kScanThreads, kScanSmem, a.stream>>>(
       a.h0, p.seg_m, p.seg_b, seg_s, pl.nseg);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   p.mode = MODE_SEG_OUTPUT;
-  kda_prefill_bf16_kernel<kPre><<<(unsigned)(items * pl.nseg), kThreads, SMEM_BYTES, a.stream>>>(
+  kda_prefill_bf16_kernel<kPre><<<grid(items * pl.nseg), kThreads, SMEM_BYTES, a.stream>>>(
       mq, mk, mg, mv, mo, p);
   return cudaGetLastError();
 }
@@ -1558,6 +1602,7 @@ cudaError_t launch_prefill_bf16(const FwdArgs& a) {
   p.out = a.out;
   p.hT = a.hT;
   p.H = a.H;
+  p.nchains = (int)items;
   p.scale = a.scale;
   p.out_bf16 = a.out_dtype == KDA_BF16;
   p.status = a.status;

@@ -234,6 +234,26 @@ def test_prefill_gate_scale_8(kda, oracle_mod, dtype, d, per_head):
     assert rel_err(hT, h_ref) <= TOL[dtype]
 
 
+@pytest.mark.parametrize("per_head", [False, True], ids=["per-channel", "per-head"])
+def test_prefill_more_chains_than_sms(kda, oracle_mod, per_head):
+    """320 (sequence, head) chains of mixed lengths: the persistent CTAs each take
+    several chains in turn, with the gate activation and the norms fused."""
+    gen = torch.Generator().manual_seed(660)
+    lens = torch.randint(1, 200, (40,), generator=gen).tolist()
+    x = _raw_packed(lens, 8, 128, torch.bfloat16, seed=661)
+    if per_head:
+        x.g = x.g[..., 0].contiguous()
+    a = _gate_scale(8, 662)
+    o, hT = kda.fwd_preproc(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens, h0=x.h0,
+                            gate_per_head=per_head, gate_scale=a)
+    torch.cuda.synchronize()
+    fq, fk, fg, fb = oracle_mod.preprocess(x.q, x.k, x.g, x.beta, gate_per_head=per_head,
+                                           gate_scale=a)
+    o_ref, h_ref = oracle_mod.recurrent(fq, fk, x.v, fg, fb, cu_seqlens=x.cu_seqlens, h0=x.h0)
+    assert rel_err(o, o_ref) <= TOL_BF16
+    assert rel_err(hT, h_ref) <= TOL_BF16
+
+
 def test_decode_gate_scale_8(kda, oracle_mod):
     x = kda_inputs.draw_raw((5, 8), 3, 128, 128, dtype=torch.bfloat16, device=DEV, seed=650,
                             num_states=5, h0_std=0.1)
