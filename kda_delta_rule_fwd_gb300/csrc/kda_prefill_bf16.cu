@@ -78,7 +78,7 @@ constexpr uint32_t Y_TB_HI = 0, Y_TB_LO = 8192, Y_AQK_HI = 16384, Y_AQK_LO = 245
 constexpr uint32_t Y_RED = 16384, Y_KQ = 16384 + 8192;
 constexpr uint32_t SM_LL = 196608;       // [L; L] 128 x 64 bf16 (lower-triangular ones)
 constexpr uint32_t SM_MISC = 212992;
-constexpr uint32_t MISC_RHO = 0, MISC_GL = 512, MISC_C = 1024, MISC_GAMC = 2048,
+constexpr uint32_t MISC_RHO = 0, MISC_GL = 512, MISC_C = 1024, MISC_NRHO = 1536, MISC_GAMC = 2048,
                    MISC_BETA = 2560, MISC_BAR = 2816, MISC_TMEM = 2848, MISC_FLAG = 2852;
 // (MISC_FLAG + 4: the current work item, broadcast by thread 0)
 constexpr uint32_t SM_NEGI = 216064;     // -I (64 x 64 bf16, K-major): adds -V^T on the tensor core
@@ -106,9 +106,6 @@ constexpr uint32_t TM_COLS = 512;
 __device__ __forceinline__ uint32_t off_kmaj(int r, int k, int kdim) {
   return (r >> 3) * (kdim >> 3) * 128 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
 }
-__device__ __forceinline__ uint32_t off_mnmaj(int r, int k, int kdim) {
-  return (r >> 3) * (kdim >> 3) * 128 + (k >> 3) * 128 + (k & 7) * 16 + (r & 7) * 2;
-}
 
 // Byte offset of channels 8 cg .. 8 cg + 7 of token t in a q or k tile: each
 // 64-channel half is 64 rows of 128 bytes (one per token) whose 16-byte chunks
@@ -129,10 +126,11 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 // hi/lo split of two values, each part packed as bf16x2 (first value in the low half)
+// (the remainder x - hi is exact in float32; one packed fma forms both)
 __device__ __forceinline__ void split_pack2(float a, float b, uint32_t& hi, uint32_t& lo) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+  const float2 r = fma2(__bfloat1622float2(h), make_float2(-1.f, -1.f), make_float2(a, b));
+  const __nv_bfloat162 l = __floats2bfloat162_rn(r.x, r.y);
   hi = *reinterpret_cast<const uint32_t*>(&h);
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
@@ -163,7 +161,9 @@ __device__ __forceinline__ void st8_split(unsigned char* phi, unsigned char* plo
   *reinterpret_cast<uint4*>(phi) = h;
   *reinterpret_cast<uint4*>(plo) = l;
 }
-// CTA-local named barrier over the first `count` threads (warps 0..count/32-1)
+// CTA-local named barrier `id` for `count` threads (whole warps: the barrier
+// counts arrivals, the callers choose which warps arrive; here 1 = warps 0-7,
+// 2 = warps 8-15)
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
@@ -349,6 +349,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   float* s_rho = reinterpret_cast<float*>(smem + SM_MISC + MISC_RHO);
   float* s_gl = reinterpret_cast<float*>(smem + SM_MISC + MISC_GL);
   float* s_c = reinterpret_cast<float*>(smem + SM_MISC + MISC_C);
+  float* s_nrho = reinterpret_cast<float*>(smem + SM_MISC + MISC_NRHO);
   float* s_gamc = reinterpret_cast<float*>(smem + SM_MISC + MISC_GAMC);
   float* s_beta = reinterpret_cast<float*>(smem + SM_MISC + MISC_BETA);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM_MISC + MISC_BAR);
@@ -888,28 +889,32 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       ++g_issued;
     }
 
-    // ---- P3 (pass A): per-channel reference, the decayed key/query operands
-    // (the previous chunk's output store reads X until it completes)
+    // ---- P3 (pass A): per-channel reference, the decayed key/query operands,
+    // in two halves of 64 key channels: the tensor core runs [Akk; Aqk]'s first
+    // four K steps while the threads produce the second half (the previous
+    // chunk's output store reads X until it completes)
     if (tid == 0) bulk_wait_read();
     const int t = row & 63;
-    const int cg0 = (NCOL * (row >> 6) + cq) * GPT;  // first 8-channel group of this thread
+    const int cgA = NCOL * (row >> 6) + cq;  // this thread's 8-channel groups: cgA, cgA + 8
     const bool valid = t < nv;
-    float gam[GPT * 8];
-    {
-      float a[GPT * 8 / 16][16];
+    float gam[2][8];
+    tmem_ld8(tb + lane_base + TM_ACC1 + cgA * 8, gam[0]);
+    tmem_ld8(tb + lane_base + TM_ACC1 + (cgA + 8) * 8, gam[1]);
+    tmem_wait_ld();
+    if (t == rho_t)  // log2 c per channel (s_rho, and its negative, hold it from here on)
 #pragma unroll
-      for (int q = 0; q < GPT * 8 / 16; ++q)
-        tmem_ld16(tb + lane_base + TM_ACC1 + cg0 * 8 + q * 16, a[q]);
-      tmem_wait_ld();
+      for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
-      for (int e = 0; e < GPT * 8; ++e) gam[e] = a[e >> 4][e & 15];
-    }
-    if (t == rho_t)  // log2 c per channel (s_rho holds it from here on)
-#pragma unroll
-      for (int e = 0; e < GPT * 8; ++e) s_rho[cg0 * 8 + e] = ref_log2(gam[e]);
+        for (int e = 0; e < 8; ++e) {
+          const float r = ref_log2(gam[hf][e]);
+          s_rho[(cgA + 8 * hf) * 8 + e] = r;
+          s_nrho[(cgA + 8 * hf) * 8 + e] = -r;
+        }
     if (t == nv - 1)
 #pragma unroll
-      for (int e = 0; e < GPT * 8; ++e) s_gl[cg0 * 8 + e] = gam[e];
+      for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s_gl[(cgA + 8 * hf) * 8 + e] = gam[hf][e];
     tc_fence_before();
     __syncthreads();
     float inv_k = 1.f, inv_q = 1.f;
@@ -923,34 +928,56 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       s_gamc[tid] = ex2(s_gl[tid] * kLog2e - e2);  // e^Gam_last / c
     }
     bool wide = false;  // a factor of this thread's slice leaves the exponent range (or is NaN)
+    // thread 0: [Akk; Aqk] += R Ck^T over K steps 4 half .. 4 half + 3 (channels
+    // 64 half .. 64 half + 63), three split products; the first step overwrites
+    auto issue_akk = [&](int half) {
+      const uint32_t r_hi = sbase + SM_X + X_R_HI, r_lo = sbase + SM_X + X_R_LO;
+      const uint32_t c_hi = sbase + SM_X + X_CK_HI, c_lo = sbase + SM_X + X_CK_LO;
+      const uint32_t as[3] = {r_hi, r_hi, r_lo}, bs[3] = {c_hi, c_lo, c_hi};
 #pragma unroll
-    for (int g4 = 0; g4 < GPT; ++g4) {
-      const int cg = cg0 + g4;
-      float kx[8], qx[8];
-      ld8(smem + SM_IN_K + off_sw128(t, cg), kx);
-      ld8(smem + SM_IN_Q + off_sw128(t, cg), qx);
-      if (kPre && p.pre.l2) {
+      for (int pr = 0; pr < 3; ++pr)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          kx[e] *= inv_k;  // kept in float32 into the decayed operands
-          qx[e] *= inv_q;
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int kk = 4 * half + k4;
+          mma_ss(tb + TM_ACC1, (smem_desc(as[pr], 128, 2048) + (uint64_t)(kk * 16)),
+                 (smem_desc(bs[pr], 128, 2048) + (uint64_t)(kk * 16)), idesc_kk, (pr | kk) != 0);
         }
-      }
-      const float4 e2a = *reinterpret_cast<const float4*>(s_rho + cg * 8);
-      const float4 e2b = *reinterpret_cast<const float4*>(s_rho + cg * 8 + 4);
-      const float e2[8] = {e2a.x, e2a.y, e2a.z, e2a.w, e2b.x, e2b.y, e2b.z, e2b.w};
+    };
+    // R_K, R_Q and Ck of token t, channels 8 cg .. 8 cg + 7, split into the X operands;
+    // rows past the sequence end are zero (their factors are never formed)
+    auto decayed = [&](int cg, const float (&gm)[8]) {
       float rk[8], rq[8], ck[8];
+      if (valid) {
+        float kx[8], qx[8];
+        ld8(smem + SM_IN_K + off_sw128(t, cg), kx);
+        ld8(smem + SM_IN_Q + off_sw128(t, cg), qx);
+        const float4 na = *reinterpret_cast<const float4*>(s_nrho + cg * 8);
+        const float4 nb = *reinterpret_cast<const float4*>(s_nrho + cg * 8 + 4);
+        const float nr[8] = {na.x, na.y, na.z, na.w, nb.x, nb.y, nb.z, nb.w};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        // log2(e^Gam / c); rows past the sequence end take 0 (their k and q are 0)
-        float d = valid ? fmaf(gam[g4 * 8 + e], kLog2e, -e2[e]) : 0.f;
-        wide |= !(fabsf(d) <= kMaxExp2);
-        d = fminf(fmaxf(d, -kMaxExp2), kMaxExp2);  // finite operands (unused if wide)
-        const float er = ex2(d), ec = ex2(-d);
-        const float kv = valid ? kx[e] : 0.f, qv = valid ? qx[e] : 0.f;
-        rk[e] = kv * er;
-        rq[e] = qv * er;
-        ck[e] = kv * ec;
+        for (int e = 0; e < 8; e += 2) {
+          // log2(e^Gam / c); an out-of-range chunk never uses its (infinite) operands
+          const float2 d = fma2(make_float2(gm[e], gm[e + 1]), make_float2(kLog2e, kLog2e),
+                                make_float2(nr[e], nr[e + 1]));
+          wide |= !(fabsf(d.x) <= kMaxExp2) || !(fabsf(d.y) <= kMaxExp2);
+          const float2 er = make_float2(ex2(d.x), ex2(d.y));
+          const float2 ec = make_float2(ex2(-d.x), ex2(-d.y));
+          float2 kv = make_float2(kx[e], kx[e + 1]), qv = make_float2(qx[e], qx[e + 1]);
+          if (kPre && p.pre.l2) {  // normalised in float32, unrounded
+            kv = mul2(kv, make_float2(inv_k, inv_k));
+            qv = mul2(qv, make_float2(inv_q, inv_q));
+          }
+          const float2 a = mul2(kv, er), b = mul2(qv, er), c2 = mul2(kv, ec);
+          rk[e] = a.x;
+          rk[e + 1] = a.y;
+          rq[e] = b.x;
+          rq[e + 1] = b.y;
+          ck[e] = c2.x;
+          ck[e + 1] = c2.y;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) rk[e] = rq[e] = ck[e] = 0.f;
       }
       st8_split(smem + SM_X + X_R_HI + off_kmaj(t, cg * 8, 128),
                 smem + SM_X + X_R_LO + off_kmaj(t, cg * 8, 128), rk);
@@ -958,31 +985,36 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                 smem + SM_X + X_R_LO + off_kmaj(64 + t, cg * 8, 128), rq);
       st8_split(smem + SM_X + X_CK_HI + off_kmaj(t, cg * 8, 128),
                 smem + SM_X + X_CK_LO + off_kmaj(t, cg * 8, 128), ck);
+    };
+    decayed(cgA, gam[0]);
+    fence_proxy_async_smem();
+    const bool wide0 = __syncthreads_or(wide);
+    if (!wide0 && tid == 0) {  // thread 0 issues both halves: its commit covers them
+      tc_fence_after();
+      issue_akk(0);
     }
+    decayed(cgA + 8, gam[1]);
     fence_proxy_async_smem();
     // A factor beyond 2^+-115 (an in-chunk decay span of more than about 160
     // nats on some channel, alpha = 0 included) would overflow the
-    // factorisation: the whole chunk then runs the recurrence token by token.
+    // factorisation: the whole chunk then runs the recurrence token by token,
+    // once the first half's products (if issued) have finished.
     // (A wait that ran out there is seen after the next chunk's first barrier.)
     if (__syncthreads_or(wide)) {
+      if (!wide0) {
+        if (tid == 0) mma_commit(wt.mma_bar);
+        if (wt.wait_mma()) break;
+      }
       token_chunk(ci, cs, nv);
       continue;
     }
 
-    // ---- P4: [Akk; Aqk] = R Ck^T with split operands, while every thread
+    // ---- P4: the second half of [Akk; Aqk] (thread 0), while every thread
     // rescales its slice of the state: S' = S diag(c) (transposed), bf16 parts
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t r_hi = sbase + SM_X + X_R_HI, r_lo = sbase + SM_X + X_R_LO;
-      const uint32_t c_hi = sbase + SM_X + X_CK_HI, c_lo = sbase + SM_X + X_CK_LO;
-      const uint32_t as[3] = {r_hi, r_hi, r_lo}, bs[3] = {c_hi, c_lo, c_hi};
-#pragma unroll
-      for (int pr = 0; pr < 3; ++pr)
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tb + TM_ACC1, (smem_desc(as[pr], 128, 2048) + (uint64_t)(kk * 16)),
-                 (smem_desc(bs[pr], 128, 2048) + (uint64_t)(kk * 16)), idesc_kk, (pr | kk) != 0);
-      mma_commit(wt.mma_bar);
+      issue_akk(1);
+      mma_commit(wt.mma_bar);  // both halves
     }
     {
       float sv[SCOL / 16][16];
@@ -995,10 +1027,17 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         const int c0 = cq * SCOL + q4 * 16;
         uint32_t w[16], hi[8], lo[8];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          sv[q4][e] *= s_c[c0 + e];
-          w[e] = __float_as_uint(sv[q4][e]);
+        for (int e = 0; e < 16; e += 4) {
+          const float4 c4 = *reinterpret_cast<const float4*>(s_c + c0 + e);
+          const float2 a = mul2(make_float2(sv[q4][e], sv[q4][e + 1]), make_float2(c4.x, c4.y));
+          const float2 b = mul2(make_float2(sv[q4][e + 2], sv[q4][e + 3]), make_float2(c4.z, c4.w));
+          sv[q4][e] = a.x;
+          sv[q4][e + 1] = a.y;
+          sv[q4][e + 2] = b.x;
+          sv[q4][e + 3] = b.y;
         }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(sv[q4][e]);
         tmem_st16(tb + lane_base + TM_S + c0, w);
         pack_split16(sv[q4], hi, lo);
         tmem_st8(tb + lane_base + TM_SHI + c0 / 2, hi);
@@ -1279,7 +1318,17 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         const int c0 = cq * SCOL + q4 * 16;
         uint32_t w[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(sv[q4][e] * s_gamc[c0 + e]);
+        for (int e = 0; e < 16; e += 4) {
+          const float4 g4 = *reinterpret_cast<const float4*>(s_gamc + c0 + e);
+          const float2 a = mul2(make_float2(sv[q4][e], sv[q4][e + 1]), make_float2(g4.x, g4.y));
+          const float2 b = mul2(make_float2(sv[q4][e + 2], sv[q4][e + 3]), make_float2(g4.z, g4.w));
+          sv[q4][e] = a.x;
+          sv[q4][e + 1] = a.y;
+          sv[q4][e + 2] = b.x;
+          sv[q4][e + 3] = b.y;
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(sv[q4][e]);
         tmem_st16(tb + lane_base + TM_S + c0, w);
       }
       if (ck) {
@@ -1287,7 +1336,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int q4 = 0; q4 < SCOL / 16; ++q4) {
           const int c0 = cq * SCOL + q4 * 16;
 #pragma unroll
-          for (int e = 0; e < 16; ++e) ck[(int64_t)(c0 + e) * D] = sv[q4][e] * s_gamc[c0 + e];
+          for (int e = 0; e < 16; ++e) ck[(int64_t)(c0 + e) * D] = sv[q4][e];  // rescaled above
         }
       }
       if (want_o && nv == C) {
@@ -1590,7 +1639,8 @@ cudaError_t launch_prefill_bf16(const FwdArgs& a) {
   CUtensorMap mq, mk, mg, mv, mo;
   if (!make_map_sw128(&mq, pick(a.q), map_tokens, a.H) ||
       !make_map_sw128(&mk, pick(a.k), map_tokens, a.H) ||
-      !make_map(&mg, pick(a.pre.per_head ? a.q : a.g), map_tokens, a.H, C / 2) || !make_map(&mv, pick(a.v), map_tokens, a.H) ||
+      !make_map(&mg, pick(a.pre.per_head ? a.q : a.g), map_tokens, a.H, C / 2) ||
+      !make_map(&mv, pick(a.v), map_tokens, a.H) ||
       !make_out_map(&mo, tokens > 0 ? a.out : const_cast<void*>(dummy), map_tokens, a.H,
                     tokens > 0 && a.out_dtype == KDA_BF16))
     return cudaErrorInvalidValue;
