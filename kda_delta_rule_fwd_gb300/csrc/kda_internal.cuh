@@ -275,6 +275,14 @@ __device__ __forceinline__ int64_t ckpt_base(const float* ckpt, const int32_t* o
 cudaError_t launch_schedule(const FwdArgs& a, int32_t* order_out);
 cudaError_t launch_plan_packed(const FwdArgs& a);
 cudaError_t launch_prefill_f32(const FwdArgs& a);
+// The segment scan of the long-chain split (kda_segment_scan.cu): per chain,
+// S_0 = h0 (or 0) and S_{p+1} = M_p S_p + b_p, d = 128.  Fixed length: `chains`
+// chains of nseg segments, b of all chains, then M, then the start states.
+cudaError_t launch_segment_scan(const float* h0, const float* seg_m, const float* seg_b,
+                                float* seg_s, int64_t chains, int nseg, cudaStream_t stream);
+// Packed: the split sequences of the device-written plan, H heads each.
+cudaError_t launch_segment_scan_packed(const float* h0, PlanView pv, float* states, int H,
+                                       int64_t ns_max, int64_t sms, cudaStream_t stream);
 cudaError_t launch_prefill_bf16(const FwdArgs& a);
 
 struct DecodeArgs {

@@ -1410,95 +1410,6 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 }
 
 // ---------------------------------------------------------------------------
-// Segment scan: S_{p+1} = M_p S_p + b_p along each chain, in float32.  The
-// state maps of the segments compose associatively ("Kimi K3 模型结构（7）：结构
-// 决定系统", section 上下文并行: each part contributes a local transition matrix
-// and a zero-start state, combined by a prefix scan).  One CTA per chain; each
-// thread owns an 8 x 8 tile of the D x D state.
-// ---------------------------------------------------------------------------
-constexpr int kScanThreads = 256;
-constexpr size_t kScanSmem = 2 * (size_t)D * D * sizeof(float);
-
-// One chain's scan: S_0 = h0 (or 0), written to Sp[0]; S_{p+1} = M_p S_p + b_p
-// to Sp[p+1], with M_p = Mp + p D^2, b_p = bp + p D^2, S_p = Sp + p D^2.
-__device__ void scan_chain(const float* __restrict__ h0c, const float* __restrict__ Mp,
-                           const float* __restrict__ bp, float* __restrict__ Sp, int nseg,
-                           float* sc) {
-  float* S = sc;            // current start state S_p [D][D]
-  float* MT = sc + D * D;   // M_p transposed: MT[k][i] = M_p[i][k]
-  const int tid = threadIdx.x;
-  const int i0 = (tid >> 4) * 8, j0 = (tid & 15) * 8;
-  for (int x = tid; x < D * D; x += kScanThreads) {
-    const float v = h0c ? h0c[x] : 0.f;
-    S[x] = v;
-    Sp[x] = v;
-  }
-  for (int sp = 0; sp + 1 < nseg; ++sp) {
-    const float* M = Mp + (int64_t)sp * D * D;
-    const float* b = bp + (int64_t)sp * D * D;
-    for (int x = tid; x < D * D; x += kScanThreads) MT[(x % D) * D + x / D] = M[x];
-    __syncthreads();
-    float acc[8][8];
-#pragma unroll
-    for (int r = 0; r < 8; ++r)
-#pragma unroll
-      for (int c = 0; c < 8; ++c) acc[r][c] = b[(int64_t)(i0 + r) * D + j0 + c];
-#pragma unroll 4
-    for (int k = 0; k < D; ++k) {
-      const float4 m0 = *reinterpret_cast<const float4*>(MT + k * D + i0);
-      const float4 m1 = *reinterpret_cast<const float4*>(MT + k * D + i0 + 4);
-      const float4 s0 = *reinterpret_cast<const float4*>(S + k * D + j0);
-      const float4 s1 = *reinterpret_cast<const float4*>(S + k * D + j0 + 4);
-      const float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-      const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-#pragma unroll
-      for (int r = 0; r < 8; ++r)
-#pragma unroll
-        for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(mv[r], sv[c], acc[r][c]);
-    }
-    __syncthreads();  // every thread is done reading S and MT
-    float* out = Sp + (int64_t)(sp + 1) * D * D;
-#pragma unroll
-    for (int r = 0; r < 8; ++r)
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        S[(i0 + r) * D + j0 + c] = acc[r][c];
-        out[(int64_t)(i0 + r) * D + j0 + c] = acc[r][c];
-      }
-    __syncthreads();
-  }
-}
-
-// Fixed-length batches: one CTA per chain, every chain nseg segments; b for all
-// chains, then M, then the start states (slot 0 a copy of h0).
-__global__ void __launch_bounds__(kScanThreads, 1)
-kda_segment_scan_kernel(const float* __restrict__ h0, const float* __restrict__ seg_m,
-                        const float* __restrict__ seg_b, float* __restrict__ seg_s, int nseg) {
-  extern __shared__ __align__(16) float sc[];
-  const int64_t chain = blockIdx.x;
-  scan_chain(h0 ? h0 + chain * D * D : nullptr, seg_m + chain * (nseg - 1) * D * D,
-             seg_b + chain * (nseg - 1) * D * D, seg_s + chain * nseg * D * D, nseg, sc);
-}
-
-// Packed batches: one CTA per (split sequence, head) of the plan; a CTA past
-// the plan's count leaves at once.
-__global__ void __launch_bounds__(kScanThreads, 1)
-kda_segment_scan_packed_kernel(const float* __restrict__ h0, PlanView pv,
-                               float* __restrict__ states, int H) {
-  extern __shared__ __align__(16) float sc[];
-  const int chains = pv.hdr->n_split * H;
-  for (int c = blockIdx.x; c < chains; c += gridDim.x) {
-    const int h = c % H, si = c / H;
-    const int n = pv.split[si], nseg = pv.nseg[n];
-    float* base = states + ((int64_t)pv.slot[n] * H + (int64_t)h * (3 * nseg - 2)) * D * D;
-    scan_chain(h0 ? h0 + ((int64_t)n * H + h) * D * D : nullptr,
-               base + (int64_t)(nseg - 1) * D * D, base, base + (int64_t)2 * (nseg - 1) * D * D,
-               nseg, sc);
-    __syncthreads();  // shared memory is reused by the next chain
-  }
-}
-
-// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -1570,13 +1481,6 @@ cudaError_t run_bf16(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap&
   cudaError_t e = cudaFuncSetAttribute(kda_prefill_bf16_kernel<kPre>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  if ((e = cudaFuncSetAttribute(kda_segment_scan_kernel,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)kScanSmem)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(kda_segment_scan_packed_kernel,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)kScanSmem)) != cudaSuccess)
-    return e;
   // Persistent CTAs, one per SM at most: each takes work items from its launch's
   // counter until none is left.
   const int64_t sms = a.sms > 0 ? a.sms : kGb300Sms;
@@ -1590,9 +1494,9 @@ cudaError_t run_bf16(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap&
     kda_prefill_bf16_kernel<kPre><<<grid(2 * a.H * a.ns_max), kThreads, SMEM_BYTES, a.stream>>>(
         mq, mk, mg, mv, mo, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    kda_segment_scan_packed_kernel<<<grid(a.H * a.ns_max), kScanThreads, kScanSmem, a.stream>>>(
-        a.h0, p.pv, a.seg_ws, a.H);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_segment_scan_packed(a.h0, p.pv, a.seg_ws, a.H, a.ns_max, sms, a.stream)) !=
+        cudaSuccess)
+      return e;
     p.mode = MODE_PSEG_OUTPUT;
     kda_prefill_bf16_kernel<kPre><<<grid(a.H * (a.N + a.ns_max)), kThreads, SMEM_BYTES,
                               a.stream>>>(mq, mk, mg, mv, mo, p);
@@ -1616,9 +1520,9 @@ cudaError_t run_bf16(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap&
   kda_prefill_bf16_kernel<kPre><<<grid(items * (pl.nseg - 1) * 2), kThreads, SMEM_BYTES,
                             a.stream>>>(mq, mk, mg, mv, mo, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  kda_segment_scan_kernel<<<(unsigned)items, kScanThreads, kScanSmem, a.stream>>>(
-      a.h0, p.seg_m, p.seg_b, seg_s, pl.nseg);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_segment_scan(a.h0, p.seg_m, p.seg_b, seg_s, items, pl.nseg, a.stream)) !=
+      cudaSuccess)
+    return e;
   p.mode = MODE_SEG_OUTPUT;
   kda_prefill_bf16_kernel<kPre><<<grid(items * pl.nseg), kThreads, SMEM_BYTES, a.stream>>>(
       mq, mk, mg, mv, mo, p);
