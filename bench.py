@@ -208,17 +208,21 @@ def _hbm_line(nbytes, ms, peak):
     return {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak}
 
 
-E2E_PARTS = 4  # sequences of the headline batch pipelined through the host copies
+E2E_SEQ_PARTS = 4   # the headline batch's sequences, each its own stream of kernels
+E2E_TIME_PARTS = 2  # each sequence cut in time (the later part starts from the earlier's hT)
 
 
-def make_e2e_step(kda, x, dev, parts=E2E_PARTS):
+def make_e2e_step(kda, x, dev, seq_parts=E2E_SEQ_PARTS, time_parts=E2E_TIME_PARTS):
     """One end-to-end step through the public API with HOST buffers: pinned host
     inputs in, o and hT back to pinned host memory.  The batch is cut by sequence
-    into `parts`: every part's inputs go down in turn on one copy stream, each
-    part's kda_fwd runs on a stream of its own as soon as its inputs have landed,
-    and its o and hT come back on a third stream, so the copies overlap the
-    kernels and each other (the two directions of the link are independent).
-    Returns (step, h2d_bytes, d2h_bytes)."""
+    into `seq_parts` and in time into `time_parts` contiguous pieces.  Every piece's
+    inputs go down in turn on one copy stream; each sequence's pieces run kda_fwd in
+    order on a stream of their own, a piece starting from the previous piece's final
+    state (h0 = its hT; chunk boundaries stay at multiples of 64, so the results are
+    those of one call), as soon as its inputs have landed; its o (and the last
+    piece's hT) come back on a third stream.  The copies overlap the kernels and
+    each other (the two directions of the link are independent).
+    Returns (step, h2d_bytes, d2h_bytes, buffers)."""
     import torch
     pin = lambda t: t.cpu().pin_memory()
     hin = [pin(t) for t in (x.q, x.k, x.v, x.g, x.beta)]
@@ -227,11 +231,13 @@ def make_e2e_step(kda, x, dev, parts=E2E_PARTS):
     hT = torch.empty(B, H, D, D, device=dev)
     ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     hh = torch.empty(hT.shape, dtype=hT.dtype).pin_memory()
-    per = B // parts
-    shape = kda.make_shape(x.q[:per], x.v[:per])
-    wss = [kda.new_workspace(shape, dev) for _ in range(parts)]
+    per, tl = B // seq_parts, T // time_parts
+    mid = [[torch.empty(per, H, D, D, device=dev) for _ in range(time_parts - 1)]
+           for _ in range(seq_parts)]
+    shape = kda.make_shape(x.q[:per, :tl], x.v[:per, :tl])
+    wss = [kda.new_workspace(shape, dev) for _ in range(seq_parts)]
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    s_run = [torch.cuda.Stream(device=dev) for _ in range(parts)]
+    s_run = [torch.cuda.Stream(device=dev) for _ in range(seq_parts)]
 
     def step():
         cur = torch.cuda.current_stream()
@@ -239,26 +245,31 @@ def make_e2e_step(kda, x, dev, parts=E2E_PARTS):
         start.record(cur)
         s_in.wait_event(start)
         s_out.wait_event(start)
-        for i in range(parts):
-            sl = slice(i * per, (i + 1) * per)
-            landed, done = torch.cuda.Event(), torch.cuda.Event()
-            with torch.cuda.stream(s_in):
-                for d_, h_ in zip(din, hin):
-                    d_[sl].copy_(h_[sl], non_blocking=True)
-                landed.record(s_in)
-            s_run[i].wait_event(landed)
-            with torch.cuda.stream(s_run[i]):
-                kda.fwd(*(d_[sl] for d_ in din), out=o[sl], hT=hT[sl], workspace=wss[i])
-                done.record(s_run[i])
-            s_out.wait_event(done)
-            with torch.cuda.stream(s_out):
-                ho[sl].copy_(o[sl], non_blocking=True)
-                hh[sl].copy_(hT[sl], non_blocking=True)
+        for i in range(seq_parts):
+            bs = slice(i * per, (i + 1) * per)
+            for j in range(time_parts):
+                ts = slice(j * tl, (j + 1) * tl)
+                last = j == time_parts - 1
+                landed, done = torch.cuda.Event(), torch.cuda.Event()
+                with torch.cuda.stream(s_in):
+                    for d_, h_ in zip(din, hin):
+                        d_[bs, ts].copy_(h_[bs, ts], non_blocking=True)
+                    landed.record(s_in)
+                s_run[i].wait_event(landed)
+                with torch.cuda.stream(s_run[i]):
+                    kda.fwd(*(d_[bs, ts] for d_ in din), h0=mid[i][j - 1] if j else None,
+                            out=o[bs, ts], hT=hT[bs] if last else mid[i][j], workspace=wss[i])
+                    done.record(s_run[i])
+                s_out.wait_event(done)
+                with torch.cuda.stream(s_out):
+                    ho[bs, ts].copy_(o[bs, ts], non_blocking=True)
+                    if last:
+                        hh[bs].copy_(hT[bs], non_blocking=True)
         cur.wait_stream(s_out)
 
     h2d = sum(t.numel() * t.element_size() for t in hin)
     d2h = ho.numel() * ho.element_size() + hh.numel() * hh.element_size()
-    return step, h2d, d2h, (o, hT, ho, hh)
+    return step, h2d, d2h, (o, hT, ho, hh, mid)
 
 
 def bench_long(kda, args, dev, stream, dist_on, hbm_peak):
@@ -397,7 +408,7 @@ def run_ours(args):
     e2e_step, h2d, d2h, keep = make_e2e_step(kda, x, dev)
     ms_e2e = _time_steps(e2e_step, max(3, args.steps // 4), 2, stream, dist_on)
     # the same with one part: copies in, kernel, copies out in sequence
-    e2e_serial, _, _, keep1 = make_e2e_step(kda, x, dev, parts=1)
+    e2e_serial, _, _, keep1 = make_e2e_step(kda, x, dev, seq_parts=1, time_parts=1)
     ms_e2e1 = _time_steps(e2e_serial, max(3, args.steps // 4), 2, stream, dist_on)
     del keep, keep1, e2e_step, e2e_serial
 
@@ -574,8 +585,9 @@ def run_ours(args):
         "e2e": {"value": tokens / (ms_e2e * 1e-3), "unit": "tokens/s", "ms_per_step": ms_e2e,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": f"pinned host inputs -> device -> kda_fwd -> o, hT to pinned host, "
-                       f"pipelined in {E2E_PARTS} parts by sequence (copies in on one stream, "
-                       f"a stream per part's kernel, copies out on another)",
+                       f"pipelined in {E2E_SEQ_PARTS} sequences x {E2E_TIME_PARTS} time parts "
+                       f"(copies in on one stream, a stream per sequence's kernels, each time "
+                       f"part starting from the previous part's hT, copies out on another)",
                 "serial_ms_per_step": ms_e2e1},
         "gpu_launches": args.steps,
         "clocks": clk,

@@ -635,3 +635,19 @@ def test_packed_split_fused_preprocessing(kda, oracle_mod):
     o_ref, h_ref = oracle_mod.recurrent(fq, fk, x.v, fg, fb, cu_seqlens=x.cu_seqlens, h0=x.h0)
     assert rel_err(o, o_ref) <= TOL_BF16
     assert rel_err(hT, h_ref) <= TOL_BF16
+
+
+# more (sequence, head) chains than SMs: persistent CTAs take several items each -------
+
+def test_fixed_length_more_chains_than_sms(kda, oracle_mod):
+    """B=6, H=32: 192 chains on at most 152 CTAs, each taking items in turn from the
+    launch's counter; plain, then with checkpoints every 64 tokens."""
+    x = kda_inputs.fixed(6, 130, 32, 128, dtype=torch.bfloat16, device=DEV, seed=990,
+                         h0_std=0.1)
+    _check_fwd(kda, oracle_mod, x, torch.bfloat16)
+    o, hT, ck, off = kda.fwd_checkpoints(x.q, x.k, x.v, x.g, x.beta, interval=64, h0=x.h0)
+    o2, h2 = kda.fwd(x.q, x.k, x.v, x.g, x.beta, h0=x.h0)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(hT, h2)
+    refs = _ckpt_refs(oracle_mod, x, [(b, 0, 130, b) for b in range(6)], 64)
+    _check_ckpts(ck, refs, TOL_BF16)

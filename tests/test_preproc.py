@@ -254,6 +254,12 @@ def test_prefill_more_chains_than_sms(kda, oracle_mod, per_head):
     assert rel_err(hT, h_ref) <= TOL_BF16
 
 
+def test_prefill_fixed_length_more_chains_than_sms(kda, oracle_mod):
+    """B=5, H=40 (200 chains) on raw inputs with every step fused."""
+    x = _raw_fixed(5, 90, 40, 128, torch.bfloat16, seed=670)
+    _check_prefill(kda, oracle_mod, x, torch.bfloat16)
+
+
 def test_decode_gate_scale_8(kda, oracle_mod):
     x = kda_inputs.draw_raw((5, 8), 3, 128, 128, dtype=torch.bfloat16, device=DEV, seed=650,
                             num_states=5, h0_std=0.1)
