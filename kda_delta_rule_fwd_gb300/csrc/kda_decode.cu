@@ -6,16 +6,22 @@
 // "Kimi K3 模型结构（7）：结构决定系统", section KDA 状态回滚):
 //     S <- diag(alpha) S;  p = S^T k;  u = beta (v - p);  S <- S + k u^T;
 //     o = scale S^T q = scale ((diag(alpha) S)^T q + u (k . q))
-// The second form of o lets one cross-warp reduction produce both S^T k and
-// S^T q from the decayed state.
+// The second form of o lets one reduction produce both S^T k and S^T q from
+// the decayed state.
 //
 // Layout and work split: one CTA of 256 threads per (sequence, head).  The
-// state S [D x D] (row = key channel, dv contiguous) lives in registers: warp w
-// owns rows [w*D/8, (w+1)*D/8) and lane l owns columns [l*D/32, (l+1)*D/32), so
-// every warp load/store of a state row is one contiguous, vectorised access.
-// The token loop works on pairs of a lane's columns with packed f32x2 arithmetic.
-// One head-step reads and writes 4*D*D bytes of state: HBM-bound at T_step = 1,
-// and bound by the per-token arithmetic and barriers as T_step grows.
+// state S [D x D] (row = key channel, dv contiguous) lives in registers by
+// column blocks: warp w owns the D/8 columns [w*D/8, (w+1)*D/8) over all D
+// rows, and within it lane l = 4 rg + cq owns the D/32 columns starting at
+// w*D/8 + cq*D/32 of rows [rg*D/8, (rg+1)*D/8).  The reductions over rows of
+// S^T k and S^T q then stay inside a warp: a reduce-scatter over the 8 row
+// groups (three shuffle levels) leaves each lane one column's sum, the lanes
+// holding S^T k form u, and shuffles hand u to the lanes that own its column
+// and to the lanes holding S^T q (which write o).  No CTA barrier runs in the
+// token loop; the warps only share the step's staged inputs.  The arithmetic
+// works on pairs of a lane's columns with packed f32x2 instructions.  One
+// head-step reads and writes 4*D*D bytes of state: HBM-bound at T_step = 1,
+// and bound by the per-token arithmetic as T_step grows.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -29,6 +35,42 @@ template <> struct VecF<2> { using T = float2; };
 template <> struct VecF<4> { using T = float4; };
 
 
+// 16 bytes of inputs (8 bf16 or 4 float32) from global memory as float32, and
+// the float32 values to shared memory
+__device__ __forceinline__ void ldg_chunk(const __nv_bfloat16* p, float (&x)[8]) {
+  const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    x[2 * e] = __uint_as_float(w[e] << 16);
+    x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ void ldg_chunk(const float* p, float (&x)[4]) {
+  const float4 u = __ldg(reinterpret_cast<const float4*>(p));
+  x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+}
+template <int N>
+__device__ __forceinline__ void st_chunk(float* p, const float (&x)[N]) {
+#pragma unroll
+  for (int e = 0; e < N; e += 4)
+    *reinterpret_cast<float4*>(p + e) = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+}
+
+// One level of a reduce-scatter over the lanes that differ in bit `m`: the
+// lane with that bit set keeps (and adds its partner's copy of) the upper
+// HALF values, the other lane the lower ones; the kept sums move to v[0..HALF).
+template <int HALF, int N>
+__device__ __forceinline__ void rs_level(float (&v)[N], int lane, int m) {
+  const bool up = (lane & m) != 0;
+#pragma unroll
+  for (int j = 0; j < HALF; ++j) {
+    const float send = up ? v[j] : v[HALF + j];
+    const float keep = up ? v[HALF + j] : v[j];
+    v[j] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+  }
+}
+
 // kCommit: per-sequence commit counts (num_commit) decide which state is written
 // back; otherwise the state after all Tstep tokens is.
 // kPre: the fused input preprocessing `pre` is applied while the inputs are staged.
@@ -40,79 +82,120 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                   TOut* __restrict__ out, int H, int Tstep, float scale,
                   const int32_t* __restrict__ num_commit, unsigned int* status,
                   Preproc pre) {
-  constexpr int R = D / 8;     // state rows per warp
+  constexpr int RPL = D / 8;   // state rows per lane (one row group)
   constexpr int CPL = D / 32;  // state columns per lane
   constexpr int P = CPL / 2;   // column pairs per lane (packed arithmetic)
+  constexpr int WC = D / 8;    // columns per warp
+  constexpr int DP = D + 32;   // staged row length: 4 pad floats after each row group
   using Vec = typename VecF<CPL>::T;
 
-  __shared__ __align__(16) float s_k[kMaxTstep][D];
-  __shared__ __align__(16) float s_q[kMaxTstep][D];
-  __shared__ __align__(16) float s_a[kMaxTstep][D];   // alpha = exp(g)
+  // alpha, k and q are read by row group: padding each group of RPL channels by
+  // 4 floats puts the 8 groups' 16-byte reads on distinct banks
+  __shared__ __align__(16) float s_k[kMaxTstep][DP];
+  __shared__ __align__(16) float s_q[kMaxTstep][DP];
+  __shared__ __align__(16) float s_a[kMaxTstep][DP];   // alpha = exp(g)
   __shared__ __align__(16) float s_v[kMaxTstep][D];
   __shared__ float s_b[kMaxTstep];
   __shared__ float s_kq[kMaxTstep];
-  __shared__ __align__(16) float s_red[8][2][D];      // per-warp partial S^T k and S^T q
-  __shared__ __align__(16) float s_u[D];
+  auto pidx = [](int c) { return c + (c / RPL) * 4; };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rg = lane >> 2, cq = lane & 3;
+  const int row0 = rg * RPL, col0 = warp * WC + cq * CPL;
   const int64_t nh = blockIdx.x;  // n * H + h
   const int64_t n = nh / H, h = nh % H;
 
   // Issue the state loads first: they are the HBM traffic that matters.
   float* Sg = state + nh * (int64_t)D * D;
-  float2 S[R][P];
+  float2 S[RPL][P];
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const Vec x = *reinterpret_cast<const Vec*>(Sg + (int64_t)(warp * R + r) * D + lane * CPL);
+  for (int i = 0; i < RPL; ++i) {
+    const Vec x = *reinterpret_cast<const Vec*>(Sg + (int64_t)(row0 + i) * D + col0);
     const float2* xf = reinterpret_cast<const float2*>(&x);
 #pragma unroll
-    for (int c = 0; c < P; ++c) S[r][c] = xf[c];
+    for (int c = 0; c < P; ++c) S[i][c] = xf[c];
   }
 
-  // Stage the step's inputs (Tstep tokens) in shared memory as float32 (with the
-  // fused preprocessing: a scalar gate per (token, head) is shared by the channels).
+  // Stage the step's inputs (Tstep tokens) in shared memory as float32, one
+  // 16-byte chunk per lane: warps 0-3 take q and k, a group of CR lanes per
+  // token row, and form that token's norms (fused preprocessing) and k . q by
+  // shuffles inside the group; warps 4-7 take v, the gate (a scalar gate per
+  // (token, head) is shared by the channels) and beta.
+  constexpr int kE = 16 / (int)sizeof(TIn);  // elements per chunk
+  constexpr int CR = D / kE;                 // chunks (lanes) per token row: 8 .. 32
   const float gsc = kPre && pre.gate_scale ? pre.gate_scale[h] : 1.f;
-  for (int i = tid; i < Tstep * D; i += kDecodeThreads) {
-    const int t = i / D, c = i % D;
-    const int64_t x = ((n * Tstep + t) * H + h) * D + c;
-    s_k[t][c] = to_f32(k[x]);
-    s_q[t][c] = to_f32(q[x]);
-    float gv = to_f32(g[kPre && pre.per_head ? (n * Tstep + t) * H + h : x]);
-    if (kPre && pre.gate) gv = round_to<TIn>(gsc * neg_softplus(gv));
-    s_a[t][c] = expf(gv);
-    s_v[t][c] = to_f32(v[x]);
-  }
-  if (tid < Tstep) {
-    float bv = to_f32(beta[(n * Tstep + tid) * H + h]);
-    if (kPre && pre.beta) bv = round_to<TIn>(sigmoid_f(bv));
-    s_b[tid] = bv;
-  }
-  __syncthreads();
-  // k . q per token, one warp per token (which first normalises that token's q
-  // and k when asked; each lane touches the same channels in both loops)
-  if (warp < Tstep) {
-    if (kPre && pre.l2) {
-      float sk = 0.f, sq = 0.f;
-      for (int c = lane; c < D; c += 32) {
-        sk = fmaf(s_k[warp][c], s_k[warp][c], sk);
-        sq = fmaf(s_q[warp][c], s_q[warp][c], sq);
-      }
+  const int rows = Tstep * CR;
+  if (warp < 4) {
+    for (int base = warp * 32; base < rows; base += 128) {  // warp-uniform trip count
+      const int i = base + lane, t = i / CR, c0 = (i % CR) * kE;
+      const bool on = i < rows;  // whole token rows are on or off
+      float xk[kE], xq[kE];
+      if (on) {
+        const int64_t x = ((n * Tstep + t) * H + h) * D + c0;
+        ldg_chunk(k + x, xk);
+        ldg_chunk(q + x, xq);
+      } else {
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        sk += __shfl_xor_sync(0xffffffffu, sk, o);
-        sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        for (int e = 0; e < kE; ++e) xk[e] = xq[e] = 0.f;
       }
-      const float ik = inv_l2(sk), iq = inv_l2(sq);
-      for (int c = lane; c < D; c += 32) {
-        s_k[warp][c] *= ik;  // kept in float32 (the products take float32)
-        s_q[warp][c] *= iq;
+      if (kPre && pre.l2) {
+        float sk = 0.f, sq = 0.f;
+#pragma unroll
+        for (int e = 0; e < kE; ++e) {
+          sk = fmaf(xk[e], xk[e], sk);
+          sq = fmaf(xq[e], xq[e], sq);
+        }
+#pragma unroll
+        for (int o = CR / 2; o > 0; o >>= 1) {
+          sk += __shfl_xor_sync(0xffffffffu, sk, o);
+          sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        }
+        const float ik = inv_l2(sk), iq = inv_l2(sq);
+#pragma unroll
+        for (int e = 0; e < kE; ++e) {
+          xk[e] *= ik;  // kept in float32 (the products take float32)
+          xq[e] *= iq;
+        }
+      }
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < kE; ++e) acc = fmaf(xk[e], xq[e], acc);
+#pragma unroll
+      for (int o = CR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (on) {
+        st_chunk(&s_k[t][pidx(c0)], xk);  // a chunk lies inside one row group
+        st_chunk(&s_q[t][pidx(c0)], xq);
+        if (c0 == 0) s_kq[t] = acc;
       }
     }
-    float acc = 0.f;
-    for (int c = lane; c < D; c += 32) acc += s_k[warp][c] * s_q[warp][c];
+  } else {
+    for (int i = tid - 128; i < rows; i += 128) {
+      const int t = i / CR, c0 = (i % CR) * kE;
+      const int64_t x = ((n * Tstep + t) * H + h) * D + c0;
+      float xv[kE], xa[kE];
+      ldg_chunk(v + x, xv);
+      st_chunk(&s_v[t][c0], xv);
+      if (kPre && pre.per_head) {
+        const float g1 = to_f32(g[(n * Tstep + t) * H + h]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) s_kq[warp] = acc;
+        for (int e = 0; e < kE; ++e) xa[e] = g1;
+      } else {
+        ldg_chunk(g + x, xa);
+      }
+#pragma unroll
+      for (int e = 0; e < kE; ++e) {
+        float gv = xa[e];
+        if (kPre && pre.gate) gv = round_to<TIn>(gsc * neg_softplus(gv));
+        xa[e] = expf(gv);
+      }
+      st_chunk(&s_a[t][pidx(c0)], xa);
+    }
+    if (tid - 128 < Tstep) {
+      const int t = tid - 128;
+      float bv = to_f32(beta[(n * Tstep + t) * H + h]);
+      if (kPre && pre.beta) bv = round_to<TIn>(sigmoid_f(bv));
+      s_b[t] = bv;
+    }
   }
   __syncthreads();
 
@@ -129,78 +212,78 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
   }
   auto store_state = [&]() {
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
+    for (int i = 0; i < RPL; ++i) {
       Vec x;
       float2* xf = reinterpret_cast<float2*>(&x);
 #pragma unroll
-      for (int c = 0; c < P; ++c) xf[c] = S[r][c];
-      *reinterpret_cast<Vec*>(Sg + (int64_t)(warp * R + r) * D + lane * CPL) = x;
+      for (int c = 0; c < P; ++c) xf[c] = S[i][c];
+      *reinterpret_cast<Vec*>(Sg + (int64_t)(row0 + i) * D + col0) = x;
     }
   };
+  // after the reduce-scatter: lanes of row groups 0-3 hold S^T k, lanes of row
+  // groups 4-7 S^T q, of column col0 + my_c (row groups 4 + r and r pair up)
+  const bool holds_k = rg < 4;
+  const int my_c = CPL == 4 ? (rg & 3) : ((rg >> 1) & 1);
+  const bool writes_o = !holds_k && (CPL == 4 || (rg & 1) == 0);
+  const int pa = pidx(row0);
 
   for (int t = 0; t < Tstep; ++t) {
-    // this warp's rows of alpha, k and q, read as 16-byte vectors
-    float a[R], kr[R], qr[R];
+    // this lane's rows of alpha, k and q, read as 16-byte vectors (lanes of one
+    // row group read the same addresses)
+    float a[RPL], kr[RPL], qr[RPL];
 #pragma unroll
-    for (int r4 = 0; r4 < R / 4; ++r4) {
-      const float4 av = *reinterpret_cast<const float4*>(&s_a[t][warp * R + 4 * r4]);
-      const float4 kv = *reinterpret_cast<const float4*>(&s_k[t][warp * R + 4 * r4]);
-      const float4 qv = *reinterpret_cast<const float4*>(&s_q[t][warp * R + 4 * r4]);
+    for (int r4 = 0; r4 < RPL / 4; ++r4) {
+      const float4 av = *reinterpret_cast<const float4*>(&s_a[t][pa + 4 * r4]);
+      const float4 kv = *reinterpret_cast<const float4*>(&s_k[t][pa + 4 * r4]);
+      const float4 qv = *reinterpret_cast<const float4*>(&s_q[t][pa + 4 * r4]);
       a[4 * r4] = av.x; a[4 * r4 + 1] = av.y; a[4 * r4 + 2] = av.z; a[4 * r4 + 3] = av.w;
       kr[4 * r4] = kv.x; kr[4 * r4 + 1] = kv.y; kr[4 * r4 + 2] = kv.z; kr[4 * r4 + 3] = kv.w;
       qr[4 * r4] = qv.x; qr[4 * r4 + 1] = qv.y; qr[4 * r4 + 2] = qv.z; qr[4 * r4 + 3] = qv.w;
     }
-    // decay and partial reductions over this warp's rows, two columns at a time
+    // decay and partial reductions over this lane's rows, two columns at a time
     float2 pk[P], pq[P];
 #pragma unroll
     for (int c = 0; c < P; ++c) pk[c] = pq[c] = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const float2 a2 = make_float2(a[r], a[r]), k2 = make_float2(kr[r], kr[r]);
-      const float2 q2 = make_float2(qr[r], qr[r]);
+    for (int i = 0; i < RPL; ++i) {
+      const float2 a2 = make_float2(a[i], a[i]), k2 = make_float2(kr[i], kr[i]);
+      const float2 q2 = make_float2(qr[i], qr[i]);
 #pragma unroll
       for (int c = 0; c < P; ++c) {
-        S[r][c] = mul2(S[r][c], a2);
-        pk[c] = fma2(S[r][c], k2, pk[c]);
-        pq[c] = fma2(S[r][c], q2, pq[c]);
+        S[i][c] = mul2(S[i][c], a2);
+        pk[c] = fma2(S[i][c], k2, pk[c]);
+        pq[c] = fma2(S[i][c], q2, pq[c]);
       }
     }
-    {
-      Vec vk, vq;
-      float2* fk = reinterpret_cast<float2*>(&vk);
-      float2* fq = reinterpret_cast<float2*>(&vq);
-#pragma unroll
-      for (int c = 0; c < P; ++c) { fk[c] = pk[c]; fq[c] = pq[c]; }
-      *reinterpret_cast<Vec*>(&s_red[warp][0][lane * CPL]) = vk;
-      *reinterpret_cast<Vec*>(&s_red[warp][1][lane * CPL]) = vq;
+    // sums over the 8 row groups, scattered: one (column, k or q) sum per lane
+    float red;
+    if constexpr (CPL == 4) {
+      float vals[8] = {pk[0].x, pk[0].y, pk[1].x, pk[1].y, pq[0].x, pq[0].y, pq[1].x, pq[1].y};
+      rs_level<4>(vals, lane, 16);
+      rs_level<2>(vals, lane, 8);
+      rs_level<1>(vals, lane, 4);
+      red = vals[0];
+    } else {
+      float vals[4] = {pk[0].x, pk[0].y, pq[0].x, pq[0].y};
+      rs_level<2>(vals, lane, 16);
+      rs_level<1>(vals, lane, 8);
+      red = vals[0] + __shfl_xor_sync(0xffffffffu, vals[0], 4);
     }
-    __syncthreads();
-    if (tid < D) {
-      float sk = 0.f, sq = 0.f;
+    const int col = col0 + my_c;
+    const float u = holds_k ? s_b[t] * (s_v[t][col] - red) : 0.f;
+    const float u_q = __shfl_xor_sync(0xffffffffu, u, 16);  // to the S^T q lane of the column
+    if (writes_o && (!kCommit || out))
+      out[((n * Tstep + t) * H + h) * D + col] = from_f32<TOut>(scale * fmaf(u_q, s_kq[t], red));
+    // u of this lane's columns, from the lanes that formed them
+    float uc[CPL];
 #pragma unroll
-      for (int w = 0; w < 8; ++w) {
-        sk += s_red[w][0][tid];
-        sq += s_red[w][1][tid];
-      }
-      const float u = s_b[t] * (s_v[t][tid] - sk);
-      s_u[tid] = u;
-      const float o = scale * fmaf(u, s_kq[t], sq);
-      if (!kCommit || out) out[((n * Tstep + t) * H + h) * D + tid] = from_f32<TOut>(o);
-    }
-    __syncthreads();
+    for (int c = 0; c < CPL; ++c) uc[c] = __shfl_sync(0xffffffffu, u, ((c * (4 / CPL)) << 2) | cq);
     // rank-1 write S <- S + k u^T
-    float2 u[P];
-    {
-      const Vec uv = *reinterpret_cast<const Vec*>(&s_u[lane * CPL]);
-      const float2* uf = reinterpret_cast<const float2*>(&uv);
 #pragma unroll
-      for (int c = 0; c < P; ++c) u[c] = uf[c];
-    }
+    for (int i = 0; i < RPL; ++i) {
+      const float2 k2 = make_float2(kr[i], kr[i]);
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const float2 k2 = make_float2(kr[r], kr[r]);
-#pragma unroll
-      for (int c = 0; c < P; ++c) S[r][c] = fma2(k2, u[c], S[r][c]);
+      for (int c = 0; c < P; ++c) S[i][c] = fma2(k2, make_float2(uc[2 * c], uc[2 * c + 1]), S[i][c]);
     }
     if (kCommit && t + 1 == commit) store_state();
   }

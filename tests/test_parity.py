@@ -283,6 +283,30 @@ def test_decode_commit_counts(kda, oracle_mod, dtype, d):
             assert rel_err(state[n], ref) <= tol
 
 
+@pytest.mark.parametrize("dtype,d", [(torch.float32, 64), (torch.bfloat16, 128)],
+                         ids=["f32-d64", "bf16-d128"])
+def test_decode_commit_many_chains(kda, oracle_mod, dtype, d):
+    """640 (sequence, head) chains, more than the device holds CTAs at once (two
+    per SM), so CTAs of later waves reuse the SMs.  The commit counts cycle
+    through 0..8, so neighbouring chains keep states after different prefixes."""
+    num_seqs, H = 160, 4
+    x = kda_inputs.decode_pool(num_seqs=num_seqs, H=H, d=d, T_step=8, dtype=dtype, device=DEV,
+                               seed=93)
+    counts = [n % 9 for n in range(num_seqs)]
+    state = x.h0.clone()
+    o = kda.decode_commit(x.q, x.k, x.v, x.g, x.beta, state,
+                          torch.tensor(counts, dtype=torch.int32, device=DEV))
+    torch.cuda.synchronize()
+    o_ref, _ = oracle_mod.recurrent(x.q, x.k, x.v, x.g, x.beta, h0=x.h0)
+    tol = TOL[dtype]
+    assert rel_err(o, o_ref) <= tol
+    for n, ref in enumerate(_commit_refs(oracle_mod, x, counts)):
+        if counts[n] == 0:
+            assert torch.equal(state[n], x.h0[n])
+        else:
+            assert rel_err(state[n], ref) <= tol
+
+
 @pytest.mark.parametrize("T_step", [2, 5, 8])
 def test_decode_commit_every_count(kda, oracle_mod, T_step):
     """Commit counts 0..T_step on one batch (bf16 inputs, bf16 outputs): outputs of

@@ -322,3 +322,25 @@ def test_decode_gate_scale_and_scalar_gate(kda, oracle_mod, dtype, per_head):
     o_ref, h_ref = oracle_mod.recurrent(fq, fk, x.v, fg, fb, h0=x.h0)
     assert rel_err(o, o_ref) <= TOL[dtype]
     assert rel_err(state, h_ref) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("per_head", [False, True], ids=["per-channel", "per-head"])
+def test_decode_preproc_many_chains(kda, oracle_mod, per_head):
+    """The fused preprocessing on a pool of 96 x 5 = 480 chains, more than the
+    device holds CTAs at once: every chain's scalars (beta, a per-head gate, its
+    head's gate scale) and normalised q, k must follow their chain."""
+    x = kda_inputs.draw_raw((96, 8), 5, 128, 128, dtype=torch.bfloat16, device=DEV, seed=640,
+                            num_states=96, h0_std=0.1)
+    if per_head:
+        x.g = x.g[..., 0].contiguous()
+    a = _gate_scale(5, 641)
+    state = x.h0.clone()
+    o = kda.decode_preproc(x.q, x.k, x.v, x.g, x.beta, state, qk_l2norm=True,
+                           gate_softplus=True, beta_sigmoid=True, gate_per_head=per_head,
+                           gate_scale=a)
+    torch.cuda.synchronize()
+    fq, fk, fg, fb = oracle_mod.preprocess(x.q, x.k, x.g, x.beta, gate_per_head=per_head,
+                                           gate_scale=a)
+    o_ref, h_ref = oracle_mod.recurrent(fq, fk, x.v, fg, fb, h0=x.h0)
+    assert rel_err(o, o_ref) <= TOL_BF16
+    assert rel_err(state, h_ref) <= TOL_BF16
