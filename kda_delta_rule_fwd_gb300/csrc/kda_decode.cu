@@ -169,26 +169,54 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
       }
     }
   } else {
-    for (int i = tid - 128; i < rows; i += 128) {
-      const int t = i / CR, c0 = (i % CR) * kE;
-      const int64_t x = ((n * Tstep + t) * H + h) * D + c0;
-      float xv[kE], xa[kE];
-      ldg_chunk(v + x, xv);
-      st_chunk(&s_v[t][c0], xv);
-      if (kPre && pre.per_head) {
-        const float g1 = to_f32(g[(n * Tstep + t) * H + h]);
+    // every load first (one memory round trip), then the conversions: v by
+    // chunks; an activated or per-head gate one element per thread (the
+    // activation is the longest work of the staging), a plain gate by chunks
+    constexpr int kVmax = (kMaxTstep * CR + 127) / 128;  // chunks per thread
+    constexpr int kGmax = kMaxTstep * D / 128;           // gate elements per thread
+    const int j0 = tid - 128;
+    const bool g_elems = kPre && (pre.gate || pre.per_head);
+    float xv[kVmax][kE], xa[kVmax][kE], gr[kGmax];
 #pragma unroll
-        for (int e = 0; e < kE; ++e) xa[e] = g1;
-      } else {
-        ldg_chunk(g + x, xa);
+    for (int jj = 0; jj < kVmax; ++jj) {
+      const int i = j0 + 128 * jj;
+      if (i < rows) {
+        const int64_t x = ((n * Tstep + i / CR) * H + h) * D + (i % CR) * kE;
+        ldg_chunk(v + x, xv[jj]);
+        if (!g_elems) ldg_chunk(g + x, xa[jj]);
+      }
+    }
+    if (g_elems) {
+#pragma unroll
+      for (int jj = 0; jj < kGmax; ++jj) {
+        const int i = j0 + 128 * jj;
+        if (i < Tstep * D) {
+          const int64_t xt = (n * Tstep + i / D) * H + h;
+          gr[jj] = to_f32(g[pre.per_head ? xt : xt * D + i % D]);
+        }
       }
 #pragma unroll
-      for (int e = 0; e < kE; ++e) {
-        float gv = xa[e];
-        if (kPre && pre.gate) gv = round_to<TIn>(gsc * neg_softplus(gv));
-        xa[e] = expf(gv);
+      for (int jj = 0; jj < kGmax; ++jj) {
+        const int i = j0 + 128 * jj;
+        if (i < Tstep * D) {
+          float gv = gr[jj];
+          if (pre.gate) gv = round_to<TIn>(gsc * neg_softplus(gv));
+          s_a[i / D][pidx(i % D)] = expf(gv);
+        }
       }
-      st_chunk(&s_a[t][pidx(c0)], xa);
+    }
+#pragma unroll
+    for (int jj = 0; jj < kVmax; ++jj) {
+      const int i = j0 + 128 * jj;
+      if (i < rows) {
+        const int t = i / CR, c0 = (i % CR) * kE;
+        st_chunk(&s_v[t][c0], xv[jj]);
+        if (!g_elems) {
+#pragma unroll
+          for (int e = 0; e < kE; ++e) xa[jj][e] = expf(xa[jj][e]);
+          st_chunk(&s_a[t][pidx(c0)], xa[jj]);
+        }
+      }
     }
     if (tid - 128 < Tstep) {
       const int t = tid - 128;
