@@ -79,13 +79,15 @@ constexpr uint32_t Y_RED = 16384, Y_KQ = 16384 + 8192;
 constexpr uint32_t SM_LL = 196608;       // [L; L] 128 x 64 bf16 (lower-triangular ones)
 constexpr uint32_t SM_MISC = 212992;
 constexpr uint32_t MISC_RHO = 0, MISC_GL = 512, MISC_C = 1024, MISC_NRHO = 1536, MISC_GAMC = 2048,
-                   MISC_BETA = 2560, MISC_BAR = 2816, MISC_TMEM = 2848, MISC_FLAG = 2852;
-// (MISC_FLAG + 4: the current work item, broadcast by thread 0)
+                   MISC_BETA = 2560, MISC_BAR = 2816, MISC_TMEM = 2848, MISC_FLAG = 2852,
+                   MISC_P12BAR = 2864;
+// (MISC_FLAG + 4: the current work item, broadcast by thread 0; MISC_P12BAR: the
+// output and state products, issued by two threads, each committing once)
 constexpr uint32_t SM_NEGI = 216064;     // -I (64 x 64 bf16, K-major): adds -V^T on the tensor core
 constexpr uint32_t SM_GA = SM_NEGI + 8192;  // g tile, tokens 0..31 (the two halves are
                                              // loaded a chunk ahead, outside the scratch)
 constexpr uint32_t SMEM_BYTES = SM_GA + 8192;
-static_assert(SM_MISC + 2880 <= SM_NEGI && SMEM_BYTES <= 232448, "shared memory map");
+static_assert(SM_MISC + MISC_P12BAR + 8 <= SM_NEGI && SMEM_BYTES <= 232448, "shared memory map");
 
 // ---- tensor memory map (columns) -------------------------------------------
 constexpr uint32_t TM_S = 0;       // S^T float32 (S'^T inside a chunk): lane = value channel
@@ -463,6 +465,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     mbar_init(&bars[1], 1);
     mbar_init(&bars[2], 1);
     mbar_init(&bars[3], 1);
+    mbar_init(reinterpret_cast<uint64_t*>(smem + SM_MISC + MISC_P12BAR), 2);
     *s_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tm_q);
@@ -506,6 +509,8 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   uint32_t g_issued = 0, g_waited = 0;  // g_waited: thread 0's count
   uint64_t* xo_bar = &bars[2];          // completion of the products with S'
   uint32_t xo_issued = 0;
+  uint64_t* p12_bar = reinterpret_cast<uint64_t*>(smem + SM_MISC + MISC_P12BAR);
+  uint32_t p12_phase = 0;               // the output and state products, both issuers
   uint32_t* s_item = s_flag + 1;
   unsigned int* next_item = p.status + 16 + p.mode;  // zeroed with the status word
 
@@ -1262,14 +1267,29 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     tc_fence_before();
     __syncthreads();
 
-    // ---- P12: O^T += U^T Aqk^T; S'^T += U^T Ck (all split; Ck is an MN-major B
-    // with N = key channel)
+    // ---- P12: S'^T += U^T Ck (thread 0) and O^T += U^T Aqk^T (thread 256), two
+    // accumulators issued side by side, each issuer committing once to p12_bar (all
+    // split; Ck is an MN-major B with N = key channel)
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t ah = sbase + SM_Y + Y_AQK_HI, al = sbase + SM_Y + Y_AQK_LO;
       const uint32_t kh = sbase + SM_X + X_CK_HI, kl = sbase + SM_X + X_CK_LO;
       const uint32_t ua[3] = {TM_UHI, TM_UHI, TM_ULO};
-      const uint32_t bq[3] = {ah, al, ah}, bk[3] = {kh, kl, kh};
+      const uint32_t bk[3] = {kh, kl, kh};
+#pragma unroll
+      for (int pr = 0; pr < 3; ++pr)
+#pragma unroll
+        for (int kk = 0; kk < C / 16; ++kk)
+          mma_ts(tb + TM_S, tb + ua[pr] + kk * 8,
+                 (smem_desc(bk[pr], 2048, 128) + (uint64_t)(kk * 256)), idesc_s, 1);
+      mma_commit(p12_bar);
+      // the next chunk's cumulative sum right behind them (ACC1 and U are free; a
+      // fused gate is still being activated, so that path issues it in P13)
+      if (!g_fill && ci + 1 < nchunks && !issue_cumsum(ci + 1)) wt.on_timeout();
+    } else if (tid == 256) {
+      tc_fence_after();
+      const uint32_t ah = sbase + SM_Y + Y_AQK_HI, al = sbase + SM_Y + Y_AQK_LO;
+      const uint32_t ua[3] = {TM_UHI, TM_UHI, TM_ULO};
+      const uint32_t bq[3] = {ah, al, ah};
       if (want_o)
 #pragma unroll
         for (int pr = 0; pr < 3; ++pr)
@@ -1277,13 +1297,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           for (int kk = 0; kk < C / 16; ++kk)
             mma_ts(tb + TM_O, tb + ua[pr] + kk * 8,
                    (smem_desc(bq[pr], 128, 1024) + (uint64_t)(kk * 16)), idesc_sq, 1);
-#pragma unroll
-      for (int pr = 0; pr < 3; ++pr)
-#pragma unroll
-        for (int kk = 0; kk < C / 16; ++kk)
-          mma_ts(tb + TM_S, tb + ua[pr] + kk * 8,
-                 (smem_desc(bk[pr], 2048, 128) + (uint64_t)(kk * 256)), idesc_s, 1);
-      mma_commit(wt.mma_bar);
+      mma_commit(p12_bar);  // (with no products it arrives at once)
     }
     // while these (longer) products run: the rest of the next chunk's gate (warps
     // 1-11) and its q/k sums of squares (warps 12-15; the tiles were requested in P8)
@@ -1294,11 +1308,16 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       }
       if (p.pre.l2 && warp >= 12) qk_sumsq(tma_issued - 1);
     }
-    if (wt.wait_mma()) break;
+    if (!mbar_wait(p12_bar, p12_phase)) wt.on_timeout();
+    p12_phase ^= 1u;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (*(volatile uint32_t*)s_flag) break;
 
-    // ---- P13: next chunk's cumulative log-decay (ACC1 and U are free); outputs;
-    // S^T <- S'^T diag(e^Gam_last / c)
-    if (tid == 0 && ci + 1 < nchunks && !issue_cumsum(ci + 1)) wt.on_timeout();
+    // ---- P13: outputs; S^T <- S'^T diag(e^Gam_last / c) (with a fused gate, the
+    // next chunk's cumulative log-decay first)
+    if (tid == 0 && g_fill && ci + 1 < nchunks && !issue_cumsum(ci + 1)) wt.on_timeout();
     {
       const int j = row;
       float o[TCOL], sv[SCOL / 16][16];
@@ -1399,6 +1418,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     for (uint32_t ph = wt.tma_waited; ph < tma_issued; ++ph)
       mbar_wait(wt.tma_bar, ph & 1u, 20000000ll);
     mbar_wait(wt.mma_bar, wt.mma_phase ^ 1u, 20000000ll);
+    mbar_wait(p12_bar, p12_phase ^ 1u, 20000000ll);
     if (xo_issued) mbar_wait(xo_bar, (xo_issued - 1) & 1u, 20000000ll);
     for (uint32_t ph = g_waited; ph < g_issued; ++ph) mbar_wait(g_bar, ph & 1u, 20000000ll);
   }
