@@ -165,9 +165,12 @@ __device__ __forceinline__ void st8_split(unsigned char* phi, unsigned char* plo
 }
 // CTA-local named barrier `id` for `count` threads (whole warps: the barrier
 // counts arrivals, the callers choose which warps arrive; here 1 = warps 0-7,
-// 2 = warps 8-15)
+// 2 = warps 8-15, 3 and 4 = warps 0-7 arriving and warp 8 waiting)
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_bar_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // m16n8k8 fragments (see mma_tf32x3) read from float matrices in shared memory:
@@ -948,6 +951,18 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                  (smem_desc(bs[pr], 128, 2048) + (uint64_t)(kk * 16)), idesc_kk, (pr | kk) != 0);
         }
     };
+    // U^T (+)= X'^T (-TB)^T over K step kk (tokens j of column block kk of TB), three
+    // split products; thread 256 issues step 3 once T's diagonal blocks are in TB,
+    // step 2 once blocks (1,0) and (3,2) are, steps 1 and 0 after the join
+    auto issue_u_step = [&](int kk) {
+      const uint32_t tbh = sbase + SM_Y + Y_TB_HI, tbl = sbase + SM_Y + Y_TB_LO;
+      const uint32_t xa[3] = {TM_UHI, TM_UHI, TM_ULO}, bt[3] = {tbh, tbl, tbh};
+#pragma unroll
+      for (int pr = 0; pr < 3; ++pr)
+        mma_ts(tb + TM_U, tb + xa[pr] + kk * 8,
+               (smem_desc(bt[pr], 128, 1024) + (uint64_t)(kk * 16)), idesc_sq,
+               kk != 3 || pr != 0);
+    };
     // R_K, R_Q and Ck of token t, channels 8 cg .. 8 cg + 7, split into the X operands;
     // rows past the sequence end are zero (their factors are never formed)
     auto decayed = [&](int cg, const float (&gm)[8]) {
@@ -1120,6 +1135,8 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
       }
       named_bar_sync(1, 256);
+      fence_proxy_async_smem();  // the diagonal blocks of TB: the U product's step 3
+      named_bar_arrive(3, 288);
       // 32 x 32 diagonal blocks: T[I, J] = -T[I, I] A[I, J] T[J, J] for (I, J) = (1, 0)
       // and (3, 2), two warps per block (one per 8-column n-tile), as m16n8k8 tf32
       // products with 3-term splitting; each warp only reads back its own columns.
@@ -1149,6 +1166,8 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                       smem + SM_Y + Y_TB_HI, smem + SM_Y + Y_TB_LO);
       }
       named_bar_sync(1, 256);
+      fence_proxy_async_smem();  // blocks (1,0) and (3,2) of TB: the U product's step 2
+      named_bar_arrive(4, 288);
       // lower-left 32 x 32 block: M = A[2..3, 0..1] T[0..1, 0..1], then
       // T[2..3, 0..1] = -T[2..3, 2..3] M; warp = (row block i, column block j, n-tile)
       {
@@ -1221,30 +1240,50 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         tmem_st8(tb + lane_base + TM_ULO + tt0 / 2, lo);
       }
       tmem_wait_st();
+      // all of X' split (and U read): the first steps of the U product, as soon as
+      // their blocks of TB are ready
+      tc_fence_before();
+      named_bar_sync(2, 256);
+      if (warp == 8) {
+        named_bar_sync(3, 288);
+        if (lane == 0) {
+          tc_fence_after();
+          issue_u_step(3);
+        }
+        __syncwarp();
+        named_bar_sync(4, 288);
+        if (lane == 0) {
+          tc_fence_after();
+          issue_u_step(2);
+        }
+        __syncwarp();
+      }
     }
     wt.mma_phase ^= 1u;  // [Akk; Aqk] consumed (waited above by warps 0-7 and thread 256)
     fence_proxy_async_smem();  // TB, written by the substitution, is an MMA operand next
     tc_fence_before();
     __syncthreads();
-    if (*(volatile uint32_t*)s_flag) break;
-
-    // ---- P8: prefetch chunk ci+1 (the q, k, v tiles are consumed; warps 1-5
-    // issue one part each); U^T = X'^T (-TB)^T with split operands
+    // ---- P8: the rest of U^T = X'^T (-TB)^T (thread 256, whose commit covers all
+    // four steps; committed also when the CTA leaves, so the drain sees them)
+    {
+      const bool leave = *(volatile uint32_t*)s_flag != 0;
+      if (tid == 256) {
+        tc_fence_after();
+        if (!leave) {
+          issue_u_step(1);
+          issue_u_step(0);
+        }
+        mma_commit(wt.mma_bar);
+      }
+      if (leave) {
+        wt.mma_phase ^= 1u;  // the drain waits for this commit
+        break;
+      }
+    }
+    // prefetch chunk ci+1 (the q, k, v tiles are consumed; warps 1-5 issue one part each)
     if (ci + 1 < nchunks) {
       if (lane == 0 && warp >= 1 && warp <= 5) issue_tma_part(ci + 1, warp - 1);
       ++tma_issued;
-    }
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t tbh = sbase + SM_Y + Y_TB_HI, tbl = sbase + SM_Y + Y_TB_LO;
-      const uint32_t xa[3] = {TM_UHI, TM_UHI, TM_ULO}, bt[3] = {tbh, tbl, tbh};
-#pragma unroll
-      for (int pr = 0; pr < 3; ++pr)
-#pragma unroll
-        for (int kk = 0; kk < C / 16; ++kk)
-          mma_ts(tb + TM_U, tb + xa[pr] + kk * 8,
-                 (smem_desc(bt[pr], 128, 1024) + (uint64_t)(kk * 16)), idesc_sq, (pr | kk) != 0);
-      mma_commit(wt.mma_bar);
     }
     // while U runs: rows 0..383 of the next chunk's gate (warps 4-15)
     if (g_fill && ci + 1 < nchunks && warp >= 4) {
