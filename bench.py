@@ -60,8 +60,9 @@ def profiled_traffic():
     import hashlib
     import re
     csrc = os.path.join(ROOT, "kda_delta_rule_fwd_gb300", "csrc")
-    srcs = [os.path.join(csrc, f) for f in ("kda_prefill_bf16.cu", "kda_internal.cuh",
-                                            "kda_mma_sync.cuh", "kda_sm100.cuh")]
+    srcs = [os.path.join(csrc, f) for f in ("kda_prefill_bf16.cu", "kda_prefill_common.cuh",
+                                            "kda_internal.cuh", "kda_mma_sync.cuh",
+                                            "kda_sm100.cuh")]
     prof = os.path.join(ROOT, "profiles", "prefill_bf16_B4_T4096_H32.txt")
     try:
         txt = open(prof).read()
