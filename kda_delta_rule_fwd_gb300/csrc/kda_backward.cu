@@ -546,8 +546,13 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
           if (l >= jj) vv = fmaf(-sbeta[m] * Pm[m * kSL + l], x[l], vv);
         x[m] = m < jj ? 0.f : vv;
       }
+      // T, and T diag(beta) for U below (M is the backward sweep's; free here)
+      const float bj = sbeta[jj];
 #pragma unroll
-      for (int m = 0; m < kBC; ++m) Tm[m * kSL + jj] = x[m];
+      for (int m = 0; m < kBC; ++m) {
+        Tm[m * kSL + jj] = x[m];
+        Mm[m * kSL + jj] = x[m] * bj;
+      }
     }
     // X = V - Kb S (one n-tile of 8 columns per warp)
     for (int nt = warp; nt < D / 8; nt += kBT / 32) {
@@ -561,13 +566,16 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
       }
     }
     __syncthreads();
-    for (int i = tid; i < kBC * D; i += kBT) {  // U = T diag(beta) X
-      const int t = i / D, j = i % D;
-      float acc = 0.f;
+    // U = (T diag(beta)) X (one n-tile of 8 columns per warp; T is lower triangular)
+    for (int nt = warp; nt < D / 8; nt += kBT / 32) {
+      float acc[3][4];
+      acc_zero(acc);
+      tile_mma<kBC>(acc, Mm, kSL, 1, 0, X, CLD, 1, nt * 8, g8, t4, 1.f);
 #pragma unroll
-      for (int s2 = 0; s2 < kBC; ++s2)
-        if (s2 <= t) acc = fmaf(Tm[t * kSL + s2] * sbeta[s2], X[s2 * CLD + j], acc);
-      U[t * CLD + j] = acc;
+      for (int e = 0; e < 4; ++e) {
+        const int r = g8 + 8 * (e >> 1), c = nt * 8 + 2 * t4 + (e & 1);
+        U[r * CLD + c] = acc_sum(acc, e);
+      }
     }
     __syncthreads();
   };
@@ -645,21 +653,29 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
       (isM ? dMm : dTm)[r * kSL + c] = (!isM || c <= r) ? v : 0.f;
     }
     if (tid < D) dgl[tid] = egl[tid] * (scg[tid] + scg[D + tid]);
-    // dY = T^T dU; dbeta += rowsum(dY . X); dX = diag(beta) dY in place of X (each
-    // thread reads and writes only its own elements of X)
-    for (int i = tid; i < kBC * D; i += kBT) {
-      const int t = i / D, j = i % D;
-      float dy = 0.f;
+    // dY = T^T dU (one n-tile of 8 columns per warp; T is lower triangular);
+    // dbeta += rowsum(dY . X); dX = diag(beta) dY in place of X (each thread reads
+    // and writes only its own elements of X)
+    for (int nt = warp; nt < D / 8; nt += kBT / 32) {
+      float acc[3][4];
+      acc_zero(acc);
+      tile_mma<kBC>(acc, Tm, 1, kSL, 0, DU, CLD, 1, nt * 8, g8, t4, 1.f);
+      float part[2] = {0.f, 0.f};
 #pragma unroll
-      for (int i2 = 0; i2 < kBC; ++i2)
-        if (i2 >= t) dy = fmaf(Tm[i2 * kSL + t], DU[i2 * CLD + j], dy);
-      float part = dy * X[t * CLD + j];
+      for (int e = 0; e < 4; ++e) {
+        const int r = g8 + 8 * (e >> 1), c = nt * 8 + 2 * t4 + (e & 1);
+        const float dy = acc_sum(acc, e);
+        part[e >> 1] = fmaf(dy, X[r * CLD + c], part[e >> 1]);
+        const float dx = sbeta[r] * dy;
+        X[r * CLD + c] = dx;
+        if (r < nv) p.dv[((t0 + cs + r) * H + h) * D + c] = dx;
+      }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-      if (lane == 0) atomicAdd(&sdb[t], part);
-      const float dx = sbeta[t] * dy;
-      X[t * CLD + j] = dx;
-      if (t < nv) p.dv[((t0 + cs + t) * H + h) * D + j] = dx;
+      for (int hh = 0; hh < 2; ++hh) {  // the row's 8 columns of this tile: lanes t4 = 0..3
+        part[hh] += __shfl_xor_sync(0xffffffffu, part[hh], 1);
+        part[hh] += __shfl_xor_sync(0xffffffffu, part[hh], 2);
+        if (t4 == 0) atomicAdd(&sdb[g8 + 8 * hh], part[hh]);
+      }
     }
     __syncthreads();  // dU is consumed: dG may take its buffer; dT and dM are complete
     // W = dT T^T (threads 0..255; M is consumed, so W takes its place)
