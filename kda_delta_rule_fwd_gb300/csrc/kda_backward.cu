@@ -243,16 +243,38 @@ __device__ __forceinline__ void acc_zero(float (&acc)[3][4]) {
 #pragma unroll
     for (int r = 0; r < 4; ++r) acc[q][r] = 0.f;
 }
-// four consecutive elements as float32 (8-byte bf16 or 16-byte float loads)
+// four consecutive float32 elements (one 16-byte load)
 __device__ __forceinline__ float4 ld4f(const float* p) { return *reinterpret_cast<const float4*>(p); }
-__device__ __forceinline__ float4 ld4f(const __nv_bfloat16* p) {
-  const uint2 u = *reinterpret_cast<const uint2*>(p);
-  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
-                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
-}
 __device__ __forceinline__ void st4(float* p, const float4& v) {
   p[0] = v.x; p[1] = v.y; p[2] = v.z; p[3] = v.w;
 }
+// four consecutive elements as loaded (8-byte bf16 or 16-byte float vectors), and
+// their float32 values; a load's result is only converted when it is stored, so no
+// instruction waits on it in between
+template <typename TIn> struct Raw4;
+template <> struct Raw4<float> {
+  using type = float4;
+  using scalar = float;
+};
+template <> struct Raw4<__nv_bfloat16> {
+  using type = uint2;
+  using scalar = unsigned short;
+};
+__device__ __forceinline__ float4 ldraw4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ uint2 ldraw4(const __nv_bfloat16* p) {
+  return *reinterpret_cast<const uint2*>(p);
+}
+__device__ __forceinline__ float4 cvt4(const float4& v) { return v; }
+__device__ __forceinline__ float4 cvt4(const uint2& u) {
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+}
+__device__ __forceinline__ float ldraw1(const float* p) { return *p; }
+__device__ __forceinline__ unsigned short ldraw1(const __nv_bfloat16* p) {
+  return __bfloat16_as_ushort(*p);
+}
+__device__ __forceinline__ float cvt1(float v) { return v; }
+__device__ __forceinline__ float cvt1(unsigned short v) { return __uint_as_float((uint32_t)v << 16); }
 
 // 16-byte asynchronous global -> shared copies (completion waited with cp_async_wait)
 __device__ __forceinline__ void cp_async16(float* dst, const float* src) {
@@ -323,35 +345,51 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
   auto state_row = [&](int64_t s) { return p.states + ((row0 + s) * H + h) * RF; };
   const int64_t sbase = ((int64_t)n * H + h) * D * D;
 
-  // the sub-chunk's inputs, four channels per thread, every load issued before
-  // the first store (rows past the sequence end are zero)
-  auto load_chunk = [&](int64_t cs, int nv, bool bwd) {
-    constexpr int G4 = D / 4;
+  // the sub-chunk's inputs, four channels per thread: fetch issues the loads (raw),
+  // stash converts and stores them once the buffers are free (rows past the
+  // sequence end are zero).  The next sub-chunk's loads are issued before the
+  // current step's last phase, so they land while it runs.
+  using RawT = typename Raw4<TIn>::type;
+  struct InFlight {
+    RawT k, g, x;  // x: v (forward sweep) or q (backward sweep)
+    float4 o;      // dout (backward sweep)
+    typename Raw4<TIn>::scalar b;
+  };
+  constexpr int G4 = D / 4;
+  auto fetch = [&](int64_t cs, int nv, bool bwd) {
+    InFlight f;
+    f.k = f.g = f.x = RawT{};
+    f.o = make_float4(0.f, 0.f, 0.f, 0.f);
+    f.b = 0;
+    const int t = tid / G4, c = (tid % G4) * 4;
+    if (tid < kBC * G4 && t < nv) {
+      const int64_t go = ((t0 + cs + t) * H + h) * D + c;
+      f.k = ldraw4(p.k + go);
+      f.g = ldraw4(p.g + go);
+      if (bwd) {
+        f.x = ldraw4(p.q + go);
+        f.o = *reinterpret_cast<const float4*>(p.dout + go);
+      } else {
+        f.x = ldraw4(p.v + go);
+      }
+    }
+    if (tid < nv && tid < kBC) f.b = ldraw1(p.beta + (t0 + cs + tid) * H + h);
+    return f;
+  };
+  auto stash = [&](const InFlight& f, bool bwd) {
     if (tid < kBC * G4) {
       const int t = tid / G4, c = (tid % G4) * 4;
-      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-      float4 fk = z, fg = z, fv = z, fq = z, fo = z;
-      if (t < nv) {
-        const int64_t go = ((t0 + cs + t) * H + h) * D + c;
-        fk = ld4f(p.k + go);
-        fg = ld4f(p.g + go);
-        if (bwd) {
-          fq = ld4f(p.q + go);
-          fo = ld4f(p.dout + go);
-        } else {
-          fv = ld4f(p.v + go);
-        }
-      }
-      st4(K + t * CLD + c, fk);
-      st4(G + t * CLD + c, fg);
-      if (!bwd) st4(X + t * CLD + c, fv);  // the backward sweep reads X itself
+      st4(K + t * CLD + c, cvt4(f.k));
+      st4(G + t * CLD + c, cvt4(f.g));
       if (bwd) {
-        st4(Q + t * CLD + c, fq);
-        st4(DO + t * CLD + c, fo);
+        st4(Q + t * CLD + c, cvt4(f.x));
+        st4(DO + t * CLD + c, f.o);
+      } else {
+        st4(X + t * CLD + c, cvt4(f.x));  // the backward sweep reads X itself
       }
     }
     if (tid < kBC) {
-      sbeta[tid] = tid < nv ? to_f32(p.beta[(t0 + cs + tid) * H + h]) : 0.f;
+      sbeta[tid] = cvt1(f.b);
       sdb[tid] = 0.f;
     }
   };
@@ -583,14 +621,16 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
   // ---- 1. forward sweep: the start state of every sub-chunk
   state_in(S, p.h0 ? p.h0 + sbase : nullptr);
   __syncthreads();
+  auto nv_of = [&](int64_t s) { return (int)(len - s * kBC < kBC ? len - s * kBC : kBC); };
+  InFlight nxt = fetch(0, nsub > 0 ? nv_of(0) : 0, false);
   for (int64_t s = 0; s < nsub; ++s) {
     const int64_t cs = s * kBC;
-    const int nv = (int)(len - cs < kBC ? len - cs : kBC);
     state_out(state_row(s), S);
-    load_chunk(cs, nv, false);
+    stash(nxt, false);
     __syncthreads();
     prepare(false);
     row_out(state_row(s));
+    if (s + 1 < nsub) nxt = fetch(cs + kBC, nv_of(s + 1), false);
     // S <- diag(e^Gl) S + Kh^T U
     dd_update<D, 1>(S, SLD, egl, CLD, KH, 1.f, U, nullptr, 0.f, nullptr, warp, g8, t4);
     __syncthreads();
@@ -598,11 +638,12 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
 
   // ---- 2. backward sweep
   state_in(dS, p.dhT ? p.dhT + sbase : nullptr);
+  if (nsub > 0) nxt = fetch((nsub - 1) * kBC, nv_of(nsub - 1), true);
   for (int64_t s = nsub - 1; s >= 0; --s) {
     const int64_t cs = s * kBC;
-    const int nv = (int)(len - cs < kBC ? len - cs : kBC);
+    const int nv = nv_of(s);
     row_in(state_row(s), s == nsub - 1);
-    load_chunk(cs, nv, true);
+    stash(nxt, true);
     __syncthreads();
     prepare(true);
 
@@ -618,13 +659,18 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
         DU[r * CLD + c] = acc_sum(acc, e);
       }
     }
-    if (tid < 2 * D) {  // dGl from the decay of the start state: e^Gl rowsum(dS . S), by halves
-      const int c = tid % D, j0 = (tid / D) * (D / 2);
-      float acc[2] = {0.f, 0.f};
-#pragma unroll 4
-      for (int j = 0; j < D / 2; ++j)
-        acc[j & 1] = fmaf(dS[c * SLD + j0 + j], S[c * SLD + j0 + j], acc[j & 1]);
-      scg[tid] = acc[0] + acc[1];
+    // dGl from the decay of the start state: e^Gl rowsum(dS . S); warp w takes rows
+    // 8 w .. 8 w + 7 (D / 16 at D = 64), a lane four consecutive columns of each
+    for (int c = warp * (D / 16); c < (warp + 1) * (D / 16); ++c) {
+      float v = 0.f;
+      for (int j = 4 * lane; j < D; j += 128) {
+        const float4 a = *reinterpret_cast<const float4*>(dS + c * SLD + j);
+        const float4 b = *reinterpret_cast<const float4*>(S + c * SLD + j);
+        v = fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, v))));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) scg[c] = v;
     }
     __syncthreads();
     // dT = dU (diag(beta) X)^T, dM = scale dO U^T (lower): warps 0..7 each take one
@@ -652,7 +698,7 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
       const bool isM = cb >= 2;
       (isM ? dMm : dTm)[r * kSL + c] = (!isM || c <= r) ? v : 0.f;
     }
-    if (tid < D) dgl[tid] = egl[tid] * (scg[tid] + scg[D + tid]);
+    if (tid < D) dgl[tid] = egl[tid] * scg[tid];
     // dY = T^T dU (one n-tile of 8 columns per warp; T is lower triangular);
     // dbeta += rowsum(dY . X); dX = diag(beta) dY in place of X (each thread reads
     // and writes only its own elements of X)
@@ -841,6 +887,7 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
       }
     }
     if (tid < nv) p.dbeta[(t0 + cs + tid) * H + h] = sdb[tid];
+    if (s > 0) nxt = fetch(cs - kBC, nv_of(s - 1), true);
     dd_update<D, 2>(dS, SLD, egl, CLD, QB, p.scale, DO, KB, -1.f, X, warp, g8, t4);
     __syncthreads();
   }
