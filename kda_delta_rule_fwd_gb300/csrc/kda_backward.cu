@@ -661,16 +661,28 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
     }
     // dGl from the decay of the start state: e^Gl rowsum(dS . S); warp w takes rows
     // 8 w .. 8 w + 7 (D / 16 at D = 64), a lane four consecutive columns of each
-    for (int c = warp * (D / 16); c < (warp + 1) * (D / 16); ++c) {
-      float v = 0.f;
-      for (int j = 4 * lane; j < D; j += 128) {
-        const float4 a = *reinterpret_cast<const float4*>(dS + c * SLD + j);
-        const float4 b = *reinterpret_cast<const float4*>(S + c * SLD + j);
-        v = fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, v))));
+    {
+      float v[D / 16];
+#pragma unroll
+      for (int r = 0; r < D / 16; ++r) {  // the rows' loads and sums interleave
+        const int c = warp * (D / 16) + r;
+        v[r] = 0.f;
+        if (4 * lane < D) {
+          const float4 a = *reinterpret_cast<const float4*>(dS + c * SLD + 4 * lane);
+          const float4 b = *reinterpret_cast<const float4*>(S + c * SLD + 4 * lane);
+          v[r] = fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
+        }
       }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0) scg[c] = v;
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int r = 0; r < D / 16; ++r) v[r] += __shfl_xor_sync(0xffffffffu, v[r], o);
+      if (lane < D / 16) {
+        float w = v[0];
+#pragma unroll
+        for (int r = 1; r < D / 16; ++r) w = lane == r ? v[r] : w;
+        scg[warp * (D / 16) + lane] = w;
+      }
     }
     __syncthreads();
     // dT = dU (diag(beta) X)^T, dM = scale dO U^T (lower): warps 0..7 each take one
