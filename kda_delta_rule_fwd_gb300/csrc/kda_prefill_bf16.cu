@@ -52,7 +52,6 @@ constexpr int SCOL = 128 / NCOL;      // state columns per thread
 constexpr int GPT = 16 / (2 * NCOL);  // 8-channel groups per thread in the elementwise passes
 static_assert(TCOL == 16 && SCOL % 16 == 0 && GPT >= 1, "thread mapping");
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kGateRowsP8 = 384;  // fused gate rows activated during the U product
 constexpr float kMaxExp2 = 115.f;  // |log2 of a decay factor| beyond this: the exact token path
 constexpr float kRefExp2 = 100.f;  // |log2 c| is clamped here (S' and its bf16 parts stay normal)
 
@@ -963,6 +962,12 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           issue_u_step(2);
         }
         __syncwarp();
+      } else if (g_fill && ci + 1 < nchunks) {
+        // fused gate: the next chunk's g tile activated while warps 0-7 solve for T
+        // (it was requested a chunk ahead); ordered before its cumulative sum by the
+        // proxy fence and the join below
+        activate_gate(ci + 1, tid - 288, 2 * kHalfRows, kThreads - 288);
+        fence_proxy_async_smem();
       }
     }
     wt.mma_phase ^= 1u;  // [Akk; Aqk] consumed (waited above by warps 0-7 and thread 256)
@@ -990,11 +995,6 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (ci + 1 < nchunks) {
       if (lane == 0 && warp >= 1 && warp <= 5) issue_tma_part(ci + 1, warp - 1);
       ++tma_issued;
-    }
-    // while U runs: rows 0..383 of the next chunk's gate (warps 4-15)
-    if (g_fill && ci + 1 < nchunks && warp >= 4) {
-      activate_gate(ci + 1, tid - 128, kGateRowsP8, kThreads - 128);
-      fence_proxy_async_smem();
     }
     if (wt.wait_mma()) break;
 
@@ -1028,8 +1028,8 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                  (smem_desc(bk[pr], 2048, 128) + (uint64_t)(kk * 256)), idesc_s, 1);
       mma_commit(p12_bar);
       // the next chunk's cumulative sum right behind them (ACC1 and U are free; a
-      // fused gate is still being activated, so that path issues it in P13)
-      if (!g_fill && ci + 1 < nchunks && !issue_cumsum(ci + 1)) wt.on_timeout();
+      // fused gate was activated during the substitution)
+      if (ci + 1 < nchunks && !issue_cumsum(ci + 1)) wt.on_timeout();
     } else if (tid == 256) {
       tc_fence_after();
       const uint32_t ah = sbase + SM_Y + Y_AQK_HI, al = sbase + SM_Y + Y_AQK_LO;
@@ -1044,15 +1044,9 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                    (smem_desc(bq[pr], 128, 1024) + (uint64_t)(kk * 16)), idesc_sq, 1);
       mma_commit(p12_bar);  // (with no products it arrives at once)
     }
-    // while these (longer) products run: the rest of the next chunk's gate (warps
-    // 1-11) and its q/k sums of squares (warps 12-15; the tiles were requested in P8)
-    if (kPre && ci + 1 < nchunks) {
-      if (g_fill && warp >= 1 && warp < 12) {
-        activate_gate(ci + 1, kGateRowsP8 + tid - 32, 2 * kHalfRows, 352);
-        fence_proxy_async_smem();
-      }
-      if (p.pre.l2 && warp >= 12) qk_sumsq(tma_issued - 1);
-    }
+    // while these products run: the next chunk's q/k sums of squares (warps 12-15;
+    // the tiles were requested in P8)
+    if (kPre && ci + 1 < nchunks && p.pre.l2 && warp >= 12) qk_sumsq(tma_issued - 1);
     if (!mbar_wait(p12_bar, p12_phase)) wt.on_timeout();
     p12_phase ^= 1u;
     tc_fence_before();
@@ -1060,9 +1054,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     tc_fence_after();
     if (*(volatile uint32_t*)s_flag) break;
 
-    // ---- P13: outputs; S^T <- S'^T diag(e^Gam_last / c) (with a fused gate, the
-    // next chunk's cumulative log-decay first)
-    if (tid == 0 && g_fill && ci + 1 < nchunks && !issue_cumsum(ci + 1)) wt.on_timeout();
+    // ---- P13: outputs; S^T <- S'^T diag(e^Gam_last / c)
     {
       const int j = row;
       float o[TCOL], sv[SCOL / 16][16];
