@@ -1,10 +1,10 @@
-"""Seeded random configurations, each compared with the float64 oracle element by
-element: the prefill (both input dtypes, both head sizes, fixed-length and packed
-batches with empty, one-token and chunk-edge lengths, with and without a start
-state, gates from the workloads' strength to ones that send whole chunks to the
-exact token path, alpha = 0 on some channels) and the decode (pool sizes, step
-counts, commit counts, both dtypes and head sizes).  The draws come from fixed
-seeds, so every run checks the same cases."""
+"""Seeded random configurations (48 prefill, 24 decode), each compared with the
+float64 oracle element by element: the prefill (both input dtypes, both head sizes,
+fixed-length and packed batches with empty, one-token and chunk-edge lengths, with and
+without a start state, gates from the workloads' strength to ones that send whole chunks
+to the exact token path, alpha = 0 on some channels) and the decode (pool sizes, step
+counts, commit counts, both dtypes and head sizes).  The draws come from fixed seeds, so
+every run checks the same cases."""
 import numpy as np
 import pytest
 import torch
@@ -46,7 +46,7 @@ def _prefill_case(i):
                                 f"alpha0={alpha0} h0={h0_std}")
 
 
-@pytest.mark.parametrize("i", range(24))
+@pytest.mark.parametrize("i", range(48))
 def test_prefill_random_case(kda, oracle_mod, i):
     x, dtype, out_bf16, desc = _prefill_case(i)
     out_dtype = torch.bfloat16 if out_bf16 else torch.float32
@@ -82,7 +82,7 @@ def _decode_case(i):
                               f"gates x{gate_mult} counts={counts}")
 
 
-@pytest.mark.parametrize("i", range(12))
+@pytest.mark.parametrize("i", range(24))
 def test_decode_random_case(kda, oracle_mod, i):
     x, dtype, counts, desc = _decode_case(i)
     state = x.h0.clone()
