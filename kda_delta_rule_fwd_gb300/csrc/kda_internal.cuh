@@ -80,10 +80,11 @@ inline size_t ws_order_bytes(int64_t n) { return (size_t)((n + 63) / 64) * 64 * 
 //
 // The plan minimises a model of the critical path in chunk-steps (one 64-token
 // chunk of one chain on one SM), counting waves of one CTA per SM on the
-// device's `sms` SMs: a split runs 2 (nseg - 1) transition CTAs per chain, then
-// nseg output CTAs per chain, each over seg_len / 64 chunks, plus the scan
-// (about half a chunk-step per segment); no split runs every chain whole.  A
-// split is taken only when the model saves at least 10%.
+// device's `sms` SMs: a split runs, per chain, segment 0 from the true start
+// state (with its outputs) and 2 (nseg - 2) transition items, then nseg - 1
+// output items, each over seg_len / 64 chunks, plus the scan (about half a
+// chunk-step per segment); no split runs every chain whole.  A split is taken
+// only when the model saves at least 10%.
 struct SegPlan {
   int nseg = 1;
   int64_t seg_len = 0;
@@ -95,8 +96,8 @@ inline int64_t plan_waves(int64_t ctas, int64_t sms) { return (ctas + sms - 1) /
 inline double plan_cost(int64_t chains, int64_t chunks, int64_t seg_chunks, int64_t nseg,
                         int64_t sms) {
   if (nseg < 2) return (double)plan_waves(chains, sms) * (double)chunks;
-  return (double)seg_chunks * (double)(plan_waves(2 * chains * (nseg - 1), sms) +
-                                       plan_waves(chains * nseg, sms)) +
+  return (double)seg_chunks * (double)(plan_waves(chains * (2 * nseg - 3), sms) +
+                                       plan_waves(chains * (nseg - 1), sms)) +
          0.5 * (double)nseg;
 }
 inline SegPlan seg_plan(bool packed, bool bf16_d128, int64_t chains, int64_t T, int64_t sms) {
@@ -276,10 +277,11 @@ cudaError_t launch_schedule(const FwdArgs& a, int32_t* order_out);
 cudaError_t launch_plan_packed(const FwdArgs& a);
 cudaError_t launch_prefill_f32(const FwdArgs& a);
 // The segment scan of the long-chain split (kda_segment_scan.cu): per chain,
-// S_0 = h0 (or 0) and S_{p+1} = M_p S_p + b_p, d = 128.  Fixed length: `chains`
-// chains of nseg segments, b of all chains, then M, then the start states.
-cudaError_t launch_segment_scan(const float* h0, const float* seg_m, const float* seg_b,
-                                float* seg_s, int64_t chains, int nseg, cudaStream_t stream);
+// S_{p+1} = M_p S_p + b_p, d = 128.  Fixed length: `chains` chains of nseg
+// segments, b of all chains, then M, then the start states; segment 0 ran from
+// the true start state, so S_1 = b_0 and the recursion starts at p = 1.
+cudaError_t launch_segment_scan(const float* seg_m, const float* seg_b, float* seg_s,
+                                int64_t chains, int nseg, cudaStream_t stream);
 // Packed: the split sequences of the device-written plan, H heads each.
 cudaError_t launch_segment_scan_packed(const float* h0, PlanView pv, float* states, int H,
                                        int64_t ns_max, int64_t sms, cudaStream_t stream);

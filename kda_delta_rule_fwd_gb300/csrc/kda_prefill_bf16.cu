@@ -1250,7 +1250,9 @@ cudaError_t run_bf16(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap&
   if (pl.nseg < 2 || !a.seg_ws) {
     return run(items);
   }
-  // long chains: transitions of all but the last segment, scan, then outputs
+  // long chains: segment 0 from the start state (with its outputs) beside the
+  // transitions of segments 1 .. nseg-2, the scan, then the outputs of segments
+  // 1 .. nseg-1
   const int64_t per = (int64_t)D * D;
   p.nseg = pl.nseg;
   p.seg_len = pl.seg_len;
@@ -1259,12 +1261,12 @@ cudaError_t run_bf16(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap&
   float* seg_s = a.seg_ws + 2 * items * (pl.nseg - 1) * per;
   p.seg_s = seg_s;
   p.mode = MODE_SEG_TRANSITION;
-  if ((e = run(items * (pl.nseg - 1) * 2)) != cudaSuccess) return e;
-  if ((e = launch_segment_scan(a.h0, p.seg_m, p.seg_b, seg_s, items, pl.nseg, a.stream)) !=
+  if ((e = run(items * (2 * pl.nseg - 3))) != cudaSuccess) return e;
+  if ((e = launch_segment_scan(p.seg_m, p.seg_b, seg_s, items, pl.nseg, a.stream)) !=
       cudaSuccess)
     return e;
   p.mode = MODE_SEG_OUTPUT;
-  return run(items * pl.nseg);
+  return run(items * (pl.nseg - 1));
 }
 }  // namespace
 

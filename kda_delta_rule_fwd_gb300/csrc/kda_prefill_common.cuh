@@ -208,11 +208,13 @@ struct Waits {
 // split each chain of a fixed-length batch into nseg segments of seg_len
 // tokens (the associative affine form of the recurrence: a segment maps its
 // start state S to M S + b):
-//   SEG_TRANSITION: per (chain, segment < nseg-1) two items: b = end state from
+//   SEG_TRANSITION: per chain, segment 0 from the chain's start state with its
+//                   outputs (its end state, in b_0's slot, is S_1), and for
+//                   segments 1 .. nseg-2 two items each: b = end state from
 //                   S = 0; M = end state from S = I with v = 0 (no outputs).
-//   SEG_OUTPUT:     per (chain, segment) one item from the segment's true start
-//                   state (computed by the scan kernel); writes o, and hT from
-//                   the last segment.
+//   SEG_OUTPUT:     per (chain, segment >= 1) one item from the segment's true
+//                   start state (computed by the scan kernel); writes o, and hT
+//                   from the last segment.
 // The two PSEG modes do the same for packed batches, item by item from the
 // device-written plan (PackedPlan): a CTA past the plan's count leaves at once;
 // an output item of a sequence that is not split runs it whole (as CHAIN).
@@ -266,8 +268,8 @@ struct ItemInfo {
 
 __device__ __forceinline__ int64_t item_count(const Bf16Params& p) {
   return p.mode == MODE_CHAIN ? (int64_t)p.nchains
-         : p.mode == MODE_SEG_TRANSITION ? (int64_t)p.nchains * (p.nseg - 1) * 2
-         : p.mode == MODE_SEG_OUTPUT ? (int64_t)p.nchains * p.nseg
+         : p.mode == MODE_SEG_TRANSITION ? (int64_t)p.nchains * (2 * p.nseg - 3)
+         : p.mode == MODE_SEG_OUTPUT ? (int64_t)p.nchains * (p.nseg - 1)
          : p.mode == MODE_PSEG_TRANSITION ? 2 * (int64_t)p.H * p.pv.hdr->n_trans
                                           : (int64_t)p.H * p.pv.hdr->n_out;
 }
@@ -320,17 +322,26 @@ __device__ __forceinline__ ItemInfo decode_item(const Bf16Params& p, int item) {
   } else {
     int seg, chain;
     if (p.mode == MODE_SEG_TRANSITION) {
-      const int kind = item & 1, rest = item >> 1;
-      seg = rest % (p.nseg - 1);
-      chain = rest / (p.nseg - 1);
-      r.ident = r.zero_v = kind == 1;
-      r.want_o = false;
-      r.s_out = (kind ? p.seg_m : p.seg_b) + ((int64_t)chain * (p.nseg - 1) + seg) * DD;
+      // per chain: item 0 is segment 0 from h0 with its outputs; items 1 + 2 (s - 1)
+      // + kind are segment s's b (kind 0) and M (kind 1), s = 1 .. nseg-2
+      const int per = 2 * p.nseg - 3, w = item % per;
+      chain = item / per;
+      if (w == 0) {
+        seg = 0;
+        r.s_in = p.h0 ? p.h0 + (int64_t)chain * DD : nullptr;
+        r.s_out = p.seg_b + (int64_t)chain * (p.nseg - 1) * DD;
+      } else {
+        const int kind = (w - 1) & 1;
+        seg = 1 + (w - 1) / 2;
+        r.ident = r.zero_v = kind == 1;
+        r.want_o = false;
+        r.s_out = (kind ? p.seg_m : p.seg_b) + ((int64_t)chain * (p.nseg - 1) + seg) * DD;
+      }
     } else {
-      seg = item % p.nseg;
-      chain = item / p.nseg;
-      // every segment, the first included, starts from the scan's copy: hT may
-      // alias h0 and the last segment's item writes hT while others still run
+      seg = 1 + item % (p.nseg - 1);
+      chain = item / (p.nseg - 1);
+      // segments 1 .. nseg-1 start from the scan's states; hT (which may alias h0)
+      // is written here, a launch after segment 0 has read h0
       r.s_in = p.seg_s + ((int64_t)chain * p.nseg + seg) * DD;
       if (seg == p.nseg - 1 && p.hT) r.s_out = p.hT + (int64_t)chain * DD;
     }

@@ -84,14 +84,16 @@ __device__ void scan_block(const float* __restrict__ h0c, const float* __restric
 }
 
 // Fixed-length batches: CTA (chain, column block); every chain nseg segments.
+// Segment 0 ran from the chain's true start state, so b_0 is S_1 itself and the
+// recursion starts there: S_{p+1} = M_p S_p + b_p for p = 1 .. nseg-2 (M_0 is not
+// formed; S_0's slot is not used).
 __global__ void __launch_bounds__(kThreads)
-kda_segment_scan_kernel(const float* __restrict__ h0, const float* __restrict__ seg_m,
-                        const float* __restrict__ seg_b, float* __restrict__ seg_s, int nseg) {
+kda_segment_scan_kernel(const float* __restrict__ seg_m, const float* __restrict__ seg_b,
+                        float* __restrict__ seg_s, int nseg) {
   extern __shared__ __align__(16) float sm[];
-  const int64_t chain = blockIdx.x / kBlocks;
-  scan_block(h0 ? h0 + chain * D * D : nullptr, seg_m + chain * (nseg - 1) * D * D,
-             seg_b + chain * (nseg - 1) * D * D, seg_s + chain * nseg * D * D, nseg,
-             blockIdx.x % kBlocks, sm);
+  const int64_t chain = blockIdx.x / kBlocks, per = (int64_t)(nseg - 1) * D * D;
+  scan_block(seg_b + chain * per, seg_m + chain * per + D * D, seg_b + chain * per + D * D,
+             seg_s + chain * nseg * D * D + D * D, nseg - 1, blockIdx.x % kBlocks, sm);
 }
 
 // Packed batches: (split sequence, head, column block) of the plan, grid-stride.
@@ -115,13 +117,13 @@ kda_segment_scan_packed_kernel(const float* __restrict__ h0, PlanView pv,
 
 }  // namespace
 
-cudaError_t launch_segment_scan(const float* h0, const float* seg_m, const float* seg_b,
-                                float* seg_s, int64_t chains, int nseg, cudaStream_t stream) {
+cudaError_t launch_segment_scan(const float* seg_m, const float* seg_b, float* seg_s,
+                                int64_t chains, int nseg, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kda_segment_scan_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
   if (e != cudaSuccess) return e;
   kda_segment_scan_kernel<<<(unsigned)(chains * kBlocks), kThreads, kSmem, stream>>>(
-      h0, seg_m, seg_b, seg_s, nseg);
+      seg_m, seg_b, seg_s, nseg);
   return cudaGetLastError();
 }
 

@@ -176,19 +176,21 @@ def test_binding_refuses_to_run_without_library(tmp_path):
 def test_workspace_size_long_chain_split(lib):
     """A fixed-length bf16 batch of few, very long chains reserves (3 nseg - 2)
     segment states of 128x128 fp32 per chain.  The segment count minimises the
-    waves of CTAs on 152 SMs: B=1, T=2^20, H=32 (16384 chunks) -> 8 segments
-    (448 transition CTAs in 3 waves, 256 output CTAs in 2, of 2048 chunks each,
-    against 11 waves of 1024 chunks for 16 segments); B=1, T=64*255, H=2 -> 3."""
+    waves of items on 152 SMs, where a chain's first launch runs segment 0 from its
+    start state beside 2 (nseg - 2) transition items and the second the other nseg - 1
+    segments: B=1, T=2^20, H=32 (16384 chunks) -> 5 segments (224 items in 2 waves,
+    then 128 in 1, of 3277 chunks each: 9833.5 chunk-steps, against 3 + 2 waves of
+    2048 chunks for 8 segments: 10244); B=1, T=64*255, H=2 -> 3."""
     m, L = lib
-    assert m.workspace_size(_shape(m, B=1, T=1 << 20, H=32)) == 256 + 32 * 22 * 128 * 128 * 4
+    assert m.workspace_size(_shape(m, B=1, T=1 << 20, H=32)) == 256 + 32 * 13 * 128 * 128 * 4
     assert m.workspace_size(_shape(m, B=1, T=64 * 255, H=2)) == 256 + 2 * 7 * 128 * 128 * 4
     # one chain: every split is two single waves, so more segments always model
     # faster and the cap of 64 applies (190 states)
     assert m.workspace_size(_shape(m, B=1, T=1 << 20, H=1)) == 256 + 190 * 128 * 128 * 4
-    # 8 chains of 1024 chunks: at most 16 segments of >= 64 chunks, which take 2 + 1
-    # waves of 64 chunks (192 chunk-steps + 8 of scan); every smaller count models
-    # more (the closest, 10 segments: 1 + 1 waves of 103 chunks + 5 = 211)
-    assert m.workspace_size(_shape(m, B=8, T=1 << 16, H=1)) == 256 + 8 * 46 * 128 * 128 * 4
+    # 8 chains of 1024 chunks: 11 segments of 94 chunks take 1 + 1 waves (152 and 80
+    # items; 188 chunk-steps + 5.5 of scan); 16 segments of 64 chunks take 2 + 1
+    # (192 + 8), 10 of 103 chunks 1 + 1 (206 + 5)
+    assert m.workspace_size(_shape(m, B=8, T=1 << 16, H=1)) == 256 + 8 * 31 * 128 * 128 * 4
     # float32 inputs, many chains or short chains never split; at 64 chains no split
     # saves 10% (two waves of half-length segments cost what one unsplit wave does)
     assert m.workspace_size(_shape(m, B=1, T=1 << 20, H=32, in_dtype=m.KDA_F32)) == 256
