@@ -76,7 +76,7 @@ constexpr uint32_t Y_TB_HI = 0, Y_TB_LO = 8192, Y_AQK_HI = 16384, Y_AQK_LO = 245
 constexpr uint32_t Y_RED = 16384, Y_KQ = 16384 + 8192;
 constexpr uint32_t SM_LL = 196608;       // [L; L] 128 x 64 bf16 (lower-triangular ones)
 constexpr uint32_t SM_MISC = 212992;
-constexpr uint32_t MISC_RHO = 0, MISC_GL = 512, MISC_C = 1024, MISC_NRHO = 1536, MISC_GAMC = 2048,
+constexpr uint32_t MISC_PEND = 0, MISC_GL = 512, MISC_C = 1024, MISC_NRHO = 1536, MISC_GAMC = 2048,
                    MISC_BETA = 2560, MISC_BAR = 2816, MISC_TMEM = 2848, MISC_FLAG = 2852,
                    MISC_P12BAR = 2864;
 // (MISC_FLAG + 4: the current work item, broadcast by thread 0; MISC_P12BAR: the
@@ -121,7 +121,9 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int cq = warp >> 2;         // which column slice of the accumulators this warp handles
   const int row = qd * 32 + lane;   // TMEM lane (accumulator row) of this thread
 
-  float* s_rho = reinterpret_cast<float*>(smem + SM_MISC + MISC_RHO);
+  // the factor e^Gam_last / c of the last tensor-core chunk, per key channel, that
+  // the state in TMEM still owes (1 at an item's start and after a token chunk)
+  float* s_pend = reinterpret_cast<float*>(smem + SM_MISC + MISC_PEND);
   float* s_gl = reinterpret_cast<float*>(smem + SM_MISC + MISC_GL);
   float* s_c = reinterpret_cast<float*>(smem + SM_MISC + MISC_C);
   float* s_nrho = reinterpret_cast<float*>(smem + SM_MISC + MISC_NRHO);
@@ -301,6 +303,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       tmem_st16(tb + lane_base + TM_S + c0, u);
     }
     tmem_wait_st();
+    if (tid < D) s_pend[tid] = 1.f;
   }
   tc_fence_before();
   __syncthreads();
@@ -453,11 +456,12 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       tmem_wait_ld();
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
-        sv[e] = a0[e];
-        sv[16 + e] = a1[e];
+        sv[e] = a0[e] * s_pend[cq * SCOL + e];
+        sv[16 + e] = a1[e] * s_pend[cq * SCOL + 16 + e];
       }
     }
-    __syncthreads();  // alpha and k . q in place
+    __syncthreads();  // alpha and k . q in place (and s_pend read)
+    if (tid < D) s_pend[tid] = 1.f;  // the state goes back to TMEM owing nothing
     const int j = row;
     const uint8_t* vcol = smem + SM_IN_V + (j >> 3) * (C * 16) + (j & 7) * 2;
     const int64_t obase = ((t0 + cs) * p.H + h) * D + j, ostride = (int64_t)p.H * D;
@@ -614,13 +618,12 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     tmem_ld8(tb + lane_base + TM_ACC1 + cgA * 8, gam[0]);
     tmem_ld8(tb + lane_base + TM_ACC1 + (cgA + 8) * 8, gam[1]);
     tmem_wait_ld();
-    if (t == rho_t)  // log2 c per channel (s_rho, and its negative, hold it from here on)
+    if (t == rho_t)  // log2 c per channel (s_nrho holds its negative from here on)
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float r = ref_log2(gam[hf][e]);
-          s_rho[(cgA + 8 * hf) * 8 + e] = r;
           s_nrho[(cgA + 8 * hf) * 8 + e] = -r;
         }
     if (t == nv - 1)
@@ -636,7 +639,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       inv_q = inv_l2(s_nrm[C + t]);
     }
     if (tid < D) {
-      const float e2 = s_rho[tid];
+      const float e2 = -s_nrho[tid];
       s_c[tid] = ldexpf(1.f, (int)e2);
       s_gamc[tid] = ex2(s_gl[tid] * kLog2e - e2);  // e^Gam_last / c
     }
@@ -735,7 +738,9 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
 
     // ---- P4: the second half of [Akk; Aqk] (thread 0), while every thread
-    // rescales its slice of the state: S' = S diag(c) (transposed), bf16 parts
+    // rescales its slice of the state: S = S_prev diag(e^Gam_last / c_prev), the
+    // factor the previous chunk left owing, then S' = S diag(c) (exact: c is a power
+    // of two), both transposed, with the bf16 parts of S'
     if (tid == 0) {
       tc_fence_after();
       issue_akk(1);
@@ -754,8 +759,13 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
         for (int e = 0; e < 16; e += 4) {
           const float4 c4 = *reinterpret_cast<const float4*>(s_c + c0 + e);
-          const float2 a = mul2(make_float2(sv[q4][e], sv[q4][e + 1]), make_float2(c4.x, c4.y));
-          const float2 b = mul2(make_float2(sv[q4][e + 2], sv[q4][e + 3]), make_float2(c4.z, c4.w));
+          const float4 p4 = *reinterpret_cast<const float4*>(s_pend + c0 + e);
+          // two roundings at most: the product with the owed factor, then the exact
+          // power-of-two scaling (one combined factor could underflow)
+          const float2 a = mul2(mul2(make_float2(sv[q4][e], sv[q4][e + 1]), make_float2(p4.x, p4.y)),
+                                make_float2(c4.x, c4.y));
+          const float2 b = mul2(mul2(make_float2(sv[q4][e + 2], sv[q4][e + 3]), make_float2(p4.z, p4.w)),
+                                make_float2(c4.z, c4.w));
           sv[q4][e] = a.x;
           sv[q4][e + 1] = a.y;
           sv[q4][e + 2] = b.x;
@@ -1054,47 +1064,28 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     tc_fence_after();
     if (*(volatile uint32_t*)s_flag) break;
 
-    // ---- P13: outputs; S^T <- S'^T diag(e^Gam_last / c)
+    // ---- P13: outputs.  The state stays S'^T in TMEM, owing diag(e^Gam_last / c):
+    // the next chunk's P4 (or token path, or the item's end) applies it.
     {
       const int j = row;
-      float o[TCOL], sv[SCOL / 16][16];
+      float o[TCOL];
       tmem_ld16(tb + lane_base + TM_O + cq * TCOL, o);
-#pragma unroll
-      for (int q4 = 0; q4 < SCOL / 16; ++q4)
-        tmem_ld16(tb + lane_base + TM_S + cq * SCOL + q4 * 16, sv[q4]);
-      tmem_wait_ld();
       // a checkpoint when rel0 + (ci + 1) C tokens of the sequence are done and that
       // is a multiple of the interval: state [key channel][value channel]
       const int64_t done = rel0 + cs + C;
-      float* ck = (ck_base >= 0 && nv == C && done % p.ckpt_interval == 0)
-                      ? p.ckpt + ((ck_base + done / p.ckpt_interval - 1) * p.H + h) * D * D + j
-                      : nullptr;
+      if (ck_base >= 0 && nv == C && done % p.ckpt_interval == 0) {
+        float* ck = p.ckpt + ((ck_base + done / p.ckpt_interval - 1) * p.H + h) * D * D + j;
+#pragma unroll 1
+        for (int c0 = cq * SCOL; c0 < cq * SCOL + SCOL; c0 += 16) {
+          float sv[16];
+          tmem_ld16(tb + lane_base + TM_S + c0, sv);
+          tmem_wait_ld();
 #pragma unroll
-      for (int q4 = 0; q4 < SCOL / 16; ++q4) {
-        const int c0 = cq * SCOL + q4 * 16;
-        uint32_t w[16];
-#pragma unroll
-        for (int e = 0; e < 16; e += 4) {
-          const float4 g4 = *reinterpret_cast<const float4*>(s_gamc + c0 + e);
-          const float2 a = mul2(make_float2(sv[q4][e], sv[q4][e + 1]), make_float2(g4.x, g4.y));
-          const float2 b = mul2(make_float2(sv[q4][e + 2], sv[q4][e + 3]), make_float2(g4.z, g4.w));
-          sv[q4][e] = a.x;
-          sv[q4][e + 1] = a.y;
-          sv[q4][e + 2] = b.x;
-          sv[q4][e + 3] = b.y;
-        }
-#pragma unroll
-        for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(sv[q4][e]);
-        tmem_st16(tb + lane_base + TM_S + c0, w);
-      }
-      if (ck) {
-#pragma unroll
-        for (int q4 = 0; q4 < SCOL / 16; ++q4) {
-          const int c0 = cq * SCOL + q4 * 16;
-#pragma unroll
-          for (int e = 0; e < 16; ++e) ck[(int64_t)(c0 + e) * D] = sv[q4][e];  // rescaled above
+          for (int e = 0; e < 16; ++e) ck[(int64_t)(c0 + e) * D] = sv[e] * s_gamc[c0 + e];
         }
       }
+      tmem_wait_ld();
+      if (tid < D) s_pend[tid] = s_gamc[tid];
       if (want_o && nv == C) {
         // full chunk: stage [token][value channel] in X, one bulk tensor store below
         if (p.out_bf16) {
@@ -1125,7 +1116,6 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           }
         }
       }
-      tmem_wait_st();
     }
     tc_fence_before();
     __syncthreads();
@@ -1147,7 +1137,7 @@ kda_prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       tmem_ld16(tb + lane_base + TM_S + c0, s);
       tmem_wait_ld();
 #pragma unroll
-      for (int e = 0; e < 16; ++e) hTp[(int64_t)(c0 + e) * D + j] = s[e];
+      for (int e = 0; e < 16; ++e) hTp[(int64_t)(c0 + e) * D + j] = s[e] * s_pend[c0 + e];
     }
   }
   if (aborted && tid == 0) {
