@@ -73,32 +73,51 @@ constexpr size_t kWsHeader = 256;
 inline size_t ws_order_bytes(int64_t n) { return (size_t)((n + 63) / 64) * 64 * 4; }
 
 // Long-chain split for fixed-length bf16 batches with few (sequence, head)
-// chains: each chain is cut into nseg segments of seg_len tokens so that the
-// device has enough independent work (the segments are joined exactly through
-// their affine state transitions).  A pure function of the shape, so that the
+// chains: each chain is cut into nseg segments, so that the device has enough
+// independent work (the segments are joined exactly through their affine state
+// transitions).  Segment 0 has seg0_len tokens and segments 1 .. nseg-1 seg_len
+// each (the last may be shorter).  A pure function of the shape, so that the
 // workspace size can be computed without a device.
 //
 // The plan minimises a model of the critical path in chunk-steps (one 64-token
-// chunk of one chain on one SM), counting waves of one CTA per SM on the
-// device's `sms` SMs: a split runs, per chain, segment 0 from the true start
-// state (with its outputs) and 2 (nseg - 2) transition items, then nseg - 1
-// output items, each over seg_len / 64 chunks, plus the scan (about half a
-// chunk-step per segment); no split runs every chain whole.  A split is taken
-// only when the model saves at least 10%.
+// chunk of one chain on one SM) on the device's `sms` SMs, one CTA per SM taking
+// the next item as it frees up.  Per chain, the first launch runs segment 0 from
+// the true start state (with its outputs) and 2 (nseg - 2) transition items, the
+// segment-0 items first; the second launch runs the nseg - 1 output items; the
+// scan costs about half a chunk-step per segment.  Segment 0 runs once while the
+// others run in both launches, so it may be longer than the others: its length is
+// seg_len times 1, 1.5, 2, 2.5 or 3, whichever models fastest.  A split is taken
+// only when the model saves at least 10% over running every chain whole.
 struct SegPlan {
   int nseg = 1;
-  int64_t seg_len = 0;
+  int64_t seg_len = 0;   // tokens of segments 1 .. nseg-1
+  int64_t seg0_len = 0;  // tokens of segment 0 (at least seg_len)
 };
 constexpr int64_t kGb300Sms = 152;     // the plan's SM count when no device can be queried
 constexpr int64_t kSegMinChunks = 64;  // at least this many 64-token chunks per segment
 constexpr int64_t kSegMaxSegs = 64;
 inline int64_t plan_waves(int64_t ctas, int64_t sms) { return (ctas + sms - 1) / sms; }
-inline double plan_cost(int64_t chains, int64_t chunks, int64_t seg_chunks, int64_t nseg,
-                        int64_t sms) {
+// Finishing time of n1 items of a chunk-steps, taken first, then n2 items of b <= a,
+// on m CTAs that each take the next item when free (n1 < m): the n1 CTAs of the
+// long items join the others at time a.
+inline int64_t plan_makespan(int64_t n1, int64_t a, int64_t n2, int64_t b, int64_t m) {
+  int64_t last = n1 > 0 ? a : 0, tx = 0, ty = a, rem = n2;
+  const int64_t gx = m - n1, gy = n1;
+  while (rem > 0) {
+    const bool x = gx > 0 && (tx <= ty || gy == 0);
+    const int64_t g = x ? gx : gy;
+    int64_t& t = x ? tx : ty;
+    rem -= rem < g ? rem : g;
+    if (t + b > last) last = t + b;
+    t += b;
+  }
+  return last;
+}
+inline double plan_cost(int64_t chains, int64_t chunks, int64_t seg0_chunks, int64_t seg_chunks,
+                        int64_t nseg, int64_t sms) {
   if (nseg < 2) return (double)plan_waves(chains, sms) * (double)chunks;
-  return (double)seg_chunks * (double)(plan_waves(chains * (2 * nseg - 3), sms) +
-                                       plan_waves(chains * (nseg - 1), sms)) +
-         0.5 * (double)nseg;
+  return (double)plan_makespan(chains, seg0_chunks, chains * 2 * (nseg - 2), seg_chunks, sms) +
+         (double)(plan_waves(chains * (nseg - 1), sms) * seg_chunks) + 0.5 * (double)nseg;
 }
 inline SegPlan seg_plan(bool packed, bool bf16_d128, int64_t chains, int64_t T, int64_t sms) {
   SegPlan pl;
@@ -106,20 +125,34 @@ inline SegPlan seg_plan(bool packed, bool bf16_d128, int64_t chains, int64_t T, 
   if (sms < 1) sms = kGb300Sms;
   if (packed || !bf16_d128 || chains <= 0 || chains >= sms || chunks < 2 * kSegMinChunks)
     return pl;
-  double best = 0.9 * plan_cost(chains, chunks, chunks, 1, sms);
+  double best = 0.9 * plan_cost(chains, chunks, chunks, chunks, 1, sms);
   const int64_t max_ns = chunks / kSegMinChunks < kSegMaxSegs ? chunks / kSegMinChunks
                                                               : kSegMaxSegs;
   for (int64_t ns = 2; ns <= max_ns; ++ns) {
-    const int64_t seg = (chunks + ns - 1) / ns, nseg = (chunks + seg - 1) / seg;
-    const double c = plan_cost(chains, chunks, seg, nseg, sms);
-    if (c < best) {
-      best = c;
-      pl.nseg = (int)nseg;
-      pl.seg_len = seg * 64;
+    for (int r2 = 2; r2 <= 6; ++r2) {  // segment 0 r2 / 2 times as long as the others
+      int64_t seg, seg0, nseg;
+      if (r2 == 2) {  // equal segments, the last one shorter
+        seg = (chunks + ns - 1) / ns;
+        nseg = (chunks + seg - 1) / seg;
+        seg0 = seg;
+      } else {  // segments 1 .. ns-1 of seg chunks, segment 0 the rest
+        seg = (2 * chunks + r2 + 2 * (ns - 1) - 1) / (r2 + 2 * (ns - 1));
+        nseg = ns;
+        seg0 = chunks - (ns - 1) * seg;
+        if (seg < kSegMinChunks || seg0 < seg) continue;
+      }
+      const double c = plan_cost(chains, chunks, seg0, seg, nseg, sms);
+      if (c < best) {
+        best = c;
+        pl.nseg = (int)nseg;
+        pl.seg_len = seg * 64;
+        pl.seg0_len = seg0 * 64;
+      }
     }
   }
   return pl;
 }
+
 // bytes of segment states: b and M for segments 0..nseg-2, start states for 0..nseg-1
 inline size_t seg_bytes(const SegPlan& pl, int64_t chains, int D) {
   if (pl.nseg < 2) return 0;

@@ -1246,6 +1246,7 @@ cudaError_t run_bf16(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap&
   const int64_t per = (int64_t)D * D;
   p.nseg = pl.nseg;
   p.seg_len = pl.seg_len;
+  p.seg0_len = pl.seg0_len;
   p.seg_b = a.seg_ws;
   p.seg_m = a.seg_ws + items * (pl.nseg - 1) * per;
   float* seg_s = a.seg_ws + 2 * items * (pl.nseg - 1) * per;
@@ -1292,7 +1293,7 @@ cudaError_t launch_prefill_bf16(const FwdArgs& a) {
   p.status = a.status;
   p.mode = MODE_CHAIN;
   p.nseg = 1;
-  p.seg_len = 0;
+  p.seg_len = p.seg0_len = 0;
   p.seg_b = p.seg_m = nullptr;
   p.seg_s = nullptr;
   p.ckpt = a.ckpt;

@@ -205,13 +205,15 @@ struct Waits {
 };
 
 // Work item modes.  CHAIN: one CTA per (sequence, head).  The two SEG modes
-// split each chain of a fixed-length batch into nseg segments of seg_len
-// tokens (the associative affine form of the recurrence: a segment maps its
-// start state S to M S + b):
+// split each chain of a fixed-length batch into nseg segments, segment 0 of
+// seg0_len tokens and the others of seg_len (the associative affine form of the
+// recurrence: a segment maps its start state S to M S + b):
 //   SEG_TRANSITION: per chain, segment 0 from the chain's start state with its
 //                   outputs (its end state, in b_0's slot, is S_1), and for
 //                   segments 1 .. nseg-2 two items each: b = end state from
 //                   S = 0; M = end state from S = I with v = 0 (no outputs).
+//                   The segment-0 items of all chains come first (the longest
+//                   items are taken first).
 //   SEG_OUTPUT:     per (chain, segment >= 1) one item from the segment's true
 //                   start state (computed by the scan kernel); writes o, and hT
 //                   from the last segment.
@@ -240,7 +242,8 @@ struct Bf16Params {
   unsigned int* status;  // status word; words 16 + mode count each launch's taken items
   int mode;
   int nseg;
-  int64_t seg_len;       // tokens per segment (multiple of the chunk length)
+  int64_t seg_len;       // tokens per segment 1 .. nseg-1 (multiple of the chunk length)
+  int64_t seg0_len;      // tokens of segment 0 (multiple of the chunk length)
   float* seg_b;          // [chains][nseg-1][D][D] zero-start end states
   float* seg_m;          // [chains][nseg-1][D][D] transitions
   const float* seg_s;    // [chains][nseg][D][D] segment start states (index 0 unused)
@@ -322,17 +325,19 @@ __device__ __forceinline__ ItemInfo decode_item(const Bf16Params& p, int item) {
   } else {
     int seg, chain;
     if (p.mode == MODE_SEG_TRANSITION) {
-      // per chain: item 0 is segment 0 from h0 with its outputs; items 1 + 2 (s - 1)
-      // + kind are segment s's b (kind 0) and M (kind 1), s = 1 .. nseg-2
-      const int per = 2 * p.nseg - 3, w = item % per;
-      chain = item / per;
-      if (w == 0) {
+      // items 0 .. nchains-1: segment 0 of each chain from h0 with its outputs; then
+      // per chain, items 2 (s - 1) + kind: segment s's b (kind 0) and M (kind 1),
+      // s = 1 .. nseg-2
+      if (item < p.nchains) {
+        chain = item;
         seg = 0;
         r.s_in = p.h0 ? p.h0 + (int64_t)chain * DD : nullptr;
         r.s_out = p.seg_b + (int64_t)chain * (p.nseg - 1) * DD;
       } else {
-        const int kind = (w - 1) & 1;
-        seg = 1 + (w - 1) / 2;
+        const int per = 2 * (p.nseg - 2), w = item - p.nchains;
+        chain = w / per;
+        const int kind = (w % per) & 1;
+        seg = 1 + (w % per) / 2;
         r.ident = r.zero_v = kind == 1;
         r.want_o = false;
         r.s_out = (kind ? p.seg_m : p.seg_b) + ((int64_t)chain * (p.nseg - 1) + seg) * DD;
@@ -349,11 +354,12 @@ __device__ __forceinline__ ItemInfo decode_item(const Bf16Params& p, int item) {
     r.h = chain % p.H;
     int64_t st, ln;
     p.seqs.get(r.n, st, ln);
-    const int64_t a = (int64_t)seg * p.seg_len;
+    const int64_t a = seg == 0 ? 0 : p.seg0_len + (int64_t)(seg - 1) * p.seg_len;
+    const int64_t sl = seg == 0 ? p.seg0_len : p.seg_len;
     r.rel0 = a;
     r.seq_len = ln;
     r.t0 = st + a;
-    r.len = ln - a < p.seg_len ? ln - a : p.seg_len;
+    r.len = ln - a < sl ? ln - a : sl;
     if (r.len < 0) r.len = 0;
   }
   return r;

@@ -175,12 +175,15 @@ def test_binding_refuses_to_run_without_library(tmp_path):
 
 def test_workspace_size_long_chain_split(lib):
     """A fixed-length bf16 batch of few, very long chains reserves (3 nseg - 2)
-    segment states of 128x128 fp32 per chain.  The segment count minimises the
-    waves of items on 152 SMs, where a chain's first launch runs segment 0 from its
-    start state beside 2 (nseg - 2) transition items and the second the other nseg - 1
-    segments: B=1, T=2^20, H=32 (16384 chunks) -> 5 segments (224 items in 2 waves,
-    then 128 in 1, of 3277 chunks each: 9833.5 chunk-steps, against 3 + 2 waves of
-    2048 chunks for 8 segments: 10244); B=1, T=64*255, H=2 -> 3."""
+    segment states of 128x128 fp32 per chain.  The plan minimises the finishing time
+    of the items on 152 SMs, each SM taking the next item when free: a chain's first
+    launch runs segment 0 from its start state (all chains' first) beside 2 (nseg - 2)
+    transition items, the second the other nseg - 1 segments, and segment 0 may be up
+    to 3 times as long as the others.  B=1, T=2^20, H=32 (16384 chunks) -> 5 segments,
+    segment 0 of 5460 chunks and the others of 2731: the 32 long items and 120 short
+    ones start together, the other 72 short ones follow on the 120 SMs, so the first
+    launch ends at 5462 and the second (128 items) at 2731 more: 8195.5 chunk-steps
+    with the scan, against 9833.5 for 5 equal segments; B=1, T=64*255, H=2 -> 3."""
     m, L = lib
     assert m.workspace_size(_shape(m, B=1, T=1 << 20, H=32)) == 256 + 32 * 13 * 128 * 128 * 4
     assert m.workspace_size(_shape(m, B=1, T=64 * 255, H=2)) == 256 + 2 * 7 * 128 * 128 * 4
@@ -191,10 +194,12 @@ def test_workspace_size_long_chain_split(lib):
     # items; 188 chunk-steps + 5.5 of scan); 16 segments of 64 chunks take 2 + 1
     # (192 + 8), 10 of 103 chunks 1 + 1 (206 + 5)
     assert m.workspace_size(_shape(m, B=8, T=1 << 16, H=1)) == 256 + 8 * 31 * 128 * 128 * 4
-    # float32 inputs, many chains or short chains never split; at 64 chains no split
-    # saves 10% (two waves of half-length segments cost what one unsplit wave does)
+    # 64 chains: 3 segments, segment 0 of 8192 chunks beside the 128 transition items
+    # of segment 1 (4096 chunks each, on the other 88 SMs and then 40 of them), then
+    # 128 output items: 12289.5 chunk-steps against 16384 for the chains whole
+    assert m.workspace_size(_shape(m, B=2, T=1 << 20, H=32)) == 256 + 64 * 7 * 128 * 128 * 4
+    # float32 inputs, many chains or short chains never split
     assert m.workspace_size(_shape(m, B=1, T=1 << 20, H=32, in_dtype=m.KDA_F32)) == 256
-    assert m.workspace_size(_shape(m, B=2, T=1 << 20, H=32)) == 256
     assert m.workspace_size(_shape(m, B=4, T=4096, H=32)) == 256
     assert m.workspace_size(_shape(m, B=1, T=64 * 127, H=2)) == 256
     # the split is optional: the minimum workspace is still accepted

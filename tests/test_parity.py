@@ -407,8 +407,8 @@ def test_long_chain_split_matches_oracle_and_unsplit_run(kda, oracle_mod):
 
 def test_long_chain_split_many_segments(kda, oracle_mod):
     """One chain of 2561 chunks (ragged last chunk): the plan cuts it into 40
-    segments of 65 chunks, composed by 39 steps of the segment scan; split and
-    unsplit runs both match the oracle."""
+    segments (the first of 65 chunks, the others of 64), composed by 39 steps of the
+    segment scan; split and unsplit runs both match the oracle."""
     x = kda_inputs.fixed(1, 64 * 64 * 40 + 17, 1, 128, dtype=torch.bfloat16, device=DEV,
                          seed=78, h0_std=0.1)
     shape = kda.make_shape(x.q, x.v)
@@ -421,6 +421,29 @@ def test_long_chain_split_many_segments(kda, oracle_mod):
     for o, h in ((o_s, h_s), (o_u, h_u)):
         assert rel_err(o, o_ref) <= TOL_BF16
         assert rel_err(h, h_ref) <= TOL_BF16
+
+
+def test_long_chain_split_longer_first_segment(kda, oracle_mod):
+    """32 chains of 384 chunks with start states: the plan makes segment 0 twice as
+    long as the other four (128 and 64 chunks), since it runs once, in the first
+    launch, beside the 192 transition items of the others.  Three sampled heads
+    match the oracle; every head matches the unsplit run."""
+    x = kda_inputs.fixed(1, 64 * 384, 32, 128, dtype=torch.bfloat16, device=DEV, seed=79,
+                         h0_std=0.1)
+    shape = kda.make_shape(x.q, x.v)
+    assert kda.workspace_size(shape) == 256 + 32 * (3 * 5 - 2) * 128 * 128 * 4
+    o_s, h_s = kda.fwd(x.q, x.k, x.v, x.g, x.beta, h0=x.h0)
+    small = torch.empty(256, dtype=torch.uint8, device=DEV)
+    o_u, h_u = kda.fwd(x.q, x.k, x.v, x.g, x.beta, h0=x.h0, workspace=small)
+    torch.cuda.synchronize()
+    assert rel_err(o_s, o_u.double().cpu().numpy()) <= 1e-3
+    assert rel_err(h_s, h_u.double().cpu().numpy()) <= 1e-3
+    heads = [0, 17, 31]
+    sub = lambda t: t[:, :, heads].contiguous().cpu()
+    o_ref, h_ref = oracle_mod.recurrent(*(sub(t) for t in (x.q, x.k, x.v, x.g, x.beta)),
+                                        h0=x.h0[:, heads].contiguous().cpu())
+    assert rel_err(o_s[:, :, heads], o_ref) <= TOL_BF16
+    assert rel_err(h_s[:, heads], h_ref) <= TOL_BF16
 
 
 def test_bounded_wait_runs_out_and_is_reported(kda, oracle_mod):
