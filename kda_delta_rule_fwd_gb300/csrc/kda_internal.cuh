@@ -100,7 +100,8 @@ inline int64_t plan_waves(int64_t ctas, int64_t sms) { return (ctas + sms - 1) /
 // Finishing time of n1 items of a chunk-steps, taken first, then n2 items of b <= a,
 // on m CTAs that each take the next item when free (n1 < m): the n1 CTAs of the
 // long items join the others at time a.
-inline int64_t plan_makespan(int64_t n1, int64_t a, int64_t n2, int64_t b, int64_t m) {
+__host__ __device__ inline int64_t plan_makespan(int64_t n1, int64_t a, int64_t n2, int64_t b,
+                                                 int64_t m) {
   int64_t last = n1 > 0 ? a : 0, tx = 0, ty = a, rem = n2;
   const int64_t gx = m - n1, gy = n1;
   while (rem > 0) {
@@ -159,23 +160,29 @@ inline size_t seg_bytes(const SegPlan& pl, int64_t chains, int D) {
   return (size_t)chains * (size_t)(3 * pl.nseg - 2) * (size_t)D * D * sizeof(float);
 }
 
-// Long-chain split for packed bf16 batches.  The lengths are only on the
-// device, so a planner kernel (one CTA) reads the validated cu_seqlens, picks a
-// segment length S (64-token chunks) from a cost model, and writes the plan
-// into the workspace: every sequence of at least 2 S chunks is cut into
-// floor(chunks / S) segments of equal length (up to 64), the others run whole.
-// The passes (transitions, scan, outputs) launch over grids sized by an upper
-// bound; CTAs past the plan's counts leave at once.
+// Long-chain split for packed bf16 batches, the fixed-length split applied per
+// sequence.  The lengths are only on the device, so a planner kernel (one CTA)
+// reads the validated cu_seqlens, picks a segment length S (64-token chunks) and
+// a ratio r for segment 0 from a cost model, and writes the plan into the
+// workspace: every sequence of at least 2 S chunks is cut into up to 64
+// segments, segments 1 .. nseg-1 of about S chunks and segment 0 about r times
+// as long (r = 1: equal segments, the last one shorter); the others run whole.
+// The transition pass runs each split sequence's segment 0 from its start state
+// with its outputs (its end state is S_1) and the b and M items of segments
+// 1 .. nseg-2; the output pass runs segments 1 .. nseg-1 and the whole
+// sequences.  The passes (transitions, scan, outputs) launch over grids sized by
+// an upper bound; CTAs past the plan's counts leave at once.
 //
-// Cost model, in chunk-steps on `sms` SMs with one CTA each: a pass whose
-// items (chains or segments) total W chunks, the longest L, takes about
-// max(L, W / sms + L / 2); the scan about half a chunk-step per segment.  The
-// split is taken when it saves at least 10% against running every chain
-// whole.
+// Cost model, in chunk-steps on `sms` SMs with one CTA each: the transition pass
+// as the list schedule of its segment-0 items (taken first) and then its b and M
+// items (plan_makespan, with the longest of each); the output pass, whose items
+// total W chunks, the longest L, about max(L, W / sms + L / 2); the scan about
+// half a chunk-step per segment.  The split is taken when it saves at least 10%
+// against running every chain whole.
 struct PackedPlan {
-  int32_t n_trans;   // transition items (sequence, segment < nseg - 1)
+  int32_t n_trans;   // transition entries (sequence, segment < nseg - 1), segment 0 first
   int32_t n_split;   // split sequences
-  int32_t n_out;     // output items (sequence, segment), longest first
+  int32_t n_out;     // output items (sequence, segment >= 1, or whole), longest first
   int32_t seg_chunks;  // S, or 0 when nothing is split
 };
 struct PlanItem {
@@ -191,7 +198,7 @@ inline bool packed_split_possible(bool bf16_d128, int64_t T) {
 // workspace bytes after the order list: the plan (header, per-sequence
 // arrays, item tables; 256-byte aligned), then the segment states
 inline size_t packed_plan_bytes(int64_t N, int64_t ns_max) {
-  const size_t b = sizeof(PackedPlan) + (size_t)N * 3 * sizeof(int32_t) +
+  const size_t b = sizeof(PackedPlan) + (size_t)N * 4 * sizeof(int32_t) +
                    (size_t)ns_max * sizeof(PlanItem)            // transitions
                    + (size_t)ns_max * sizeof(int32_t)           // split sequences
                    + (size_t)(N + ns_max) * sizeof(PlanItem);   // outputs
@@ -204,7 +211,8 @@ inline size_t packed_state_bytes(int64_t ns_max, int64_t H, int D) {
 struct PlanView {
   PackedPlan* hdr;
   int32_t* nseg;      // [N] segments per sequence (1: whole)
-  int32_t* seglen;    // [N] tokens per segment (split sequences)
+  int32_t* seglen;    // [N] tokens per segment 1 .. nseg-1 (split sequences)
+  int32_t* seg0len;   // [N] tokens of segment 0 (split sequences)
   int32_t* slot;      // [N] first state slot of a split sequence (x H heads)
   PlanItem* trans;    // [ns_max]
   int32_t* split;     // [ns_max]
@@ -216,8 +224,9 @@ struct PlanView {
     p += sizeof(PackedPlan);
     v.nseg = reinterpret_cast<int32_t*>(p);
     v.seglen = v.nseg + N;
-    v.slot = v.seglen + N;
-    p += (size_t)N * 3 * sizeof(int32_t);
+    v.seg0len = v.seglen + N;
+    v.slot = v.seg0len + N;
+    p += (size_t)N * 4 * sizeof(int32_t);
     v.trans = reinterpret_cast<PlanItem*>(p);
     p += (size_t)ns_max * sizeof(PlanItem);
     v.split = reinterpret_cast<int32_t*>(p);
@@ -315,9 +324,10 @@ cudaError_t launch_prefill_f32(const FwdArgs& a);
 // the true start state, so S_1 = b_0 and the recursion starts at p = 1.
 cudaError_t launch_segment_scan(const float* seg_m, const float* seg_b, float* seg_s,
                                 int64_t chains, int nseg, cudaStream_t stream);
-// Packed: the split sequences of the device-written plan, H heads each.
-cudaError_t launch_segment_scan_packed(const float* h0, PlanView pv, float* states, int H,
-                                       int64_t ns_max, int64_t sms, cudaStream_t stream);
+// Packed: the split sequences of the device-written plan, H heads each (segment
+// 0 ran from the start state there too: S_1 = b_0).
+cudaError_t launch_segment_scan_packed(PlanView pv, float* states, int H, int64_t ns_max,
+                                       int64_t sms, cudaStream_t stream);
 cudaError_t launch_prefill_bf16(const FwdArgs& a);
 
 struct DecodeArgs {

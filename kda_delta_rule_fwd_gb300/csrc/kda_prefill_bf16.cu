@@ -1230,7 +1230,7 @@ cudaError_t run_bf16(const FwdArgs& a, const CUtensorMap& mq, const CUtensorMap&
     p.pstates = a.seg_ws;
     p.mode = MODE_PSEG_TRANSITION;
     if ((e = run(2 * a.H * a.ns_max)) != cudaSuccess) return e;
-    if ((e = launch_segment_scan_packed(a.h0, p.pv, a.seg_ws, a.H, a.ns_max, sms, a.stream)) !=
+    if ((e = launch_segment_scan_packed(p.pv, a.seg_ws, a.H, a.ns_max, sms, a.stream)) !=
         cudaSuccess)
       return e;
     p.mode = MODE_PSEG_OUTPUT;

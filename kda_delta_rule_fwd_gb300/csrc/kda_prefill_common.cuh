@@ -218,8 +218,11 @@ struct Waits {
 //                   start state (computed by the scan kernel); writes o, and hT
 //                   from the last segment.
 // The two PSEG modes do the same for packed batches, item by item from the
-// device-written plan (PackedPlan): a CTA past the plan's count leaves at once;
-// an output item of a sequence that is not split runs it whole (as CHAIN).
+// device-written plan (PackedPlan): PSEG_TRANSITION runs each split sequence's
+// segment 0 from its start state with its outputs (one item per head), then the
+// b and M items of segments 1 .. nseg-2; PSEG_OUTPUT runs segments 1 .. nseg-1
+// and the sequences that are not split, whole (as CHAIN).  A CTA past the plan's
+// count leaves at once.
 enum ItemMode {
   MODE_CHAIN = 0,
   MODE_SEG_TRANSITION = 1,
@@ -273,7 +276,8 @@ __device__ __forceinline__ int64_t item_count(const Bf16Params& p) {
   return p.mode == MODE_CHAIN ? (int64_t)p.nchains
          : p.mode == MODE_SEG_TRANSITION ? (int64_t)p.nchains * (2 * p.nseg - 3)
          : p.mode == MODE_SEG_OUTPUT ? (int64_t)p.nchains * (p.nseg - 1)
-         : p.mode == MODE_PSEG_TRANSITION ? 2 * (int64_t)p.H * p.pv.hdr->n_trans
+         : p.mode == MODE_PSEG_TRANSITION
+             ? (int64_t)p.H * (2 * (int64_t)p.pv.hdr->n_trans - p.pv.hdr->n_split)
                                           : (int64_t)p.H * p.pv.hdr->n_out;
 }
 
@@ -293,10 +297,19 @@ __device__ __forceinline__ ItemInfo decode_item(const Bf16Params& p, int item) {
     r.s_in = p.h0 ? p.h0 + ((int64_t)r.n * p.H + r.h) * DD : nullptr;
     r.s_out = p.hT ? p.hT + ((int64_t)r.n * p.H + r.h) * DD : nullptr;
   } else if (p.mode == MODE_PSEG_TRANSITION || p.mode == MODE_PSEG_OUTPUT) {
+    // transition items: H per segment-0 entry (the first n_split entries), then two
+    // (b, M) per head for each later entry
     const bool trans = p.mode == MODE_PSEG_TRANSITION;
-    const int kind = trans ? (item & 1) : 0, rest = trans ? (item >> 1) : item;
+    const int n0 = trans ? p.H * p.pv.hdr->n_split : 0;
+    int kind = 0, rest = item, it;
+    if (trans && item >= n0) {
+      kind = (item - n0) & 1;
+      rest = (item - n0) >> 1;
+      it = p.pv.hdr->n_split + rest / p.H;
+    } else {
+      it = rest / p.H;
+    }
     r.h = rest % p.H;
-    const int it = rest / p.H;
     const PlanItem pi = trans ? p.pv.trans[it] : p.pv.out[it];
     r.n = pi.n;
     p.seqs.get(r.n, r.t0, r.len);
@@ -306,10 +319,16 @@ __device__ __forceinline__ ItemInfo decode_item(const Bf16Params& p, int item) {
       r.s_in = p.h0 ? p.h0 + ((int64_t)r.n * p.H + r.h) * DD : nullptr;
       r.s_out = p.hT ? p.hT + ((int64_t)r.n * p.H + r.h) * DD : nullptr;
     } else {
-      // this chain's states: b (segments 0..nseg-2), M (same), start states (0..nseg-1)
+      // this chain's states: b (segments 0..nseg-2; b_0 holds S_1), M (same; M_0 is
+      // not formed), start states (0..nseg-1; S_0 is not stored)
       float* base = p.pstates + ((int64_t)p.pv.slot[r.n] * p.H + (int64_t)r.h * (3 * nseg - 2)) * DD;
-      const int64_t sl = p.pv.seglen[r.n], a0 = (int64_t)pi.seg * sl;
-      if (trans) {
+      const int64_t s0 = p.pv.seg0len[r.n], sl = p.pv.seglen[r.n];
+      const int64_t a0 = pi.seg == 0 ? 0 : s0 + (int64_t)(pi.seg - 1) * sl;
+      const int64_t ln = pi.seg == 0 ? s0 : sl;
+      if (trans && pi.seg == 0) {  // from the start state, with outputs; its end is S_1
+        r.s_in = p.h0 ? p.h0 + ((int64_t)r.n * p.H + r.h) * DD : nullptr;
+        r.s_out = base;
+      } else if (trans) {
         r.ident = r.zero_v = kind == 1;
         r.want_o = false;
         r.s_out = base + (int64_t)(kind ? (nseg - 1) + pi.seg : pi.seg) * DD;
@@ -319,7 +338,7 @@ __device__ __forceinline__ ItemInfo decode_item(const Bf16Params& p, int item) {
       }
       r.rel0 = a0;
       r.t0 += a0;
-      r.len = r.len - a0 < sl ? r.len - a0 : sl;
+      r.len = r.len - a0 < ln ? r.len - a0 : ln;
       if (r.len < 0) r.len = 0;
     }
   } else {

@@ -48,6 +48,7 @@ __global__ void kda_order_by_length(const int32_t* __restrict__ cu, int N,
 
 // Block-wide reductions of the planner (kPlanThreads threads).
 constexpr int kPlanThreads = 256;
+constexpr int kPlanWarps = kPlanThreads / 32;
 __device__ __forceinline__ int64_t block_sum(int64_t x, int64_t* sh) {
   sh[threadIdx.x] = x;
   __syncthreads();
@@ -79,6 +80,70 @@ __device__ __forceinline__ double pass_cost(int64_t W, int64_t L, int64_t sms) {
 __device__ __forceinline__ int64_t seq_chunks(const int32_t* cu, int n) {
   return ((int64_t)cu[n + 1] - cu[n] + 63) / 64;
 }
+__device__ __forceinline__ int64_t imax(int64_t a, int64_t b) { return a > b ? a : b; }
+
+// The segments of a sequence of c chunks for the candidate (S, r2): their count
+// ns, the length s of segments 1 .. ns-1 and s0 of segment 0, in chunks.  With
+// r2 > 2, segment 0 is about r2 / 2 times as long as the others and the last
+// one is whole; with r2 = 2 (or where that leaves segments shorter than the
+// minimum) the c / S segments are equal and the last one is shorter.  ns = 1:
+// the sequence runs whole (fewer than 2 S chunks).
+struct SegChoice {
+  int64_t ns, s, s0;
+};
+__device__ __forceinline__ SegChoice seg_choice(int64_t c, int64_t S, int r2) {
+  if (c < 2 * S) return SegChoice{1, 0, 0};
+  if (r2 > 2) {
+    int64_t ns = (2 * c - r2 * S) / (2 * S) + 1;
+    ns = ns < 2 ? 2 : (ns < kSegMaxSegs ? ns : kSegMaxSegs);
+    const int64_t den = r2 + 2 * (ns - 1), s = (2 * c + den - 1) / den, s0 = c - (ns - 1) * s;
+    if (s >= kSegMinChunks && s0 >= s) return SegChoice{ns, s, s0};
+  }
+  int64_t ns = c / S;
+  ns = ns < kSegMaxSegs ? ns : kSegMaxSegs;
+  const int64_t s = (c + ns - 1) / ns;
+  return SegChoice{ns, s, s};
+}
+
+// Per-candidate totals of the planner: sums (split sequences, b and M items per
+// head, output work, segments) and maxima (segment 0, segments >= 1, longest
+// output item, segments of one sequence).
+struct PlanAcc {
+  int64_t nsp, n2, w1, w2, tot, a, b, l2, nsm;
+};
+__device__ __forceinline__ void acc_combine(PlanAcc& x, const PlanAcc& y) {
+  x.nsp += y.nsp;
+  x.n2 += y.n2;
+  x.w1 += y.w1;
+  x.w2 += y.w2;
+  x.tot += y.tot;
+  x.a = imax(x.a, y.a);
+  x.b = imax(x.b, y.b);
+  x.l2 = imax(x.l2, y.l2);
+  x.nsm = imax(x.nsm, y.nsm);
+}
+// the block's totals, the same in every thread (warp shuffles, then the warps)
+__device__ PlanAcc block_reduce(PlanAcc x, PlanAcc* sh) {
+  for (int o = 16; o > 0; o >>= 1) {
+    PlanAcc y;
+    y.nsp = __shfl_xor_sync(0xffffffffu, x.nsp, o);
+    y.n2 = __shfl_xor_sync(0xffffffffu, x.n2, o);
+    y.w1 = __shfl_xor_sync(0xffffffffu, x.w1, o);
+    y.w2 = __shfl_xor_sync(0xffffffffu, x.w2, o);
+    y.tot = __shfl_xor_sync(0xffffffffu, x.tot, o);
+    y.a = __shfl_xor_sync(0xffffffffu, x.a, o);
+    y.b = __shfl_xor_sync(0xffffffffu, x.b, o);
+    y.l2 = __shfl_xor_sync(0xffffffffu, x.l2, o);
+    y.nsm = __shfl_xor_sync(0xffffffffu, x.nsm, o);
+    acc_combine(x, y);
+  }
+  if ((threadIdx.x & 31) == 0) sh[threadIdx.x / 32] = x;
+  __syncthreads();
+  PlanAcc r = sh[0];
+  for (int w = 1; w < kPlanWarps; ++w) acc_combine(r, sh[w]);
+  __syncthreads();
+  return r;
+}
 
 // The long-chain split plan of a packed batch (see PackedPlan).  One CTA.
 // `order` holds the sequences longest first (kda_order_by_length).
@@ -87,6 +152,7 @@ kda_plan_packed_split(const int32_t* __restrict__ cu, const int32_t* __restrict_
                       int H, int64_t sms, int64_t ns_max, void* plan_base,
                       unsigned int* __restrict__ status) {
   __shared__ int64_t sh[kPlanThreads];
+  __shared__ PlanAcc sha[kPlanWarps];
   const int tid = threadIdx.x;
   PlanView pv = PlanView::at(plan_base, N, ns_max);
   if (status && *(volatile const unsigned int*)status == (unsigned)KDA_ERR_BAD_SEQLENS) {
@@ -101,53 +167,53 @@ kda_plan_packed_split(const int32_t* __restrict__ cu, const int32_t* __restrict_
   }
   const int64_t maxc = block_max(mc, sh), W0 = block_sum(w, sh) * H;
   const double cost0 = pass_cost(W0, maxc, sms);
-  // candidate segment lengths 64, 80, 96, 128, 160, 192, ... while 2 S <= maxc
+  // candidates: S = 64, 80, 96, 128, 160, 192, ... while 2 S <= maxc, each with
+  // segment 0 r2 / 2 = 1, 1.5, 2, 2.5 or 3 times as long
   double best = 0.9 * cost0;
   int64_t bestS = 0;
+  int bestR = 2;
   for (int i = 0;; ++i) {
     const int64_t S = (int64_t)(64 + 16 * (i % 3)) << (i / 3);
     if (2 * S > maxc) break;
-    int64_t w1 = 0, l1 = 0, w2 = 0, l2 = 0, nsm = 0, tot = 0;
-    for (int n = tid; n < N; n += kPlanThreads) {
-      const int64_t c = seq_chunks(cu, n);
-      if (c >= 2 * S) {
-        int64_t ns = c / S;
-        ns = ns < kSegMaxSegs ? ns : kSegMaxSegs;
-        const int64_t sl = (c + ns - 1) / ns;
-        w1 += 2 * (ns - 1) * sl;
-        w2 += ns * sl;
-        l1 = sl > l1 ? sl : l1;
-        l2 = sl > l2 ? sl : l2;
-        nsm = ns > nsm ? ns : nsm;
-        tot += ns;
-      } else {
-        w2 += c;
-        l2 = c > l2 ? c : l2;
+    for (int r2 = 2; r2 <= 6; ++r2) {
+      PlanAcc x{0, 0, 0, 0, 0, 0, 0, 0, 0};
+      for (int n = tid; n < N; n += kPlanThreads) {
+        const int64_t c = seq_chunks(cu, n);
+        const SegChoice g = seg_choice(c, S, r2);
+        if (g.ns >= 2) {
+          x.nsp += 1;
+          x.n2 += 2 * (g.ns - 2);
+          x.w1 += g.s0 + 2 * (g.ns - 2) * g.s;
+          x.w2 += (g.ns - 1) * g.s;
+          x.tot += g.ns;
+          x.a = imax(x.a, g.s0);
+          x.b = imax(x.b, g.s);
+          x.l2 = imax(x.l2, g.s);
+          x.nsm = imax(x.nsm, g.ns);
+        } else {
+          x.w2 += c;
+          x.l2 = imax(x.l2, c);
+        }
       }
-    }
-    w1 = block_sum(w1, sh) * H;
-    w2 = block_sum(w2, sh) * H;
-    tot = block_sum(tot, sh);
-    l1 = block_max(l1, sh);
-    l2 = block_max(l2, sh);
-    nsm = block_max(nsm, sh);
-    const double c = pass_cost(w1, l1, sms) + 0.5 * (double)nsm + pass_cost(w2, l2, sms);
-    if (tot <= ns_max && c < best) {  // (uniform across the CTA: reduced values)
-      best = c;
-      bestS = S;
+      const PlanAcc t = block_reduce(x, sha);
+      const int64_t n1 = t.nsp * H;
+      const double c1 = n1 < sms ? (double)plan_makespan(n1, t.a, t.n2 * H, t.b, sms)
+                                 : pass_cost(t.w1 * H, t.a, sms);
+      const double c = c1 + 0.5 * (double)t.nsm + pass_cost(t.w2 * H, t.l2, sms);
+      if (t.tot <= ns_max && c < best) {  // (uniform across the CTA: reduced values)
+        best = c;
+        bestS = S;
+        bestR = r2;
+      }
     }
   }
   // per-sequence segments; thread 0 then builds the tables (few split sequences)
   for (int n = tid; n < N; n += kPlanThreads) {
-    const int64_t c = seq_chunks(cu, n);
-    int64_t ns = 1, sl = 0;
-    if (bestS > 0 && c >= 2 * bestS) {
-      ns = c / bestS;
-      ns = ns < kSegMaxSegs ? ns : kSegMaxSegs;
-      sl = (c + ns - 1) / ns;
-    }
-    pv.nseg[n] = (int32_t)ns;
-    pv.seglen[n] = (int32_t)(sl * 64);
+    const SegChoice g = bestS > 0 ? seg_choice(seq_chunks(cu, n), bestS, bestR)
+                                  : SegChoice{1, 0, 0};
+    pv.nseg[n] = (int32_t)g.ns;
+    pv.seglen[n] = (int32_t)(g.s * 64);
+    pv.seg0len[n] = (int32_t)(g.s0 * 64);
   }
   __syncthreads();
   if (tid != 0) return;
@@ -164,14 +230,25 @@ kda_plan_packed_split(const int32_t* __restrict__ cu, const int32_t* __restrict_
     }
     pv.split[j] = n;
   }
+  // transition entries: every split sequence's segment 0 first, longest first
+  // (insertion by segment-0 length), then segments 1 .. nseg-2
   for (int i = 0; i < n_split; ++i) {
     const int32_t n = pv.split[i];
     pv.slot[n] = slot;
     slot += 3 * pv.nseg[n] - 2;
-    for (int32_t sg = 0; sg + 1 < pv.nseg[n]; ++sg) pv.trans[n_trans++] = PlanItem{n, sg};
+    int32_t j = n_trans++;
+    while (j > 0 && pv.seg0len[pv.trans[j - 1].n] < pv.seg0len[n]) {
+      pv.trans[j] = pv.trans[j - 1];
+      --j;
+    }
+    pv.trans[j] = PlanItem{n, 0};
   }
-  // outputs longest first: merge the split sequences' segments with the whole
-  // sequences (both lists already in decreasing length)
+  for (int i = 0; i < n_split; ++i) {
+    const int32_t n = pv.split[i];
+    for (int32_t sg = 1; sg + 1 < pv.nseg[n]; ++sg) pv.trans[n_trans++] = PlanItem{n, sg};
+  }
+  // outputs longest first: merge the split sequences' segments 1 .. nseg-1 with the
+  // whole sequences (both lists already in decreasing length)
   int i = 0, r = 0;
   while (true) {
     while (r < N && pv.nseg[order[r]] >= 2) ++r;  // split ones come from the other list
@@ -181,7 +258,7 @@ kda_plan_packed_split(const int32_t* __restrict__ cu, const int32_t* __restrict_
     const int64_t lseq = has_seq ? (int64_t)cu[order[r] + 1] - cu[order[r]] : -1;
     if (has_seg && lseg >= lseq) {
       const int32_t n = pv.split[i++];
-      for (int32_t sg = 0; sg < pv.nseg[n]; ++sg) pv.out[n_out++] = PlanItem{n, sg};
+      for (int32_t sg = 1; sg < pv.nseg[n]; ++sg) pv.out[n_out++] = PlanItem{n, sg};
     } else {
       pv.out[n_out++] = PlanItem{order[r++], 0};
     }

@@ -97,9 +97,10 @@ kda_segment_scan_kernel(const float* __restrict__ seg_m, const float* __restrict
 }
 
 // Packed batches: (split sequence, head, column block) of the plan, grid-stride.
+// As for fixed-length batches, segment 0 ran from the sequence's start state and
+// b_0 is S_1: S_{p+1} = M_p S_p + b_p for p = 1 .. nseg-2.
 __global__ void __launch_bounds__(kThreads)
-kda_segment_scan_packed_kernel(const float* __restrict__ h0, PlanView pv,
-                               float* __restrict__ states, int H) {
+kda_segment_scan_packed_kernel(PlanView pv, float* __restrict__ states, int H) {
   extern __shared__ __align__(16) float sm[];
   const int64_t work = (int64_t)pv.hdr->n_split * H * kBlocks;
   for (int64_t w = blockIdx.x; w < work; w += gridDim.x) {
@@ -108,9 +109,8 @@ kda_segment_scan_packed_kernel(const float* __restrict__ h0, PlanView pv,
     const int h = (int)(chain % H), si = (int)(chain / H);
     const int n = pv.split[si], nseg = pv.nseg[n];
     float* base = states + ((int64_t)pv.slot[n] * H + (int64_t)h * (3 * nseg - 2)) * D * D;
-    scan_block(h0 ? h0 + ((int64_t)n * H + h) * D * D : nullptr,
-               base + (int64_t)(nseg - 1) * D * D, base, base + (int64_t)2 * (nseg - 1) * D * D,
-               nseg, cb, sm);
+    scan_block(base, base + (int64_t)nseg * D * D, base + (int64_t)D * D,
+               base + (int64_t)(2 * (nseg - 1) + 1) * D * D, nseg - 1, cb, sm);
     __syncthreads();  // shared memory is reused by the next block
   }
 }
@@ -127,15 +127,15 @@ cudaError_t launch_segment_scan(const float* seg_m, const float* seg_b, float* s
   return cudaGetLastError();
 }
 
-cudaError_t launch_segment_scan_packed(const float* h0, PlanView pv, float* states, int H,
-                                       int64_t ns_max, int64_t sms, cudaStream_t stream) {
+cudaError_t launch_segment_scan_packed(PlanView pv, float* states, int H, int64_t ns_max,
+                                       int64_t sms, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kda_segment_scan_packed_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
   if (e != cudaSuccess) return e;
   // (at most ns_max / 2 sequences are split; three CTAs fit an SM)
   const int64_t work = (ns_max / 2 + 1) * H * kBlocks, cap = 3 * (sms > 0 ? sms : kGb300Sms);
   kda_segment_scan_packed_kernel<<<(unsigned)(work < cap ? work : cap), kThreads, kSmem,
-                                   stream>>>(h0, pv, states, H);
+                                   stream>>>(pv, states, H);
   return cudaGetLastError();
 }
 

@@ -281,14 +281,14 @@ def test_bwd_workspace_and_argument_errors(lib):
 
 def test_workspace_size_packed_long_chain_split(lib):
     """A packed bf16 batch of at least 2 * 64 chunks may hold a sequence the device
-    planner splits: the workspace then reserves the plan (header, three int32 per
+    planner splits: the workspace then reserves the plan (header, four int32 per
     sequence, the item tables) and 3 * ns_max float32 states per head, ns_max =
     T / 4096 + T / 524288 + 2 bounding the split sequences' segments."""
     m, L = lib
     assert m.workspace_size(_shape(m, B=1, T=8191, H=32, num_seqs=4)) == 256 + 256
     T, H, N = 267445, 2, 4
     ns = T // 4096 + T // 524288 + 2
-    plan = 16 + N * 12 + ns * 8 + ns * 4 + (N + ns) * 8
+    plan = 16 + N * 16 + ns * 8 + ns * 4 + (N + ns) * 8
     plan = (plan + 255) // 256 * 256
     assert m.workspace_size(_shape(m, B=1, T=T, H=H, num_seqs=N)) == \
         256 + 256 + plan + 3 * ns * H * 128 * 128 * 4

@@ -619,15 +619,17 @@ def _packed_plan(ws, N):
 
 def test_packed_long_chain_split(kda, oracle_mod):
     """[2^18, 300, 1, 5000] tokens, H=2: the planner cuts the 4096-chunk sequence
-    into 64 segments of 64 chunks and leaves the others whole; the split run and
-    a run without the split (minimum workspace) both match the oracle."""
+    into 63 segments, segment 0 of 128 chunks (run from the start state with its
+    outputs in the transition pass) and the others of 64, and leaves the others
+    whole: 62 transition entries, 62 + 3 output items.  The split run and a run
+    without the split (minimum workspace) both match the oracle."""
     lens = [1 << 18, 300, 1, 5000]
     x = kda_inputs.packed(lens, 2, 128, dtype=torch.bfloat16, device=DEV, seed=960, h0_std=0.1)
     shape = kda.make_shape(x.q, x.v, packed_seqs=4)
     ws = kda.new_workspace(shape, DEV)
     o, hT = kda.fwd(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens, h0=x.h0, workspace=ws)
     assert kda.read_device_status(ws) == kda.KDA_OK
-    assert _packed_plan(ws, 4) == [63, 1, 64 + 3, 64]
+    assert _packed_plan(ws, 4) == [62, 1, 62 + 3, 64]
     small = torch.empty(512, dtype=torch.uint8, device=DEV)
     o_u, h_u = kda.fwd(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens, h0=x.h0,
                        workspace=small)
