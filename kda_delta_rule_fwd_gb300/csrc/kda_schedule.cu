@@ -145,6 +145,39 @@ __device__ PlanAcc block_reduce(PlanAcc x, PlanAcc* sh) {
   return r;
 }
 
+// one sequence of c chunks into a candidate's totals
+__device__ __forceinline__ void acc_add(PlanAcc& x, int64_t c, int64_t S, int r2) {
+  const SegChoice g = seg_choice(c, S, r2);
+  if (g.ns >= 2) {
+    x.nsp += 1;
+    x.n2 += 2 * (g.ns - 2);
+    x.w1 += g.s0 + 2 * (g.ns - 2) * g.s;
+    x.w2 += (g.ns - 1) * g.s;
+    x.tot += g.ns;
+    x.a = imax(x.a, g.s0);
+    x.b = imax(x.b, g.s);
+    x.l2 = imax(x.l2, g.s);
+    x.nsm = imax(x.nsm, g.ns);
+  } else {
+    x.w2 += c;
+    x.l2 = imax(x.l2, c);
+  }
+}
+// modelled chunk-steps of a candidate from its totals (infinite past ns_max)
+__device__ __forceinline__ double cand_cost(const PlanAcc& t, int H, int64_t sms, int64_t ns_max) {
+  if (t.tot > ns_max) return 1e300;
+  const int64_t n1 = t.nsp * H;
+  const double c1 = n1 < sms ? (double)plan_makespan(n1, t.a, t.n2 * H, t.b, sms)
+                             : pass_cost(t.w1 * H, t.a, sms);
+  return c1 + 0.5 * (double)t.nsm + pass_cost(t.w2 * H, t.l2, sms);
+}
+// candidate k: S = 64, 80, 96, 128, 160, 192, ... (index k / 5), r2 = 2 + k % 5
+__device__ __forceinline__ int64_t cand_S(int k) {
+  const int i = k / 5;
+  return (int64_t)(64 + 16 * (i % 3)) << (i / 3);
+}
+constexpr int kPlanSmallN = 512;  // up to this many sequences a thread costs a whole candidate
+
 // The long-chain split plan of a packed batch (see PackedPlan).  One CTA.
 // `order` holds the sequences longest first (kda_order_by_length).
 __global__ void __launch_bounds__(kPlanThreads)
@@ -168,45 +201,61 @@ kda_plan_packed_split(const int32_t* __restrict__ cu, const int32_t* __restrict_
   const int64_t maxc = block_max(mc, sh), W0 = block_sum(w, sh) * H;
   const double cost0 = pass_cost(W0, maxc, sms);
   // candidates: S = 64, 80, 96, 128, 160, 192, ... while 2 S <= maxc, each with
-  // segment 0 r2 / 2 = 1, 1.5, 2, 2.5 or 3 times as long
-  double best = 0.9 * cost0;
-  int64_t bestS = 0;
-  int bestR = 2;
-  for (int i = 0;; ++i) {
-    const int64_t S = (int64_t)(64 + 16 * (i % 3)) << (i / 3);
-    if (2 * S > maxc) break;
-    for (int r2 = 2; r2 <= 6; ++r2) {
+  // segment 0 r2 / 2 = 1, 1.5, 2, 2.5 or 3 times as long; the cheapest (the first
+  // of equals) is taken if it saves 10% against cost0
+  int ncand = 0;
+  while (2 * cand_S(ncand) <= maxc) ncand += 5;
+  double best = 1e300;
+  int bestk = -1;
+  if (N <= kPlanSmallN) {
+    // few sequences: each thread costs whole candidates, then one arg-min
+    for (int k = tid; k < ncand; k += kPlanThreads) {
       PlanAcc x{0, 0, 0, 0, 0, 0, 0, 0, 0};
-      for (int n = tid; n < N; n += kPlanThreads) {
-        const int64_t c = seq_chunks(cu, n);
-        const SegChoice g = seg_choice(c, S, r2);
-        if (g.ns >= 2) {
-          x.nsp += 1;
-          x.n2 += 2 * (g.ns - 2);
-          x.w1 += g.s0 + 2 * (g.ns - 2) * g.s;
-          x.w2 += (g.ns - 1) * g.s;
-          x.tot += g.ns;
-          x.a = imax(x.a, g.s0);
-          x.b = imax(x.b, g.s);
-          x.l2 = imax(x.l2, g.s);
-          x.nsm = imax(x.nsm, g.ns);
-        } else {
-          x.w2 += c;
-          x.l2 = imax(x.l2, c);
-        }
-      }
-      const PlanAcc t = block_reduce(x, sha);
-      const int64_t n1 = t.nsp * H;
-      const double c1 = n1 < sms ? (double)plan_makespan(n1, t.a, t.n2 * H, t.b, sms)
-                                 : pass_cost(t.w1 * H, t.a, sms);
-      const double c = c1 + 0.5 * (double)t.nsm + pass_cost(t.w2 * H, t.l2, sms);
-      if (t.tot <= ns_max && c < best) {  // (uniform across the CTA: reduced values)
+      const int64_t S = cand_S(k);
+      for (int n = 0; n < N; ++n) acc_add(x, seq_chunks(cu, n), S, 2 + k % 5);
+      const double c = cand_cost(x, H, sms, ns_max);
+      if (c < best) {
         best = c;
-        bestS = S;
-        bestR = r2;
+        bestk = k;
+      }
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+      const double ob = __shfl_xor_sync(0xffffffffu, best, o);
+      const int ok = __shfl_xor_sync(0xffffffffu, bestk, o);
+      if (ob < best || (ob == best && ok >= 0 && (bestk < 0 || ok < bestk))) {
+        best = ob;
+        bestk = ok;
+      }
+    }
+    __shared__ double shb[kPlanWarps];
+    __shared__ int shk[kPlanWarps];
+    if ((tid & 31) == 0) {
+      shb[tid / 32] = best;
+      shk[tid / 32] = bestk;
+    }
+    __syncthreads();
+    best = shb[0];
+    bestk = shk[0];
+    for (int w2 = 1; w2 < kPlanWarps; ++w2)
+      if (shb[w2] < best || (shb[w2] == best && shk[w2] >= 0 && (bestk < 0 || shk[w2] < bestk))) {
+        best = shb[w2];
+        bestk = shk[w2];
+      }
+  } else {
+    // many sequences: candidate by candidate, the totals by block reductions
+    for (int k = 0; k < ncand; ++k) {
+      PlanAcc x{0, 0, 0, 0, 0, 0, 0, 0, 0};
+      for (int n = tid; n < N; n += kPlanThreads) acc_add(x, seq_chunks(cu, n), cand_S(k), 2 + k % 5);
+      const double c = cand_cost(block_reduce(x, sha), H, sms, ns_max);
+      if (c < best) {  // (uniform across the CTA: reduced values)
+        best = c;
+        bestk = k;
       }
     }
   }
+  const bool split = bestk >= 0 && best < 0.9 * cost0;
+  const int64_t bestS = split ? cand_S(bestk) : 0;
+  const int bestR = split ? 2 + bestk % 5 : 2;
   // per-sequence segments; thread 0 then builds the tables (few split sequences)
   for (int n = tid; n < N; n += kPlanThreads) {
     const SegChoice g = bestS > 0 ? seg_choice(seq_chunks(cu, n), bestS, bestR)
