@@ -77,10 +77,10 @@ typedef struct {
  * counts as a packed call, which for a fixed-length call only over-estimates).
  * For a fixed-length bf16 batch with fewer (sequence, head) chains than SMs and
  * long sequences this includes the segment states of the long-chain split: each
- * chain is cut into up to 64 segments joined through their affine state maps, as
- * many as a model of the waves of CTAs on the current device's SMs favours (152,
- * a GB300's count, when no device can be queried), and 3 * nseg - 2 float32
- * dk x dv states per chain are reserved.  The minimum a call accepts is 256
+ * chain is cut into up to 64 segments joined through their affine state maps (the
+ * first up to 3 times as long as the others), as a model of the work items' schedule
+ * on the current device's SMs favours (152, a GB300's count, when no device can be
+ * queried), and 3 * nseg - 2 float32 dk x dv states per chain are reserved.  The minimum a call accepts is 256
  * bytes plus, for packed batches, 4 bytes per sequence rounded up to 64
  * sequences; with less than kda_workspace_size the split is skipped.  Returns 0
  * if `s` is NULL. */
