@@ -711,9 +711,12 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
       (isM ? dMm : dTm)[r * kSL + c] = (!isM || c <= r) ? v : 0.f;
     }
     if (tid < D) dgl[tid] = egl[tid] * scg[tid];
+    __syncthreads();  // the scratch area is read: the dY tiles' row sums take it
     // dY = T^T dU (one n-tile of 8 columns per warp; T is lower triangular);
-    // dbeta += rowsum(dY . X); dX = diag(beta) dY in place of X (each thread reads
-    // and writes only its own elements of X)
+    // dbeta += rowsum(dY . X), each tile's part to the scratch area and summed in a
+    // fixed order below (so that dbeta does not depend on the warps' timing);
+    // dX = diag(beta) dY in place of X (each thread reads and writes only its own
+    // elements of X)
     for (int nt = warp; nt < D / 8; nt += kBT / 32) {
       float acc[3][4];
       acc_zero(acc);
@@ -732,11 +735,19 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
       for (int hh = 0; hh < 2; ++hh) {  // the row's 8 columns of this tile: lanes t4 = 0..3
         part[hh] += __shfl_xor_sync(0xffffffffu, part[hh], 1);
         part[hh] += __shfl_xor_sync(0xffffffffu, part[hh], 2);
-        if (t4 == 0) atomicAdd(&sdb[g8 + 8 * hh], part[hh]);
+        if (t4 == 0) scr[nt * kBC + g8 + 8 * hh] = part[hh];
       }
     }
     __syncthreads();  // dU is consumed: dG may take its buffer; dT and dM are complete
-    // W = dT T^T (threads 0..255; M is consumed, so W takes its place)
+    // W = dT T^T (threads 0..255; M is consumed, so W takes its place); threads
+    // 256 .. 256 + 15 add the dY tiles' row sums to dbeta in tile order
+    if (tid >= 256 && tid < 256 + kBC) {
+      const int r = tid - 256;
+      float a = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < D / 8; ++nt) a += scr[nt * kBC + r];
+      sdb[r] += a;
+    }
     if (tid < 256) {
       const int wi = tid >> 4, wj = tid & 15;
       float acc = 0.f;
@@ -782,7 +793,7 @@ __global__ void __launch_bounds__(kBT, 1) kda_bwd_kernel(const BwdParams<TIn> p)
       float part = acc * Pm[ai * kSL + aj];
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-      if ((tid & 15) == 0) atomicAdd(&sdb[ai], part);
+      if ((tid & 15) == 0) sdb[ai] += part;  // one thread per row
       dTm[ai * kSL + aj] = sbeta[ai] * acc;  // dP (dT is consumed by W)
     }
     // dQb = scale dO S^T: dq = dQb e^Gam; dGam += Qb dQb   (U is consumed: dq takes it)

@@ -119,3 +119,17 @@ def test_bad_cu_seqlens_is_reported(kda):
     ws = torch.empty(kda.bwd_workspace_size(shape), dtype=torch.uint8, device=DEV)
     kda.bwd(x.q, x.k, x.v, x.g, x.beta, do, cu_seqlens=bad, workspace=ws)
     assert kda.read_device_status(ws) == kda.KDA_ERR_BAD_SEQLENS
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_repeatable_bit_for_bit(kda, d):
+    """Two calls on the same inputs give the same gradients bit for bit: every
+    cross-warp sum (dbeta's row sums among them) is taken in a fixed order."""
+    x = kda_inputs.fixed(2, 300, 4, d, dtype=torch.bfloat16, device=DEV, seed=760 + d,
+                         h0_std=0.1)
+    do, dh = _cotangents(x, 761)
+    a = kda.bwd(x.q, x.k, x.v, x.g, x.beta, do, h0=x.h0, dhT=dh)
+    b = kda.bwd(x.q, x.k, x.v, x.g, x.beta, do, h0=x.h0, dhT=dh)
+    torch.cuda.synchronize()
+    for name, u, v in zip(NAMES, a, b):
+        assert torch.equal(u, v), name
