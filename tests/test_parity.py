@@ -641,6 +641,32 @@ def test_packed_long_chain_split(kda, oracle_mod):
         assert rel_err(hh, h_ref) <= TOL_BF16
 
 
+def test_packed_split_longer_first_segments(kda, oracle_mod):
+    """[65536, 40000, 9000] tokens, H=4, start states: the planner (S = 64 chunks,
+    segment 0 twice as long) cuts the first two sequences into 15 segments of 64
+    chunks after a segment 0 of 128, and 8 of 70 after one of 135 (their segment-0
+    items run first, the longer first), while the third, too short for that, gets 2
+    equal segments of 71: 14 + 7 + 1 transition entries and as many output items.
+    Every head matches the oracle, and the run without the split."""
+    lens = [65536, 40000, 9000]
+    x = kda_inputs.packed(lens, 4, 128, dtype=torch.bfloat16, device=DEV, seed=965, h0_std=0.1)
+    shape = kda.make_shape(x.q, x.v, packed_seqs=3)
+    ws = kda.new_workspace(shape, DEV)
+    o, hT = kda.fwd(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens, h0=x.h0, workspace=ws)
+    assert kda.read_device_status(ws) == kda.KDA_OK
+    assert _packed_plan(ws, 3) == [22, 3, 22, 64]
+    small = torch.empty(512, dtype=torch.uint8, device=DEV)
+    o_u, h_u = kda.fwd(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens, h0=x.h0,
+                       workspace=small)
+    torch.cuda.synchronize()
+    assert rel_err(o, o_u.double().cpu().numpy()) <= 1e-3
+    assert rel_err(hT, h_u.double().cpu().numpy()) <= 1e-3
+    o_ref, h_ref = oracle_mod.recurrent(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens,
+                                        h0=x.h0)
+    assert rel_err(o, o_ref) <= TOL_BF16
+    assert rel_err(hT, h_ref) <= TOL_BF16
+
+
 def test_packed_split_mixed_with_checkpoints(kda, oracle_mod):
     """Two split sequences of different segment lengths, an empty and short ones,
     strong gates inside a split sequence (token path in the transition passes),
