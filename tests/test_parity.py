@@ -667,6 +667,26 @@ def test_packed_split_longer_first_segments(kda, oracle_mod):
     assert rel_err(hT, h_ref) <= TOL_BF16
 
 
+def test_packed_split_many_sequences(kda, oracle_mod):
+    """600 packed sequences, one of 20000 tokens and 599 of 1 to 50: past 512
+    sequences the planner costs its candidates one by one with block reductions
+    (below, a thread costs each candidate over every sequence); it splits the long
+    sequence and leaves the others whole.  Every element matches the oracle."""
+    lens = [20000] + [1 + (i * 37) % 50 for i in range(599)]
+    x = kda_inputs.packed(lens, 2, 128, dtype=torch.bfloat16, device=DEV, seed=975, h0_std=0.1)
+    shape = kda.make_shape(x.q, x.v, packed_seqs=len(lens))
+    ws = kda.new_workspace(shape, DEV)
+    o, hT = kda.fwd(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens, h0=x.h0, workspace=ws)
+    assert kda.read_device_status(ws) == kda.KDA_OK
+    n_trans, n_split, n_out, S = _packed_plan(ws, len(lens))
+    assert n_split == 1 and S >= 64 and n_out == n_trans + 599
+    torch.cuda.synchronize()
+    o_ref, h_ref = oracle_mod.recurrent(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens,
+                                        h0=x.h0)
+    assert rel_err(o, o_ref) <= TOL_BF16
+    assert rel_err(hT, h_ref) <= TOL_BF16
+
+
 def test_packed_split_mixed_with_checkpoints(kda, oracle_mod):
     """Two split sequences of different segment lengths, an empty and short ones,
     strong gates inside a split sequence (token path in the transition passes),
