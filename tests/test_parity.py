@@ -446,6 +446,29 @@ def test_long_chain_split_longer_first_segment(kda, oracle_mod):
     assert rel_err(h_s[:, heads], h_ref) <= TOL_BF16
 
 
+def test_checkpoints_longer_first_segment(kda, oracle_mod):
+    """The split of 32 chains of 384 chunks (segment 0 of 128 chunks, four of 64) with
+    a checkpoint every 2048 tokens: those inside and at the end of segment 0 come from
+    the first launch, the others from the second, at positions counted from the
+    sequence's start.  Three sampled heads match the oracle's prefix states, and o
+    and hT equal kda_fwd's."""
+    x = kda_inputs.fixed(1, 64 * 384, 32, 128, dtype=torch.bfloat16, device=DEV, seed=81,
+                         h0_std=0.1)
+    o, hT, ck, off = kda.fwd_checkpoints(x.q, x.k, x.v, x.g, x.beta, h0=x.h0, interval=2048)
+    o2, h2 = kda.fwd(x.q, x.k, x.v, x.g, x.beta, h0=x.h0)
+    torch.cuda.synchronize()
+    assert off.tolist() == [0, 12]
+    assert torch.equal(o, o2) and torch.equal(hT, h2)
+    heads = [0, 17, 31]
+    q, k, v, g, b = (t[:, :, heads].contiguous().cpu() for t in (x.q, x.k, x.v, x.g, x.beta))
+    state = x.h0[:, heads].contiguous().cpu()
+    for r in range(12):
+        sl = lambda t: t[:, r * 2048:(r + 1) * 2048].contiguous()
+        _, h = oracle_mod.recurrent(sl(q), sl(k), sl(v), sl(g), sl(b), h0=state)
+        assert rel_err(ck[r][heads], h[0]) <= TOL_BF16, f"checkpoint {r}"
+        state = torch.from_numpy(h).float()
+
+
 def test_bounded_wait_runs_out_and_is_reported(kda, oracle_mod):
     """A device wait that can never complete gives up after its budget, latches
     KDA_ERR_DEVICE_TIMEOUT, and leaves the context usable for the next call."""
