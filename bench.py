@@ -617,6 +617,7 @@ def run_case(name):
       prefill   the headline batch, B=4, T=4096, H=32, d=128, bf16
       packed    the 16-sequence packed batch with h0
       long      B=1, T=65,536, H=32 (one chain per head split into segments)
+      long1m    B=1, T=1,048,576, H=32: the long-context call (segment split)
       decode1   1-token decode on a pool of 256 sequences x 32 heads
       decode8   8-token decode on the same pool
       bwd       the backward on B=1, T=512, H=4, d=128, bf16, with h0
@@ -625,9 +626,10 @@ def run_case(name):
     import kda_inputs
     import kda_delta_rule_fwd_gb300 as kda
     dev = torch.device("cuda:0")
-    if name in ("prefill", "packed", "long"):
+    if name in ("prefill", "packed", "long", "long1m"):
         x = (kda_inputs.workload(1, device=dev) if name == "prefill" else
              kda_inputs.workload(2, device=dev) if name == "packed" else
+             kda_inputs.workload(3, device=dev) if name == "long1m" else
              kda_inputs.fixed(1, 1 << 16, H, D, device=dev, seed=1003))
         for _ in range(2):
             out = kda.fwd(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens, h0=x.h0)
